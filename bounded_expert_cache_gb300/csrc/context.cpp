@@ -1,0 +1,591 @@
+// Context, cache admission, miss staging and the C ABI entry points.
+//
+// "MawForge" §IV-C: the worker allocates compact per-layer slot tensors; the
+// slot count follows from the cache bytes and the per-slot expert size; a
+// miss materialises the expert block into an available slot and updates the
+// route-to-slot metadata. "Nanite for Experts" §5.4: experts are copied as
+// 256 KiB virtual tiles rotating over three streams, and persistent device
+// page-table entries carry generations; §3.2: an invalid slot or generation
+// fails closed; §3.4: asynchronous copies need pinned host memory and
+// non-default streams. "Paging the Experts" §3.2: entries are pinned while
+// their layer is evaluated; §4.2: materialised bytes = misses x payload.
+//
+// Device state per layer: slot pool [S][slot_stride], page table pt[E]
+// (slot or -1), pt_gen[E] (generation the entry expects) and gen[S]
+// (generation of the slot's content). Admission writes pt/pt_gen; staging
+// writes gen only after every tile of the step has landed, so a kernel that
+// runs without the staging (or after a failed one) sees gen != pt_gen and
+// reads nothing from that slot.
+#include <cstdio>
+#include <cstring>
+
+#include "internal.h"
+
+namespace {
+
+thread_local std::string g_create_err;
+
+#define CK(call)                                                                   \
+  do {                                                                             \
+    cudaError_t e_ = (call);                                                       \
+    if (e_ != cudaSuccess) {                                                       \
+      ctx->err = std::string(#call) + ": " + cudaGetErrorString(e_);               \
+      return MOE_ERR_CUDA;                                                         \
+    }                                                                              \
+  } while (0)
+
+moe_status_t fail(moe_ctx_t* ctx, moe_status_t st, const std::string& msg) {
+  if (ctx) ctx->err = msg;
+  return st;
+}
+
+bool valid_layer(const moe_ctx_t* ctx, int32_t layer) {
+  return layer >= 0 && layer < ctx->cfg.n_layers;
+}
+
+int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
+
+}  // namespace
+
+namespace moe {
+
+ExpertGeom expert_geom(int32_t H, int32_t I, int32_t quant) {
+  ExpertGeom g;
+  g.H = H;
+  g.I = I;
+  g.quant = quant;
+  const int32_t rows[3] = {I, I, H};
+  const int32_t ks[3] = {H, H, I};
+  int64_t off = 0;
+  for (int m = 0; m < 3; ++m) {
+    const int64_t n = static_cast<int64_t>(rows[m]) * ks[m];
+    g.qbytes[m] = quant == MOE_Q8_0 ? n : n / 2;
+    g.sbytes[m] = n / 32 * 2;
+    g.qoff[m] = off;
+    off += g.qbytes[m];
+    g.soff[m] = off;
+    off += g.sbytes[m];
+  }
+  g.bytes = off;
+  return g;
+}
+
+}  // namespace moe
+
+extern "C" const char* moe_last_error(const moe_ctx_t* ctx) {
+  return ctx ? ctx->err.c_str() : g_create_err.c_str();
+}
+
+extern "C" void moe_destroy(moe_ctx_t* ctx) {
+  if (!ctx) return;
+  for (auto s : ctx->streams)
+    if (s) cudaStreamSynchronize(s);
+  cudaDeviceSynchronize();
+  for (auto s : ctx->slots) moe_slots_destroy(s);
+  for (auto e : ctx->ev_stage)
+    if (e) cudaEventDestroy(e);
+  if (ctx->ev_compute) cudaEventDestroy(ctx->ev_compute);
+  for (auto s : ctx->streams)
+    if (s) cudaStreamDestroy(s);
+  cudaFree(ctx->d_pool);
+  cudaFree(ctx->d_pt);
+  cudaFree(ctx->d_ptgen);
+  cudaFree(ctx->d_gen);
+  cudaFree(ctx->d_lest);
+  cudaFree(ctx->d_lbnd);
+  cudaFree(ctx->d_ticket);
+  cudaFree(ctx->d_repairs);
+  cudaFree(ctx->d_h);
+  cudaFree(ctx->d_err);
+  cudaFreeHost(ctx->h_pt);
+  cudaFreeHost(ctx->h_ptgen);
+  cudaFreeHost(ctx->h_gen);
+  cudaFreeHost(ctx->h_err);
+  cudaFreeHost(ctx->h_union);
+  delete ctx;
+}
+
+extern "C" moe_status_t moe_create(const moe_config_t* cfg, moe_ctx_t** out) {
+  if (!out) return MOE_ERR_ARG;
+  *out = nullptr;
+  if (!cfg) {
+    g_create_err = "moe_create: cfg is NULL";
+    return MOE_ERR_ARG;
+  }
+  const moe_config_t& c = *cfg;
+  std::string why;
+  if (c.n_layers < 1) why = "n_layers < 1";
+  else if (c.n_experts < 1 || c.n_experts > 1024) why = "n_experts outside 1..1024";
+  else if (c.top_k < 1 || c.top_k > 16 || c.top_k > c.n_experts) why = "top_k outside 1..min(16, E)";
+  else if (c.hidden < 32 || c.hidden % 32) why = "hidden not a positive multiple of 32";
+  else if (c.inter < 32 || c.inter % 32) why = "inter not a positive multiple of 32";
+  else if (c.shared_inter < 0 || c.shared_inter % 32) why = "shared_inter not a multiple of 32";
+  else if (c.quant != MOE_Q8_0 && c.quant != MOE_Q4_0) why = "unknown quant";
+  else if (c.slots_per_layer < 1 || c.slots_per_layer > c.n_experts) why = "slots_per_layer outside 1..E";
+  else if (c.policy != MOE_LRU && c.policy != MOE_RANDOM) why = "unknown policy";
+  else if (c.n_streams < 1 || c.n_streams > 8) why = "n_streams outside 1..8";
+  else if (c.tile_bytes < 16 || c.tile_bytes % 16) why = "tile_bytes not a positive multiple of 16";
+  else if (c.max_tokens < 1) why = "max_tokens < 1";
+  if (!why.empty()) {
+    g_create_err = "moe_create: " + why;
+    return MOE_ERR_ARG;
+  }
+  auto* ctx = new moe_ctx();
+  ctx->cfg = c;
+  moe_status_t st = MOE_OK;
+  auto bail = [&](moe_status_t s) {
+    g_create_err = ctx->err;
+    moe_destroy(ctx);
+    return s;
+  };
+#define CKC(call)                                                                  \
+  do {                                                                             \
+    cudaError_t e_ = (call);                                                       \
+    if (e_ != cudaSuccess) {                                                       \
+      ctx->err = std::string("moe_create: ") + #call + ": " + cudaGetErrorString(e_); \
+      return bail(MOE_ERR_CUDA);                                                   \
+    }                                                                              \
+  } while (0)
+  CKC(cudaGetDevice(&ctx->device));
+  CKC(cudaDeviceGetAttribute(&ctx->num_sms, cudaDevAttrMultiProcessorCount, ctx->device));
+  const int L = c.n_layers, E = c.n_experts, S = c.slots_per_layer;
+  ctx->geom = moe::expert_geom(c.hidden, c.inter, c.quant);
+  if (c.shared_inter > 0) ctx->sgeom = moe::expert_geom(c.hidden, c.shared_inter, c.quant);
+  ctx->slot_stride = round_up(ctx->geom.bytes, 256);
+  const size_t pool = static_cast<size_t>(L) * S * ctx->slot_stride + 256;
+  CKC(cudaMalloc(&ctx->d_pool, pool));
+  CKC(cudaMalloc(&ctx->d_pt, sizeof(int32_t) * L * E));
+  CKC(cudaMalloc(&ctx->d_ptgen, sizeof(uint32_t) * L * E));
+  CKC(cudaMalloc(&ctx->d_gen, sizeof(uint32_t) * L * S));
+  CKC(cudaMemset(ctx->d_pt, 0xFF, sizeof(int32_t) * L * E));
+  CKC(cudaMemset(ctx->d_ptgen, 0, sizeof(uint32_t) * L * E));
+  CKC(cudaMemset(ctx->d_gen, 0, sizeof(uint32_t) * L * S));
+  CKC(cudaHostAlloc(&ctx->h_pt, sizeof(int32_t) * L * E, cudaHostAllocDefault));
+  CKC(cudaHostAlloc(&ctx->h_ptgen, sizeof(uint32_t) * L * E, cudaHostAllocDefault));
+  CKC(cudaHostAlloc(&ctx->h_gen, sizeof(uint32_t) * L * S, cudaHostAllocDefault));
+  std::fill(ctx->h_pt, ctx->h_pt + L * E, -1);
+  std::fill(ctx->h_ptgen, ctx->h_ptgen + L * E, 0u);
+  std::fill(ctx->h_gen, ctx->h_gen + L * S, 0u);
+  const size_t te = static_cast<size_t>(c.max_tokens) * E;
+  CKC(cudaMalloc(&ctx->d_lest, sizeof(double) * te));
+  CKC(cudaMalloc(&ctx->d_lbnd, sizeof(double) * te));
+  CKC(cudaMalloc(&ctx->d_ticket, sizeof(unsigned int)));
+  CKC(cudaMemset(ctx->d_ticket, 0, sizeof(unsigned int)));
+  CKC(cudaMalloc(&ctx->d_repairs, sizeof(unsigned long long) * L));
+  CKC(cudaMemset(ctx->d_repairs, 0, sizeof(unsigned long long) * L));
+  ctx->ldh = static_cast<int32_t>(round_up(std::max(c.inter, c.shared_inter), 32));
+  const int tdec = std::min(c.max_tokens, 8);
+  CKC(cudaMalloc(&ctx->d_h, sizeof(float) * static_cast<size_t>(tdec * c.top_k + tdec) * ctx->ldh));
+  CKC(cudaMalloc(&ctx->d_err, sizeof(uint32_t)));
+  CKC(cudaMemset(ctx->d_err, 0, sizeof(uint32_t)));
+  CKC(cudaHostAlloc(&ctx->h_err, sizeof(uint32_t), cudaHostAllocDefault));
+  CKC(cudaHostAlloc(&ctx->h_union, sizeof(int32_t) * (2 * E + 2), cudaHostAllocDefault));
+  ctx->streams.assign(c.n_streams, nullptr);
+  ctx->ev_stage.assign(c.n_streams, nullptr);
+  for (int i = 0; i < c.n_streams; ++i) {
+    CKC(cudaStreamCreateWithFlags(&ctx->streams[i], cudaStreamNonBlocking));
+    CKC(cudaEventCreateWithFlags(&ctx->ev_stage[i], cudaEventDisableTiming));
+  }
+  CKC(cudaEventCreateWithFlags(&ctx->ev_compute, cudaEventDisableTiming));
+  ctx->shared.assign(L, nullptr);
+  ctx->tiles_staged.assign(L, 0);
+  ctx->bytes_staged.assign(L, 0);
+  for (int l = 0; l < L; ++l) {
+    moe_slots_t* s = nullptr;
+    st = moe_slots_create(E, S, c.policy, c.seed, l, ctx->geom.bytes, &s);
+    if (st != MOE_OK) {
+      ctx->err = "moe_create: slot manager";
+      return bail(st);
+    }
+    ctx->slots.push_back(s);
+  }
+  CKC(cudaDeviceSynchronize());
+#undef CKC
+  *out = ctx;
+  return MOE_OK;
+}
+
+extern "C" int64_t moe_payload_bytes(const moe_ctx_t* ctx) { return ctx ? ctx->geom.bytes : 0; }
+extern "C" int64_t moe_shared_payload_bytes(const moe_ctx_t* ctx) {
+  return ctx && ctx->cfg.shared_inter > 0 ? ctx->sgeom.bytes : 0;
+}
+
+extern "C" moe_status_t moe_bind_store(moe_ctx_t* ctx, const void* store, size_t bytes) {
+  if (!ctx) return MOE_ERR_ARG;
+  const size_t want = static_cast<size_t>(ctx->cfg.n_layers) * ctx->cfg.n_experts * ctx->geom.bytes;
+  if (!store || bytes != want)
+    return fail(ctx, MOE_ERR_ARG, "moe_bind_store: size must be L*E*payload = " + std::to_string(want));
+  cudaPointerAttributes attr{};
+  cudaError_t e = cudaPointerGetAttributes(&attr, store);
+  if (e != cudaSuccess || attr.type != cudaMemoryTypeHost) {
+    cudaGetLastError();
+    return fail(ctx, MOE_ERR_ARG, "moe_bind_store: store is not page-locked host memory");
+  }
+  ctx->store = static_cast<const uint8_t*>(store);
+  ctx->store_bytes = bytes;
+  return MOE_OK;
+}
+
+extern "C" moe_status_t moe_bind_shared(moe_ctx_t* ctx, int32_t layer, const void* dev_shared) {
+  if (!ctx) return MOE_ERR_ARG;
+  if (!valid_layer(ctx, layer)) return fail(ctx, MOE_ERR_ARG, "moe_bind_shared: bad layer");
+  if (ctx->cfg.shared_inter == 0) return fail(ctx, MOE_ERR_ARG, "moe_bind_shared: no shared expert configured");
+  if (!dev_shared || reinterpret_cast<uintptr_t>(dev_shared) % 16)
+    return fail(ctx, MOE_ERR_ARG, "moe_bind_shared: pointer must be non-null and 16-byte aligned");
+  ctx->shared[layer] = static_cast<const uint8_t*>(dev_shared);
+  return MOE_OK;
+}
+
+// ------------------------------------------------------------ routing
+static moe_status_t route_impl(moe_ctx_t* ctx, int32_t layer, const void* x, int32_t xt, int32_t T,
+                               const float* w_router, const float* bias, int32_t* topk_idx,
+                               float* topk_w, const moe_plan_t* plan, cudaStream_t st) {
+  if (!valid_layer(ctx, layer)) return fail(ctx, MOE_ERR_ARG, "route: bad layer");
+  if (T < 1 || T > ctx->cfg.max_tokens) return fail(ctx, MOE_ERR_ARG, "route: T outside 1..max_tokens");
+  if (xt != MOE_F32 && xt != MOE_BF16) return fail(ctx, MOE_ERR_ARG, "route: bad activation dtype");
+  if (!x || !w_router || !topk_idx || !topk_w) return fail(ctx, MOE_ERR_ARG, "route: null pointer");
+  if (T > 64) return fail(ctx, MOE_ERR_ARG, "route: T > 64 needs the prefill router, which is not built");
+  if (plan && plan->capacity < T * ctx->cfg.top_k)
+    return fail(ctx, MOE_ERR_ARG, "route: plan capacity < T*k");
+  moe::RouteArgs a{};
+  a.x = x;
+  a.xt = xt;
+  a.T = T;
+  a.H = ctx->cfg.hidden;
+  a.E = ctx->cfg.n_experts;
+  a.k = ctx->cfg.top_k;
+  a.w = w_router;
+  a.bias = bias;
+  a.topk_idx = topk_idx;
+  a.topk_w = topk_w;
+  a.l_est = ctx->d_lest;
+  a.l_bnd = ctx->d_lbnd;
+  a.ticket = ctx->d_ticket;
+  a.repairs = ctx->d_repairs + layer;
+  a.err = ctx->d_err;
+  if (plan) a.plan = *plan;
+  CK(moe::launch_route(a, ctx->num_sms, st));
+  return MOE_OK;
+}
+
+extern "C" moe_status_t moe_route(moe_ctx_t* ctx, int32_t layer, const void* x, int32_t xt, int32_t T,
+                                  const float* w_router, const float* bias, int32_t* topk_idx,
+                                  float* topk_w, moe_stream_t stream) {
+  if (!ctx) return MOE_ERR_ARG;
+  return route_impl(ctx, layer, x, xt, T, w_router, bias, topk_idx, topk_w, nullptr,
+                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+static bool plan_ok(const moe_plan_t* p) {
+  return p && p->counts && p->offsets && p->uniq && p->n_uniq && p->perm_tok && p->perm_rank &&
+         p->perm_w && p->inv;
+}
+
+extern "C" moe_status_t moe_plan_union(moe_ctx_t* ctx, const int32_t* topk_idx, const float* topk_w,
+                                       int32_t T, const moe_plan_t* plan, moe_stream_t stream) {
+  if (!ctx) return MOE_ERR_ARG;
+  if (!plan_ok(plan) || !topk_idx || !topk_w) return fail(ctx, MOE_ERR_ARG, "plan: null pointer");
+  if (T < 1 || T > ctx->cfg.max_tokens) return fail(ctx, MOE_ERR_ARG, "plan: T outside 1..max_tokens");
+  if (plan->capacity < T * ctx->cfg.top_k) return fail(ctx, MOE_ERR_ARG, "plan: capacity < T*k");
+  moe::PlanArgs a{};
+  a.idx = topk_idx;
+  a.w = topk_w;
+  a.T = T;
+  a.k = ctx->cfg.top_k;
+  a.E = ctx->cfg.n_experts;
+  a.plan = *plan;
+  a.err = ctx->d_err;
+  CK(moe::launch_plan(a, reinterpret_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
+// ------------------------------------------------------------ cache
+static void publish_page_table_host(moe_ctx_t* ctx, int32_t layer) {
+  const int E = ctx->cfg.n_experts, S = ctx->cfg.slots_per_layer;
+  const moe_slots* s = ctx->slots[layer];
+  const int32_t* pt = moe::slots_pt(s);
+  const uint32_t* gen = moe::slots_gen(s);
+  int32_t* hpt = ctx->h_pt + static_cast<size_t>(layer) * E;
+  uint32_t* hpg = ctx->h_ptgen + static_cast<size_t>(layer) * E;
+  for (int e = 0; e < E; ++e) {
+    hpt[e] = pt[e];
+    hpg[e] = pt[e] >= 0 ? gen[pt[e]] : 0u;
+  }
+  (void)S;
+}
+
+extern "C" moe_status_t moe_cache_admit(moe_ctx_t* ctx, int32_t layer, const moe_plan_t* plan,
+                                        moe_miss_list_t* misses, moe_stream_t stream) {
+  if (!ctx) return MOE_ERR_ARG;
+  if (!valid_layer(ctx, layer)) return fail(ctx, MOE_ERR_ARG, "admit: bad layer");
+  if (!plan_ok(plan) || !misses) return fail(ctx, MOE_ERR_ARG, "admit: null pointer");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int E = ctx->cfg.n_experts;
+  int32_t* hu = ctx->h_union;
+  CK(cudaMemcpyAsync(hu + 2 * E, plan->n_uniq, sizeof(int32_t), cudaMemcpyDeviceToHost, st));
+  CK(cudaMemcpyAsync(hu, plan->uniq, sizeof(int32_t) * E, cudaMemcpyDeviceToHost, st));
+  CK(cudaMemcpyAsync(hu + E, plan->counts, sizeof(int32_t) * E, cudaMemcpyDeviceToHost, st));
+  CK(cudaStreamSynchronize(st));
+  const int32_t nu = hu[2 * E];
+  if (nu < 0 || nu > E) return fail(ctx, MOE_ERR_STATE, "admit: plan holds no valid union");
+  if (nu > ctx->cfg.slots_per_layer)
+    return fail(ctx, MOE_ERR_CAPACITY,
+                "admit: the step's union is larger than the slots; the decode path evaluates "
+                "a layer with all its experts resident");
+  moe_status_t s = moe::slots_step(ctx->slots[layer], hu, nu, hu + E, misses, &ctx->err);
+  if (s != MOE_OK) return s;
+  publish_page_table_host(ctx, layer);
+  const size_t off = static_cast<size_t>(layer) * E;
+  CK(cudaMemcpyAsync(ctx->d_pt + off, ctx->h_pt + off, sizeof(int32_t) * E, cudaMemcpyHostToDevice, st));
+  CK(cudaMemcpyAsync(ctx->d_ptgen + off, ctx->h_ptgen + off, sizeof(uint32_t) * E,
+                     cudaMemcpyHostToDevice, st));
+  return MOE_OK;
+}
+
+extern "C" moe_status_t moe_stage_tiles(moe_ctx_t* ctx, int32_t layer, const moe_miss_list_t* misses,
+                                        moe_stream_t compute_stream) {
+  if (!ctx) return MOE_ERR_ARG;
+  if (!valid_layer(ctx, layer) || !misses || misses->layer != layer)
+    return fail(ctx, MOE_ERR_ARG, "stage: bad layer or miss list");
+  if (misses->n > 0 && !ctx->store) return fail(ctx, MOE_ERR_STATE, "stage: no store bound");
+  cudaStream_t cst = reinterpret_cast<cudaStream_t>(compute_stream);
+  const int E = ctx->cfg.n_experts, S = ctx->cfg.slots_per_layer;
+  const int ns = static_cast<int>(ctx->streams.size());
+  if (misses->n == 0) return MOE_OK;
+  // slots are overwritten only after the compute enqueued so far
+  CK(cudaEventRecord(ctx->ev_compute, cst));
+  for (int i = 0; i < ns; ++i) CK(cudaStreamWaitEvent(ctx->streams[i], ctx->ev_compute, 0));
+  const moe::ExpertGeom& g = ctx->geom;
+  const int64_t tile = ctx->cfg.tile_bytes;
+  int64_t issued = 0, bytes = 0;
+  bool injected = false;
+  for (int i = 0; i < misses->n && !injected; ++i) {
+    const int e = misses->expert[i], slot = misses->slot[i];
+    if (e < 0 || e >= E || slot < 0 || slot >= S) return fail(ctx, MOE_ERR_ARG, "stage: fill out of range");
+    const uint8_t* src = ctx->store + (static_cast<size_t>(layer) * E + e) * g.bytes;
+    uint8_t* dst = ctx->d_pool + (static_cast<size_t>(layer) * S + slot) * ctx->slot_stride;
+    for (int m = 0; m < 3 && !injected; ++m) {
+      const int64_t mo = g.qoff[m], mb = g.qbytes[m] + g.sbytes[m];
+      for (int64_t o = 0; o < mb; o += tile) {
+        if (ctx->fail_after_tiles >= 0 && issued == ctx->fail_after_tiles) {
+          injected = true;
+          break;
+        }
+        const int64_t len = std::min(tile, mb - o);
+        CK(cudaMemcpyAsync(dst + mo + o, src + mo + o, static_cast<size_t>(len), cudaMemcpyHostToDevice,
+                           ctx->streams[issued % ns]));
+        ++issued;
+        bytes += len;
+      }
+    }
+  }
+  for (int i = 0; i < ns; ++i) {
+    CK(cudaEventRecord(ctx->ev_stage[i], ctx->streams[i]));
+    CK(cudaStreamWaitEvent(cst, ctx->ev_stage[i], 0));
+  }
+  ctx->tiles_staged[layer] += issued;
+  ctx->bytes_staged[layer] += bytes;
+  if (injected) {
+    ctx->fail_after_tiles = -1;
+    return fail(ctx, MOE_ERR_CUDA, "stage: injected copy failure (test hook); slots not published");
+  }
+  // publish the new generations of the filled slots
+  const uint32_t* gen = moe::slots_gen(ctx->slots[layer]);
+  uint32_t* hg = ctx->h_gen + static_cast<size_t>(layer) * S;
+  for (int i = 0; i < misses->n; ++i) hg[misses->slot[i]] = gen[misses->slot[i]];
+  CK(cudaMemcpyAsync(ctx->d_gen + static_cast<size_t>(layer) * S, hg, sizeof(uint32_t) * S,
+                     cudaMemcpyHostToDevice, cst));
+  return MOE_OK;
+}
+
+extern "C" moe_status_t moe_cache_evict(moe_ctx_t* ctx, int32_t layer, int32_t expert) {
+  if (!ctx) return MOE_ERR_ARG;
+  if (!valid_layer(ctx, layer)) return fail(ctx, MOE_ERR_ARG, "evict: bad layer");
+  CK(cudaDeviceSynchronize());
+  moe_status_t s = moe::slots_evict(ctx->slots[layer], expert, &ctx->err);
+  if (s != MOE_OK) return s;
+  publish_page_table_host(ctx, layer);
+  const size_t off = static_cast<size_t>(layer) * ctx->cfg.n_experts;
+  CK(cudaMemcpy(ctx->d_pt + off, ctx->h_pt + off, sizeof(int32_t) * ctx->cfg.n_experts,
+                cudaMemcpyHostToDevice));
+  CK(cudaMemcpy(ctx->d_ptgen + off, ctx->h_ptgen + off, sizeof(uint32_t) * ctx->cfg.n_experts,
+                cudaMemcpyHostToDevice));
+  return MOE_OK;
+}
+
+extern "C" moe_status_t moe_cache_preload(moe_ctx_t* ctx, int32_t layer, const int32_t* experts,
+                                          int32_t n) {
+  if (!ctx) return MOE_ERR_ARG;
+  if (!valid_layer(ctx, layer) || n < 0 || (n > 0 && !experts))
+    return fail(ctx, MOE_ERR_ARG, "preload: bad arguments");
+  if (!ctx->store) return fail(ctx, MOE_ERR_STATE, "preload: no store bound");
+  CK(cudaDeviceSynchronize());
+  std::vector<int32_t> filled, fslots;
+  moe_status_t s = moe::slots_preload(ctx->slots[layer], experts, n, &filled, &fslots, &ctx->err);
+  if (s != MOE_OK) return s;
+  const int E = ctx->cfg.n_experts, S = ctx->cfg.slots_per_layer;
+  for (size_t i = 0; i < filled.size(); ++i) {
+    const uint8_t* src = ctx->store + (static_cast<size_t>(layer) * E + filled[i]) * ctx->geom.bytes;
+    uint8_t* dst = ctx->d_pool + (static_cast<size_t>(layer) * S + fslots[i]) * ctx->slot_stride;
+    CK(cudaMemcpy(dst, src, ctx->geom.bytes, cudaMemcpyHostToDevice));
+  }
+  publish_page_table_host(ctx, layer);
+  const uint32_t* gen = moe::slots_gen(ctx->slots[layer]);
+  uint32_t* hg = ctx->h_gen + static_cast<size_t>(layer) * S;
+  for (int i = 0; i < S; ++i) hg[i] = gen[i];
+  const size_t off = static_cast<size_t>(layer) * E;
+  CK(cudaMemcpy(ctx->d_pt + off, ctx->h_pt + off, sizeof(int32_t) * E, cudaMemcpyHostToDevice));
+  CK(cudaMemcpy(ctx->d_ptgen + off, ctx->h_ptgen + off, sizeof(uint32_t) * E, cudaMemcpyHostToDevice));
+  CK(cudaMemcpy(ctx->d_gen + static_cast<size_t>(layer) * S, hg, sizeof(uint32_t) * S,
+                cudaMemcpyHostToDevice));
+  return MOE_OK;
+}
+
+// ------------------------------------------------------------ FFN
+extern "C" moe_status_t moe_expert_ffn(moe_ctx_t* ctx, int32_t layer, const void* x, int32_t xt,
+                                       int32_t T, const moe_plan_t* plan, float* y, int32_t mode,
+                                       moe_stream_t stream) {
+  if (!ctx) return MOE_ERR_ARG;
+  if (!valid_layer(ctx, layer)) return fail(ctx, MOE_ERR_ARG, "ffn: bad layer");
+  if (!plan_ok(plan) || !x || !y) return fail(ctx, MOE_ERR_ARG, "ffn: null pointer");
+  if (T < 1 || T > ctx->cfg.max_tokens) return fail(ctx, MOE_ERR_ARG, "ffn: T outside 1..max_tokens");
+  if (xt != MOE_F32 && xt != MOE_BF16) return fail(ctx, MOE_ERR_ARG, "ffn: bad activation dtype");
+  if (plan->capacity < T * ctx->cfg.top_k) return fail(ctx, MOE_ERR_ARG, "ffn: plan capacity < T*k");
+  if (ctx->cfg.shared_inter > 0 && !ctx->shared[layer])
+    return fail(ctx, MOE_ERR_STATE, "ffn: shared expert of this layer not bound");
+  if (mode == MOE_MODE_AUTO) mode = T <= 8 ? MOE_MODE_DECODE : MOE_MODE_PREFILL;
+  if (mode == MOE_MODE_PREFILL)
+    return fail(ctx, MOE_ERR_ARG, "ffn: the prefill grouped-GEMM path is not built");
+  if (mode != MOE_MODE_DECODE || T > 8) return fail(ctx, MOE_ERR_ARG, "ffn: decode mode needs T <= 8");
+  const int E = ctx->cfg.n_experts, S = ctx->cfg.slots_per_layer;
+  moe::FfnArgs a{};
+  a.x = x;
+  a.xt = xt;
+  a.T = T;
+  a.H = ctx->cfg.hidden;
+  a.I = ctx->cfg.inter;
+  a.Is = ctx->cfg.shared_inter;
+  a.k = ctx->cfg.top_k;
+  a.E = E;
+  a.quant = ctx->cfg.quant;
+  a.pool = ctx->d_pool + static_cast<size_t>(layer) * S * ctx->slot_stride;
+  a.slot_stride = ctx->slot_stride;
+  a.pt = ctx->d_pt + static_cast<size_t>(layer) * E;
+  a.ptgen = ctx->d_ptgen + static_cast<size_t>(layer) * E;
+  a.gen = ctx->d_gen + static_cast<size_t>(layer) * S;
+  a.S = S;
+  a.shared = ctx->shared[layer];
+  a.g = ctx->geom;
+  a.gs = ctx->sgeom;
+  a.plan = *plan;
+  a.h = ctx->d_h;
+  a.ldh = ctx->ldh;
+  a.y = y;
+  a.err = ctx->d_err;
+  CK(moe::launch_ffn_decode(a, ctx->num_sms, reinterpret_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
+extern "C" moe_status_t moe_layer_forward(moe_ctx_t* ctx, int32_t layer, const void* x, int32_t xt,
+                                          int32_t T, const float* w_router, const float* bias,
+                                          int32_t* topk_idx, float* topk_w, const moe_plan_t* plan,
+                                          float* y, moe_miss_list_t* misses, moe_stream_t stream) {
+  if (!ctx) return MOE_ERR_ARG;
+  if (!plan_ok(plan)) return fail(ctx, MOE_ERR_ARG, "layer_forward: plan has a null array");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  moe_status_t s = route_impl(ctx, layer, x, xt, T, w_router, bias, topk_idx, topk_w, plan, st);
+  if (s != MOE_OK) return s;
+  moe_miss_list_t local{};
+  moe_miss_list_t* ml = misses ? misses : &local;
+  s = moe_cache_admit(ctx, layer, plan, ml, stream);
+  if (s != MOE_OK) return s;
+  s = moe_stage_tiles(ctx, layer, ml, stream);
+  if (s != MOE_OK) return s;
+  return moe_expert_ffn(ctx, layer, x, xt, T, plan, y, MOE_MODE_AUTO, stream);
+}
+
+extern "C" moe_status_t moe_check_device_errors(moe_ctx_t* ctx, moe_stream_t stream) {
+  if (!ctx) return MOE_ERR_ARG;
+  CK(cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)));
+  CK(cudaMemcpy(ctx->h_err, ctx->d_err, sizeof(uint32_t), cudaMemcpyDeviceToHost));
+  const uint32_t e = *ctx->h_err;
+  if (e == 0) return MOE_OK;
+  CK(cudaMemset(ctx->d_err, 0, sizeof(uint32_t)));
+  if (e & MOE_DEVERR_STALE)
+    return fail(ctx, MOE_ERR_STALE, "device: an expert's page-table entry or slot generation was invalid");
+  if (e & MOE_DEVERR_TIMEOUT) return fail(ctx, MOE_ERR_TIMEOUT, "device: a bounded wait ran out");
+  if (e & MOE_DEVERR_NONFINITE)
+    return fail(ctx, MOE_ERR_UNCERTIFIED, "device: non-finite router input; routing undefined");
+  return fail(ctx, MOE_ERR_ARG, "device: expert id out of range in a plan input");
+}
+
+// ------------------------------------------------------------ inspection
+extern "C" moe_status_t moe_get_stats(const moe_ctx_t* cctx, int32_t layer, moe_stats_t* out) {
+  moe_ctx_t* ctx = const_cast<moe_ctx_t*>(cctx);
+  if (!ctx || !out) return MOE_ERR_ARG;
+  if (layer != -1 && !valid_layer(ctx, layer)) return fail(ctx, MOE_ERR_ARG, "stats: bad layer");
+  const int L = ctx->cfg.n_layers;
+  std::vector<unsigned long long> rep(L);
+  CK(cudaDeviceSynchronize());
+  CK(cudaMemcpy(rep.data(), ctx->d_repairs, sizeof(unsigned long long) * L, cudaMemcpyDeviceToHost));
+  moe_stats_t t{};
+  for (int l = 0; l < L; ++l) {
+    if (layer != -1 && l != layer) continue;
+    moe_stats_t s = moe::slots_stats(ctx->slots[l]);
+    t.steps += s.steps;
+    t.hits += s.hits;
+    t.misses += s.misses;
+    t.evictions += s.evictions;
+    t.materialized_bytes += s.materialized_bytes;
+    t.tiles_staged += ctx->tiles_staged[l];
+    t.bytes_staged += ctx->bytes_staged[l];
+    t.uncertified_repairs += static_cast<int64_t>(rep[l]);
+  }
+  *out = t;
+  return MOE_OK;
+}
+
+extern "C" moe_status_t moe_read_page_table(moe_ctx_t* ctx, int32_t layer, int32_t* host_pt,
+                                            uint32_t* host_gen) {
+  if (!ctx) return MOE_ERR_ARG;
+  if (!valid_layer(ctx, layer)) return fail(ctx, MOE_ERR_ARG, "read_page_table: bad layer");
+  CK(cudaDeviceSynchronize());
+  const int E = ctx->cfg.n_experts, S = ctx->cfg.slots_per_layer;
+  if (host_pt)
+    CK(cudaMemcpy(host_pt, ctx->d_pt + static_cast<size_t>(layer) * E, sizeof(int32_t) * E,
+                  cudaMemcpyDeviceToHost));
+  if (host_gen)
+    CK(cudaMemcpy(host_gen, ctx->d_gen + static_cast<size_t>(layer) * S, sizeof(uint32_t) * S,
+                  cudaMemcpyDeviceToHost));
+  return MOE_OK;
+}
+
+extern "C" moe_status_t moe_read_slot(moe_ctx_t* ctx, int32_t layer, int32_t slot, void* host_out,
+                                      size_t bytes) {
+  if (!ctx) return MOE_ERR_ARG;
+  if (!valid_layer(ctx, layer) || slot < 0 || slot >= ctx->cfg.slots_per_layer || !host_out ||
+      bytes > static_cast<size_t>(ctx->geom.bytes))
+    return fail(ctx, MOE_ERR_ARG, "read_slot: bad arguments");
+  CK(cudaDeviceSynchronize());
+  const uint8_t* src =
+      ctx->d_pool + (static_cast<size_t>(layer) * ctx->cfg.slots_per_layer + slot) * ctx->slot_stride;
+  CK(cudaMemcpy(host_out, src, bytes, cudaMemcpyDeviceToHost));
+  return MOE_OK;
+}
+
+extern "C" moe_status_t moe_debug_fail_staging_after(moe_ctx_t* ctx, int32_t fail_after_tiles) {
+  if (!ctx) return MOE_ERR_ARG;
+  ctx->fail_after_tiles = fail_after_tiles < 0 ? -1 : fail_after_tiles;
+  return MOE_OK;
+}
+
+extern "C" moe_status_t moe_debug_corrupt_generation(moe_ctx_t* ctx, int32_t layer, int32_t expert) {
+  if (!ctx) return MOE_ERR_ARG;
+  if (!valid_layer(ctx, layer) || expert < 0 || expert >= ctx->cfg.n_experts)
+    return fail(ctx, MOE_ERR_ARG, "corrupt_generation: bad arguments");
+  CK(cudaDeviceSynchronize());
+  const size_t off = static_cast<size_t>(layer) * ctx->cfg.n_experts + expert;
+  ctx->h_ptgen[off] += 0x10000u;
+  CK(cudaMemcpy(ctx->d_ptgen + off, ctx->h_ptgen + off, sizeof(uint32_t), cudaMemcpyHostToDevice));
+  return MOE_OK;
+}

@@ -1,0 +1,129 @@
+// Library-internal declarations shared by the host (.cpp) and device (.cu)
+// translation units of libmoecache. Not part of the public ABI.
+#pragma once
+
+#include <algorithm>
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include <cuda_runtime.h>
+
+#include "../../include/moecache.h"
+
+// Device error bits, OR-ed into the context's error word by kernels.
+enum : uint32_t {
+  MOE_DEVERR_STALE = 1u,       // unit whose slot is absent or of another generation
+  MOE_DEVERR_TIMEOUT = 2u,     // a bounded wait ran out
+  MOE_DEVERR_NONFINITE = 4u,   // router input or weight not finite
+  MOE_DEVERR_BADIDX = 8u,      // expert id out of range in a plan input
+};
+
+namespace moe {
+
+moe_slots* slots_new(int32_t E, int32_t S, int32_t policy, uint64_t seed, int32_t layer,
+                     int64_t payload);
+moe_status_t slots_step(moe_slots* s, const int32_t* uniq, int32_t n_uniq, const int32_t* counts,
+                        moe_miss_list_t* out, std::string* err);
+moe_status_t slots_preload(moe_slots* s, const int32_t* experts, int32_t n,
+                           std::vector<int32_t>* filled, std::vector<int32_t>* filled_slots,
+                           std::string* err);
+moe_status_t slots_evict(moe_slots* s, int32_t e, std::string* err);
+const int32_t* slots_pt(const moe_slots* s);
+const uint32_t* slots_gen(const moe_slots* s);
+moe_stats_t slots_stats(const moe_slots* s);
+
+// Geometry of one expert payload in the split-plane layout.
+struct ExpertGeom {
+  int32_t H = 0, I = 0, quant = 0;
+  int64_t qbytes[3] = {0, 0, 0};  // quant-plane bytes of gate, up, down
+  int64_t sbytes[3] = {0, 0, 0};  // scale-plane bytes
+  int64_t qoff[3] = {0, 0, 0};    // quant-plane offsets within the payload
+  int64_t soff[3] = {0, 0, 0};    // scale-plane offsets
+  int64_t bytes = 0;              // payload bytes
+};
+ExpertGeom expert_geom(int32_t H, int32_t I, int32_t quant);
+
+// Arguments of the router launch.
+struct RouteArgs {
+  const void* x;
+  int32_t xt, T, H, E, k;
+  const float* w;
+  const float* bias;
+  int32_t* topk_idx;
+  float* topk_w;
+  double* l_est;        // [T][E] scratch
+  double* l_bnd;        // [T][E] scratch
+  unsigned int* ticket; // last-block counter, zero between launches
+  unsigned long long* repairs;  // repaired-token counter of the layer
+  uint32_t* err;
+  // optional fused plan (plan.counts == nullptr: none)
+  moe_plan_t plan;
+};
+cudaError_t launch_route(const RouteArgs& a, int num_sms, cudaStream_t st);
+
+struct PlanArgs {
+  const int32_t* idx;
+  const float* w;
+  int32_t T, k, E;
+  moe_plan_t plan;
+  uint32_t* err;
+};
+cudaError_t launch_plan(const PlanArgs& a, cudaStream_t st);
+
+// Arguments of the decode FFN launches.
+struct FfnArgs {
+  const void* x;
+  int32_t xt, T, H, I, Is, k, E, quant;
+  const uint8_t* pool;        // slot pool of the layer
+  int64_t slot_stride;
+  const int32_t* pt;          // [E] page table of the layer
+  const uint32_t* ptgen;      // [E]
+  const uint32_t* gen;        // [S]
+  int32_t S;
+  const uint8_t* shared;      // shared payload or nullptr
+  ExpertGeom g, gs;           // routed and shared geometry
+  moe_plan_t plan;
+  float* h;                   // scratch [(T*k + T)][ldh]
+  int32_t ldh;
+  float* y;                   // [T][H]
+  uint32_t* err;
+};
+cudaError_t launch_ffn_decode(const FfnArgs& a, int num_sms, cudaStream_t st);
+
+}  // namespace moe
+
+struct moe_ctx {
+  moe_config_t cfg{};
+  int device = 0;
+  int num_sms = 0;
+  moe::ExpertGeom geom, sgeom;
+  int64_t slot_stride = 0;
+  uint8_t* d_pool = nullptr;     // [L][S][slot_stride] (+ tail)
+  int32_t* d_pt = nullptr;       // [L][E]
+  uint32_t* d_ptgen = nullptr;   // [L][E]
+  uint32_t* d_gen = nullptr;     // [L][S]
+  int32_t* h_pt = nullptr;       // pinned mirrors
+  uint32_t* h_ptgen = nullptr;
+  uint32_t* h_gen = nullptr;
+  std::vector<moe_slots*> slots;
+  const uint8_t* store = nullptr;
+  size_t store_bytes = 0;
+  std::vector<const uint8_t*> shared;
+  // scratch
+  double* d_lest = nullptr;
+  double* d_lbnd = nullptr;
+  unsigned int* d_ticket = nullptr;
+  unsigned long long* d_repairs = nullptr;  // [L]
+  float* d_h = nullptr;
+  int32_t ldh = 0;
+  uint32_t* d_err = nullptr;
+  uint32_t* h_err = nullptr;
+  int32_t* h_union = nullptr;  // pinned: uniq [E], counts [E], n_uniq
+  std::vector<cudaStream_t> streams;
+  std::vector<cudaEvent_t> ev_stage;
+  cudaEvent_t ev_compute = nullptr;
+  int32_t fail_after_tiles = -1;
+  std::vector<int64_t> tiles_staged, bytes_staged;
+  std::string err;
+};

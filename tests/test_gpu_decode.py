@@ -1,0 +1,239 @@
+"""GPU parity of the decode path against the CPU oracle (through the C ABI).
+
+Bit-exact: top-k indices, expert-major plans, page tables, slot generations,
+hit/miss counters, staged slot bytes. Within tolerance (relative L2 <= 5e-3,
+max |diff| <= 2e-2 * RMS): layer outputs.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from oracle.cache import SlotCache
+
+from gpu_common import (ExpertCache, bind_all, make_context, pinned_store, tolerance_ok, x_to_f64,
+                        x_to_torch)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def bec():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import bounded_expert_cache_gb300 as m
+    return m
+
+
+def _route_gpu(bec, ctx, layer, x_t, Wr, bias, k):
+    T = x_t.shape[0]
+    idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    wt = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    ctx.route(layer, x_t, Wr, bias, idx, wt)
+    torch.cuda.synchronize()
+    ctx.check_device_errors()
+    return idx.cpu().numpy(), wt.cpu().numpy()
+
+
+@pytest.mark.parametrize("name,T", [("tiny", 4), ("decode", 1), ("decode", 4), ("mtp_decode", 4),
+                                    ("prefill", 3)])
+def test_route_matches_oracle(bec, name, T):
+    w = W.WORKLOADS[name]
+    ctx = make_context(bec, w, 1, max_tokens=T)
+    n_tok = min(w.n_tokens, 12)
+    Wr = W.router_weights(w, 0)
+    bias = W.router_bias(w, 0)
+    x = W.activations(w, 0, n_tok)
+    Wr_t = torch.from_numpy(Wr).cuda()
+    b_t = None if bias is None else torch.from_numpy(bias).cuda()
+    for s in range(0, n_tok - T + 1, T):
+        xs = x[s:s + T]
+        idx, wt = _route_gpu(bec, ctx, 0, x_to_torch(w, xs), Wr_t, b_t, w.top_k)
+        ridx, rw, _ = oracle.route(x_to_f64(w, xs), Wr, bias, w.top_k)
+        assert np.array_equal(idx, ridx), (s, idx, ridx)
+        assert np.allclose(wt, rw, rtol=1e-5, atol=1e-7)
+    ctx.close()
+
+
+def test_route_exact_ties_and_repair(bec):
+    # duplicated router rows give exactly equal logits: the fast bounds cannot
+    # order them, the exact repair must, with ties to the lower expert id
+    E, H, k = 64, 256, 4
+    rng = np.random.default_rng(5)
+    Wr = (rng.standard_normal((E, H)) * 0.02).astype(np.float32)
+    for (a, b) in ((10, 3), (40, 41), (63, 0), (7, 22)):
+        Wr[a] = Wr[b]
+    x = rng.standard_normal((6, H)).astype(np.float32)
+    x[5] = 0.0  # all logits zero -> experts 0..k-1
+    ctx = bec.Context(1, E, k, H, 128, 0, 0, E, 0, 1, 0, 262144, 8)
+    idx, wt = _route_gpu(bec, ctx, 0, torch.from_numpy(x).cuda(), torch.from_numpy(Wr).cuda(), None, k)
+    ridx, rw, _ = oracle.route(x.astype(np.float64), Wr, None, k)
+    assert np.array_equal(idx, ridx)
+    assert idx[5].tolist() == [0, 1, 2, 3]
+    assert np.allclose(wt, rw, rtol=1e-5, atol=1e-7)
+    assert ctx.stats()["uncertified_repairs"] >= 1
+    ctx.close()
+
+
+def test_plan_matches_oracle(bec):
+    rng = np.random.default_rng(7)
+    for (T, E, k) in ((1, 256, 8), (4, 256, 8), (8, 16, 2), (64, 128, 8), (37, 1024, 16)):
+        idx = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+        wts = rng.random((T, k)).astype(np.float32)
+        ctx = bec.Context(1, E, k, 256, 128, 0, 0, min(E, 8), 0, 1, 0, 262144, T)
+        plan = bec.Plan(E, k, T)
+        ctx.plan_union(torch.from_numpy(idx).cuda(), torch.from_numpy(wts).cuda(), T, plan)
+        torch.cuda.synchronize()
+        ref = oracle.plan_union(idx, wts.astype(np.float64), E)
+        nu = int(plan.n_uniq.item())
+        assert nu == len(ref["uniq"])
+        assert plan.uniq[:nu].cpu().numpy().tolist() == ref["uniq"].tolist()
+        for key in ("counts", "offsets"):
+            assert np.array_equal(getattr(plan, key).cpu().numpy(), ref[key]), key
+        A = T * k
+        for key in ("perm_tok", "perm_rank", "inv"):
+            assert np.array_equal(getattr(plan, key)[:A].cpu().numpy(), ref[key]), key
+        assert np.array_equal(plan.perm_w[:A].cpu().numpy(), ref["perm_w"].astype(np.float32))
+        ctx.close()
+
+
+def _run_trace(bec, w, layers, steps, ffn_steps, policy=None, seed=0, tile_bytes=262144,
+               slots=None, preload=False, check_every_step=True):
+    """Run layer_forward for every (step, layer) on the GPU and replay the
+    same trace in the oracle; compare bit-exact state each step and outputs on
+    ffn_steps. Returns the GPU outputs {(layer, step): y}."""
+    T = w.tokens_per_step
+    store = pinned_store(w, layers)
+    pol = w.policy if policy is None else policy
+    S = slots or w.slots
+    ctx = make_context(bec, w, layers, policy=pol, slots=S, seed=seed, tile_bytes=tile_bytes)
+    keep = bind_all(ctx, w, layers, store)
+    experts = ExpertCache(w)
+    plan = bec.Plan(w.n_experts, w.top_k, T)
+    idx_t = torch.empty((T, w.top_k), dtype=torch.int32, device="cuda")
+    wt_t = torch.empty((T, w.top_k), dtype=torch.float32, device="cuda")
+    y_t = torch.empty((T, w.hidden), dtype=torch.float32, device="cuda")
+    outs = {}
+    for l in range(layers):
+        Wr = W.router_weights(w, l)
+        bias = W.router_bias(w, l)
+        Wr_t = torch.from_numpy(Wr).cuda()
+        b_t = None if bias is None else torch.from_numpy(bias).cuda()
+        x = W.activations(w, l, steps * T)
+        cache = SlotCache(w.n_experts, S, pol, seed=seed, layer=l, payload_bytes=w.payload_bytes)
+        if preload:
+            ctx.preload(l, list(range(w.n_experts)))
+            cache.preload(range(w.n_experts))
+        shared = experts.get(l, w.n_experts) if w.shared_inter else None
+        for s in range(steps):
+            xs = x[s * T:(s + 1) * T]
+            ctx.layer_forward(l, x_to_torch(w, xs), Wr_t, b_t, idx_t, wt_t, plan, y_t)
+            ctx.check_device_errors()
+            y = y_t.cpu().numpy().copy()
+            outs[(l, s)] = y
+            x64 = x_to_f64(w, xs)
+            ridx, rw, _ = oracle.route(x64, Wr, bias, w.top_k)
+            rplan = oracle.plan_union(ridx, rw, w.n_experts)
+            rec = cache.step(rplan["uniq"], rplan["counts"])
+            assert np.array_equal(idx_t.cpu().numpy(), ridx), (l, s)
+            if check_every_step or s == steps - 1:
+                pt, gen = ctx.read_page_table(l)
+                assert pt == rec["pt"], (l, s)
+                assert gen == rec["gen"], (l, s)
+            if s in ffn_steps:
+                ref = oracle.moe_layer(x64, ridx, rw, lambda e: experts.get(l, e), shared)
+                ok, rel, mx = tolerance_ok(y, ref)
+                assert ok, (l, s, rel, mx)
+                assert rel < 1e-4, (l, s, rel)  # fp32 path: far inside the bar
+        st = ctx.stats(l)
+        rs = cache.stats()
+        for key in ("hits", "misses", "evictions", "materialized_bytes"):
+            assert st[key] == rs[key], (l, key, st[key], rs[key])
+    ctx.close()
+    del keep
+    return outs
+
+
+def test_layer_tiny_trace(bec):
+    w = W.with_changes(W.WORKLOADS["tiny"], n_steps=16)
+    _run_trace(bec, w, 1, 16, set(range(16)))
+
+
+def test_layer_decode_full_size(bec):
+    w = W.WORKLOADS["decode"]
+    _run_trace(bec, w, 2, 24, {0, 5, 23})
+
+
+@pytest.mark.parametrize("policy,seed", [(0, 0), (1, 0), (1, 3)])
+def test_layer_mtp_decode_q4(bec, policy, seed):
+    w = W.with_changes(W.WORKLOADS["mtp_decode"], slots=40)  # >= T*k, small enough to evict
+    _run_trace(bec, w, 1, 14, {0, 13}, policy=policy, seed=seed)
+
+
+def test_cache_transparency_bitwise(bec):
+    # outputs must not depend on cache state, eviction policy or tile size
+    w = W.with_changes(W.WORKLOADS["decode"], n_layers=1)
+    a = _run_trace(bec, w, 1, 8, set(), policy=0, check_every_step=False)
+    b = _run_trace(bec, w, 1, 8, set(), policy=1, seed=4, check_every_step=False)
+    c = _run_trace(bec, w, 1, 8, set(), slots=w.n_experts, preload=True, tile_bytes=4096,
+                   check_every_step=False)
+    for key in a:
+        assert np.array_equal(a[key], b[key]) and np.array_equal(a[key], c[key]), key
+
+
+def test_staged_slot_bytes_equal_store(bec):
+    w = W.with_changes(W.WORKLOADS["decode"], n_layers=1)
+    store = pinned_store(w, 1)
+    for tile in (262144, 4096, 1000 * 16):
+        ctx = make_context(bec, w, 1, tile_bytes=tile)
+        bind_all(ctx, w, 1, store)
+        plan = bec.Plan(w.n_experts, w.top_k, 1)
+        idx = torch.tensor([[3, 9, 17, 100, 200, 255, 0, 1]], dtype=torch.int32, device="cuda")
+        wt = torch.full((1, 8), 0.125, device="cuda")
+        ctx.plan_union(idx, wt, 1, plan)
+        ml = ctx.cache_admit(0, plan)
+        ctx.stage_tiles(0, ml)
+        torch.cuda.synchronize()
+        tiles = oracle.tile_partition(w.hidden, w.inter, w.quant, tile)
+        assert ctx.stats(0)["tiles_staged"] == 8 * len(tiles)
+        assert ctx.stats(0)["bytes_staged"] == 8 * w.payload_bytes
+        for e, s in zip(ml.expert, ml.slot):
+            got = np.frombuffer(ctx.read_slot(0, s), dtype=np.uint8)
+            assert np.array_equal(got, store[0, e].numpy()), (tile, e)
+        ctx.close()
+
+
+def test_fail_closed_on_failed_staging_and_stale_generation(bec):
+    w = W.with_changes(W.WORKLOADS["tiny"], n_steps=3)
+    store = pinned_store(w, 1)
+    ctx = make_context(bec, w, 1)
+    bind_all(ctx, w, 1, store)
+    plan = bec.Plan(w.n_experts, w.top_k, 4)
+    x = x_to_torch(w, W.activations(w, 0, 4))
+    Wr = torch.from_numpy(W.router_weights(w, 0)).cuda()
+    idx = torch.empty((4, 2), dtype=torch.int32, device="cuda")
+    wt = torch.empty((4, 2), device="cuda")
+    y = torch.empty((4, w.hidden), device="cuda")
+    ctx.route(0, x, Wr, None, idx, wt)
+    ctx.plan_union(idx, wt, 4, plan)
+    ml = ctx.cache_admit(0, plan)
+    assert ml.n > 1
+    ctx.debug_fail_staging_after(1)
+    with pytest.raises(bec.MoeError):
+        ctx.stage_tiles(0, ml)
+    ctx.expert_ffn(0, x, plan, y)
+    with pytest.raises(bec.MoeError) as ei:
+        ctx.check_device_errors()
+    assert ei.value.status == 4  # MOE_ERR_STALE: unpublished slots were not read
+    ctx.check_device_errors()  # cleared
+    # a good staging publishes the slots; then corrupting one generation fails closed
+    ctx.stage_tiles(0, ml)
+    ctx.expert_ffn(0, x, plan, y)
+    ctx.check_device_errors()
+    ctx.debug_corrupt_generation(0, ml.expert[0])
+    ctx.expert_ffn(0, x, plan, y)
+    with pytest.raises(bec.MoeError) as ei:
+        ctx.check_device_errors()
+    assert ei.value.status == 4
+    ctx.close()
