@@ -1,0 +1,372 @@
+#!/usr/bin/env python
+"""MoE-layer throughput of the bounded-expert-cache layer on one GB300.
+
+A step is one decode step of the "decode" workload: one bf16 token through 40
+routed MoE layers (hidden 2048, 256 experts top-8 + 1 shared, expert
+intermediate 512, Q8_0), each layer running the whole path — router + top-k,
+expert-major union, cache admit (15% of experts per layer, LRU), miss staging
+of 256 KiB tiles from pinned host memory on three streams, fused dequant
+SwiGLU FFN with shared expert and combine. The trace has 128 steps per layer
+(AR(1) inputs, rho = 0.9); warm-up steps continue the same trace, so the
+timed steps run on a warm cache. Every step reads over 1 GB of distinct
+weights, far more than L2.
+
+Prints one JSON line (rank 0). ``--impl reference`` times the CPU oracle
+instead, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+WORKLOAD = "decode"
+METRIC = "MoE-layer tokens/s at 1 GB300; achieved HBM GB/s (decode) & TFLOP/s (prefill)"
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+# ---------------------------------------------------------------- helpers
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def recorded_traffic(kernel_file: str, name: str):
+    """dram bytes per launch from the committed ncu summary, or None if the
+    kernel source changed since the counters were taken."""
+    prof = os.path.join(ROOT, "profiles", f"{name}.md")
+    if not os.path.exists(prof):
+        return None
+    txt = open(prof).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    h = re.search(r"source_sha256:\s*([0-9a-f]{64})", txt)
+    if not m or not h:
+        return None
+    src = open(os.path.join(ROOT, "bounded_expert_cache_gb300", "csrc", kernel_file), "rb").read()
+    if hashlib.sha256(src).hexdigest() != h.group(1):
+        return None
+    return float(m.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.f = tempfile.TemporaryFile(mode="w+")
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        self.proc.wait()
+        self.f.seek(0)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.f:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- CPU oracle
+def oracle_decode_sample(w: W.Workload, budget_s: float, max_layers: int):
+    """Oracle cost of the decode path on a bounded sample: the first step of
+    each layer (cold cache), layer after layer until ``budget_s`` is spent.
+    Returns (seconds per full 40-layer step, layers timed)."""
+    import oracle
+    done, spent = 0, 0.0
+    for l in range(max_layers):
+        Wr = W.router_weights(w, l)
+        x = oracle.bf16_bits_to_f64(W.activations(w, l, w.tokens_per_step))
+        t0 = time.perf_counter()
+        idx, wt, _ = oracle.route(x, Wr, None, w.top_k)
+        plan = oracle.plan_union(idx, wt, w.n_experts)
+        cache = oracle.SlotCache(w.n_experts, w.slots, w.policy, payload_bytes=w.payload_bytes)
+        cache.step(plan["uniq"], plan["counts"])
+        mats = {e: oracle.expert_matrices(W.expert_payload(w, l, e), w.hidden, w.inter, w.quant)
+                for e in plan["uniq"].tolist()}
+        shared = oracle.expert_matrices(W.expert_payload(w, l, w.n_experts), w.hidden,
+                                        w.shared_inter, w.quant)
+        oracle.moe_layer(x, idx, wt, lambda e: mats[e], shared)
+        spent += time.perf_counter() - t0
+        done += 1
+        if spent >= budget_s:
+            break
+    return spent / done * w.n_layers, done
+
+
+# ---------------------------------------------------------------- GPU arm
+def run_ours(args, rank, world, dev):
+    import torch
+    import bounded_expert_cache_gb300 as bec
+
+    w = W.WORKLOADS[WORKLOAD]
+    if args.layers != w.n_layers:
+        w = W.with_changes(w, n_layers=args.layers)  # small profiling case only
+    L, T, E, k, H = w.n_layers, w.tokens_per_step, w.n_experts, w.top_k, w.hidden
+    n_steps = args.warmup + args.steps
+    assert n_steps <= w.n_steps, f"warmup + steps must be <= {w.n_steps} (the trace length)"
+
+    t0 = time.time()
+    store = torch.empty((L, E, w.payload_bytes), dtype=torch.uint8, pin_memory=True)
+    W.fill_store(w, store.numpy())
+    log(f"[bench] store {store.numel() / 2**30:.1f} GiB pinned + filled in {time.time() - t0:.1f}s")
+    shared = [torch.from_numpy(W.expert_payload(w, l, E)).to(dev) for l in range(L)]
+    routers = torch.stack([torch.from_numpy(W.router_weights(w, l)) for l in range(L)]).to(dev)
+    x_host = np.stack([W.activations(w, l, n_steps * T) for l in range(L)])  # [L, steps*T, H] bf16 bits
+    x_pin = torch.from_numpy(x_host.view(np.int16)).view(torch.bfloat16).pin_memory()
+    x_dev = x_pin.to(dev)
+
+    def make_ctx():
+        ctx = bec.Context(L, E, k, H, w.inter, w.shared_inter, w.quant, w.slots, w.policy, 3, 0,
+                          262144, T)
+        ctx.bind_store(store)
+        for l in range(L):
+            ctx.bind_shared(l, shared[l])
+        return ctx
+
+    plan = bec.Plan(E, k, T, dev)
+    idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+    wt = torch.empty((T, k), dtype=torch.float32, device=dev)
+    y = torch.empty((L, T, H), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ctx, s, e2e=None):
+        for l in range(L):
+            xs = x_dev[l, s * T:(s + 1) * T]
+            if e2e is not None:
+                xs = e2e["x"][l]
+                xs.copy_(x_pin[l, s * T:(s + 1) * T], non_blocking=True)
+            ctx.layer_forward(l, xs, routers[l], None, idx, wt, plan, y[l])
+            if e2e is not None:
+                e2e["y"][l].copy_(y[l], non_blocking=True)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+
+    def max_over_ranks(v: float) -> float:
+        if world == 1:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        return float(t.item())
+
+    # ---- device-resident inputs
+    ctx = make_ctx()
+    for s in range(args.warmup):
+        step(ctx, s)
+    ctx.check_device_errors()
+    st0 = ctx.stats()
+    ctx.kernel_times()  # reset
+    ctx.set_kernel_timing(True)
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    clocks.start()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    ev0.record(stream)
+    for s in range(args.warmup, n_steps):
+        step(ctx, s)
+    ev1.record(stream)
+    barrier()
+    elapsed_ms = max_over_ranks(ev0.elapsed_time(ev1))
+    clk = clocks.stop()
+    kt = ctx.kernel_times()
+    ctx.set_kernel_timing(False)
+    ctx.check_device_errors()
+    st1 = ctx.stats()
+    ctx.close()
+
+    tokens = args.steps * T * world
+    value = tokens / (elapsed_ms / 1e3)
+    e2e_value, e2e_ms = None, None
+    if args.skip_e2e:
+        return finish(args, w, world, value, elapsed_ms, None, kt, st0, st1, clk), w
+    # ---- end to end through host buffers (fresh context, same trace)
+    e2e = {"x": torch.empty((L, T, H), dtype=torch.bfloat16, device=dev),
+           "y": torch.empty((L, T, H), dtype=torch.float32).pin_memory()}
+    ctx = make_ctx()
+    for s in range(args.warmup):
+        step(ctx, s, e2e)
+    barrier()
+    ev0.record(stream)
+    for s in range(args.warmup, n_steps):
+        step(ctx, s, e2e)
+    ev1.record(stream)
+    barrier()
+    e2e_ms = max_over_ranks(ev0.elapsed_time(ev1))
+    ctx.check_device_errors()
+    ctx.close()
+    e2e_value = tokens / (e2e_ms / 1e3)
+    return finish(args, w, world, value, elapsed_ms, e2e_value, kt, st0, st1, clk), w
+
+
+def finish(args, w, world, value, elapsed_ms, e2e_value, kt, st0, st1, clk):
+    L, T, E, k, H = w.n_layers, w.tokens_per_step, w.n_experts, w.top_k, w.hidden
+    # roofline of the dominant kernel (ffn gate/up): algorithmic bytes per
+    # launch = (k routed + 1 shared) units x (gate + up) Q8_0 matrices + x + h
+    mat = w.matrix_bytes(w.inter, w.hidden)
+    units = min(k * T, E) + 1
+    gu_bytes = units * 2 * mat + T * H * 2 + units * T * w.inter * 4
+    dn_bytes = units * mat + units * T * w.inter * 4 + T * H * 4
+    gu_ms, gu_n = kt["ffn_gateup"]
+    dn_ms, dn_n = kt["ffn_down"]
+    peak, peak_kind = peaks()
+    gu_gbs = gu_bytes / (gu_ms / gu_n / 1e3) / 1e9 if gu_n else None
+    dn_gbs = dn_bytes / (dn_ms / dn_n / 1e3) / 1e9 if dn_n else None
+    launches = sum(n for _, n in kt.values())
+    dh = st1["hits"] - st0["hits"]
+    dm = st1["misses"] - st0["misses"]
+    staged = st1["bytes_staged"] - st0["bytes_staged"]
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(elapsed_ms / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded: Q8_0 U[-127,127] quants, fp16 scales U[1e-3,2e-2], router "
+                "N(0,0.02), bf16 AR(1) rho=0.9 tokens)",
+        "config": {"workload": "decode: hidden 2048, 256 experts top-8 + 1 shared, inter 512, "
+                               "Q8_0, bf16, 1 token/step x 40 layers, 15% cache (38 slots) LRU",
+                   "tokens_per_step": T, "layers": L, "trace_steps": w.n_steps,
+                   "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (>1 GB of distinct weights per step)"},
+        "roofline": {"bound": "hbm", "kernel": "ffn_gateup (dequant-GEMV gate/up + SwiGLU)",
+                     "achieved": round(gu_gbs, 1) if gu_gbs else None, "peak": peak,
+                     "peak_source": peak_kind, "unit": "GB/s",
+                     "frac": round(gu_gbs / peak, 4) if gu_gbs else None,
+                     "traffic": recorded_traffic("ffn_decode.cu", "ffn_gateup_decode"),
+                     "bytes_per_launch": gu_bytes,
+                     "avg_launch_us": round(gu_ms / gu_n * 1e3, 3) if gu_n else None},
+        "kernels": {kname: {"ms": round(ms, 3), "launches": n,
+                            "avg_us": round(ms / n * 1e3, 3) if n else None}
+                    for kname, (ms, n) in kt.items()},
+        "ffn_down": {"achieved_gbs": round(dn_gbs, 1) if dn_gbs else None,
+                     "frac": round(dn_gbs / peak, 4) if dn_gbs else None, "bytes_per_launch": dn_bytes},
+        "cache": {"hits": dh, "misses": dm,
+                  "hit_rate": round(dh / max(1, dh + dm), 4),
+                  "bytes_staged": staged,
+                  "staging_gbs_avg_over_step": round(staged / (elapsed_ms / 1e3) / 1e9, 2)},
+        "gpu_launches": launches,
+        "clocks": clk,
+        "e2e": None if e2e_value is None else {
+            "value": round(e2e_value, 2), "unit": "tokens/s",
+            "h2d_bytes_per_step": L * T * H * 2, "d2h_bytes_per_step": L * T * H * 4},
+    }
+    return out
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=112)
+    ap.add_argument("--warmup", type=int, default=16)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=15.0,
+                    help="seconds of oracle work for the CPU baseline")
+    ap.add_argument("--layers", type=int, default=40,
+                    help="layers of the decode stack (40; fewer only for small profiling cases)")
+    ap.add_argument("--skip-e2e", action="store_true", help="profiling: skip the host-buffer pass")
+    ap.add_argument("--skip-cpu", action="store_true", help="profiling: skip the oracle baseline")
+    args = ap.parse_args()
+    assert args.warmup >= 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        # the oracle on the host cores: rank 0 only
+        if rank != 0:
+            return
+        w = W.WORKLOADS[WORKLOAD]
+        per_step, layers = [], 0
+        for _ in range(args.warmup):
+            oracle_decode_sample(w, 0.0, 1)
+        for _ in range(args.steps):
+            s, n = oracle_decode_sample(w, args.cpu_budget / max(1, args.steps), w.n_layers)
+            per_step.append(s)
+            layers = n
+        sec = statistics.mean(per_step)
+        value = w.tokens_per_step / sec
+        cores = os.cpu_count()
+        sample = (f"each step: the first decode step of {layers} of 40 layers (oracle route, union, "
+                  f"cache, fp64 FFN), scaled to 40 layers")
+        print(json.dumps({
+            "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(sec * 1e3, 2), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "decode (same as the GPU arm)"},
+            "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": cores,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}))
+        return
+
+    import torch
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    out, w = run_ours(args, rank, world, dev)
+    if rank == 0 and world == 1 and not args.skip_cpu:
+        sec, layers = oracle_decode_sample(w, args.cpu_budget, w.n_layers)
+        out["cpu_baseline"] = {
+            "value": round(w.tokens_per_step / sec, 4), "unit": "tokens/s", "cores": os.cpu_count(),
+            "kind": "oracle",
+            "sample": f"the first decode step of {layers} of 40 layers (oracle route, union, cache, "
+                      f"fp64 FFN), scaled to 40 layers"}
+    if rank == 0:
+        print(json.dumps(out))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

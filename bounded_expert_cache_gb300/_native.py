@@ -19,6 +19,7 @@ Q8_0, Q4_0 = 0, 1
 LRU, RANDOM = 0, 1
 F32, BF16 = 0, 1
 MODE_AUTO, MODE_DECODE, MODE_PREFILL = 0, 1, 2
+KERNEL_KINDS = ("route", "plan", "ffn_gateup", "ffn_down")
 
 
 class Config(C.Structure):
@@ -84,6 +85,8 @@ SIGNATURES = [
     ("moe_get_stats", _st, [_vp, _i32, C.POINTER(Stats)]),
     ("moe_read_page_table", _st, [_vp, _i32, C.POINTER(_i32), C.POINTER(C.c_uint32)]),
     ("moe_read_slot", _st, [_vp, _i32, _i32, _vp, _sz]),
+    ("moe_set_kernel_timing", _st, [_vp, _i32]),
+    ("moe_get_kernel_times", _st, [_vp, C.POINTER(C.c_double), C.POINTER(_i64)]),
     ("moe_debug_fail_staging_after", _st, [_vp, _i32]),
     ("moe_debug_corrupt_generation", _st, [_vp, _i32, _i32]),
     ("moe_slots_create", _st, [_i32, _i32, _i32, _u64, _i32, _i64, C.POINTER(_vp)]),

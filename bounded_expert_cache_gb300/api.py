@@ -183,6 +183,16 @@ class Context:
         self._ck(lib.moe_read_slot(self.h, layer, slot, buf, n))
         return bytes(buf)
 
+    def set_kernel_timing(self, enable: bool):
+        self._ck(lib.moe_set_kernel_timing(self.h, 1 if enable else 0))
+
+    def kernel_times(self) -> dict:
+        """{kind: (total_ms, launches)} since the last call; synchronises."""
+        ms = (C.c_double * 4)()
+        n = (C.c_int64 * 4)()
+        self._ck(lib.moe_get_kernel_times(self.h, ms, n))
+        return {k: (ms[i], n[i]) for i, k in enumerate(N.KERNEL_KINDS)}
+
     def debug_fail_staging_after(self, n_tiles: int):
         self._ck(lib.moe_debug_fail_staging_after(self.h, n_tiles))
 

@@ -45,6 +45,34 @@ bool valid_layer(const moe_ctx_t* ctx, int32_t layer) {
 
 int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
 
+cudaEvent_t timing_event(moe_ctx_t* ctx) {
+  if (!ctx->ev_pool.empty()) {
+    cudaEvent_t e = ctx->ev_pool.back();
+    ctx->ev_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+// Fold finished timed launches into the per-kind totals and recycle events.
+cudaError_t resolve_timing(moe_ctx_t* ctx) {
+  for (auto& r : ctx->timed) {
+    cudaError_t e = cudaEventSynchronize(r.b);
+    if (e != cudaSuccess) return e;
+    float ms = 0.f;
+    e = cudaEventElapsedTime(&ms, r.a, r.b);
+    if (e != cudaSuccess) return e;
+    ctx->kt_ms[r.kind] += ms;
+    ctx->kt_n[r.kind] += 1;
+    ctx->ev_pool.push_back(r.a);
+    ctx->ev_pool.push_back(r.b);
+  }
+  ctx->timed.clear();
+  return cudaSuccess;
+}
+
 }  // namespace
 
 namespace moe {
@@ -84,6 +112,11 @@ extern "C" void moe_destroy(moe_ctx_t* ctx) {
   for (auto s : ctx->slots) moe_slots_destroy(s);
   for (auto e : ctx->ev_stage)
     if (e) cudaEventDestroy(e);
+  for (auto& r : ctx->timed) {
+    cudaEventDestroy(r.a);
+    cudaEventDestroy(r.b);
+  }
+  for (auto e : ctx->ev_pool) cudaEventDestroy(e);
   if (ctx->ev_compute) cudaEventDestroy(ctx->ev_compute);
   for (auto s : ctx->streams)
     if (s) cudaStreamDestroy(s);
@@ -264,7 +297,15 @@ static moe_status_t route_impl(moe_ctx_t* ctx, int32_t layer, const void* x, int
   a.repairs = ctx->d_repairs + layer;
   a.err = ctx->d_err;
   if (plan) a.plan = *plan;
-  CK(moe::launch_route(a, ctx->num_sms, st));
+  if (ctx->timing) {
+    moe_ctx::TimedLaunch r{MOE_KT_ROUTE, timing_event(ctx), timing_event(ctx)};
+    CK(cudaEventRecord(r.a, st));
+    CK(moe::launch_route(a, ctx->num_sms, st));
+    CK(cudaEventRecord(r.b, st));
+    ctx->timed.push_back(r);
+  } else {
+    CK(moe::launch_route(a, ctx->num_sms, st));
+  }
   return MOE_OK;
 }
 
@@ -295,7 +336,16 @@ extern "C" moe_status_t moe_plan_union(moe_ctx_t* ctx, const int32_t* topk_idx, 
   a.E = ctx->cfg.n_experts;
   a.plan = *plan;
   a.err = ctx->d_err;
-  CK(moe::launch_plan(a, reinterpret_cast<cudaStream_t>(stream)));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (ctx->timing) {
+    moe_ctx::TimedLaunch r{MOE_KT_PLAN, timing_event(ctx), timing_event(ctx)};
+    CK(cudaEventRecord(r.a, st));
+    CK(moe::launch_plan(a, st));
+    CK(cudaEventRecord(r.b, st));
+    ctx->timed.push_back(r);
+  } else {
+    CK(moe::launch_plan(a, st));
+  }
   return MOE_OK;
 }
 
@@ -482,7 +532,15 @@ extern "C" moe_status_t moe_expert_ffn(moe_ctx_t* ctx, int32_t layer, const void
   a.ldh = ctx->ldh;
   a.y = y;
   a.err = ctx->d_err;
+  if (ctx->timing) {
+    for (int i = 0; i < 4; ++i) a.ev[i] = timing_event(ctx);
+  }
   CK(moe::launch_ffn_decode(a, ctx->num_sms, reinterpret_cast<cudaStream_t>(stream)));
+  if (ctx->timing) {
+    ctx->timed.push_back({MOE_KT_GATEUP, a.ev[0], a.ev[1]});
+    ctx->timed.push_back({MOE_KT_DOWN, a.ev[2], a.ev[3]});
+    if (ctx->timed.size() > 16384) CK(resolve_timing(ctx));
+  }
   return MOE_OK;
 }
 
@@ -587,5 +645,23 @@ extern "C" moe_status_t moe_debug_corrupt_generation(moe_ctx_t* ctx, int32_t lay
   const size_t off = static_cast<size_t>(layer) * ctx->cfg.n_experts + expert;
   ctx->h_ptgen[off] += 0x10000u;
   CK(cudaMemcpy(ctx->d_ptgen + off, ctx->h_ptgen + off, sizeof(uint32_t), cudaMemcpyHostToDevice));
+  return MOE_OK;
+}
+
+extern "C" moe_status_t moe_set_kernel_timing(moe_ctx_t* ctx, int32_t enable) {
+  if (!ctx) return MOE_ERR_ARG;
+  ctx->timing = enable != 0;
+  return MOE_OK;
+}
+
+extern "C" moe_status_t moe_get_kernel_times(moe_ctx_t* ctx, double* ms, int64_t* launches) {
+  if (!ctx) return MOE_ERR_ARG;
+  CK(resolve_timing(ctx));
+  for (int k = 0; k < MOE_KT_COUNT; ++k) {
+    if (ms) ms[k] = ctx->kt_ms[k];
+    if (launches) launches[k] = ctx->kt_n[k];
+    ctx->kt_ms[k] = 0.0;
+    ctx->kt_n[k] = 0;
+  }
   return MOE_OK;
 }

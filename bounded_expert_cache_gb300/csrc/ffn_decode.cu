@@ -426,14 +426,18 @@ cudaError_t launch_tm(const FfnArgs& a, int num_sms, cudaStream_t st) {
   if (err != cudaSuccess) return err;
   const int items1 = max_units * (std::max(a.I, a.Is) / kRowsPerItem);
   const int grid1 = std::max(1, std::min((items1 + kWarps - 1) / kWarps, num_sms * 2));
+  if (a.ev[0]) cudaEventRecord(a.ev[0], st);
   if (a.xt == MOE_BF16)
     gateup_kernel<Q, TM, MOE_BF16><<<grid1, kThreads, smem1, st>>>(a);
   else
     gateup_kernel<Q, TM, MOE_F32><<<grid1, kThreads, smem1, st>>>(a);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
+  if (a.ev[1]) cudaEventRecord(a.ev[1], st);
   const int grid2 = (a.H + kDownRows - 1) / kDownRows;
+  if (a.ev[2]) cudaEventRecord(a.ev[2], st);
   down_kernel<Q, TM><<<grid2, kThreads, smem2, st>>>(a);
+  if (a.ev[3]) cudaEventRecord(a.ev[3], st);
   return cudaGetLastError();
 }
 

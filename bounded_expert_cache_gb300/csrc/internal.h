@@ -88,6 +88,7 @@ struct FfnArgs {
   int32_t ldh;
   float* y;                   // [T][H]
   uint32_t* err;
+  cudaEvent_t ev[4];          // optional timing events around gate/up and down
 };
 cudaError_t launch_ffn_decode(const FfnArgs& a, int num_sms, cudaStream_t st);
 
@@ -124,6 +125,16 @@ struct moe_ctx {
   std::vector<cudaEvent_t> ev_stage;
   cudaEvent_t ev_compute = nullptr;
   int32_t fail_after_tiles = -1;
+  // kernel timing
+  struct TimedLaunch {
+    int kind;
+    cudaEvent_t a, b;
+  };
+  bool timing = false;
+  std::vector<TimedLaunch> timed;
+  std::vector<cudaEvent_t> ev_pool;
+  double kt_ms[MOE_KT_COUNT] = {0, 0, 0, 0};
+  int64_t kt_n[MOE_KT_COUNT] = {0, 0, 0, 0};
   std::vector<int64_t> tiles_staged, bytes_staged;
   std::string err;
 };

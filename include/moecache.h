@@ -247,6 +247,22 @@ moe_status_t moe_read_page_table(moe_ctx_t* ctx, int32_t layer, int32_t* host_pt
 moe_status_t moe_read_slot(moe_ctx_t* ctx, int32_t layer, int32_t slot, void* host_out,
                            size_t bytes);
 
+/* Kernel timing (tracing aid). While enabled, the context records CUDA
+ * events on the launching stream around every kernel it launches.
+ * moe_get_kernel_times synchronises those events and returns, per kind
+ * (route incl. fused plan, standalone plan, FFN gate/up, FFN down), the
+ * summed device milliseconds and the launch count since the last call, then
+ * resets them. Either output may be NULL. */
+typedef enum {
+  MOE_KT_ROUTE = 0,
+  MOE_KT_PLAN = 1,
+  MOE_KT_GATEUP = 2,
+  MOE_KT_DOWN = 3,
+  MOE_KT_COUNT = 4
+} moe_kernel_kind_t;
+moe_status_t moe_set_kernel_timing(moe_ctx_t* ctx, int32_t enable);
+moe_status_t moe_get_kernel_times(moe_ctx_t* ctx, double* ms, int64_t* launches);
+
 /* Test hooks for fail-closed paths, all on the host side: make the next
  * moe_stage_tiles fail after `fail_after_tiles` tiles (-1 = off), or set a
  * layer's device page-table generation for an expert to a wrong value. */

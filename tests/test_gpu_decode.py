@@ -218,7 +218,7 @@ def test_fail_closed_on_failed_staging_and_stale_generation(bec):
     ctx.route(0, x, Wr, None, idx, wt)
     ctx.plan_union(idx, wt, 4, plan)
     ml = ctx.cache_admit(0, plan)
-    assert ml.n > 1
+    assert ml.misses > 1
     ctx.debug_fail_staging_after(1)
     with pytest.raises(bec.MoeError):
         ctx.stage_tiles(0, ml)
