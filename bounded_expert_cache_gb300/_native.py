@@ -73,6 +73,7 @@ SIGNATURES = [
     ("moe_bind_store", _st, [_vp, _vp, _sz]),
     ("moe_bind_shared", _st, [_vp, _i32, _vp]),
     ("moe_route", _st, [_vp, _i32, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp]),
+    ("moe_route_noalloc", _st, [_vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp]),
     ("moe_plan_union", _st, [_vp, _vp, _vp, _i32, C.POINTER(PlanT), _vp]),
     ("moe_cache_admit", _st, [_vp, _i32, C.POINTER(PlanT), C.POINTER(MissList), _vp]),
     ("moe_cache_evict", _st, [_vp, _i32, _i32]),

@@ -77,6 +77,8 @@ cudaError_t resolve_timing(moe_ctx_t* ctx) {
 
 namespace moe {
 
+void set_thread_error(const std::string& msg) { g_create_err = msg; }
+
 ExpertGeom expert_geom(int32_t H, int32_t I, int32_t quant) {
   ExpertGeom g;
   g.H = H;

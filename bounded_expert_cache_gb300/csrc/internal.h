@@ -71,6 +71,9 @@ struct PlanArgs {
 };
 cudaError_t launch_plan(const PlanArgs& a, cudaStream_t st);
 
+// Message returned by moe_last_error(NULL) on this thread.
+void set_thread_error(const std::string& msg);
+
 // Arguments of the decode FFN launches.
 struct FfnArgs {
   const void* x;

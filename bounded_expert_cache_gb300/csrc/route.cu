@@ -24,6 +24,8 @@
 // stable (token-ascending) scatter of the assignments.
 #include <cfloat>
 #include <climits>
+#include <mutex>
+#include <string>
 
 #include "internal.h"
 
@@ -552,3 +554,108 @@ cudaError_t launch_plan(const PlanArgs& a, cudaStream_t st) {
 }
 
 }  // namespace moe
+
+// ------------------------------------------------------------ no-allocation router
+// A standalone router entry point for callers that cannot allocate device
+// memory: code running inside another framework's memory pool or arena, hosts
+// that forbid cudaMalloc after start-up, or pipelines being captured into a
+// CUDA graph where an allocation would break the capture. Its scratch (fast
+// logits, their bounds, the last-block counter, the repair counter and an
+// error word) lives in one file-scope device array below, sized for at most
+// kNoAllocMaxTE = 16384 (token, expert) logits (256 KiB of logits and bounds);
+// every GPU that loads this library holds that array until the process exits.
+namespace moe {
+namespace {
+
+constexpr int kNoAllocMaxTE = 16384;
+constexpr int kNoAllocMaxDevices = 64;
+
+// [0, TE) fast logits, [TE, 2 TE) bounds, then a 32-byte header:
+// ticket (u32), error word (u32), repaired-token counter (u64).
+static __device__ __align__(256) double g_route_scratch[2 * kNoAllocMaxTE + 4];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+
+}  // namespace
+}  // namespace moe
+
+extern "C" moe_status_t moe_route_noalloc(const void* x, int32_t xt, int32_t T, int32_t H,
+                                          int32_t E, int32_t k, const float* w_router,
+                                          const float* bias, int32_t* topk_idx, float* topk_w,
+                                          moe_stream_t stream) {
+  using namespace moe;
+  if (!x || !w_router || !topk_idx || !topk_w) {
+    set_thread_error("moe_route_noalloc: null pointer");
+    return MOE_ERR_ARG;
+  }
+  if (xt != MOE_F32 && xt != MOE_BF16) {
+    set_thread_error("moe_route_noalloc: activation dtype must be MOE_F32 or MOE_BF16");
+    return MOE_ERR_ARG;
+  }
+  if (T < 1 || T > kRouteMaxT || H < 1 || E < 1 || E > 1024 || k < 1 || k > 16 || k > E) {
+    set_thread_error("moe_route_noalloc: need 1 <= T <= 64, H >= 1, 1 <= E <= 1024, "
+                     "1 <= k <= min(16, E)");
+    return MOE_ERR_ARG;
+  }
+  if (static_cast<int64_t>(T) * E > kNoAllocMaxTE) {
+    set_thread_error("moe_route_noalloc: T*E = " + std::to_string(static_cast<int64_t>(T) * E) +
+                     " exceeds the static scratch limit of " + std::to_string(kNoAllocMaxTE) +
+                     " logits");
+    return MOE_ERR_ARG;
+  }
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) {
+    set_thread_error(std::string("moe_route_noalloc: cudaGetDevice: ") + cudaGetErrorString(e));
+    return MOE_ERR_CUDA;
+  }
+  void* base = nullptr;
+  {
+    // once per device, with that device current: the host-side name of a
+    // __device__ array is not a device address; ask the runtime for it
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+      e = cudaGetSymbolAddress(&g_noalloc_ptr[dev], g_route_scratch);
+      if (e != cudaSuccess) {
+        g_noalloc_ptr[dev] = nullptr;
+        set_thread_error(std::string("moe_route_noalloc: cudaGetSymbolAddress: ") +
+                         cudaGetErrorString(e));
+        return MOE_ERR_CUDA;
+      }
+    }
+    base = g_noalloc_ptr[dev];
+  }
+  double* scratch = static_cast<double*>(base);
+  const size_t te = static_cast<size_t>(T) * E;
+  unsigned char* header = reinterpret_cast<unsigned char*>(scratch + 2 * kNoAllocMaxTE);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // the counter and flags must start at zero; the array keeps the last call's contents
+  e = cudaMemsetAsync(header, 0, 32, st);
+  if (e != cudaSuccess) {
+    set_thread_error(std::string("moe_route_noalloc: cudaMemsetAsync: ") + cudaGetErrorString(e));
+    return MOE_ERR_CUDA;
+  }
+  RouteArgs a{};
+  a.x = x;
+  a.xt = xt;
+  a.T = T;
+  a.H = H;
+  a.E = E;
+  a.k = k;
+  a.w = w_router;
+  a.bias = bias;
+  a.topk_idx = topk_idx;
+  a.topk_w = topk_w;
+  a.l_est = scratch;
+  a.l_bnd = scratch + te;
+  a.ticket = reinterpret_cast<unsigned int*>(header);
+  a.err = reinterpret_cast<uint32_t*>(header + 4);
+  a.repairs = reinterpret_cast<unsigned long long*>(header + 8);
+  e = launch_route(a, 0, st);
+  if (e != cudaSuccess) {
+    set_thread_error(std::string("moe_route_noalloc: launch: ") + cudaGetErrorString(e));
+    return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}

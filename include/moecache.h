@@ -171,6 +171,31 @@ moe_status_t moe_route(moe_ctx_t* ctx, int32_t layer, const void* x, int32_t xt,
                        const float* w_router, const float* bias, int32_t* topk_idx,
                        float* topk_w, moe_stream_t stream);
 
+/* Router + top-k that allocates nothing, for callers that cannot call
+ * cudaMalloc: code running inside another framework's memory pool or arena,
+ * services that forbid device allocation after start-up, or work being
+ * captured into a CUDA graph, where an allocation would break the capture.
+ * None of the pages has a counterpart to this call; it exists for such
+ * embedders. It needs no context: the caller passes x (device [T,H],
+ * MOE_F32 or MOE_BF16), w_router (device fp32 [E,H]), bias (device fp32 [E]
+ * or NULL) and the outputs topk_idx (int32 [T,k]) and topk_w (fp32 [T,k]);
+ * the selection and weights are those of moe_route.
+ * Scratch: one static device array inside the library, sized for
+ * T*E <= 16384 logits (about 256 KiB), which every GPU that loads the library
+ * holds until the process exits. Limits: 1 <= T <= 64, 1 <= E <= 1024,
+ * 1 <= k <= min(16, E), T*E <= 16384; anything larger returns MOE_ERR_ARG
+ * with a message in moe_last_error(NULL) and launches nothing.
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture. No call allocates (no cudaMalloc, cudaFree or allocating library
+ * routine). Every call shares the one array: it clears its counters on the
+ * stream before the launch, and calls whose kernels overlap on the GPU (on
+ * different streams, or from several threads) race on it — serialise them.
+ * Device-side flags (non-finite inputs) are not reported by this call. */
+moe_status_t moe_route_noalloc(const void* x, int32_t xt, int32_t T, int32_t H, int32_t E,
+                               int32_t k, const float* w_router, const float* bias,
+                               int32_t* topk_idx, float* topk_w, moe_stream_t stream);
+
 /* Expert-major union and permutation of a routed step ([NfE] §5.3, §5.5).
  * topk_idx/topk_w: device [T,k]. Fills every array of *plan (device).
  * Errors: MOE_ERR_ARG if plan->capacity < T*k. */
