@@ -163,9 +163,9 @@ def run_ours(args, rank, world, dev):
     x_pin = torch.from_numpy(x_host.view(np.int16)).view(torch.bfloat16).pin_memory()
     x_dev = x_pin.to(dev)
 
-    def make_ctx():
+    def make_ctx(device_admit=True):
         ctx = bec.Context(L, E, k, H, w.inter, w.shared_inter, w.quant, w.slots, w.policy, 3, 0,
-                          262144, T)
+                          262144, T, admit_on_device=device_admit)
         ctx.bind_store(store)
         for l in range(L):
             ctx.bind_shared(l, shared[l])
@@ -199,7 +199,54 @@ def run_ours(args, rank, world, dev):
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         return float(t.item())
 
-    # ---- device-resident inputs
+    def timed(fn):
+        """Run fn(s) for the timed steps between CUDA events; max over ranks."""
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        ev0.record(stream)
+        for s in range(args.warmup, n_steps):
+            fn(s)
+        ev1.record(stream)
+        barrier()
+        return max_over_ranks(ev0.elapsed_time(ev1))
+
+    # ---- pass 1 (headline): device-resident inputs, on-device admission, the
+    # 40-layer step replayed as one CUDA graph
+    ctx = make_ctx()
+    x_step = torch.empty((L, T, H), dtype=torch.bfloat16, device=dev)
+    graph = None
+    if args.no_graph:
+        for s in range(args.warmup):
+            step(ctx, s)
+    else:
+        for s in range(args.warmup - 1):
+            step(ctx, s)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for l in range(L):
+                ctx.layer_forward(l, x_step[l], routers[l], None, idx, wt, plan, y[l])
+
+    def graph_step(s):
+        x_step.copy_(x_dev[:, s * T:(s + 1) * T], non_blocking=True)
+        graph.replay()
+
+    if graph is not None:
+        graph_step(args.warmup - 1)  # the last warm-up step; its replay uploads the graph
+    torch.cuda.synchronize(dev)
+    ctx.check_device_errors()
+
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    clocks.start()
+    elapsed_ms = timed(graph_step if graph is not None else (lambda s: step(ctx, s)))
+    clk = clocks.stop()
+    ctx.check_device_errors()
+    st_graph = ctx.stats()
+    used_graph = graph is not None
+    del graph
+    ctx.close()
+
+    # ---- pass 2: the same steps, launched call by call with library-side
+    # CUDA events around every kernel (roofline and kernel breakdown)
     ctx = make_ctx()
     for s in range(args.warmup):
         step(ctx, s)
@@ -207,48 +254,59 @@ def run_ours(args, rank, world, dev):
     st0 = ctx.stats()
     ctx.kernel_times()  # reset
     ctx.set_kernel_timing(True)
-    clocks = ClockSampler(dev.index if dev.index is not None else 0)
-    clocks.start()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier()
-    ev0.record(stream)
-    for s in range(args.warmup, n_steps):
-        step(ctx, s)
-    ev1.record(stream)
-    barrier()
-    elapsed_ms = max_over_ranks(ev0.elapsed_time(ev1))
-    clk = clocks.stop()
+    events_ms = timed(lambda s: step(ctx, s))
     kt = ctx.kernel_times()
     ctx.set_kernel_timing(False)
     ctx.check_device_errors()
     st1 = ctx.stats()
     ctx.close()
+    assert st1["misses"] - st0["misses"] == st_graph["misses"] - st0["misses"], "graph pass diverged"
 
     tokens = args.steps * T * world
     value = tokens / (elapsed_ms / 1e3)
-    e2e_value, e2e_ms = None, None
+    extra = {"h2d_copy_engine_gbs": h2d_bandwidth(torch, dev),
+             "per_call_launch_tokens_per_s": round(tokens / (events_ms / 1e3), 2),
+             "graph": used_graph}
+    if not args.skip_e2e:
+        # pass 3: admission and staging on the host (one sync per layer)
+        ctx = make_ctx(device_admit=False)
+        for s in range(args.warmup):
+            step(ctx, s)
+        host_ms = timed(lambda s: step(ctx, s))
+        ctx.close()
+        extra["host_admission_tokens_per_s"] = round(tokens / (host_ms / 1e3), 2)
     if args.skip_e2e:
-        return finish(args, w, world, value, elapsed_ms, None, kt, st0, st1, clk), w
-    # ---- end to end through host buffers (fresh context, same trace)
+        return finish(args, w, world, value, elapsed_ms, None, kt, st0, st1, clk, extra), w
+    # ---- pass 4: end to end through host buffers, call by call
     e2e = {"x": torch.empty((L, T, H), dtype=torch.bfloat16, device=dev),
            "y": torch.empty((L, T, H), dtype=torch.float32).pin_memory()}
     ctx = make_ctx()
     for s in range(args.warmup):
         step(ctx, s, e2e)
-    barrier()
-    ev0.record(stream)
-    for s in range(args.warmup, n_steps):
-        step(ctx, s, e2e)
-    ev1.record(stream)
-    barrier()
-    e2e_ms = max_over_ranks(ev0.elapsed_time(ev1))
+    e2e_ms = timed(lambda s: step(ctx, s, e2e))
     ctx.check_device_errors()
     ctx.close()
     e2e_value = tokens / (e2e_ms / 1e3)
-    return finish(args, w, world, value, elapsed_ms, e2e_value, kt, st0, st1, clk), w
+    return finish(args, w, world, value, elapsed_ms, e2e_value, kt, st0, st1, clk, extra), w
 
 
-def finish(args, w, world, value, elapsed_ms, e2e_value, kt, st0, st1, clk):
+def h2d_bandwidth(torch, dev):
+    """Copy-engine bandwidth of a 1 GiB pinned host -> device copy (best of 3)."""
+    src = torch.empty(1 << 30, dtype=torch.uint8).pin_memory()
+    dst = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
+    best = 0.0
+    for _ in range(3):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        dst.copy_(src, non_blocking=True)
+        b.record()
+        b.synchronize()
+        best = max(best, (1 << 30) / (a.elapsed_time(b) / 1e3) / 1e9)
+    del src, dst
+    return round(best, 1)
+
+
+def finish(args, w, world, value, elapsed_ms, e2e_value, kt, st0, st1, clk, extra):
     L, T, E, k, H = w.n_layers, w.tokens_per_step, w.n_experts, w.top_k, w.hidden
     # roofline of the dominant kernel (ffn gate/up): algorithmic bytes per
     # launch = (k routed + 1 shared) units x (gate + up) Q8_0 matrices + x + h
@@ -291,8 +349,13 @@ def finish(args, w, world, value, elapsed_ms, e2e_value, kt, st0, st1, clk):
         "cache": {"hits": dh, "misses": dm,
                   "hit_rate": round(dh / max(1, dh + dm), 4),
                   "bytes_staged": staged,
-                  "staging_gbs_avg_over_step": round(staged / (elapsed_ms / 1e3) / 1e9, 2)},
+                  "staging_gbs_avg_over_step": round(staged / (elapsed_ms / 1e3) / 1e9, 2),
+                  "stage_copy_kernel_gbs": round(staged / (kt["stage_copy"][0] / 1e3) / 1e9, 1)
+                  if kt["stage_copy"][0] else None,
+                  "admission": "on device (router's last block), staging kernel over the host link"},
+        **extra,
         "gpu_launches": launches,
+        "uncertified_repairs": st1["uncertified_repairs"] - st0["uncertified_repairs"],
         "clocks": clk,
         "e2e": None if e2e_value is None else {
             "value": round(e2e_value, 2), "unit": "tokens/s",
@@ -313,6 +376,7 @@ def main():
                     help="layers of the decode stack (40; fewer only for small profiling cases)")
     ap.add_argument("--skip-e2e", action="store_true", help="profiling: skip the host-buffer pass")
     ap.add_argument("--skip-cpu", action="store_true", help="profiling: skip the oracle baseline")
+    ap.add_argument("--no-graph", action="store_true", help="launch the headline pass call by call")
     args = ap.parse_args()
     assert args.warmup >= 3
 

@@ -86,10 +86,10 @@ class Context:
 
     def __init__(self, n_layers, n_experts, top_k, hidden, inter, shared_inter=0, quant=N.Q8_0,
                  slots_per_layer=None, policy=N.LRU, n_streams=3, seed=0, tile_bytes=262144,
-                 max_tokens=8):
+                 max_tokens=8, admit_on_device=False):
         self.cfg = N.Config(n_layers, n_experts, top_k, hidden, inter, shared_inter, quant,
                             slots_per_layer or n_experts, policy, n_streams, seed, tile_bytes,
-                            max_tokens)
+                            max_tokens, 1 if admit_on_device else 0)
         h = C.c_void_p()
         _check(lib.moe_create(C.byref(self.cfg), C.byref(h)), None)
         self.h = h
@@ -188,8 +188,8 @@ class Context:
 
     def kernel_times(self) -> dict:
         """{kind: (total_ms, launches)} since the last call; synchronises."""
-        ms = (C.c_double * 4)()
-        n = (C.c_int64 * 4)()
+        ms = (C.c_double * len(N.KERNEL_KINDS))()
+        n = (C.c_int64 * len(N.KERNEL_KINDS))()
         self._ck(lib.moe_get_kernel_times(self.h, ms, n))
         return {k: (ms[i], n[i]) for i, k in enumerate(N.KERNEL_KINDS)}
 

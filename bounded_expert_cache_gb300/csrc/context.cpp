@@ -126,12 +126,21 @@ extern "C" void moe_destroy(moe_ctx_t* ctx) {
   cudaFree(ctx->d_pt);
   cudaFree(ctx->d_ptgen);
   cudaFree(ctx->d_gen);
-  cudaFree(ctx->d_lest);
-  cudaFree(ctx->d_lbnd);
+  cudaFree(ctx->d_keys);
   cudaFree(ctx->d_ticket);
   cudaFree(ctx->d_repairs);
   cudaFree(ctx->d_h);
   cudaFree(ctx->d_err);
+  cudaFree(ctx->d_units);
+  cudaFree(ctx->d_owner);
+  cudaFree(ctx->d_sgen);
+  cudaFree(ctx->d_last);
+  cudaFree(ctx->d_tick);
+  cudaFree(ctx->d_rng);
+  cudaFree(ctx->d_stats);
+  cudaFree(ctx->d_fills);
+  cudaFree(ctx->d_done);
+  cudaFreeHost(ctx->h_units);
   cudaFreeHost(ctx->h_pt);
   cudaFreeHost(ctx->h_ptgen);
   cudaFreeHost(ctx->h_gen);
@@ -161,6 +170,7 @@ extern "C" moe_status_t moe_create(const moe_config_t* cfg, moe_ctx_t** out) {
   else if (c.n_streams < 1 || c.n_streams > 8) why = "n_streams outside 1..8";
   else if (c.tile_bytes < 16 || c.tile_bytes % 16) why = "tile_bytes not a positive multiple of 16";
   else if (c.max_tokens < 1) why = "max_tokens < 1";
+  else if (c.admit_on_device != 0 && c.admit_on_device != 1) why = "admit_on_device must be 0 or 1";
   if (!why.empty()) {
     g_create_err = "moe_create: " + why;
     return MOE_ERR_ARG;
@@ -202,8 +212,7 @@ extern "C" moe_status_t moe_create(const moe_config_t* cfg, moe_ctx_t** out) {
   std::fill(ctx->h_ptgen, ctx->h_ptgen + L * E, 0u);
   std::fill(ctx->h_gen, ctx->h_gen + L * S, 0u);
   const size_t te = static_cast<size_t>(c.max_tokens) * E;
-  CKC(cudaMalloc(&ctx->d_lest, sizeof(double) * te));
-  CKC(cudaMalloc(&ctx->d_lbnd, sizeof(double) * te));
+  CKC(cudaMalloc(&ctx->d_keys, sizeof(unsigned long long) * 3 * te));
   CKC(cudaMalloc(&ctx->d_ticket, sizeof(unsigned int)));
   CKC(cudaMemset(ctx->d_ticket, 0, sizeof(unsigned int)));
   CKC(cudaMalloc(&ctx->d_repairs, sizeof(unsigned long long) * L));
@@ -215,6 +224,33 @@ extern "C" moe_status_t moe_create(const moe_config_t* cfg, moe_ctx_t** out) {
   CKC(cudaMemset(ctx->d_err, 0, sizeof(uint32_t)));
   CKC(cudaHostAlloc(&ctx->h_err, sizeof(uint32_t), cudaHostAllocDefault));
   CKC(cudaHostAlloc(&ctx->h_union, sizeof(int32_t) * (2 * E + 2), cudaHostAllocDefault));
+  ctx->max_units = std::min(E, c.max_tokens * c.top_k) + 1;
+  const size_t unit_ints = moe::kUnitHeader + moe::kUnitInts * static_cast<size_t>(ctx->max_units);
+  CKC(cudaMalloc(&ctx->d_units, sizeof(int32_t) * unit_ints));
+  CKC(cudaMemset(ctx->d_units, 0, sizeof(int32_t) * unit_ints));
+  CKC(cudaHostAlloc(&ctx->h_units, sizeof(int32_t) * unit_ints, cudaHostAllocDefault));
+  ctx->dev_admit = c.admit_on_device == 1;
+  if (ctx->dev_admit) {
+    ctx->max_fills = std::min(E, std::min(c.max_tokens, 64) * c.top_k);
+    CKC(cudaMalloc(&ctx->d_owner, sizeof(int32_t) * L * S));
+    CKC(cudaMemset(ctx->d_owner, 0xFF, sizeof(int32_t) * L * S));
+    CKC(cudaMalloc(&ctx->d_sgen, sizeof(uint32_t) * L * S));
+    CKC(cudaMemset(ctx->d_sgen, 0, sizeof(uint32_t) * L * S));
+    CKC(cudaMalloc(&ctx->d_last, sizeof(unsigned long long) * L * S));
+    CKC(cudaMemset(ctx->d_last, 0, sizeof(unsigned long long) * L * S));
+    CKC(cudaMalloc(&ctx->d_tick, sizeof(unsigned long long) * L));
+    CKC(cudaMemset(ctx->d_tick, 0, sizeof(unsigned long long) * L));
+    CKC(cudaMalloc(&ctx->d_rng, sizeof(unsigned long long) * L));
+    std::vector<unsigned long long> rng(L);
+    for (int l = 0; l < L; ++l) rng[l] = c.seed ^ (static_cast<unsigned long long>(l) * 0x9E3779B97F4A7C15ull);
+    CKC(cudaMemcpy(ctx->d_rng, rng.data(), sizeof(unsigned long long) * L, cudaMemcpyHostToDevice));
+    CKC(cudaMalloc(&ctx->d_stats, sizeof(long long) * L * moe::kStatCount));
+    CKC(cudaMemset(ctx->d_stats, 0, sizeof(long long) * L * moe::kStatCount));
+    CKC(cudaMalloc(&ctx->d_fills, sizeof(int32_t) * (1 + 2 * ctx->max_fills)));
+    CKC(cudaMemset(ctx->d_fills, 0, sizeof(int32_t) * (1 + 2 * ctx->max_fills)));
+    CKC(cudaMalloc(&ctx->d_done, sizeof(unsigned int) * ctx->max_fills));
+    CKC(cudaMemset(ctx->d_done, 0, sizeof(unsigned int) * ctx->max_fills));
+  }
   ctx->streams.assign(c.n_streams, nullptr);
   ctx->ev_stage.assign(c.n_streams, nullptr);
   for (int i = 0; i < c.n_streams; ++i) {
@@ -256,7 +292,16 @@ extern "C" moe_status_t moe_bind_store(moe_ctx_t* ctx, const void* store, size_t
     cudaGetLastError();
     return fail(ctx, MOE_ERR_ARG, "moe_bind_store: store is not page-locked host memory");
   }
+  void* dev = nullptr;
+  e = cudaHostGetDevicePointer(&dev, const_cast<void*>(store), 0);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    if (ctx->dev_admit)
+      return fail(ctx, MOE_ERR_ARG, "moe_bind_store: store has no device mapping (on-device staging needs one)");
+    dev = nullptr;
+  }
   ctx->store = static_cast<const uint8_t*>(store);
+  ctx->store_dev = static_cast<const uint8_t*>(dev);
   ctx->store_bytes = bytes;
   return MOE_OK;
 }
@@ -272,13 +317,30 @@ extern "C" moe_status_t moe_bind_shared(moe_ctx_t* ctx, int32_t layer, const voi
 }
 
 // ------------------------------------------------------------ routing
+static moe::DevCacheLayer dev_cache(moe_ctx_t* ctx, int32_t layer) {
+  const size_t E = ctx->cfg.n_experts, S = ctx->cfg.slots_per_layer;
+  moe::DevCacheLayer c{};
+  c.pt = ctx->d_pt + layer * E;
+  c.ptgen = ctx->d_ptgen + layer * E;
+  c.owner = ctx->d_owner + layer * S;
+  c.sgen = ctx->d_sgen + layer * S;
+  c.last = ctx->d_last + layer * S;
+  c.tick = ctx->d_tick + layer;
+  c.rng = ctx->d_rng + layer;
+  c.stats = ctx->d_stats + layer * moe::kStatCount;
+  return c;
+}
+
 static moe_status_t route_impl(moe_ctx_t* ctx, int32_t layer, const void* x, int32_t xt, int32_t T,
                                const float* w_router, const float* bias, int32_t* topk_idx,
-                               float* topk_w, const moe_plan_t* plan, cudaStream_t st) {
+                               float* topk_w, const moe_plan_t* plan, cudaStream_t st,
+                               bool admit = false) {
   if (!valid_layer(ctx, layer)) return fail(ctx, MOE_ERR_ARG, "route: bad layer");
   if (T < 1 || T > ctx->cfg.max_tokens) return fail(ctx, MOE_ERR_ARG, "route: T outside 1..max_tokens");
   if (xt != MOE_F32 && xt != MOE_BF16) return fail(ctx, MOE_ERR_ARG, "route: bad activation dtype");
   if (!x || !w_router || !topk_idx || !topk_w) return fail(ctx, MOE_ERR_ARG, "route: null pointer");
+  if (reinterpret_cast<uintptr_t>(x) % 16 || reinterpret_cast<uintptr_t>(w_router) % 16)
+    return fail(ctx, MOE_ERR_ARG, "route: x and w_router must be 16-byte aligned");
   if (T > 64) return fail(ctx, MOE_ERR_ARG, "route: T > 64 needs the prefill router, which is not built");
   if (plan && plan->capacity < T * ctx->cfg.top_k)
     return fail(ctx, MOE_ERR_ARG, "route: plan capacity < T*k");
@@ -293,12 +355,26 @@ static moe_status_t route_impl(moe_ctx_t* ctx, int32_t layer, const void* x, int
   a.bias = bias;
   a.topk_idx = topk_idx;
   a.topk_w = topk_w;
-  a.l_est = ctx->d_lest;
-  a.l_bnd = ctx->d_lbnd;
+  a.keys = ctx->d_keys;
   a.ticket = ctx->d_ticket;
   a.repairs = ctx->d_repairs + layer;
   a.err = ctx->d_err;
   if (plan) a.plan = *plan;
+  if (admit) {
+    a.admit.enabled = 1;
+    a.admit.E = ctx->cfg.n_experts;
+    a.admit.S = ctx->cfg.slots_per_layer;
+    a.admit.policy = ctx->cfg.policy;
+    a.admit.has_shared = ctx->cfg.shared_inter > 0 ? 1 : 0;
+    a.admit.T = T;
+    a.admit.payload = ctx->geom.bytes;
+    a.admit.c = dev_cache(ctx, layer);
+    a.admit.fills = ctx->d_fills;
+    a.admit.units = ctx->d_units;
+    a.admit.done = ctx->d_done;
+    a.admit.max_fills = ctx->max_fills;
+    ctx->dev_state_used = true;
+  }
   if (ctx->timing) {
     moe_ctx::TimedLaunch r{MOE_KT_ROUTE, timing_event(ctx), timing_event(ctx)};
     CK(cudaEventRecord(r.a, st));
@@ -371,6 +447,8 @@ extern "C" moe_status_t moe_cache_admit(moe_ctx_t* ctx, int32_t layer, const moe
   if (!ctx) return MOE_ERR_ARG;
   if (!valid_layer(ctx, layer)) return fail(ctx, MOE_ERR_ARG, "admit: bad layer");
   if (!plan_ok(plan) || !misses) return fail(ctx, MOE_ERR_ARG, "admit: null pointer");
+  if (ctx->dev_admit)
+    return fail(ctx, MOE_ERR_STATE, "admit: this context admits on the device (moe_layer_forward)");
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const int E = ctx->cfg.n_experts;
   int32_t* hu = ctx->h_union;
@@ -391,6 +469,34 @@ extern "C" moe_status_t moe_cache_admit(moe_ctx_t* ctx, int32_t layer, const moe
   CK(cudaMemcpyAsync(ctx->d_pt + off, ctx->h_pt + off, sizeof(int32_t) * E, cudaMemcpyHostToDevice, st));
   CK(cudaMemcpyAsync(ctx->d_ptgen + off, ctx->h_ptgen + off, sizeof(uint32_t) * E,
                      cudaMemcpyHostToDevice, st));
+  // unit table of the step: routed experts in union order, then the shared one
+  const int32_t* pt = moe::slots_pt(ctx->slots[layer]);
+  const uint32_t* gen = moe::slots_gen(ctx->slots[layer]);
+  int32_t* ut = ctx->h_units;
+  int p0 = 0, nu_tab = 0;
+  std::vector<int32_t> p0_of(E, 0);
+  for (int e = 0; e < E; ++e) {
+    p0_of[e] = p0;
+    p0 += hu[E + e];
+  }
+  for (int i = 0; i < nu; ++i) {
+    const int e = hu[i];
+    int32_t* U = ut + moe::kUnitHeader + moe::kUnitInts * nu_tab++;
+    U[0] = pt[e];
+    U[1] = p0_of[e];
+    U[2] = hu[E + e];
+    U[3] = static_cast<int32_t>(gen[pt[e]]);
+  }
+  if (ctx->cfg.shared_inter > 0) {
+    int32_t* U = ut + moe::kUnitHeader + moe::kUnitInts * nu_tab++;
+    U[0] = -1;
+    U[1] = -1;
+    U[2] = p0 / ctx->cfg.top_k;  // tokens of the step
+    U[3] = 0;
+  }
+  ut[0] = nu_tab;
+  CK(cudaMemcpyAsync(ctx->d_units, ut, sizeof(int32_t) * (moe::kUnitHeader + moe::kUnitInts * nu_tab),
+                     cudaMemcpyHostToDevice, st));
   return MOE_OK;
 }
 
@@ -400,6 +506,8 @@ extern "C" moe_status_t moe_stage_tiles(moe_ctx_t* ctx, int32_t layer, const moe
   if (!valid_layer(ctx, layer) || !misses || misses->layer != layer)
     return fail(ctx, MOE_ERR_ARG, "stage: bad layer or miss list");
   if (misses->n > 0 && !ctx->store) return fail(ctx, MOE_ERR_STATE, "stage: no store bound");
+  if (ctx->dev_admit)
+    return fail(ctx, MOE_ERR_STATE, "stage: this context stages on the device (moe_layer_forward)");
   cudaStream_t cst = reinterpret_cast<cudaStream_t>(compute_stream);
   const int E = ctx->cfg.n_experts, S = ctx->cfg.slots_per_layer;
   const int ns = static_cast<int>(ctx->streams.size());
@@ -454,6 +562,21 @@ extern "C" moe_status_t moe_cache_evict(moe_ctx_t* ctx, int32_t layer, int32_t e
   if (!ctx) return MOE_ERR_ARG;
   if (!valid_layer(ctx, layer)) return fail(ctx, MOE_ERR_ARG, "evict: bad layer");
   CK(cudaDeviceSynchronize());
+  if (ctx->dev_admit) {
+    if (expert < 0 || expert >= ctx->cfg.n_experts) return fail(ctx, MOE_ERR_ARG, "evict: bad expert");
+    moe::DevCacheLayer c = dev_cache(ctx, layer);
+    int32_t slot = -1;
+    CK(cudaMemcpy(&slot, c.pt + expert, sizeof(int32_t), cudaMemcpyDeviceToHost));
+    if (slot < 0) return MOE_OK;
+    const int32_t none = -1;
+    long long ev = 0;
+    CK(cudaMemcpy(c.pt + expert, &none, sizeof(int32_t), cudaMemcpyHostToDevice));
+    CK(cudaMemcpy(c.owner + slot, &none, sizeof(int32_t), cudaMemcpyHostToDevice));
+    CK(cudaMemcpy(&ev, c.stats + moe::kStatEvictions, sizeof(long long), cudaMemcpyDeviceToHost));
+    ++ev;
+    CK(cudaMemcpy(c.stats + moe::kStatEvictions, &ev, sizeof(long long), cudaMemcpyHostToDevice));
+    return MOE_OK;
+  }
   moe_status_t s = moe::slots_evict(ctx->slots[layer], expert, &ctx->err);
   if (s != MOE_OK) return s;
   publish_page_table_host(ctx, layer);
@@ -471,6 +594,8 @@ extern "C" moe_status_t moe_cache_preload(moe_ctx_t* ctx, int32_t layer, const i
   if (!valid_layer(ctx, layer) || n < 0 || (n > 0 && !experts))
     return fail(ctx, MOE_ERR_ARG, "preload: bad arguments");
   if (!ctx->store) return fail(ctx, MOE_ERR_STATE, "preload: no store bound");
+  if (ctx->dev_admit && ctx->dev_state_used)
+    return fail(ctx, MOE_ERR_STATE, "preload: on-device admission already ran on this context");
   CK(cudaDeviceSynchronize());
   std::vector<int32_t> filled, fslots;
   moe_status_t s = moe::slots_preload(ctx->slots[layer], experts, n, &filled, &fslots, &ctx->err);
@@ -490,6 +615,17 @@ extern "C" moe_status_t moe_cache_preload(moe_ctx_t* ctx, int32_t layer, const i
   CK(cudaMemcpy(ctx->d_ptgen + off, ctx->h_ptgen + off, sizeof(uint32_t) * E, cudaMemcpyHostToDevice));
   CK(cudaMemcpy(ctx->d_gen + static_cast<size_t>(layer) * S, hg, sizeof(uint32_t) * S,
                 cudaMemcpyHostToDevice));
+  if (ctx->dev_admit) {
+    // the device-side cache state starts from the host manager's
+    moe::DevCacheLayer c = dev_cache(ctx, layer);
+    const moe_slots* sl = ctx->slots[layer];
+    std::vector<unsigned long long> last(moe::slots_last(sl), moe::slots_last(sl) + S);
+    const unsigned long long tick = moe::slots_tick(sl);
+    CK(cudaMemcpy(c.owner, moe::slots_owner(sl), sizeof(int32_t) * S, cudaMemcpyHostToDevice));
+    CK(cudaMemcpy(c.sgen, moe::slots_gen(sl), sizeof(uint32_t) * S, cudaMemcpyHostToDevice));
+    CK(cudaMemcpy(c.last, last.data(), sizeof(unsigned long long) * S, cudaMemcpyHostToDevice));
+    CK(cudaMemcpy(c.tick, &tick, sizeof(unsigned long long), cudaMemcpyHostToDevice));
+  }
   return MOE_OK;
 }
 
@@ -522,8 +658,7 @@ extern "C" moe_status_t moe_expert_ffn(moe_ctx_t* ctx, int32_t layer, const void
   a.quant = ctx->cfg.quant;
   a.pool = ctx->d_pool + static_cast<size_t>(layer) * S * ctx->slot_stride;
   a.slot_stride = ctx->slot_stride;
-  a.pt = ctx->d_pt + static_cast<size_t>(layer) * E;
-  a.ptgen = ctx->d_ptgen + static_cast<size_t>(layer) * E;
+  a.units = ctx->d_units;
   a.gen = ctx->d_gen + static_cast<size_t>(layer) * S;
   a.S = S;
   a.shared = ctx->shared[layer];
@@ -553,6 +688,46 @@ extern "C" moe_status_t moe_layer_forward(moe_ctx_t* ctx, int32_t layer, const v
   if (!ctx) return MOE_ERR_ARG;
   if (!plan_ok(plan)) return fail(ctx, MOE_ERR_ARG, "layer_forward: plan has a null array");
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (ctx->dev_admit) {
+    // route + plan + admission in one launch, then staging and the FFN; no
+    // host synchronisation (the step can be captured in a CUDA graph)
+    if (!ctx->store_dev) return fail(ctx, MOE_ERR_STATE, "layer_forward: no store bound");
+    moe_status_t s = route_impl(ctx, layer, x, xt, T, w_router, bias, topk_idx, topk_w, plan, st, true);
+    if (s != MOE_OK) return s;
+    const moe::ExpertGeom& g = ctx->geom;
+    moe::StageArgs sa{};
+    const size_t E = ctx->cfg.n_experts, S = ctx->cfg.slots_per_layer;
+    sa.store = ctx->store_dev + static_cast<size_t>(layer) * E * g.bytes;
+    sa.pool = ctx->d_pool + static_cast<size_t>(layer) * S * ctx->slot_stride;
+    sa.slot_stride = ctx->slot_stride;
+    sa.payload = g.bytes;
+    sa.fills = ctx->d_fills;
+    sa.done = ctx->d_done;
+    sa.sgen = ctx->d_sgen + static_cast<size_t>(layer) * S;
+    sa.gen = ctx->d_gen + static_cast<size_t>(layer) * S;
+    sa.stats = ctx->d_stats + static_cast<size_t>(layer) * moe::kStatCount;
+    sa.tile_bytes = ctx->cfg.tile_bytes;
+    sa.tiles_per_expert = 0;
+    sa.chunks_per_expert = 0;
+    for (int m = 0; m < 3; ++m) {
+      sa.mat_off[m] = g.qoff[m];
+      sa.mat_bytes[m] = g.qbytes[m] + g.sbytes[m];
+      sa.tiles_per_expert += static_cast<int>((sa.mat_bytes[m] + sa.tile_bytes - 1) / sa.tile_bytes);
+      sa.chunks[m] = static_cast<int>((sa.mat_bytes[m] + moe::kStageChunkBytes - 1) / moe::kStageChunkBytes);
+      sa.chunks_per_expert += sa.chunks[m];
+    }
+    sa.max_fills = std::min(ctx->max_fills, std::min(T * ctx->cfg.top_k, ctx->cfg.n_experts));
+    if (ctx->timing) {
+      moe_ctx::TimedLaunch r{MOE_KT_STAGE, timing_event(ctx), timing_event(ctx)};
+      CK(cudaEventRecord(r.a, st));
+      CK(moe::launch_stage_copy(sa, st));
+      CK(cudaEventRecord(r.b, st));
+      ctx->timed.push_back(r);
+    } else {
+      CK(moe::launch_stage_copy(sa, st));
+    }
+    return moe_expert_ffn(ctx, layer, x, xt, T, plan, y, MOE_MODE_AUTO, stream);
+  }
   moe_status_t s = route_impl(ctx, layer, x, xt, T, w_router, bias, topk_idx, topk_w, plan, st);
   if (s != MOE_OK) return s;
   moe_miss_list_t local{};
@@ -574,6 +749,8 @@ extern "C" moe_status_t moe_check_device_errors(moe_ctx_t* ctx, moe_stream_t str
   if (e & MOE_DEVERR_STALE)
     return fail(ctx, MOE_ERR_STALE, "device: an expert's page-table entry or slot generation was invalid");
   if (e & MOE_DEVERR_TIMEOUT) return fail(ctx, MOE_ERR_TIMEOUT, "device: a bounded wait ran out");
+  if (e & MOE_DEVERR_CAPACITY)
+    return fail(ctx, MOE_ERR_CAPACITY, "device: a step's union did not fit the slots; it was not admitted");
   if (e & MOE_DEVERR_NONFINITE)
     return fail(ctx, MOE_ERR_UNCERTIFIED, "device: non-finite router input; routing undefined");
   return fail(ctx, MOE_ERR_ARG, "device: expert id out of range in a plan input");
@@ -588,10 +765,25 @@ extern "C" moe_status_t moe_get_stats(const moe_ctx_t* cctx, int32_t layer, moe_
   std::vector<unsigned long long> rep(L);
   CK(cudaDeviceSynchronize());
   CK(cudaMemcpy(rep.data(), ctx->d_repairs, sizeof(unsigned long long) * L, cudaMemcpyDeviceToHost));
+  std::vector<long long> ds;
+  if (ctx->dev_admit) {
+    ds.resize(static_cast<size_t>(L) * moe::kStatCount);
+    CK(cudaMemcpy(ds.data(), ctx->d_stats, sizeof(long long) * ds.size(), cudaMemcpyDeviceToHost));
+  }
   moe_stats_t t{};
   for (int l = 0; l < L; ++l) {
     if (layer != -1 && l != layer) continue;
     moe_stats_t s = moe::slots_stats(ctx->slots[l]);
+    if (ctx->dev_admit) {
+      const long long* d = ds.data() + static_cast<size_t>(l) * moe::kStatCount;
+      s.steps = d[moe::kStatSteps];
+      s.hits = d[moe::kStatHits];
+      s.misses = d[moe::kStatMisses];
+      s.evictions += d[moe::kStatEvictions];
+      s.materialized_bytes = d[moe::kStatMaterialized];
+      t.tiles_staged += d[moe::kStatTiles];
+      t.bytes_staged += d[moe::kStatBytes];
+    }
     t.steps += s.steps;
     t.hits += s.hits;
     t.misses += s.misses;
@@ -644,9 +836,16 @@ extern "C" moe_status_t moe_debug_corrupt_generation(moe_ctx_t* ctx, int32_t lay
   if (!valid_layer(ctx, layer) || expert < 0 || expert >= ctx->cfg.n_experts)
     return fail(ctx, MOE_ERR_ARG, "corrupt_generation: bad arguments");
   CK(cudaDeviceSynchronize());
-  const size_t off = static_cast<size_t>(layer) * ctx->cfg.n_experts + expert;
-  ctx->h_ptgen[off] += 0x10000u;
-  CK(cudaMemcpy(ctx->d_ptgen + off, ctx->h_ptgen + off, sizeof(uint32_t), cudaMemcpyHostToDevice));
+  // the slot's published generation no longer matches the page-table entry,
+  // as if its content had been replaced behind the table's back
+  const size_t E = ctx->cfg.n_experts, S = ctx->cfg.slots_per_layer;
+  int32_t slot = -1;
+  CK(cudaMemcpy(&slot, ctx->d_pt + layer * E + expert, sizeof(int32_t), cudaMemcpyDeviceToHost));
+  if (slot < 0) return fail(ctx, MOE_ERR_ARG, "corrupt_generation: expert not resident");
+  uint32_t g = 0;
+  CK(cudaMemcpy(&g, ctx->d_gen + layer * S + slot, sizeof(uint32_t), cudaMemcpyDeviceToHost));
+  g += 0x10000u;
+  CK(cudaMemcpy(ctx->d_gen + layer * S + slot, &g, sizeof(uint32_t), cudaMemcpyHostToDevice));
   return MOE_OK;
 }
 

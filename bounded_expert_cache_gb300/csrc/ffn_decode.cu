@@ -124,34 +124,39 @@ struct UnitRef {
   int64_t soff[3];      // scale-plane offsets
   int M;                // tokens of the unit
   int p0;               // first expert-major assignment (routed) or -1 (shared)
-  bool ok;
+  int slot;             // slot (routed) or -1 (shared)
+  uint32_t egen;        // generation the slot must hold
 };
 
-// Resolve unit u: u < n_uniq is the u-th expert of the union, u == n_uniq the
-// shared expert. A routed expert is usable only if its page-table entry names
-// a slot whose generation matches the entry's.
-__device__ __forceinline__ UnitRef resolve_unit(const FfnArgs& a, int u, int nu) {
+// Unit u of the step's unit table: routed experts of the union (in union
+// order) then the shared expert. Only the entry is read here; the slot's
+// generation is checked by unit_ok, issued alongside the weight loads.
+__device__ __forceinline__ UnitRef resolve_unit(const FfnArgs& a, int u) {
+  const int4 d = __ldg(reinterpret_cast<const int4*>(a.units + kUnitHeader) + u);
   UnitRef r;
-  if (u < nu) {
-    const int e = __ldg(a.plan.uniq + u);
-    const int slot = (e >= 0 && e < a.E) ? __ldg(a.pt + e) : -1;
-    r.ok = slot >= 0 && slot < a.S && __ldg(a.gen + slot) == __ldg(a.ptgen + e);
-    r.base = r.ok ? a.pool + static_cast<int64_t>(slot) * a.slot_stride : nullptr;
-    r.p0 = r.ok ? __ldg(a.plan.offsets + e) : 0;
-    r.M = r.ok ? __ldg(a.plan.offsets + e + 1) - r.p0 : 0;
-  } else {
-    r.ok = true;
-    r.base = a.shared;
-    r.p0 = -1;
-    r.M = a.T;
-  }
-  const bool routed = u < nu;
+  r.slot = d.x;
+  r.p0 = d.y;
+  r.M = d.z;
+  r.egen = static_cast<uint32_t>(d.w);
+  const bool routed = d.x >= 0;
+  // an out-of-range slot or a missing shared payload points at slot 0 (always
+  // mapped) and is refused by unit_ok, so no load leaves the pool
+  r.base = routed ? a.pool + static_cast<int64_t>(d.x < a.S ? d.x : 0) * a.slot_stride
+                  : (a.shared ? a.shared : a.pool);
 #pragma unroll
   for (int m = 0; m < 3; ++m) {
     r.qoff[m] = routed ? a.g.qoff[m] : a.gs.qoff[m];
     r.soff[m] = routed ? a.g.soff[m] : a.gs.soff[m];
   }
   return r;
+}
+
+// A routed unit is usable only if its slot holds the generation the page
+// table expects (every tile of its last fill has landed); the shared expert
+// always is.
+__device__ __forceinline__ bool unit_ok(const FfnArgs& a, const UnitRef& U) {
+  if (U.slot < 0) return a.shared != nullptr;
+  return U.slot < a.S && __ldg(a.gen + U.slot) == U.egen;
 }
 
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
@@ -167,7 +172,8 @@ __global__ void __launch_bounds__(kThreads) gateup_kernel(FfnArgs a) {
     xs[t * H + swz(k)] = load_act<XT>(a.x, i);
   }
   __syncthreads();
-  const int nu = __ldg(a.plan.n_uniq);
+  const int n_units = __ldg(a.units);
+  const int nu = n_units - (a.shared ? 1 : 0);  // routed units
   const int per_routed = a.I / kRowsPerItem;
   const int per_shared = a.shared ? a.Is / kRowsPerItem : 0;
   const int items = nu * per_routed + per_shared;
@@ -183,11 +189,8 @@ __global__ void __launch_bounds__(kThreads) gateup_kernel(FfnArgs a) {
       u = nu;
       r0 = (it - nu * per_routed) * kRowsPerItem;
     }
-    const UnitRef U = resolve_unit(a, u, nu);
-    if (!U.ok) {
-      if (lane == 0) atomicOr(a.err, MOE_DEVERR_STALE);
-      continue;
-    }
+    const UnitRef U = resolve_unit(a, u);
+    const bool ok = unit_ok(a, U);
     const uint8_t* q[2 * kRowsPerItem];
     const uint8_t* s[2 * kRowsPerItem];
 #pragma unroll
@@ -246,6 +249,10 @@ __global__ void __launch_bounds__(kThreads) gateup_kernel(FfnArgs a) {
 #pragma unroll
           for (int off = 16; off; off >>= 1)
             acc[r][m] += __shfl_xor_sync(0xffffffffu, acc[r][m], off);
+      if (!ok) {
+        if (lane == 0) atomicOr(a.err, MOE_DEVERR_STALE);
+        break;
+      }
       if (lane == 0) {
 #pragma unroll
         for (int m = 0; m < TM; ++m) {
@@ -277,22 +284,20 @@ __global__ void __launch_bounds__(kThreads) down_kernel(FfnArgs a) {
     hs[p * ldh + swz(k)] = __ldcg(a.h + i);
   }
   __syncthreads();
-  const int nu = __ldg(a.plan.n_uniq);
-  const int units = nu + (a.shared ? 1 : 0);
+  const int units = __ldg(a.units);
   const int o0 = blockIdx.x * kDownRows;
   constexpr int kPairs = kDownRows / kRowsPerItem;
   const int items = units * kPairs;
   for (int it = warp; it < items; it += kWarps) {
     const int u = it / kPairs, rp = it - u * kPairs;
-    const UnitRef U = resolve_unit(a, u, nu);
+    const UnitRef U = resolve_unit(a, u);
+    const bool ok = unit_ok(a, U);
     float acc[kRowsPerItem][TM];
 #pragma unroll
     for (int r = 0; r < kRowsPerItem; ++r)
 #pragma unroll
       for (int m = 0; m < TM; ++m) acc[r][m] = 0.f;
-    if (!U.ok) {
-      if (lane == 0) atomicOr(a.err, MOE_DEVERR_STALE);
-    } else {
+    {
       const int K = U.p0 >= 0 ? a.I : a.Is;
       const int rowbytes = Q == MOE_Q8_0 ? K : K / 2;
       const int nch = rowbytes / 16;
@@ -363,6 +368,7 @@ __global__ void __launch_bounds__(kThreads) down_kernel(FfnArgs a) {
             }
           }
         }
+        if (!ok) break;
         // weight by the combine weight, accumulate per token (T <= TM)
 #pragma unroll
         for (int m = 0; m < TM; ++m) {
@@ -375,6 +381,13 @@ __global__ void __launch_bounds__(kThreads) down_kernel(FfnArgs a) {
           }
         }
       }
+    }
+    if (!ok) {
+      if (lane == 0) atomicOr(a.err, MOE_DEVERR_STALE);
+#pragma unroll
+      for (int r = 0; r < kRowsPerItem; ++r)
+#pragma unroll
+        for (int m = 0; m < TM; ++m) acc[r][m] = 0.f;
     }
 #pragma unroll
     for (int r = 0; r < kRowsPerItem; ++r)

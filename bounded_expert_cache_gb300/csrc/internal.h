@@ -17,6 +17,7 @@ enum : uint32_t {
   MOE_DEVERR_TIMEOUT = 2u,     // a bounded wait ran out
   MOE_DEVERR_NONFINITE = 4u,   // router input or weight not finite
   MOE_DEVERR_BADIDX = 8u,      // expert id out of range in a plan input
+  MOE_DEVERR_CAPACITY = 16u,   // on-device admission: union larger than the slots allow
 };
 
 namespace moe {
@@ -30,6 +31,10 @@ moe_status_t slots_preload(moe_slots* s, const int32_t* experts, int32_t n,
                            std::string* err);
 moe_status_t slots_evict(moe_slots* s, int32_t e, std::string* err);
 const int32_t* slots_pt(const moe_slots* s);
+const int32_t* slots_owner(const moe_slots* s);
+const uint64_t* slots_last(const moe_slots* s);
+uint64_t slots_tick(const moe_slots* s);
+uint64_t slots_rng(const moe_slots* s);
 const uint32_t* slots_gen(const moe_slots* s);
 moe_stats_t slots_stats(const moe_slots* s);
 
@@ -44,6 +49,39 @@ struct ExpertGeom {
 };
 ExpertGeom expert_geom(int32_t H, int32_t I, int32_t quant);
 
+// Per-layer cache state kept on the device when admission runs on the GPU.
+struct DevCacheLayer {
+  int32_t* pt;                 // [E] expert -> slot or -1
+  uint32_t* ptgen;             // [E] generation the entry expects
+  int32_t* owner;              // [S] slot -> expert or -1
+  uint32_t* sgen;              // [S] fill count of the slot (the manager's generation)
+  unsigned long long* last;    // [S] tick of the slot's last access
+  unsigned long long* tick;    // [1]
+  unsigned long long* rng;     // [1] SplitMix64 state
+  long long* stats;            // [8] see kStat*
+};
+enum { kStatSteps = 0, kStatHits, kStatMisses, kStatEvictions, kStatMaterialized, kStatTiles,
+       kStatBytes, kStatCount = 8 };
+
+// Unit table read by the FFN kernels: int32 [kUnitHeader + 4 * max_units]:
+// count (then padding to 16 bytes), then per unit {slot (-1: shared expert),
+// p0 (first expert-major assignment, -1: shared), M (tokens), generation the
+// slot must hold}. Routed units come first, in union order.
+constexpr int kUnitHeader = 4;
+constexpr int kUnitInts = 4;
+
+// On-device admission, run by the router's last block after the plan.
+struct AdmitArgs {
+  int enabled;
+  int E, S, policy, has_shared, T;
+  long long payload;
+  DevCacheLayer c;
+  int32_t* fills;      // [1 + 2 * max_fills]: n, then (expert, slot) pairs
+  int32_t* units;      // unit table
+  unsigned int* done;  // [max_fills] tiles copied per fill
+  int max_fills;
+};
+
 // Arguments of the router launch.
 struct RouteArgs {
   const void* x;
@@ -52,13 +90,14 @@ struct RouteArgs {
   const float* bias;
   int32_t* topk_idx;
   float* topk_w;
-  double* l_est;        // [T][E] scratch
-  double* l_bnd;        // [T][E] scratch
+  unsigned long long* keys;  // [3][T][E] scratch: logit, lower, upper keys
   unsigned int* ticket; // last-block counter, zero between launches
   unsigned long long* repairs;  // repaired-token counter of the layer
   uint32_t* err;
   // optional fused plan (plan.counts == nullptr: none)
   moe_plan_t plan;
+  // optional fused admission (requires the fused plan)
+  AdmitArgs admit;
 };
 cudaError_t launch_route(const RouteArgs& a, int num_sms, cudaStream_t st);
 
@@ -74,15 +113,36 @@ cudaError_t launch_plan(const PlanArgs& a, cudaStream_t st);
 // Message returned by moe_last_error(NULL) on this thread.
 void set_thread_error(const std::string& msg);
 
+// Device-driven staging of the fills listed by on-device admission: copy
+// each filled expert's tiles from the pinned store (read over the host link)
+// into its slot, then publish the slot's generation.
+struct StageArgs {
+  const uint8_t* store;      // pinned host store of the layer: [E][payload]
+  uint8_t* pool;             // slot pool of the layer
+  int64_t slot_stride, payload;
+  const int32_t* fills;      // from admission
+  unsigned int* done;        // [max_fills]
+  const uint32_t* sgen;      // [S] manager generations
+  uint32_t* gen;             // [S] published generations
+  long long* stats;          // [kStatCount]
+  int64_t mat_off[3], mat_bytes[3];
+  int64_t tile_bytes;
+  int tiles_per_expert;      // 256 KiB tiles of one expert (accounting unit)
+  int chunks[3];             // copy chunks per matrix
+  int chunks_per_expert;
+  int max_fills;
+};
+constexpr int64_t kStageChunkBytes = 32768;  // one CTA's copy: 256 threads x 8 x 16 B
+cudaError_t launch_stage_copy(const StageArgs& a, cudaStream_t st);
+
 // Arguments of the decode FFN launches.
 struct FfnArgs {
   const void* x;
   int32_t xt, T, H, I, Is, k, E, quant;
   const uint8_t* pool;        // slot pool of the layer
   int64_t slot_stride;
-  const int32_t* pt;          // [E] page table of the layer
-  const uint32_t* ptgen;      // [E]
-  const uint32_t* gen;        // [S]
+  const int32_t* units;       // unit table of this step
+  const uint32_t* gen;        // [S] published slot generations
   int32_t S;
   const uint8_t* shared;      // shared payload or nullptr
   ExpertGeom g, gs;           // routed and shared geometry
@@ -112,11 +172,11 @@ struct moe_ctx {
   uint32_t* h_gen = nullptr;
   std::vector<moe_slots*> slots;
   const uint8_t* store = nullptr;
+  const uint8_t* store_dev = nullptr;  // device alias of the pinned store
   size_t store_bytes = 0;
   std::vector<const uint8_t*> shared;
   // scratch
-  double* d_lest = nullptr;
-  double* d_lbnd = nullptr;
+  unsigned long long* d_keys = nullptr;
   unsigned int* d_ticket = nullptr;
   unsigned long long* d_repairs = nullptr;  // [L]
   float* d_h = nullptr;
@@ -124,6 +184,21 @@ struct moe_ctx {
   uint32_t* d_err = nullptr;
   uint32_t* h_err = nullptr;
   int32_t* h_union = nullptr;  // pinned: uniq [E], counts [E], n_uniq
+  int32_t* d_units = nullptr;  // unit table (device)
+  int32_t* h_units = nullptr;  // pinned staging of the unit table (host admission)
+  int32_t max_units = 0;
+  // on-device admission
+  bool dev_admit = false;
+  bool dev_state_used = false;
+  int32_t* d_owner = nullptr;             // [L][S]
+  uint32_t* d_sgen = nullptr;             // [L][S]
+  unsigned long long* d_last = nullptr;   // [L][S]
+  unsigned long long* d_tick = nullptr;   // [L]
+  unsigned long long* d_rng = nullptr;    // [L]
+  long long* d_stats = nullptr;           // [L][kStatCount]
+  int32_t* d_fills = nullptr;             // [1 + 2 * max_fills]
+  unsigned int* d_done = nullptr;         // [max_fills]
+  int32_t max_fills = 0;
   std::vector<cudaStream_t> streams;
   std::vector<cudaEvent_t> ev_stage;
   cudaEvent_t ev_compute = nullptr;
@@ -136,8 +211,8 @@ struct moe_ctx {
   bool timing = false;
   std::vector<TimedLaunch> timed;
   std::vector<cudaEvent_t> ev_pool;
-  double kt_ms[MOE_KT_COUNT] = {0, 0, 0, 0};
-  int64_t kt_n[MOE_KT_COUNT] = {0, 0, 0, 0};
+  double kt_ms[MOE_KT_COUNT] = {};
+  int64_t kt_n[MOE_KT_COUNT] = {};
   std::vector<int64_t> tiles_staged, bytes_staged;
   std::string err;
 };

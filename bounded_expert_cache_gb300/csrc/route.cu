@@ -49,6 +49,24 @@ __device__ __forceinline__ float load_x(const void* x, size_t i) {
   }
 }
 
+// Four consecutive activations (i a multiple of 4; rows 16-byte aligned).
+template <int XT>
+__device__ __forceinline__ void load_x4(const void* x, size_t i, float* v) {
+  if (XT == MOE_BF16) {
+    const uint2 b = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(x) + i));
+    v[0] = __uint_as_float(b.x << 16);
+    v[1] = __uint_as_float(b.x & 0xFFFF0000u);
+    v[2] = __uint_as_float(b.y << 16);
+    v[3] = __uint_as_float(b.y & 0xFFFF0000u);
+  } else {
+    const float4 f = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(x) + i));
+    v[0] = f.x;
+    v[1] = f.y;
+    v[2] = f.z;
+    v[3] = f.w;
+  }
+}
+
 // Error-free sum: a + b == s + e exactly (Knuth's TwoSum).
 __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
   s = __fadd_rn(a, b);
@@ -196,87 +214,139 @@ __device__ bool warp_exact_logit(const void* x, size_t xoff, const float* wrow, 
 }
 
 // ------------------------------------------------------------ selection
-struct Cand {
-  double v;
-  int e;
+// Selection and certification compare order-preserving integer keys of the
+// fp64 logits and of their bound intervals (FP64 compares are slow on this
+// GPU; integer ones are not). okey is strictly monotone on non-NaN doubles,
+// maps -0 and +0 to the same key and NaN below everything.
+__device__ __forceinline__ unsigned long long okey(double x) {
+  if (isnan(x)) return 0ull;
+  x = x + 0.0;  // -0 -> +0
+  const long long b = __double_as_longlong(x);
+  return b >= 0 ? (static_cast<unsigned long long>(b) | 0x8000000000000000ull)
+                : ~static_cast<unsigned long long>(b);
+}
+__device__ __forceinline__ double okey_value(unsigned long long k) {
+  const unsigned long long b = (k & 0x8000000000000000ull) ? (k & 0x7FFFFFFFFFFFFFFFull) : ~k;
+  return __longlong_as_double(static_cast<long long>(b));
+}
+
+struct TokenKeys {
+  const unsigned long long* l;   // [E] logit keys
+  const unsigned long long* lo;  // [E] lower-bound keys (rounded down)
+  const unsigned long long* hi;  // [E] upper-bound keys (rounded up)
 };
-__device__ __forceinline__ bool better(double v, int e, double bv, int be) {
+
+__device__ __forceinline__ bool kbetter(unsigned long long v, int e, unsigned long long bv, int be) {
   return v > bv || (v == bv && e < be);
 }
 
-// Top-k of one token by a warp. Returns the selection in sel (all lanes) and
-// whether the bounds certify it.
-__device__ bool warp_select(const double* l, const double* bnd, int E, int k, int* sel,
-                            bool certify) {
+// Top-k of one token by a warp: lane owns experts lane, lane+32, ...
+// (E <= 32*NPL). Returns the selection in sel and its keys in selk (all lanes;
+// descending logit, ties to the lower id) and, if certify, whether the bound
+// intervals of consecutive selections and of the k-th against every other
+// expert are disjoint.
+template <int NPL>
+__device__ bool warp_select_keys(const TokenKeys& K, int E, int k, int* sel,
+                                 unsigned long long* selk, bool certify) {
   const int lane = threadIdx.x & 31;
-  uint32_t taken = 0;
+  unsigned long long v[NPL];
+  uint32_t live = 0;
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) {
+    const int e = i * 32 + lane;
+    v[i] = e < E ? __ldcg(K.l + e) : 0ull;
+    if (e < E) live |= 1u << i;
+  }
   for (int r = 0; r < k; ++r) {
-    double bv = -DBL_MAX;
+    unsigned long long bv = 0ull;
     int be = INT_MAX;
-    for (int i = 0; i * 32 + lane < E; ++i) {
-      if ((taken >> i) & 1u) continue;
-      int e = i * 32 + lane;
-      double v = __ldcg(l + e);
-      if (be == INT_MAX || better(v, e, bv, be)) {
-        bv = v;
-        be = e;
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) {
+      if (((live >> i) & 1u) && (be == INT_MAX || kbetter(v[i], i * 32 + lane, bv, be))) {
+        bv = v[i];
+        be = i * 32 + lane;
       }
     }
+#pragma unroll
     for (int off = 16; off; off >>= 1) {
-      double ov = __shfl_xor_sync(0xffffffffu, bv, off);
-      int oe = __shfl_xor_sync(0xffffffffu, be, off);
-      if (oe != INT_MAX && (be == INT_MAX || better(ov, oe, bv, be))) {
+      const unsigned long long ov = __shfl_xor_sync(0xffffffffu, bv, off);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+      if (oe != INT_MAX && (be == INT_MAX || kbetter(ov, oe, bv, be))) {
         bv = ov;
         be = oe;
       }
     }
     sel[r] = be;
-    if ((be & 31) == lane) taken |= 1u << (be >> 5);
+    selk[r] = bv;
+    if ((be & 31) == lane) live &= ~(1u << (be >> 5));
   }
   if (!certify) return true;
-  // interval [l - b, l + b] widened by 2^-50 |l| so that disjoint intervals
-  // also separate the correctly rounded fp64 images
-  auto lower = [&](int e) {
-    double v = __ldcg(l + e), b = __ldcg(bnd + e);
-    return v - b - fabs(v) * 0x1p-50;
-  };
-  auto upper = [&](int e) {
-    double v = __ldcg(l + e), b = __ldcg(bnd + e);
-    return v + b + fabs(v) * 0x1p-50;
-  };
-  bool ok = true;
-  for (int j = 0; j + 1 < k; ++j) ok &= lower(sel[j]) > upper(sel[j + 1]);
-  double up = -DBL_MAX;
-  bool any = false;
-  for (int i = 0; i * 32 + lane < E; ++i) {
-    if ((taken >> i) & 1u) continue;
-    double u = upper(i * 32 + lane);
-    if (!any || !(u <= up)) up = u;  // NaN propagates as "uncertified"
-    any = true;
+  // bounds of the selection (lane j < k holds selection j's), and the
+  // largest upper bound outside it
+  unsigned long long my_lo = 0ull, my_hi = 0ull;
+  if (lane < k) {
+    int sj = 0;
+    for (int j = 0; j < k; ++j)
+      if (j == lane) sj = sel[j];
+    my_lo = __ldcg(K.lo + sj);
+    my_hi = __ldcg(K.hi + sj);
   }
-  for (int off = 16; off; off >>= 1) {
-    double o = __shfl_xor_sync(0xffffffffu, up, off);
-    int oa = __shfl_xor_sync(0xffffffffu, any ? 1 : 0, off);
-    if (oa) {
-      if (!any || !(o <= up)) up = o;
+  unsigned long long rest = 0ull;
+  bool any = false;
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) {
+    if ((live >> i) & 1u) {
+      const unsigned long long h = __ldcg(K.hi + i * 32 + lane);
+      rest = (!any || h > rest) ? h : rest;
       any = true;
     }
   }
-  if (any) ok &= lower(sel[k - 1]) > up;
+#pragma unroll
+  for (int off = 16; off; off >>= 1) {
+    const unsigned long long o = __shfl_xor_sync(0xffffffffu, rest, off);
+    const int oa = __shfl_xor_sync(0xffffffffu, any ? 1 : 0, off);
+    if (oa) {
+      rest = (!any || o > rest) ? o : rest;
+      any = true;
+    }
+  }
+  // lane j < k-1 checks lower(sel j) > upper(sel j+1); lane k-1 checks the rest
+  const unsigned long long next_hi = __shfl_down_sync(0xffffffffu, my_hi, 1);
+  bool ok = true;
+  if (lane + 1 < k) ok = my_lo > next_hi;
+  if (lane == k - 1 && any) ok = my_lo > rest;
   return __all_sync(0xffffffffu, ok);
 }
 
-__device__ void warp_write_selection(const double* l, const int* sel, int k, int32_t* idx,
-                                     float* w) {
+__device__ bool warp_select(const TokenKeys& K, int E, int k, int* sel, unsigned long long* selk,
+                            bool certify) {
+  if (E <= 32) return warp_select_keys<1>(K, E, k, sel, selk, certify);
+  if (E <= 64) return warp_select_keys<2>(K, E, k, sel, selk, certify);
+  if (E <= 128) return warp_select_keys<4>(K, E, k, sel, selk, certify);
+  if (E <= 256) return warp_select_keys<8>(K, E, k, sel, selk, certify);
+  if (E <= 512) return warp_select_keys<16>(K, E, k, sel, selk, certify);
+  return warp_select_keys<32>(K, E, k, sel, selk, certify);
+}
+
+// Combine weights of a selection: softmax over the k selected logits, the
+// differences taken in fp64 and exponentiated in fp32.
+__device__ void warp_write_selection(const int* sel, const unsigned long long* selk, int k,
+                                     int32_t* idx, float* w) {
   const int lane = threadIdx.x & 31;
-  double m = __ldcg(l + sel[0]);
-  double z = 0.0;
-  if (lane < k) z = exp(__ldcg(l + sel[lane]) - m);
-  double sum = 0.0;
+  float z = 0.f;
+  int sj = 0;
+  unsigned long long kj = selk[0];
+  for (int j = 0; j < k; ++j)
+    if (j == lane) {
+      sj = sel[j];
+      kj = selk[j];
+    }
+  if (lane < k) z = expf(static_cast<float>(okey_value(kj) - okey_value(selk[0])));
+  float sum = 0.f;
   for (int j = 0; j < k; ++j) sum += __shfl_sync(0xffffffffu, z, j);  // fixed order
   if (lane < k) {
-    idx[lane] = sel[lane];
-    w[lane] = static_cast<float>(z / sum);
+    idx[lane] = sj;
+    w[lane] = z / sum;
   }
 }
 
@@ -395,6 +465,264 @@ __device__ void plan_block(const int32_t* idx, const float* w, int A, int k, int
   }
 }
 
+
+// ------------------------------------------------------------ on-device admission
+__device__ __forceinline__ unsigned long long splitmix64_next(unsigned long long& st) {
+  unsigned long long z = (st += 0x9E3779B97F4A7C15ull);
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
+// Cache resolve of one step by one warp, the same policy as the host slot
+// manager ("MawForge" §IV-C materialise into an available slot and update the
+// route-to-slot map; "Paging the Experts" §3.2 entries pinned per layer,
+// §4.1 LRU and seeded random eviction): resident experts of the union are
+// touched in ascending id, then missing experts are admitted in ascending id,
+// one tick per access; a miss takes the lowest free slot, else the LRU victim
+// (oldest tick) or cand[next() mod n] over resident experts outside the
+// union listed by slot. The layer's slot state and the union's page-table
+// entries are read once into shared memory, decided there, and written back;
+// the warp then writes the fill list, the FFN's unit table, and resets the
+// staging counters.
+__host__ __device__ constexpr size_t admit_smem_bytes(int E, int S, int max_units) {
+  return 8 * static_cast<size_t>(S)                    // last
+         + 4 * static_cast<size_t>(S) * 2              // owner, sgen
+         + 4 * static_cast<size_t>((E + 31) / 32)      // union bitmap
+         + 4 * static_cast<size_t>(max_units) * 2 + 16;  // union ids, their slots
+}
+
+__device__ void admit_warp(const AdmitArgs& A, const moe_plan_t& P, unsigned char* smem,
+                           uint32_t* err) {
+  const int lane = threadIdx.x & 31;
+  const int E = A.E, S = A.S;
+  const DevCacheLayer c = A.c;
+  const int nu = __ldcg(P.n_uniq);
+  unsigned long long* s_last = reinterpret_cast<unsigned long long*>(smem);
+  int* s_owner = reinterpret_cast<int*>(s_last + S);
+  uint32_t* s_sgen = reinterpret_cast<uint32_t*>(s_owner + S);
+  unsigned* bm = reinterpret_cast<unsigned*>(s_sgen + S);
+  int* uq = reinterpret_cast<int*>(bm + (E + 31) / 32);
+  int* upt = uq + nu;
+  const int nwords = (E + 31) / 32;
+  for (int w = lane; w < nwords; w += 32) bm[w] = 0u;
+  for (int s = lane; s < S; s += 32) {
+    s_last[s] = __ldcg(c.last + s);
+    s_owner[s] = __ldcg(c.owner + s);
+    s_sgen[s] = __ldcg(c.sgen + s);
+  }
+  __syncwarp();
+  for (int u = lane; u < nu; u += 32) {
+    const int e = __ldcg(P.uniq + u);
+    uq[u] = e;
+    upt[u] = __ldcg(c.pt + e);
+    atomicOr(&bm[e >> 5], 1u << (e & 31));
+  }
+  __syncwarp();
+  auto in_u = [&](int o) { return o >= 0 && ((bm[o >> 5] >> (o & 31)) & 1u); };
+  // counts before any change, so a refused step leaves the state untouched
+  int nmiss = 0, nfree = 0, res_in_u = 0;
+  for (int u0 = 0; u0 < nu; u0 += 32) {
+    const int u = u0 + lane;
+    nmiss += __popc(__ballot_sync(0xffffffffu, u < nu && upt[u] < 0));
+  }
+  for (int s0 = 0; s0 < S; s0 += 32) {
+    const int s = s0 + lane;
+    const int o = s < S ? s_owner[s] : -2;
+    nfree += __popc(__ballot_sync(0xffffffffu, o == -1));
+    res_in_u += __popc(__ballot_sync(0xffffffffu, in_u(o)));
+  }
+  const int cand0 = (S - nfree) - res_in_u;
+  if (nu > S || (A.policy == MOE_RANDOM && nmiss > nfree + cand0)) {
+    if (lane == 0) {
+      atomicOr(err, MOE_DEVERR_CAPACITY);
+      A.units[0] = 0;
+      A.fills[0] = 0;
+    }
+    return;
+  }
+  unsigned long long tick = __ldcg(c.tick);
+  // hits in ascending id, consecutive ticks
+  for (int u0 = 0; u0 < nu; u0 += 32) {
+    const int u = u0 + lane;
+    const int slot = u < nu ? upt[u] : -1;
+    const unsigned hm = __ballot_sync(0xffffffffu, slot >= 0);
+    if (slot >= 0) s_last[slot] = tick + 1 + __popc(hm & ((1u << lane) - 1u));
+    tick += __popc(hm);
+  }
+  __syncwarp();
+  // misses in ascending id, one at a time
+  unsigned long long rng = __ldcg(c.rng);
+  int nfill = 0, nevict = 0;
+  for (int u = 0; u < nu; ++u) {
+    if (upt[u] >= 0) continue;
+    const int e = uq[u];
+    ++tick;
+    int slot = -1;
+    for (int s0 = 0; s0 < S && slot < 0; s0 += 32) {
+      const int s = s0 + lane;
+      const unsigned fm = __ballot_sync(0xffffffffu, s < S && s_owner[s] < 0);
+      if (fm) slot = s0 + __ffs(fm) - 1;
+    }
+    if (slot < 0) {
+      if (A.policy == MOE_LRU) {
+        unsigned long long best = ~0ull;
+        int bs = INT_MAX;
+        for (int s = lane; s < S; s += 32) {
+          const unsigned long long v = s_last[s];
+          if (v < best || (v == best && s < bs)) {
+            best = v;
+            bs = s;
+          }
+        }
+        for (int off = 16; off; off >>= 1) {
+          const unsigned long long ov = __shfl_xor_sync(0xffffffffu, best, off);
+          const int os = __shfl_xor_sync(0xffffffffu, bs, off);
+          if (ov < best || (ov == best && os < bs)) {
+            best = ov;
+            bs = os;
+          }
+        }
+        slot = bs;
+      } else {
+        int n = 0;
+        for (int s0 = 0; s0 < S; s0 += 32) {
+          const int s = s0 + lane;
+          const int o = s < S ? s_owner[s] : -1;
+          n += __popc(__ballot_sync(0xffffffffu, o >= 0 && !in_u(o)));
+        }
+        const unsigned long long r = splitmix64_next(rng);
+        int target = static_cast<int>(r % static_cast<unsigned long long>(n));
+        for (int s0 = 0; s0 < S && slot < 0; s0 += 32) {
+          const int s = s0 + lane;
+          const int o = s < S ? s_owner[s] : -1;
+          unsigned cm = __ballot_sync(0xffffffffu, o >= 0 && !in_u(o));
+          const int pc = __popc(cm);
+          if (target < pc) {
+            for (int i = 0; i < target; ++i) cm &= cm - 1;
+            slot = s0 + __ffs(cm) - 1;
+          } else {
+            target -= pc;
+          }
+        }
+      }
+      if (lane == 0) c.pt[s_owner[slot]] = -1;  // victims are never in the union
+      ++nevict;
+    }
+    if (lane == 0) {
+      s_owner[slot] = e;
+      s_sgen[slot] += 1u;
+      s_last[slot] = tick;
+      upt[u] = slot;
+      A.fills[1 + 2 * nfill] = e;
+      A.fills[2 + 2 * nfill] = slot;
+      A.done[nfill] = 0u;
+    }
+    ++nfill;
+    __syncwarp();
+  }
+  // write back the slot state and the union's page-table entries
+  for (int s = lane; s < S; s += 32) {
+    c.last[s] = s_last[s];
+    c.owner[s] = s_owner[s];
+    c.sgen[s] = s_sgen[s];
+  }
+  long long assignments = 0;
+  for (int u = lane; u < nu; u += 32) {
+    const int e = uq[u], slot = upt[u];
+    const int cnt = __ldcg(P.counts + e);
+    assignments += cnt;
+    c.pt[e] = slot;
+    c.ptgen[e] = s_sgen[slot];
+    // unit table: routed units in union order, then the shared expert
+    int* U = A.units + kUnitHeader + kUnitInts * u;
+    U[0] = slot;
+    U[1] = __ldcg(P.offsets + e);
+    U[2] = cnt;
+    U[3] = static_cast<int>(s_sgen[slot]);
+  }
+  for (int off = 16; off; off >>= 1) assignments += __shfl_xor_sync(0xffffffffu, assignments, off);
+  if (lane == 0) {
+    if (A.has_shared) {
+      int* U = A.units + kUnitHeader + kUnitInts * nu;
+      U[0] = -1;
+      U[1] = -1;
+      U[2] = A.T;
+      U[3] = 0;
+    }
+    A.units[0] = nu + (A.has_shared ? 1 : 0);
+    A.fills[0] = nfill;
+    c.tick[0] = tick;
+    c.rng[0] = rng;
+    c.stats[kStatSteps] += 1;
+    c.stats[kStatHits] += assignments - nfill;
+    c.stats[kStatMisses] += nfill;
+    c.stats[kStatEvictions] += nevict;
+    c.stats[kStatMaterialized] += static_cast<long long>(nfill) * A.payload;
+  }
+}
+
+// Expert-major plan of A <= 32 assignments by one warp (every decode step):
+// same outputs as plan_block. smem: counts[E], offsets[E].
+__device__ void plan_warp(const int32_t* idx, const float* w, int A, int k, int E,
+                          const moe_plan_t& P, int* smem, uint32_t* err) {
+  const int lane = threadIdx.x & 31;
+  int* cnt = smem;
+  int* off = smem + E;
+  for (int e = lane; e < E; e += 32) cnt[e] = 0;
+  __syncwarp();
+  const bool live = lane < A;
+  int e = live ? __ldcg(idx + lane) : -1;
+  const bool valid = live && e >= 0 && e < E;
+  if (live && !valid) atomicOr(err, MOE_DEVERR_BADIDX);
+  const unsigned peers = __match_any_sync(0xffffffffu, valid ? e : -1 - lane);
+  const int rank = __popc(peers & ((1u << lane) - 1u));
+  if (valid && (__ffs(peers) - 1) == lane) cnt[e] = __popc(peers);
+  __syncwarp();
+  // exclusive scans of counts and of (count > 0) over the experts; lane owns
+  // a contiguous range of experts
+  const int per = (E + 31) / 32, b0 = lane * per;
+  int sc = 0, sn = 0;
+  for (int i = 0; i < per; ++i)
+    if (b0 + i < E) {
+      sc += cnt[b0 + i];
+      sn += cnt[b0 + i] > 0;
+    }
+  int ic = sc, in = sn;
+  for (int d = 1; d < 32; d <<= 1) {
+    const int oc = __shfl_up_sync(0xffffffffu, ic, d);
+    const int on = __shfl_up_sync(0xffffffffu, in, d);
+    if (lane >= d) {
+      ic += oc;
+      in += on;
+    }
+  }
+  int rc = ic - sc, rn = in - sn;
+  for (int i = 0; i < per; ++i) {
+    const int ee = b0 + i;
+    if (ee < E) {
+      const int c = cnt[ee];
+      off[ee] = rc;
+      P.counts[ee] = c;
+      P.offsets[ee] = rc;
+      if (c > 0) P.uniq[rn++] = ee;
+      rc += c;
+    }
+  }
+  if (lane == 31) {
+    P.offsets[E] = ic;
+    *P.n_uniq = in;
+  }
+  __syncwarp();
+  if (valid) {
+    const int pos = off[e] + rank;  // lanes are assignments in token order
+    P.perm_tok[pos] = lane / k;
+    P.perm_rank[pos] = lane % k;
+    P.perm_w[pos] = __ldcg(w + lane);
+    P.inv[lane] = pos;
+  }
+}
+
 constexpr int kPlanThreads = 256;
 
 size_t plan_smem_bytes(int E) {
@@ -413,30 +741,40 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a) {
   const int e = blockIdx.x;
   const int H = a.H, E = a.E, T = a.T;
   const float* wrow = a.w + static_cast<size_t>(e) * H;
-  const int nterm = (H + kRouteThreads - 1) / kRouteThreads;
+  const int nterm = 4 * ((H / 4 + kRouteThreads - 1) / kRouteThreads);  // terms per thread
 
   for (int t0 = 0; t0 < T; t0 += kRouteTB) {
     float s[kRouteTB], c[kRouteTB], ab[kRouteTB];
 #pragma unroll
     for (int i = 0; i < kRouteTB; ++i) s[i] = c[i] = ab[i] = 0.f;
-    for (int kk = tid; kk < H; kk += kRouteThreads) {
-      const float wv = __ldg(wrow + kk);
+    // four consecutive weights per load; the unrolled loop issues every
+    // load of the row before the first product
+    const int nvec = H >> 2;
+#pragma unroll 4
+    for (int v = tid; v < nvec; v += kRouteThreads) {
+      const float4 w4 = __ldg(reinterpret_cast<const float4*>(wrow) + v);
+      const float wv[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
       for (int i = 0; i < kRouteTB; ++i) {
         if (t0 + i < T) {
-          const float xv = load_x<XT>(a.x, static_cast<size_t>(t0 + i) * H + kk);
-          const float p = __fmul_rn(xv, wv);
-          const float ep = fmaf(xv, wv, -p);  // exact low part of the product
-          float ns, es;
-          two_sum(s[i], p, ns, es);
-          s[i] = ns;
-          c[i] = __fadd_rn(c[i], __fadd_rn(ep, es));
-          ab[i] = fmaf(fabsf(xv), fabsf(wv), ab[i]);
+          float xv[4];
+          load_x4<XT>(a.x, static_cast<size_t>(t0 + i) * H + 4 * v, xv);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float p = __fmul_rn(xv[j], wv[j]);
+            const float ep = fmaf(xv[j], wv[j], -p);  // exact low part of the product
+            float ns, es;
+            two_sum(s[i], p, ns, es);
+            s[i] = ns;
+            c[i] = __fadd_rn(c[i], __fadd_rn(ep, es));
+            ab[i] = fmaf(fabsf(xv[j]), fabsf(wv[j]), ab[i]);
+          }
         }
       }
     }
 #pragma unroll
     for (int i = 0; i < kRouteTB; ++i) {
+      if (t0 + i >= T) continue;  // uniform across the block
       for (int off = 16; off; off >>= 1) {
         const float s2 = __shfl_xor_sync(0xffffffffu, s[i], off);
         const float c2 = __shfl_xor_sync(0xffffffffu, c[i], off);
@@ -471,9 +809,16 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a) {
       const double Du = static_cast<double>(nterm + 5 + 3 + 2) * 0x1p-24;
       const double bnd = Du * Du * (1.0 + 2.0 * Du) * 1.01 * static_cast<double>(AB) +
                          fabs(l) * 0x1p-51 + static_cast<double>(H + 1) * 0x1p-140;
+      // interval keys, rounded outward; widened by 2^-50 |l| so that
+      // disjoint intervals also separate the correctly rounded fp64 images
+      const double wid = __dadd_ru(bnd, __dmul_ru(fabs(l), 0x1p-50));
+      const double lower = __dsub_rd(l, wid), upper = __dadd_ru(l, wid);
       const size_t o = static_cast<size_t>(t0 + tid) * E + e;
-      a.l_est[o] = l;
-      a.l_bnd[o] = isfinite(bnd) ? bnd : INFINITY;
+      const size_t te = static_cast<size_t>(T) * E;
+      const bool fin = isfinite(l) && isfinite(wid);
+      a.keys[o] = okey(l);
+      a.keys[te + o] = fin ? okey(lower) : 0ull;
+      a.keys[2 * te + o] = fin ? okey(upper) : ~0ull;
     }
     __syncthreads();
   }
@@ -487,12 +832,14 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a) {
   if (tid == 0) s_nflag = 0;
   __syncthreads();
   int sel[16];
+  unsigned long long selk[16];
+  const size_t te = static_cast<size_t>(T) * E;
   for (int t = warp; t < T; t += kRouteWarps) {
-    const double* l = a.l_est + static_cast<size_t>(t) * E;
-    const double* b = a.l_bnd + static_cast<size_t>(t) * E;
-    bool ok = warp_select(l, b, E, a.k, sel, true);
+    const size_t o = static_cast<size_t>(t) * E;
+    const TokenKeys K{a.keys + o, a.keys + te + o, a.keys + 2 * te + o};
+    const bool ok = warp_select(K, E, a.k, sel, selk, true);
     if (ok) {
-      warp_write_selection(l, sel, a.k, a.topk_idx + static_cast<size_t>(t) * a.k,
+      warp_write_selection(sel, selk, a.k, a.topk_idx + static_cast<size_t>(t) * a.k,
                            a.topk_w + static_cast<size_t>(t) * a.k);
     } else if (lane == 0) {
       s_flagged[atomicAdd(&s_nflag, 1)] = t;
@@ -509,30 +856,43 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a) {
                                             a.w + static_cast<size_t>(ee) * H, H, a.bias, ee, v);
       if (lane == 0) {
         if (!fin) atomicOr(a.err, MOE_DEVERR_NONFINITE);
-        a.l_est[static_cast<size_t>(t) * E + ee] = v;
-        a.l_bnd[static_cast<size_t>(t) * E + ee] = 0.0;
+        const size_t o = static_cast<size_t>(t) * E + ee;
+        a.keys[o] = a.keys[te + o] = a.keys[2 * te + o] = okey(v);
       }
     }
   }
   __syncthreads();
   for (int fi = warp; fi < nflag; fi += kRouteWarps) {
     const int t = s_flagged[fi];
-    const double* l = a.l_est + static_cast<size_t>(t) * E;
-    warp_select(l, nullptr, E, a.k, sel, false);
-    warp_write_selection(l, sel, a.k, a.topk_idx + static_cast<size_t>(t) * a.k,
+    const size_t o = static_cast<size_t>(t) * E;
+    const TokenKeys K{a.keys + o, a.keys + te + o, a.keys + 2 * te + o};
+    warp_select(K, E, a.k, sel, selk, false);
+    warp_write_selection(sel, selk, a.k, a.topk_idx + static_cast<size_t>(t) * a.k,
                          a.topk_w + static_cast<size_t>(t) * a.k);
     if (lane == 0) atomicAdd(a.repairs, 1ull);
   }
   if (a.plan.counts != nullptr) {
     __syncthreads();
-    plan_block<kRouteThreads>(a.topk_idx, a.topk_w, T * a.k, a.k, E, a.plan, dyn_smem, a.err);
+    if (T * a.k <= 32) {
+      if (warp == 0) plan_warp(a.topk_idx, a.topk_w, T * a.k, a.k, E, a.plan, dyn_smem, a.err);
+    } else {
+      plan_block<kRouteThreads>(a.topk_idx, a.topk_w, T * a.k, a.k, E, a.plan, dyn_smem, a.err);
+    }
+    if (a.admit.enabled) {
+      __syncthreads();
+      if (warp == 0) admit_warp(a.admit, a.plan, reinterpret_cast<unsigned char*>(dyn_smem), a.err);
+    }
   }
   if (tid == 0) *a.ticket = 0u;
 }
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
   extern __shared__ int dyn_smem[];
-  plan_block<kPlanThreads>(a.idx, a.w, a.T * a.k, a.k, a.E, a.plan, dyn_smem, a.err);
+  if (a.T * a.k <= 32) {
+    if (threadIdx.x < 32) plan_warp(a.idx, a.w, a.T * a.k, a.k, a.E, a.plan, dyn_smem, a.err);
+  } else {
+    plan_block<kPlanThreads>(a.idx, a.w, a.T * a.k, a.k, a.E, a.plan, dyn_smem, a.err);
+  }
 }
 
 }  // namespace
@@ -540,7 +900,17 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
 cudaError_t launch_route(const RouteArgs& a, int num_sms, cudaStream_t st) {
   (void)num_sms;
   if (a.T < 1 || a.T > kRouteMaxT || a.k > 16 || a.E > 1024) return cudaErrorInvalidValue;
-  const size_t smem = a.plan.counts ? plan_smem_bytes(a.E) : 0;
+  size_t smem = a.plan.counts ? plan_smem_bytes(a.E) : 0;
+  if (a.admit.enabled)
+    smem = std::max(smem, admit_smem_bytes(a.E, a.admit.S, std::min(a.E, a.T * a.k)));
+  if (smem > 48 * 1024) {
+    cudaError_t e = a.xt == MOE_BF16
+        ? cudaFuncSetAttribute(route_kernel<MOE_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(smem))
+        : cudaFuncSetAttribute(route_kernel<MOE_F32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
   if (a.xt == MOE_BF16)
     route_kernel<MOE_BF16><<<a.E, kRouteThreads, smem, st>>>(a);
   else
@@ -562,17 +932,17 @@ cudaError_t launch_plan(const PlanArgs& a, cudaStream_t st) {
 // CUDA graph where an allocation would break the capture. Its scratch (fast
 // logits, their bounds, the last-block counter, the repair counter and an
 // error word) lives in one file-scope device array below, sized for at most
-// kNoAllocMaxTE = 16384 (token, expert) logits (256 KiB of logits and bounds);
+// kNoAllocMaxTE = 8192 (token, expert) logits (192 KiB of logit and bound keys);
 // every GPU that loads this library holds that array until the process exits.
 namespace moe {
 namespace {
 
-constexpr int kNoAllocMaxTE = 16384;
+constexpr int kNoAllocMaxTE = 8192;
 constexpr int kNoAllocMaxDevices = 64;
 
-// [0, TE) fast logits, [TE, 2 TE) bounds, then a 32-byte header:
+// [0, 3 TE) logit, lower-bound and upper-bound keys, then a 32-byte header:
 // ticket (u32), error word (u32), repaired-token counter (u64).
-static __device__ __align__(256) double g_route_scratch[2 * kNoAllocMaxTE + 4];
+static __device__ __align__(256) unsigned long long g_route_scratch[3 * kNoAllocMaxTE + 4];
 
 std::mutex g_noalloc_mu;
 void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
@@ -593,9 +963,13 @@ extern "C" moe_status_t moe_route_noalloc(const void* x, int32_t xt, int32_t T, 
     set_thread_error("moe_route_noalloc: activation dtype must be MOE_F32 or MOE_BF16");
     return MOE_ERR_ARG;
   }
-  if (T < 1 || T > kRouteMaxT || H < 1 || E < 1 || E > 1024 || k < 1 || k > 16 || k > E) {
-    set_thread_error("moe_route_noalloc: need 1 <= T <= 64, H >= 1, 1 <= E <= 1024, "
-                     "1 <= k <= min(16, E)");
+  if (T < 1 || T > kRouteMaxT || H < 4 || H % 4 || E < 1 || E > 1024 || k < 1 || k > 16 || k > E) {
+    set_thread_error("moe_route_noalloc: need 1 <= T <= 64, H a positive multiple of 4, "
+                     "1 <= E <= 1024, 1 <= k <= min(16, E)");
+    return MOE_ERR_ARG;
+  }
+  if (reinterpret_cast<uintptr_t>(x) % 16 || reinterpret_cast<uintptr_t>(w_router) % 16) {
+    set_thread_error("moe_route_noalloc: x and w_router must be 16-byte aligned");
     return MOE_ERR_ARG;
   }
   if (static_cast<int64_t>(T) * E > kNoAllocMaxTE) {
@@ -626,9 +1000,8 @@ extern "C" moe_status_t moe_route_noalloc(const void* x, int32_t xt, int32_t T, 
     }
     base = g_noalloc_ptr[dev];
   }
-  double* scratch = static_cast<double*>(base);
-  const size_t te = static_cast<size_t>(T) * E;
-  unsigned char* header = reinterpret_cast<unsigned char*>(scratch + 2 * kNoAllocMaxTE);
+  unsigned long long* scratch = static_cast<unsigned long long*>(base);
+  unsigned char* header = reinterpret_cast<unsigned char*>(scratch + 3 * kNoAllocMaxTE);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   // the counter and flags must start at zero; the array keeps the last call's contents
   e = cudaMemsetAsync(header, 0, 32, st);
@@ -647,8 +1020,7 @@ extern "C" moe_status_t moe_route_noalloc(const void* x, int32_t xt, int32_t T, 
   a.bias = bias;
   a.topk_idx = topk_idx;
   a.topk_w = topk_w;
-  a.l_est = scratch;
-  a.l_bnd = scratch + te;
+  a.keys = scratch;
   a.ticket = reinterpret_cast<unsigned int*>(header);
   a.err = reinterpret_cast<uint32_t*>(header + 4);
   a.repairs = reinterpret_cast<unsigned long long*>(header + 8);

@@ -215,6 +215,10 @@ moe_status_t slots_evict(moe_slots* s, int32_t e, std::string* err) {
 }
 
 const int32_t* slots_pt(const moe_slots* s) { return s->pt.data(); }
+const int32_t* slots_owner(const moe_slots* s) { return s->owner.data(); }
+const uint64_t* slots_last(const moe_slots* s) { return s->last.data(); }
+uint64_t slots_tick(const moe_slots* s) { return s->tick; }
+uint64_t slots_rng(const moe_slots* s) { return s->rng; }
 const uint32_t* slots_gen(const moe_slots* s) { return s->gen.data(); }
 moe_stats_t slots_stats(const moe_slots* s) { return s->stats; }
 

@@ -80,6 +80,8 @@ typedef struct {
   uint64_t seed;           /* random-eviction seed */
   int64_t tile_bytes;      /* staging tile size, multiple of 16 (262144 in [NfE] §5.4) */
   int32_t max_tokens;      /* largest T of any call on this context */
+  int32_t admit_on_device; /* 0: host slot manager (admit syncs the stream);
+                              1: admission and staging on the GPU, no host sync */
 } moe_config_t;
 
 /* Expert-major plan ([NfE] §5.3, §5.5). Device arrays owned by the caller.
@@ -161,7 +163,7 @@ moe_status_t moe_bind_shared(moe_ctx_t* ctx, int32_t layer, const void* dev_shar
 
 /* Router + top-k ([NfE] §3.1 authoritative routing; [RT] §3.1 top-eight).
  * x: device [T,H] (xt = MOE_F32 or MOE_BF16); w_router: device fp32 [E,H];
- * bias: device fp32 [E] or NULL. Writes topk_idx int32 [T,k] (descending
+ * both 16-byte aligned (MOE_ERR_ARG otherwise); bias: device fp32 [E] or NULL. Writes topk_idx int32 [T,k] (descending
  * logit, ties to the lower id) and topk_w fp32 [T,k] (softmax over the k
  * selected logits). The selection equals the one made on the correctly
  * rounded exact logits sum_i x_i*w_i (+b): fast fp32-pair logits carry an
@@ -181,10 +183,11 @@ moe_status_t moe_route(moe_ctx_t* ctx, int32_t layer, const void* x, int32_t xt,
  * or NULL) and the outputs topk_idx (int32 [T,k]) and topk_w (fp32 [T,k]);
  * the selection and weights are those of moe_route.
  * Scratch: one static device array inside the library, sized for
- * T*E <= 16384 logits (about 256 KiB), which every GPU that loads the library
- * holds until the process exits. Limits: 1 <= T <= 64, 1 <= E <= 1024,
- * 1 <= k <= min(16, E), T*E <= 16384; anything larger returns MOE_ERR_ARG
- * with a message in moe_last_error(NULL) and launches nothing.
+ * T*E <= 8192 logits (about 192 KiB), which every GPU that loads the library
+ * holds until the process exits. Limits: 1 <= T <= 64, H a multiple of 4,
+ * 1 <= E <= 1024, 1 <= k <= min(16, E), T*E <= 8192, x and w_router 16-byte
+ * aligned; anything else returns MOE_ERR_ARG with a message in
+ * moe_last_error(NULL) and launches nothing.
  * The first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before any stream
  * capture. No call allocates (no cudaMalloc, cudaFree or allocating library
@@ -275,7 +278,8 @@ moe_status_t moe_read_slot(moe_ctx_t* ctx, int32_t layer, int32_t slot, void* ho
 /* Kernel timing (tracing aid). While enabled, the context records CUDA
  * events on the launching stream around every kernel it launches.
  * moe_get_kernel_times synchronises those events and returns, per kind
- * (route incl. fused plan, standalone plan, FFN gate/up, FFN down), the
+ * (route incl. fused plan and on-device admission, standalone plan, FFN
+ * gate/up, FFN down, on-device staging copy), the
  * summed device milliseconds and the launch count since the last call, then
  * resets them. Either output may be NULL. */
 typedef enum {
@@ -283,14 +287,16 @@ typedef enum {
   MOE_KT_PLAN = 1,
   MOE_KT_GATEUP = 2,
   MOE_KT_DOWN = 3,
-  MOE_KT_COUNT = 4
+  MOE_KT_STAGE = 4,
+  MOE_KT_COUNT = 5
 } moe_kernel_kind_t;
 moe_status_t moe_set_kernel_timing(moe_ctx_t* ctx, int32_t enable);
 moe_status_t moe_get_kernel_times(moe_ctx_t* ctx, double* ms, int64_t* launches);
 
 /* Test hooks for fail-closed paths, all on the host side: make the next
- * moe_stage_tiles fail after `fail_after_tiles` tiles (-1 = off), or set a
- * layer's device page-table generation for an expert to a wrong value. */
+ * moe_stage_tiles fail after `fail_after_tiles` tiles (-1 = off), or change
+ * the published generation of the slot holding a resident expert so that it
+ * no longer matches the page-table entry. */
 moe_status_t moe_debug_fail_staging_after(moe_ctx_t* ctx, int32_t fail_after_tiles);
 moe_status_t moe_debug_corrupt_generation(moe_ctx_t* ctx, int32_t layer, int32_t expert);
 

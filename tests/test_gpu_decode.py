@@ -99,7 +99,7 @@ def test_plan_matches_oracle(bec):
 
 
 def _run_trace(bec, w, layers, steps, ffn_steps, policy=None, seed=0, tile_bytes=262144,
-               slots=None, preload=False, check_every_step=True):
+               slots=None, preload=False, check_every_step=True, device_admit=False):
     """Run layer_forward for every (step, layer) on the GPU and replay the
     same trace in the oracle; compare bit-exact state each step and outputs on
     ffn_steps. Returns the GPU outputs {(layer, step): y}."""
@@ -107,7 +107,8 @@ def _run_trace(bec, w, layers, steps, ffn_steps, policy=None, seed=0, tile_bytes
     store = pinned_store(w, layers)
     pol = w.policy if policy is None else policy
     S = slots or w.slots
-    ctx = make_context(bec, w, layers, policy=pol, slots=S, seed=seed, tile_bytes=tile_bytes)
+    ctx = make_context(bec, w, layers, policy=pol, slots=S, seed=seed, tile_bytes=tile_bytes,
+                       device_admit=device_admit)
     keep = bind_all(ctx, w, layers, store)
     experts = ExpertCache(w)
     plan = bec.Plan(w.n_experts, w.top_k, T)
@@ -155,31 +156,46 @@ def _run_trace(bec, w, layers, steps, ffn_steps, policy=None, seed=0, tile_bytes
     return outs
 
 
-def test_layer_tiny_trace(bec):
+@pytest.mark.parametrize("device_admit", [False, True])
+def test_layer_tiny_trace(bec, device_admit):
     w = W.with_changes(W.WORKLOADS["tiny"], n_steps=16)
-    _run_trace(bec, w, 1, 16, set(range(16)))
+    _run_trace(bec, w, 1, 16, set(range(16)), device_admit=device_admit)
 
 
-def test_layer_decode_full_size(bec):
+@pytest.mark.parametrize("device_admit", [False, True])
+def test_layer_decode_full_size(bec, device_admit):
     w = W.WORKLOADS["decode"]
-    _run_trace(bec, w, 2, 24, {0, 5, 23})
+    _run_trace(bec, w, 2, 24, {0, 5, 23}, device_admit=device_admit)
 
 
+@pytest.mark.parametrize("device_admit", [False, True])
 @pytest.mark.parametrize("policy,seed", [(0, 0), (1, 0), (1, 3)])
-def test_layer_mtp_decode_q4(bec, policy, seed):
+def test_layer_mtp_decode_q4(bec, policy, seed, device_admit):
     w = W.with_changes(W.WORKLOADS["mtp_decode"], slots=40)  # >= T*k, small enough to evict
-    _run_trace(bec, w, 1, 14, {0, 13}, policy=policy, seed=seed)
+    _run_trace(bec, w, 1, 14, {0, 13}, policy=policy, seed=seed, device_admit=device_admit)
+
+
+def test_layer_decode_long_trace_device_admission(bec):
+    # the whole 128-step trace of one layer, cache state bit-exact every step
+    w = W.WORKLOADS["decode"]
+    _run_trace(bec, w, 1, 128, {127}, device_admit=True)
 
 
 def test_cache_transparency_bitwise(bec):
-    # outputs must not depend on cache state, eviction policy or tile size
+    # outputs must not depend on cache state, eviction policy, tile size or
+    # where admission runs
     w = W.with_changes(W.WORKLOADS["decode"], n_layers=1)
     a = _run_trace(bec, w, 1, 8, set(), policy=0, check_every_step=False)
     b = _run_trace(bec, w, 1, 8, set(), policy=1, seed=4, check_every_step=False)
     c = _run_trace(bec, w, 1, 8, set(), slots=w.n_experts, preload=True, tile_bytes=4096,
                    check_every_step=False)
+    d = _run_trace(bec, w, 1, 8, set(), policy=1, seed=2, check_every_step=False,
+                   device_admit=True)
+    e = _run_trace(bec, w, 1, 8, set(), slots=w.n_experts, preload=True, tile_bytes=8192,
+                   check_every_step=False, device_admit=True)
     for key in a:
-        assert np.array_equal(a[key], b[key]) and np.array_equal(a[key], c[key]), key
+        for other in (b, c, d, e):
+            assert np.array_equal(a[key], other[key]), key
 
 
 def test_staged_slot_bytes_equal_store(bec):
@@ -202,6 +218,30 @@ def test_staged_slot_bytes_equal_store(bec):
             got = np.frombuffer(ctx.read_slot(0, s), dtype=np.uint8)
             assert np.array_equal(got, store[0, e].numpy()), (tile, e)
         ctx.close()
+
+
+def test_fail_closed_stale_generation_device_admission(bec):
+    w = W.with_changes(W.WORKLOADS["tiny"], n_steps=2)
+    store = pinned_store(w, 1)
+    ctx = make_context(bec, w, 1, device_admit=True)
+    bind_all(ctx, w, 1, store)
+    plan = bec.Plan(w.n_experts, w.top_k, 4)
+    x = x_to_torch(w, W.activations(w, 0, 4))
+    Wr = torch.from_numpy(W.router_weights(w, 0)).cuda()
+    idx = torch.empty((4, 2), dtype=torch.int32, device="cuda")
+    wt = torch.empty((4, 2), device="cuda")
+    y = torch.empty((4, w.hidden), device="cuda")
+    ctx.layer_forward(0, x, Wr, None, idx, wt, plan, y)
+    ctx.check_device_errors()
+    with pytest.raises(bec.MoeError):
+        ctx.cache_admit(0, plan)  # host admission is refused on this context
+    e0 = int(idx[0, 0].item())
+    ctx.debug_corrupt_generation(0, e0)
+    ctx.expert_ffn(0, x, plan, y)
+    with pytest.raises(bec.MoeError) as ei:
+        ctx.check_device_errors()
+    assert ei.value.status == 4
+    ctx.close()
 
 
 def test_fail_closed_on_failed_staging_and_stale_generation(bec):
