@@ -140,6 +140,7 @@ extern "C" void moe_destroy(moe_ctx_t* ctx) {
   cudaFree(ctx->d_stats);
   cudaFree(ctx->d_fills);
   cudaFree(ctx->d_done);
+  cudaFree(ctx->d_ffn_ticket);
   cudaFreeHost(ctx->h_units);
   cudaFreeHost(ctx->h_pt);
   cudaFreeHost(ctx->h_ptgen);
@@ -170,7 +171,7 @@ extern "C" moe_status_t moe_create(const moe_config_t* cfg, moe_ctx_t** out) {
   else if (c.n_streams < 1 || c.n_streams > 8) why = "n_streams outside 1..8";
   else if (c.tile_bytes < 16 || c.tile_bytes % 16) why = "tile_bytes not a positive multiple of 16";
   else if (c.max_tokens < 1) why = "max_tokens < 1";
-  else if (c.admit_on_device != 0 && c.admit_on_device != 1) why = "admit_on_device must be 0 or 1";
+  else if (c.admit_on_device < 0 || c.admit_on_device > 2) why = "admit_on_device must be 0, 1 or 2";
   if (!why.empty()) {
     g_create_err = "moe_create: " + why;
     return MOE_ERR_ARG;
@@ -229,7 +230,10 @@ extern "C" moe_status_t moe_create(const moe_config_t* cfg, moe_ctx_t** out) {
   CKC(cudaMalloc(&ctx->d_units, sizeof(int32_t) * unit_ints));
   CKC(cudaMemset(ctx->d_units, 0, sizeof(int32_t) * unit_ints));
   CKC(cudaHostAlloc(&ctx->h_units, sizeof(int32_t) * unit_ints, cudaHostAllocDefault));
-  ctx->dev_admit = c.admit_on_device == 1;
+  ctx->dev_admit = c.admit_on_device >= 1;
+  ctx->read_through = c.admit_on_device == 2;
+  CKC(cudaMalloc(&ctx->d_ffn_ticket, sizeof(unsigned int)));
+  CKC(cudaMemset(ctx->d_ffn_ticket, 0, sizeof(unsigned int)));
   if (ctx->dev_admit) {
     ctx->max_fills = std::min(E, std::min(c.max_tokens, 64) * c.top_k);
     CKC(cudaMalloc(&ctx->d_owner, sizeof(int32_t) * L * S));
@@ -362,6 +366,7 @@ static moe_status_t route_impl(moe_ctx_t* ctx, int32_t layer, const void* x, int
   if (plan) a.plan = *plan;
   if (admit) {
     a.admit.enabled = 1;
+    a.admit.read_through = ctx->read_through ? 1 : 0;
     a.admit.E = ctx->cfg.n_experts;
     a.admit.S = ctx->cfg.slots_per_layer;
     a.admit.policy = ctx->cfg.policy;
@@ -660,6 +665,18 @@ extern "C" moe_status_t moe_expert_ffn(moe_ctx_t* ctx, int32_t layer, const void
   a.slot_stride = ctx->slot_stride;
   a.units = ctx->d_units;
   a.gen = ctx->d_gen + static_cast<size_t>(layer) * S;
+  if (ctx->read_through) {
+    if (!ctx->store_dev) return fail(ctx, MOE_ERR_STATE, "ffn: no store bound");
+    a.store = ctx->store_dev + static_cast<size_t>(layer) * E * ctx->geom.bytes;
+    a.payload = ctx->geom.bytes;
+    a.sgen = ctx->d_sgen + static_cast<size_t>(layer) * S;
+    a.ticket = ctx->d_ffn_ticket;
+    a.stats = ctx->d_stats + static_cast<size_t>(layer) * moe::kStatCount;
+    a.tiles_per_expert = 0;
+    for (int m = 0; m < 3; ++m)
+      a.tiles_per_expert += static_cast<int>((ctx->geom.qbytes[m] + ctx->geom.sbytes[m] +
+                                              ctx->cfg.tile_bytes - 1) / ctx->cfg.tile_bytes);
+  }
   a.S = S;
   a.shared = ctx->shared[layer];
   a.g = ctx->geom;
@@ -694,6 +711,8 @@ extern "C" moe_status_t moe_layer_forward(moe_ctx_t* ctx, int32_t layer, const v
     if (!ctx->store_dev) return fail(ctx, MOE_ERR_STATE, "layer_forward: no store bound");
     moe_status_t s = route_impl(ctx, layer, x, xt, T, w_router, bias, topk_idx, topk_w, plan, st, true);
     if (s != MOE_OK) return s;
+    if (ctx->read_through)  // misses are materialised by the FFN as it reads them
+      return moe_expert_ffn(ctx, layer, x, xt, T, plan, y, MOE_MODE_AUTO, stream);
     const moe::ExpertGeom& g = ctx->geom;
     moe::StageArgs sa{};
     const size_t E = ctx->cfg.n_experts, S = ctx->cfg.slots_per_layer;

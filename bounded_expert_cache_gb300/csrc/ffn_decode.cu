@@ -80,6 +80,22 @@ __device__ __forceinline__ float ld_scale(const uint8_t* p) {
   return __half2float(__ushort_as_half(b));
 }
 
+// Loads from a miss's source: the pinned store, read over the host link.
+__device__ __forceinline__ uint4 ld_host(const void* p) {
+  return __ldcs(reinterpret_cast<const uint4*>(p));
+}
+__device__ __forceinline__ float ld_scale_host(const uint8_t* p) {
+  const unsigned short b = __ldcs(reinterpret_cast<const unsigned short*>(p));
+  return __half2float(__ushort_as_half(b));
+}
+
+// Copy one row of fp16 scales (n of them) from a miss's source to its slot.
+__device__ __forceinline__ void copy_scale_row(const uint8_t* src, uint8_t* dst, int n, int lane) {
+  const unsigned short* s = reinterpret_cast<const unsigned short*>(src);
+  unsigned short* d = reinterpret_cast<unsigned short*>(dst);
+  for (int i = lane; i < n; i += 32) d[i] = __ldcs(s + i);
+}
+
 // q (Q8_0 byte) -> float, exact: bits 0x4B0000uu = 2^23 + uu with uu = q + 128.
 __device__ __forceinline__ float q8_to_f(uint32_t biased, int b) {
   return __uint_as_float(__byte_perm(biased, 0x4B000000u, 0x7540u | b)) - 8388736.0f;
@@ -126,6 +142,8 @@ struct UnitRef {
   int p0;               // first expert-major assignment (routed) or -1 (shared)
   int slot;             // slot (routed) or -1 (shared)
   uint32_t egen;        // generation the slot must hold
+  bool miss;            // materialised by this step: read from the store, write to dst
+  uint8_t* dst;         // slot payload being filled (miss only)
 };
 
 // Unit u of the step's unit table: routed experts of the union (in union
@@ -134,15 +152,25 @@ struct UnitRef {
 __device__ __forceinline__ UnitRef resolve_unit(const FfnArgs& a, int u) {
   const int4 d = __ldg(reinterpret_cast<const int4*>(a.units + kUnitHeader) + u);
   UnitRef r;
-  r.slot = d.x;
+  r.miss = d.x <= -2;
+  r.slot = r.miss ? -2 - d.x : d.x;
   r.p0 = d.y;
   r.M = d.z;
   r.egen = static_cast<uint32_t>(d.w);
-  const bool routed = d.x >= 0;
+  const bool routed = r.slot >= 0;
+  const bool in_range = r.slot < a.S && (!r.miss || (a.store && d.w >= 0 && d.w < a.E));
   // an out-of-range slot or a missing shared payload points at slot 0 (always
   // mapped) and is refused by unit_ok, so no load leaves the pool
-  r.base = routed ? a.pool + static_cast<int64_t>(d.x < a.S ? d.x : 0) * a.slot_stride
-                  : (a.shared ? a.shared : a.pool);
+  const int64_t slot_off = static_cast<int64_t>(routed && in_range ? r.slot : 0) * a.slot_stride;
+  if (r.miss && in_range) {
+    r.base = a.store + static_cast<int64_t>(d.w) * a.payload;
+    r.dst = a.pool + slot_off;
+  } else {
+    r.base = routed ? a.pool + slot_off : (a.shared ? a.shared : a.pool);
+    r.dst = nullptr;
+    r.miss = false;
+    if (d.x <= -2) r.slot = a.S;  // refused below
+  }
 #pragma unroll
   for (int m = 0; m < 3; ++m) {
     r.qoff[m] = routed ? a.g.qoff[m] : a.gs.qoff[m];
@@ -155,6 +183,7 @@ __device__ __forceinline__ UnitRef resolve_unit(const FfnArgs& a, int u) {
 // table expects (every tile of its last fill has landed); the shared expert
 // always is.
 __device__ __forceinline__ bool unit_ok(const FfnArgs& a, const UnitRef& U) {
+  if (U.miss) return true;
   if (U.slot < 0) return a.shared != nullptr;
   return U.slot < a.S && __ldg(a.gen + U.slot) == U.egen;
 }
@@ -201,6 +230,14 @@ __global__ void __launch_bounds__(kThreads) gateup_kernel(FfnArgs a) {
         s[m * kRowsPerItem + r] = U.base + U.soff[m] + static_cast<int64_t>(r0 + r) * sc_row;
       }
     }
+    if (U.miss) {
+#pragma unroll
+      for (int r = 0; r < kRowsPerItem; ++r)
+#pragma unroll
+        for (int m = 0; m < 2; ++m)
+          copy_scale_row(s[m * kRowsPerItem + r], U.dst + U.soff[m] + static_cast<int64_t>(r0 + r) * sc_row,
+                         H / 32, lane);
+    }
     for (int m0 = 0; m0 < U.M; m0 += TM) {
       const int mcount = min(TM, U.M - m0);
       int tok[TM];
@@ -216,10 +253,23 @@ __global__ void __launch_bounds__(kThreads) gateup_kernel(FfnArgs a) {
       for (int c = lane; c < nch; c += 32) {
         uint4 w[2 * kRowsPerItem];
         float d[2 * kRowsPerItem];
+        if (U.miss) {
 #pragma unroll
-        for (int r = 0; r < 2 * kRowsPerItem; ++r) {
-          w[r] = ldg_stream(q[r] + c * 16);
-          d[r] = ld_scale(s[r] + (Q == MOE_Q8_0 ? (c >> 1) : c) * 2);
+          for (int r = 0; r < 2 * kRowsPerItem; ++r) {
+            w[r] = ld_host(q[r] + c * 16);
+            d[r] = ld_scale_host(s[r] + (Q == MOE_Q8_0 ? (c >> 1) : c) * 2);
+          }
+          if (m0 == 0) {
+#pragma unroll
+            for (int r = 0; r < 2 * kRowsPerItem; ++r)
+              *reinterpret_cast<uint4*>(U.dst + (q[r] - U.base) + c * 16) = w[r];
+          }
+        } else {
+#pragma unroll
+          for (int r = 0; r < 2 * kRowsPerItem; ++r) {
+            w[r] = ldg_stream(q[r] + c * 16);
+            d[r] = ld_scale(s[r] + (Q == MOE_Q8_0 ? (c >> 1) : c) * 2);
+          }
         }
 #pragma unroll
         for (int m = 0; m < TM; ++m) {
@@ -311,6 +361,8 @@ __global__ void __launch_bounds__(kThreads) down_kernel(FfnArgs a) {
         rv[r] = o < a.H;
         q[r] = U.base + U.qoff[2] + static_cast<int64_t>(rv[r] ? o : 0) * rowbytes;
         s[r] = U.base + U.soff[2] + static_cast<int64_t>(rv[r] ? o : 0) * sc_row;
+        if (U.miss && rv[r])
+          copy_scale_row(s[r], U.dst + (s[r] - U.base), K / 32, lane);
       }
       for (int m0 = 0; m0 < U.M; m0 += TM) {
         const int mcount = min(TM, U.M - m0);
@@ -343,10 +395,19 @@ __global__ void __launch_bounds__(kThreads) down_kernel(FfnArgs a) {
         for (int c = lane; c < nch; c += 32) {
           uint4 w[kRowsPerItem];
           float d[kRowsPerItem];
+          if (U.miss) {
 #pragma unroll
-          for (int r = 0; r < kRowsPerItem; ++r) {
-            w[r] = rv[r] ? ldg_stream(q[r] + c * 16) : make_uint4(0, 0, 0, 0);
-            d[r] = rv[r] ? ld_scale(s[r] + (Q == MOE_Q8_0 ? (c >> 1) : c) * 2) : 0.f;
+            for (int r = 0; r < kRowsPerItem; ++r) {
+              w[r] = rv[r] ? ld_host(q[r] + c * 16) : make_uint4(0, 0, 0, 0);
+              d[r] = rv[r] ? ld_scale_host(s[r] + (Q == MOE_Q8_0 ? (c >> 1) : c) * 2) : 0.f;
+              if (rv[r] && m0 == 0) *reinterpret_cast<uint4*>(U.dst + (q[r] - U.base) + c * 16) = w[r];
+            }
+          } else {
+#pragma unroll
+            for (int r = 0; r < kRowsPerItem; ++r) {
+              w[r] = rv[r] ? ldg_stream(q[r] + c * 16) : make_uint4(0, 0, 0, 0);
+              d[r] = rv[r] ? ld_scale(s[r] + (Q == MOE_Q8_0 ? (c >> 1) : c) * 2) : 0.f;
+            }
           }
 #pragma unroll
           for (int m = 0; m < TM; ++m) {
@@ -412,6 +473,34 @@ __global__ void __launch_bounds__(kThreads) down_kernel(FfnArgs a) {
     float v = 0.f;
     for (int u = 0; u < units; ++u) v += part[((u * kPairs + rp) * kRowsPerItem + rr) * TM + t];
     a.y[static_cast<int64_t>(t) * a.H + o] = v;
+  }
+  if (a.store) {
+    // read-through: once every block has written its rows, the misses' slots
+    // are complete; the last block publishes their generations
+    __shared__ unsigned int s_ticket;
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_ticket = atomicAdd(a.ticket, 1u);
+    __syncthreads();
+    if (s_ticket == gridDim.x - 1) {
+      __threadfence();
+      int nmiss = 0;
+      for (int u = tid; u < units; u += kThreads) {
+        const int sl = __ldg(a.units + kUnitHeader + kUnitInts * u);
+        if (sl <= -2 && -2 - sl < a.S) {
+          a.gen[-2 - sl] = __ldcg(a.sgen + (-2 - sl));
+          ++nmiss;
+        }
+      }
+      for (int off = 16; off; off >>= 1) nmiss += __shfl_xor_sync(0xffffffffu, nmiss, off);
+      if (lane == 0 && nmiss) {
+        atomicAdd(reinterpret_cast<unsigned long long*>(a.stats + kStatTiles),
+                  static_cast<unsigned long long>(nmiss) * a.tiles_per_expert);
+        atomicAdd(reinterpret_cast<unsigned long long*>(a.stats + kStatBytes),
+                  static_cast<unsigned long long>(nmiss) * a.payload);
+      }
+      if (tid == 0) *a.ticket = 0u;
+    }
   }
 }
 

@@ -64,15 +64,18 @@ enum { kStatSteps = 0, kStatHits, kStatMisses, kStatEvictions, kStatMaterialized
        kStatBytes, kStatCount = 8 };
 
 // Unit table read by the FFN kernels: int32 [kUnitHeader + 4 * max_units]:
-// count (then padding to 16 bytes), then per unit {slot (-1: shared expert),
-// p0 (first expert-major assignment, -1: shared), M (tokens), generation the
-// slot must hold}. Routed units come first, in union order.
+// count (then padding to 16 bytes), then per unit {slot, p0 (first
+// expert-major assignment, -1: shared), M (tokens), generation the slot must
+// hold}. slot -1 is the shared expert; slot <= -2 marks a miss that the FFN
+// materialises while reading it (slot -2 - s, and the 4th field holds the
+// expert id instead of a generation). Routed units come first, in union order.
 constexpr int kUnitHeader = 4;
 constexpr int kUnitInts = 4;
 
 // On-device admission, run by the router's last block after the plan.
 struct AdmitArgs {
   int enabled;
+  int read_through;  // misses are materialised by the FFN while it reads them
   int E, S, policy, has_shared, T;
   long long payload;
   DevCacheLayer c;
@@ -139,11 +142,18 @@ cudaError_t launch_stage_copy(const StageArgs& a, cudaStream_t st);
 struct FfnArgs {
   const void* x;
   int32_t xt, T, H, I, Is, k, E, quant;
-  const uint8_t* pool;        // slot pool of the layer
+  uint8_t* pool;              // slot pool of the layer (written by read-through misses)
   int64_t slot_stride;
   const int32_t* units;       // unit table of this step
-  const uint32_t* gen;        // [S] published slot generations
+  uint32_t* gen;              // [S] published slot generations
   int32_t S;
+  // read-through materialisation of misses (store == nullptr: off)
+  const uint8_t* store;       // device alias of the layer's pinned store [E][payload]
+  int64_t payload;
+  const uint32_t* sgen;       // [S] manager generations, published at the end
+  unsigned int* ticket;       // last-block counter of the down kernel
+  long long* stats;           // [kStatCount] of the layer
+  int tiles_per_expert;
   const uint8_t* shared;      // shared payload or nullptr
   ExpertGeom g, gs;           // routed and shared geometry
   moe_plan_t plan;
@@ -199,6 +209,8 @@ struct moe_ctx {
   int32_t* d_fills = nullptr;             // [1 + 2 * max_fills]
   unsigned int* d_done = nullptr;         // [max_fills]
   int32_t max_fills = 0;
+  bool read_through = false;              // misses materialised by the FFN
+  unsigned int* d_ffn_ticket = nullptr;
   std::vector<cudaStream_t> streams;
   std::vector<cudaEvent_t> ev_stage;
   cudaEvent_t ev_compute = nullptr;

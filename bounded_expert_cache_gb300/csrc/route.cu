@@ -613,7 +613,7 @@ __device__ void admit_warp(const AdmitArgs& A, const moe_plan_t& P, unsigned cha
       s_owner[slot] = e;
       s_sgen[slot] += 1u;
       s_last[slot] = tick;
-      upt[u] = slot;
+      upt[u] = -2 - slot;  // filled this step
       A.fills[1 + 2 * nfill] = e;
       A.fills[2 + 2 * nfill] = slot;
       A.done[nfill] = 0u;
@@ -629,17 +629,20 @@ __device__ void admit_warp(const AdmitArgs& A, const moe_plan_t& P, unsigned cha
   }
   long long assignments = 0;
   for (int u = lane; u < nu; u += 32) {
-    const int e = uq[u], slot = upt[u];
+    const int e = uq[u];
+    const bool was_miss = upt[u] <= -2;
+    const int slot = was_miss ? -2 - upt[u] : upt[u];
     const int cnt = __ldcg(P.counts + e);
     assignments += cnt;
     c.pt[e] = slot;
     c.ptgen[e] = s_sgen[slot];
     // unit table: routed units in union order, then the shared expert
     int* U = A.units + kUnitHeader + kUnitInts * u;
-    U[0] = slot;
+    const bool filled = A.read_through && was_miss;
+    U[0] = filled ? -2 - slot : slot;
     U[1] = __ldcg(P.offsets + e);
     U[2] = cnt;
-    U[3] = static_cast<int>(s_sgen[slot]);
+    U[3] = filled ? e : static_cast<int>(s_sgen[slot]);
   }
   for (int off = 16; off; off >>= 1) assignments += __shfl_xor_sync(0xffffffffu, assignments, off);
   if (lane == 0) {

@@ -80,8 +80,12 @@ typedef struct {
   uint64_t seed;           /* random-eviction seed */
   int64_t tile_bytes;      /* staging tile size, multiple of 16 (262144 in [NfE] §5.4) */
   int32_t max_tokens;      /* largest T of any call on this context */
-  int32_t admit_on_device; /* 0: host slot manager (admit syncs the stream);
-                              1: admission and staging on the GPU, no host sync */
+  int32_t admit_on_device; /* 0: host slot manager, tiles staged on n_streams
+                                 copy streams (admit syncs the stream);
+                              1: admission on the GPU, misses staged by a copy
+                                 kernel over the host link, no host sync;
+                              2: admission on the GPU, misses materialised by
+                                 the FFN while it reads them from the store */
 } moe_config_t;
 
 /* Expert-major plan ([NfE] §5.3, §5.5). Device arrays owned by the caller.

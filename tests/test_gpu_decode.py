@@ -156,29 +156,33 @@ def _run_trace(bec, w, layers, steps, ffn_steps, policy=None, seed=0, tile_bytes
     return outs
 
 
-@pytest.mark.parametrize("device_admit", [False, True])
+MODES = [0, 1, 2]  # host admission; device admission + staging kernel; + read-through
+
+
+@pytest.mark.parametrize("device_admit", MODES)
 def test_layer_tiny_trace(bec, device_admit):
     w = W.with_changes(W.WORKLOADS["tiny"], n_steps=16)
     _run_trace(bec, w, 1, 16, set(range(16)), device_admit=device_admit)
 
 
-@pytest.mark.parametrize("device_admit", [False, True])
+@pytest.mark.parametrize("device_admit", MODES)
 def test_layer_decode_full_size(bec, device_admit):
     w = W.WORKLOADS["decode"]
     _run_trace(bec, w, 2, 24, {0, 5, 23}, device_admit=device_admit)
 
 
-@pytest.mark.parametrize("device_admit", [False, True])
+@pytest.mark.parametrize("device_admit", MODES)
 @pytest.mark.parametrize("policy,seed", [(0, 0), (1, 0), (1, 3)])
 def test_layer_mtp_decode_q4(bec, policy, seed, device_admit):
     w = W.with_changes(W.WORKLOADS["mtp_decode"], slots=40)  # >= T*k, small enough to evict
     _run_trace(bec, w, 1, 14, {0, 13}, policy=policy, seed=seed, device_admit=device_admit)
 
 
-def test_layer_decode_long_trace_device_admission(bec):
+@pytest.mark.parametrize("device_admit", [1, 2])
+def test_layer_decode_long_trace_device_admission(bec, device_admit):
     # the whole 128-step trace of one layer, cache state bit-exact every step
     w = W.WORKLOADS["decode"]
-    _run_trace(bec, w, 1, 128, {127}, device_admit=True)
+    _run_trace(bec, w, 1, 128, {127}, device_admit=device_admit)
 
 
 def test_cache_transparency_bitwise(bec):
@@ -193,8 +197,10 @@ def test_cache_transparency_bitwise(bec):
                    device_admit=True)
     e = _run_trace(bec, w, 1, 8, set(), slots=w.n_experts, preload=True, tile_bytes=8192,
                    check_every_step=False, device_admit=True)
+    f = _run_trace(bec, w, 1, 8, set(), policy=1, seed=1, check_every_step=False,
+                   device_admit=2)
     for key in a:
-        for other in (b, c, d, e):
+        for other in (b, c, d, e, f):
             assert np.array_equal(a[key], other[key]), key
 
 
@@ -220,10 +226,11 @@ def test_staged_slot_bytes_equal_store(bec):
         ctx.close()
 
 
-def test_fail_closed_stale_generation_device_admission(bec):
+@pytest.mark.parametrize("device_admit", [1, 2])
+def test_fail_closed_stale_generation_device_admission(bec, device_admit):
     w = W.with_changes(W.WORKLOADS["tiny"], n_steps=2)
     store = pinned_store(w, 1)
-    ctx = make_context(bec, w, 1, device_admit=True)
+    ctx = make_context(bec, w, 1, device_admit=device_admit)
     bind_all(ctx, w, 1, store)
     plan = bec.Plan(w.n_experts, w.top_k, 4)
     x = x_to_torch(w, W.activations(w, 0, 4))
@@ -231,6 +238,10 @@ def test_fail_closed_stale_generation_device_admission(bec):
     idx = torch.empty((4, 2), dtype=torch.int32, device="cuda")
     wt = torch.empty((4, 2), device="cuda")
     y = torch.empty((4, w.hidden), device="cuda")
+    ctx.layer_forward(0, x, Wr, None, idx, wt, plan, y)
+    ctx.check_device_errors()
+    # the same step again: every expert now hits, so the FFN reads the slots
+    # (a miss would be read from the store and never consult the slot)
     ctx.layer_forward(0, x, Wr, None, idx, wt, plan, y)
     ctx.check_device_errors()
     with pytest.raises(bec.MoeError):
