@@ -20,6 +20,7 @@
 #include <cstring>
 
 #include "internal.h"
+#include "prefill.h"
 
 namespace {
 
@@ -141,6 +142,15 @@ extern "C" void moe_destroy(moe_ctx_t* ctx) {
   cudaFree(ctx->d_fills);
   cudaFree(ctx->d_done);
   cudaFree(ctx->d_ffn_ticket);
+  cudaFree(ctx->d_x16);
+  cudaFree(ctx->d_hp);
+  cudaFree(ctx->d_yp);
+  cudaFree(ctx->d_items0);
+  cudaFree(ctx->d_items1);
+  cudaFree(ctx->d_nitems);
+  cudaFree(ctx->d_plan_local);
+  cudaFree(ctx->d_norms);
+  cudaFree(ctx->d_flags);
   cudaFreeHost(ctx->h_units);
   cudaFreeHost(ctx->h_pt);
   cudaFreeHost(ctx->h_ptgen);
@@ -230,12 +240,31 @@ extern "C" moe_status_t moe_create(const moe_config_t* cfg, moe_ctx_t** out) {
   CKC(cudaMalloc(&ctx->d_units, sizeof(int32_t) * unit_ints));
   CKC(cudaMemset(ctx->d_units, 0, sizeof(int32_t) * unit_ints));
   CKC(cudaHostAlloc(&ctx->h_units, sizeof(int32_t) * unit_ints, cudaHostAllocDefault));
+  if (c.max_tokens > 8) {
+    // prefill scratch: expert-major activations, h, weighted rows, work items
+    ctx->prefill = true;
+    const int64_t rows = static_cast<int64_t>(c.max_tokens) * (c.top_k + 1);
+    ctx->ldh_p = static_cast<int>(round_up(std::max(c.inter, c.shared_inter), 64));
+    const int64_t mtiles = (rows + 127) / 128 + std::min<int64_t>(E, static_cast<int64_t>(c.max_tokens) * c.top_k) + 1;
+    ctx->max_items0 = static_cast<int>(mtiles * ((std::max(c.inter, c.shared_inter) + 127) / 128));
+    ctx->max_items1 = static_cast<int>(mtiles * ((c.hidden + 255) / 256));
+    CKC(cudaMalloc(&ctx->d_x16, sizeof(uint16_t) * rows * c.hidden));
+    CKC(cudaMalloc(&ctx->d_hp, sizeof(uint16_t) * rows * ctx->ldh_p));
+    CKC(cudaMalloc(&ctx->d_yp, sizeof(float) * rows * c.hidden));
+    CKC(cudaMalloc(&ctx->d_items0, sizeof(int32_t) * 4 * ctx->max_items0));
+    CKC(cudaMalloc(&ctx->d_items1, sizeof(int32_t) * 4 * ctx->max_items1));
+    CKC(cudaMalloc(&ctx->d_nitems, sizeof(int32_t) * 2));
+    CKC(cudaMalloc(&ctx->d_plan_local,
+                   sizeof(int32_t) * moe::plan_blocks(c.max_tokens * c.top_k) * static_cast<int64_t>(E)));
+    CKC(cudaMalloc(&ctx->d_norms, sizeof(float) * (c.max_tokens + E)));
+    CKC(cudaMalloc(&ctx->d_flags, sizeof(int32_t) * c.max_tokens));
+  }
   ctx->dev_admit = c.admit_on_device >= 1;
   ctx->read_through = c.admit_on_device == 2;
   CKC(cudaMalloc(&ctx->d_ffn_ticket, sizeof(unsigned int)));
   CKC(cudaMemset(ctx->d_ffn_ticket, 0, sizeof(unsigned int)));
   if (ctx->dev_admit) {
-    ctx->max_fills = std::min(E, std::min(c.max_tokens, 64) * c.top_k);
+    ctx->max_fills = std::min(E, c.max_tokens * c.top_k);
     CKC(cudaMalloc(&ctx->d_owner, sizeof(int32_t) * L * S));
     CKC(cudaMemset(ctx->d_owner, 0xFF, sizeof(int32_t) * L * S));
     CKC(cudaMalloc(&ctx->d_sgen, sizeof(uint32_t) * L * S));
@@ -345,9 +374,9 @@ static moe_status_t route_impl(moe_ctx_t* ctx, int32_t layer, const void* x, int
   if (!x || !w_router || !topk_idx || !topk_w) return fail(ctx, MOE_ERR_ARG, "route: null pointer");
   if (reinterpret_cast<uintptr_t>(x) % 16 || reinterpret_cast<uintptr_t>(w_router) % 16)
     return fail(ctx, MOE_ERR_ARG, "route: x and w_router must be 16-byte aligned");
-  if (T > 64) return fail(ctx, MOE_ERR_ARG, "route: T > 64 needs the prefill router, which is not built");
   if (plan && plan->capacity < T * ctx->cfg.top_k)
     return fail(ctx, MOE_ERR_ARG, "route: plan capacity < T*k");
+  if (T > 64 && !ctx->d_norms) return fail(ctx, MOE_ERR_ARG, "route: T > 64 needs max_tokens > 8");
   moe::RouteArgs a{};
   a.x = x;
   a.xt = xt;
@@ -366,7 +395,7 @@ static moe_status_t route_impl(moe_ctx_t* ctx, int32_t layer, const void* x, int
   if (plan) a.plan = *plan;
   if (admit) {
     a.admit.enabled = 1;
-    a.admit.read_through = ctx->read_through ? 1 : 0;
+    a.admit.read_through = (ctx->read_through && T <= 8) ? 1 : 0;
     a.admit.E = ctx->cfg.n_experts;
     a.admit.S = ctx->cfg.slots_per_layer;
     a.admit.policy = ctx->cfg.policy;
@@ -380,14 +409,24 @@ static moe_status_t route_impl(moe_ctx_t* ctx, int32_t layer, const void* x, int
     a.admit.max_fills = ctx->max_fills;
     ctx->dev_state_used = true;
   }
+  moe_ctx::TimedLaunch r{MOE_KT_ROUTE, nullptr, nullptr};
   if (ctx->timing) {
-    moe_ctx::TimedLaunch r{MOE_KT_ROUTE, timing_event(ctx), timing_event(ctx)};
+    r.a = timing_event(ctx);
+    r.b = timing_event(ctx);
     CK(cudaEventRecord(r.a, st));
-    CK(moe::launch_route(a, ctx->num_sms, st));
-    CK(cudaEventRecord(r.b, st));
-    ctx->timed.push_back(r);
+  }
+  if (T > 64) {
+    // many tokens: tiled logits, per-token selection, exact repair; the plan
+    // and admission run as their own launches
+    a.plan = moe_plan_t{};
+    a.admit.enabled = 0;
+    CK(moe::launch_route_large(a, ctx->d_norms, ctx->d_flags, st));
   } else {
     CK(moe::launch_route(a, ctx->num_sms, st));
+  }
+  if (ctx->timing) {
+    CK(cudaEventRecord(r.b, st));
+    ctx->timed.push_back(r);
   }
   return MOE_OK;
 }
@@ -420,14 +459,21 @@ extern "C" moe_status_t moe_plan_union(moe_ctx_t* ctx, const int32_t* topk_idx, 
   a.plan = *plan;
   a.err = ctx->d_err;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const bool large = T * ctx->cfg.top_k > 256;
+  if (large && !ctx->d_plan_local) return fail(ctx, MOE_ERR_ARG, "plan: T*k > 256 needs max_tokens > 8");
+  moe_ctx::TimedLaunch r{MOE_KT_PLAN, nullptr, nullptr};
   if (ctx->timing) {
-    moe_ctx::TimedLaunch r{MOE_KT_PLAN, timing_event(ctx), timing_event(ctx)};
+    r.a = timing_event(ctx);
+    r.b = timing_event(ctx);
     CK(cudaEventRecord(r.a, st));
+  }
+  if (large)
+    CK(moe::launch_plan_large(a, ctx->d_plan_local, st));
+  else
     CK(moe::launch_plan(a, st));
+  if (ctx->timing) {
     CK(cudaEventRecord(r.b, st));
     ctx->timed.push_back(r);
-  } else {
-    CK(moe::launch_plan(a, st));
   }
   return MOE_OK;
 }
@@ -647,10 +693,52 @@ extern "C" moe_status_t moe_expert_ffn(moe_ctx_t* ctx, int32_t layer, const void
   if (ctx->cfg.shared_inter > 0 && !ctx->shared[layer])
     return fail(ctx, MOE_ERR_STATE, "ffn: shared expert of this layer not bound");
   if (mode == MOE_MODE_AUTO) mode = T <= 8 ? MOE_MODE_DECODE : MOE_MODE_PREFILL;
-  if (mode == MOE_MODE_PREFILL)
-    return fail(ctx, MOE_ERR_ARG, "ffn: the prefill grouped-GEMM path is not built");
-  if (mode != MOE_MODE_DECODE || T > 8) return fail(ctx, MOE_ERR_ARG, "ffn: decode mode needs T <= 8");
   const int E = ctx->cfg.n_experts, S = ctx->cfg.slots_per_layer;
+  if (mode == MOE_MODE_PREFILL) {
+    const moe_config_t& c = ctx->cfg;
+    if (!ctx->prefill) return fail(ctx, MOE_ERR_ARG, "ffn: the prefill path needs max_tokens > 8");
+    if (c.quant != MOE_Q8_0) return fail(ctx, MOE_ERR_ARG, "ffn: the prefill path reads Q8_0 experts");
+    if (c.hidden % 64 || c.inter % 64 || c.shared_inter % 64 || E > 1023)
+      return fail(ctx, MOE_ERR_ARG, "ffn: the prefill path needs H, I, I_s multiples of 64 and E <= 1023");
+    moe::PrefillArgs p{};
+    p.x = x;
+    p.xt = xt;
+    p.T = T;
+    p.k = c.top_k;
+    p.H = c.hidden;
+    p.I = c.inter;
+    p.Is = c.shared_inter;
+    p.S = S;
+    p.units = ctx->d_units;
+    p.plan = *plan;
+    p.pool = ctx->d_pool + static_cast<size_t>(layer) * S * ctx->slot_stride;
+    p.slot_stride = ctx->slot_stride;
+    p.shared = ctx->shared[layer];
+    p.g = ctx->geom;
+    p.gs = ctx->sgeom;
+    p.x16 = reinterpret_cast<__half*>(ctx->d_x16);
+    p.h = ctx->d_hp;
+    p.ldh = ctx->ldh_p;
+    p.yp = ctx->d_yp;
+    p.y = y;
+    p.items0 = ctx->d_items0;
+    p.items1 = ctx->d_items1;
+    p.n_items0 = ctx->d_nitems;
+    p.n_items1 = ctx->d_nitems + 1;
+    p.max_items0 = ctx->max_items0;
+    p.max_items1 = ctx->max_items1;
+    p.err = ctx->d_err;
+    p.gen = ctx->d_gen + static_cast<size_t>(layer) * S;
+    if (ctx->timing)
+      for (int i = 0; i < 4; ++i) p.ev[i] = timing_event(ctx);
+    CK(moe::prefill_ffn(p, reinterpret_cast<cudaStream_t>(stream)));
+    if (ctx->timing) {
+      ctx->timed.push_back({MOE_KT_GATEUP, p.ev[0], p.ev[1]});
+      ctx->timed.push_back({MOE_KT_DOWN, p.ev[2], p.ev[3]});
+    }
+    return MOE_OK;
+  }
+  if (mode != MOE_MODE_DECODE || T > 8) return fail(ctx, MOE_ERR_ARG, "ffn: decode mode needs T <= 8");
   moe::FfnArgs a{};
   a.x = x;
   a.xt = xt;
@@ -711,7 +799,28 @@ extern "C" moe_status_t moe_layer_forward(moe_ctx_t* ctx, int32_t layer, const v
     if (!ctx->store_dev) return fail(ctx, MOE_ERR_STATE, "layer_forward: no store bound");
     moe_status_t s = route_impl(ctx, layer, x, xt, T, w_router, bias, topk_idx, topk_w, plan, st, true);
     if (s != MOE_OK) return s;
-    if (ctx->read_through)  // misses are materialised by the FFN as it reads them
+    if (T > 64) {
+      // many tokens: the plan and the admission are separate launches
+      s = moe_plan_union(ctx, topk_idx, topk_w, T, plan, stream);
+      if (s != MOE_OK) return s;
+      moe::AdmitArgs ad{};
+      ad.enabled = 1;
+      ad.read_through = 0;
+      ad.E = ctx->cfg.n_experts;
+      ad.S = ctx->cfg.slots_per_layer;
+      ad.policy = ctx->cfg.policy;
+      ad.has_shared = ctx->cfg.shared_inter > 0 ? 1 : 0;
+      ad.T = T;
+      ad.payload = ctx->geom.bytes;
+      ad.c = dev_cache(ctx, layer);
+      ad.fills = ctx->d_fills;
+      ad.units = ctx->d_units;
+      ad.done = ctx->d_done;
+      ad.max_fills = ctx->max_fills;
+      ctx->dev_state_used = true;
+      CK(moe::launch_admit(ad, *plan, std::min(ctx->cfg.n_experts, T * ctx->cfg.top_k), ctx->d_err, st));
+    }
+    if (ctx->read_through && T <= 8)  // misses are materialised by the FFN as it reads them
       return moe_expert_ffn(ctx, layer, x, xt, T, plan, y, MOE_MODE_AUTO, stream);
     const moe::ExpertGeom& g = ctx->geom;
     moe::StageArgs sa{};
@@ -749,6 +858,10 @@ extern "C" moe_status_t moe_layer_forward(moe_ctx_t* ctx, int32_t layer, const v
   }
   moe_status_t s = route_impl(ctx, layer, x, xt, T, w_router, bias, topk_idx, topk_w, plan, st);
   if (s != MOE_OK) return s;
+  if (T > 64) {
+    s = moe_plan_union(ctx, topk_idx, topk_w, T, plan, stream);
+    if (s != MOE_OK) return s;
+  }
   moe_miss_list_t local{};
   moe_miss_list_t* ml = misses ? misses : &local;
   s = moe_cache_admit(ctx, layer, plan, ml, stream);

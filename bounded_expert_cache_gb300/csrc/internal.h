@@ -112,6 +112,14 @@ struct PlanArgs {
   uint32_t* err;
 };
 cudaError_t launch_plan(const PlanArgs& a, cudaStream_t st);
+// Many-token routing (any T): norms [T + E] and flags [T] are scratch.
+cudaError_t launch_route_large(const RouteArgs& a, float* norms, int* flags, cudaStream_t st);
+// Multi-block plan for any T*k: local is scratch [plan_blocks(T*k)][E].
+int plan_blocks(int A);
+cudaError_t launch_plan_large(const PlanArgs& a, int* local, cudaStream_t st);
+// On-device admission of one step as its own launch (one warp).
+cudaError_t launch_admit(const AdmitArgs& A, const moe_plan_t& P, int max_units, uint32_t* err,
+                         cudaStream_t st);
 
 // Message returned by moe_last_error(NULL) on this thread.
 void set_thread_error(const std::string& msg);
@@ -211,6 +219,18 @@ struct moe_ctx {
   int32_t max_fills = 0;
   bool read_through = false;              // misses materialised by the FFN
   unsigned int* d_ffn_ticket = nullptr;
+  // prefill path (max_tokens > 8)
+  bool prefill = false;
+  uint16_t* d_x16 = nullptr;               // fp16 [rows][H]
+  uint16_t* d_hp = nullptr;                // bf16 [rows][ldh_p]
+  float* d_yp = nullptr;                   // fp32 [rows][H]
+  int32_t* d_items0 = nullptr;
+  int32_t* d_items1 = nullptr;
+  int32_t* d_nitems = nullptr;             // [2]
+  int max_items0 = 0, max_items1 = 0, ldh_p = 0;
+  int32_t* d_plan_local = nullptr;         // multi-block plan scratch
+  float* d_norms = nullptr;                // many-token router scratch
+  int32_t* d_flags = nullptr;
   std::vector<cudaStream_t> streams;
   std::vector<cudaEvent_t> ev_stage;
   cudaEvent_t ev_compute = nullptr;

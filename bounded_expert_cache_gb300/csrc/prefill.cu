@@ -1,0 +1,227 @@
+// Prefill expert FFN driver: gather -> grouped gate/up GEMM -> grouped down
+// GEMM -> combine.
+//
+// "Nanite for Experts" §5.3: each unique expert is scheduled once over all its
+// tokens (expert-major rows); §5.5: per-expert results merge back into the
+// tokens' original positions. The combine adds, per token, the shared
+// expert's row and then its k routed rows in selection order, so the output
+// is independent of scheduling and of the cache state.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "internal.h"
+#include "prefill.h"
+
+namespace moe {
+namespace {
+
+// fp16 copy of the activations in expert-major order: row p < T*k is token
+// perm_tok[p]; rows T*k .. T*k+T-1 are tokens 0..T-1 (the shared expert's).
+template <int XT>
+__global__ void __launch_bounds__(256) gather_kernel(const void* x, int T, int k, int H,
+                                                     const int32_t* perm_tok, __half* out) {
+  const int p = blockIdx.x;
+  const int A = T * k;
+  const int t = p < A ? __ldg(perm_tok + p) : p - A;
+  __half* dst = out + static_cast<int64_t>(p) * H;
+  for (int i = threadIdx.x * 8; i < H; i += 256 * 8) {
+    float v[8];
+    if (XT == MOE_BF16) {
+      const uint4 b = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) +
+                                                          static_cast<int64_t>(t) * H + i));
+      const uint32_t w[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        v[2 * j] = __uint_as_float(w[j] << 16);
+        v[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+      }
+    } else {
+      const float4* s = reinterpret_cast<const float4*>(static_cast<const float*>(x) +
+                                                        static_cast<int64_t>(t) * H + i);
+      const float4 a = __ldg(s), b = __ldg(s + 1);
+      v[0] = a.x, v[1] = a.y, v[2] = a.z, v[3] = a.w, v[4] = b.x, v[5] = b.y, v[6] = b.z, v[7] = b.w;
+    }
+    __half2 h[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) h[j] = __floats2half2_rn(v[2 * j], v[2 * j + 1]);
+    *reinterpret_cast<uint4*>(dst + i) = *reinterpret_cast<uint4*>(h);
+  }
+}
+
+// Work items of both GEMMs from the unit table: per unit, 128-row tiles times
+// weight-row tiles (128 gate+up rows, or 256 down rows); m varies fastest so
+// consecutive CTAs share a weight tile.
+__global__ void __launch_bounds__(1024) items_kernel(const int32_t* units, int I, int Is, int H,
+                                                     int32_t* items0, int32_t* n0, int32_t* items1,
+                                                     int32_t* n1) {
+  __shared__ int c0[1025], c1[1025];
+  const int nu = __ldg(units);
+  const int u = threadIdx.x;
+  int a = 0, b = 0, mt = 0, nt0 = 0, nt1 = 0;
+  if (u < nu) {
+    const int4 U = __ldg(reinterpret_cast<const int4*>(units + kUnitHeader) + u);
+    mt = (U.z + 127) / 128;
+    nt0 = ((U.x == -1 ? Is : I) + 127) / 128;
+    nt1 = (H + 255) / 256;
+    a = mt * nt0;
+    b = mt * nt1;
+  }
+  c0[u] = a;
+  c1[u] = b;
+  __syncthreads();
+  if (u == 0) {
+    int s0 = 0, s1 = 0;
+    for (int i = 0; i < min(nu, 1024); ++i) {
+      const int x0 = c0[i], x1 = c1[i];
+      c0[i] = s0;
+      c1[i] = s1;
+      s0 += x0;
+      s1 += x1;
+    }
+    *n0 = s0;
+    *n1 = s1;
+  }
+  __syncthreads();
+  if (u < nu) {
+    int o = c0[u];
+    for (int n = 0; n < nt0; ++n)
+      for (int m = 0; m < mt; ++m, ++o) reinterpret_cast<int4*>(items0)[o] = make_int4(u, m * 128, n * 128, 0);
+    o = c1[u];
+    for (int n = 0; n < nt1; ++n)
+      for (int m = 0; m < mt; ++m, ++o) reinterpret_cast<int4*>(items1)[o] = make_int4(u, m * 128, n * 256, 0);
+  }
+}
+
+__global__ void __launch_bounds__(256) combine_kernel(const float* yp, const int32_t* inv, int T, int k,
+                                                      int H, int has_shared, float* y) {
+  const int t = blockIdx.x;
+  const int A = T * k;
+  for (int i = threadIdx.x * 4; i < H; i += 256 * 4) {
+    float4 acc = has_shared ? __ldg(reinterpret_cast<const float4*>(yp + static_cast<int64_t>(A + t) * H + i))
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < k; ++j) {
+      const int p = __ldg(inv + t * k + j);
+      const float4 v = __ldg(reinterpret_cast<const float4*>(yp + static_cast<int64_t>(p) * H + i));
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    *reinterpret_cast<float4*>(y + static_cast<int64_t>(t) * H + i) = acc;
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+cudaError_t encoder() {
+  if (g_encode) return cudaSuccess;
+  cudaDriverEntryPointQueryResult q;
+  cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", reinterpret_cast<void**>(&g_encode),
+                                                   12000, cudaEnableDefault, &q);
+  if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !g_encode) return cudaErrorNotSupported;
+  return cudaSuccess;
+}
+
+// 16-bit [rows][cols] operand, 64 x 128 boxes, 128-byte swizzle.
+cudaError_t map16(CUtensorMap* m, const void* base, CUtensorMapDataType t, int64_t rows, int64_t cols) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  cuuint32_t box[2] = {64, 128};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = g_encode(m, t, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// Q8_0 quant plane of one matrix in every slot: bytes x rows x slots.
+cudaError_t mapq(CUtensorMap* m, const void* base, int64_t kbytes, int64_t rows, int64_t slots,
+                 int64_t slot_stride, int box_rows) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kbytes), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(slots)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(kbytes), static_cast<cuuint64_t>(slot_stride)};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t prefill_ffn(const PrefillArgs& p, cudaStream_t st) {
+  cudaError_t e = encoder();
+  if (e != cudaSuccess) return e;
+  const int A = p.T * p.k, rows = A + p.T;
+  const ExpertGeom& g = p.g;
+  const ExpertGeom& gs = p.gs;
+  // 1. activations in expert-major order, fp16
+  if (p.xt == MOE_BF16)
+    gather_kernel<MOE_BF16><<<rows, 256, 0, st>>>(p.x, p.T, p.k, p.H, p.plan.perm_tok, p.x16);
+  else
+    gather_kernel<MOE_F32><<<rows, 256, 0, st>>>(p.x, p.T, p.k, p.H, p.plan.perm_tok, p.x16);
+  // 2. work items
+  items_kernel<<<1, 1024, 0, st>>>(p.units, p.I, p.Is, p.H, p.items0, p.n_items0, p.items1, p.n_items1);
+  // 3. tensor maps (pointers are fixed per context and layer)
+  GemmMaps m0{}, m1{};
+  const int64_t S = p.S;
+  if ((e = map16(&m0.a, p.x16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, rows, p.H)) != cudaSuccess) return e;
+  if ((e = mapq(&m0.q0, p.pool + g.qoff[0], p.H, p.I, S, p.slot_stride, 128)) != cudaSuccess) return e;
+  if ((e = mapq(&m0.q1, p.pool + g.qoff[1], p.H, p.I, S, p.slot_stride, 128)) != cudaSuccess) return e;
+  if ((e = map16(&m1.a, p.h, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rows, p.ldh)) != cudaSuccess) return e;
+  if ((e = mapq(&m1.q0, p.pool + g.qoff[2], p.I, p.H, S, p.slot_stride, 256)) != cudaSuccess) return e;
+  m1.q1 = m1.q0;
+  if (p.shared) {
+    if ((e = mapq(&m0.sq0, p.shared + gs.qoff[0], p.H, p.Is, 1, gs.bytes, 128)) != cudaSuccess) return e;
+    if ((e = mapq(&m0.sq1, p.shared + gs.qoff[1], p.H, p.Is, 1, gs.bytes, 128)) != cudaSuccess) return e;
+    if ((e = mapq(&m1.sq0, p.shared + gs.qoff[2], p.Is, p.H, 1, gs.bytes, 256)) != cudaSuccess) return e;
+  } else {
+    m0.sq0 = m0.sq1 = m0.q0;
+    m1.sq0 = m1.q0;
+  }
+  m1.sq1 = m1.sq0;
+  GemmArgs a{};
+  a.units = p.units;
+  a.pool = p.pool;
+  a.slot_stride = p.slot_stride;
+  a.shared = p.shared;
+  for (int i = 0; i < 3; ++i) {
+    a.r_soff[i] = g.soff[i];
+    a.s_soff[i] = gs.soff[i];
+  }
+  a.H = p.H;
+  a.I = p.I;
+  a.Is = p.Is;
+  a.rows_routed = A;
+  a.h = p.h;
+  a.ldh = p.ldh;
+  a.yp = p.yp;
+  a.perm_w = p.plan.perm_w;
+  a.err = p.err;
+  a.gen = p.gen;
+  a.S = p.S;
+  // 4. gate/up + SwiGLU
+  a.items = p.items0;
+  a.n_items = p.n_items0;
+  a.kmax = p.H;
+  a.stages = gemm_stages(a.kmax);
+  if (a.stages == 0) return cudaErrorInvalidValue;
+  if (p.ev[0]) cudaEventRecord(p.ev[0], st);
+  if ((e = launch_gemm(0, m0, a, p.max_items0, st)) != cudaSuccess) return e;
+  if (p.ev[1]) cudaEventRecord(p.ev[1], st);
+  // 5. down, weighted by the combine weights
+  a.items = p.items1;
+  a.n_items = p.n_items1;
+  a.kmax = p.shared ? std::max(p.I, p.Is) : p.I;
+  a.stages = gemm_stages(a.kmax);
+  if (a.stages == 0) return cudaErrorInvalidValue;
+  if (p.ev[2]) cudaEventRecord(p.ev[2], st);
+  if ((e = launch_gemm(1, m1, a, p.max_items1, st)) != cudaSuccess) return e;
+  if (p.ev[3]) cudaEventRecord(p.ev[3], st);
+  // 6. combine into the tokens' positions
+  combine_kernel<<<p.T, 256, 0, st>>>(p.yp, p.plan.inv, p.T, p.k, p.H, p.shared ? 1 : 0, p.y);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

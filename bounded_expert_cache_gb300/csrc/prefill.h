@@ -1,0 +1,66 @@
+// Library-internal declarations of the prefill path (grouped dequant-GEMM).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cudaTypedefs.h>
+
+#include "internal.h"
+
+namespace moe {
+
+// Tensor maps of one GEMM launch: the activation operand, the routed quant
+// planes (3-D: bytes, rows, slot) and the shared expert's quant planes
+// (3-D with one slot). q1/sq1 are the up planes (gate/up GEMM only).
+struct GemmMaps {
+  CUtensorMap a, q0, q1, sq0, sq1;
+};
+
+struct GemmArgs {
+  const int32_t* units;     // unit table of the step
+  const int32_t* items;     // int4 per work item {unit, m0, n0, 0}
+  const int32_t* n_items;   // [1]
+  const uint8_t* pool;      // slot pool of the layer
+  int64_t slot_stride;
+  const uint8_t* shared;    // shared expert payload (or nullptr)
+  int64_t r_soff[3], s_soff[3];  // scale-plane offsets (routed, shared)
+  int H, I, Is;
+  int rows_routed;          // expert-major rows of routed assignments (T*k)
+  uint16_t* h;              // bf16 [rows][ldh]
+  int ldh;
+  float* yp;                // fp32 [rows][H], rows scaled by their combine weight
+  const float* perm_w;      // [T*k]
+  uint32_t* err;
+  const uint32_t* gen;      // [S] published slot generations (fail-closed check)
+  int S;
+  int stages, kmax;
+};
+
+// One prefill FFN call: gather, both GEMMs, combine.
+struct PrefillArgs {
+  const void* x;
+  int xt, T, k, H, I, Is, S;
+  const int32_t* units;
+  moe_plan_t plan;
+  const uint8_t* pool;
+  int64_t slot_stride;
+  const uint8_t* shared;
+  ExpertGeom g, gs;
+  __half* x16;              // [rows][H]
+  uint16_t* h;              // bf16 [rows][ldh]
+  int ldh;
+  float* yp;                // [rows][H]
+  float* y;                 // [T][H]
+  int32_t *items0, *n_items0, *items1, *n_items1;
+  int max_items0, max_items1;
+  uint32_t* err;
+  const uint32_t* gen;
+  cudaEvent_t ev[4];        // optional timing around the two GEMMs
+};
+cudaError_t prefill_ffn(const PrefillArgs& p, cudaStream_t st);
+
+int gemm_stages(int K);
+size_t gemm_smem_bytes(int stages, int K);
+cudaError_t launch_gemm(int phase, const GemmMaps& m, const GemmArgs& a, int grid, cudaStream_t st);
+
+}  // namespace moe

@@ -1034,3 +1034,290 @@ extern "C" moe_status_t moe_route_noalloc(const void* x, int32_t xt, int32_t T, 
   }
   return MOE_OK;
 }
+
+// ------------------------------------------------------------ many-token routing
+// Prefill chunks route thousands of tokens at once. Logits come from a tiled
+// fp32 GEMM that sums each 32-term chunk with plain FMAs and folds the chunk
+// sums into an error-free (hi, lo) pair; the chunk error is at most
+// gamma_32 * sum|x w| <= gamma_32 * ||x|| * ||w|| (Cauchy-Schwarz), so the
+// same integer-key certification applies, and uncertified tokens are
+// recomputed exactly as in the few-token router.
+namespace moe {
+namespace {
+
+constexpr int kLT = 64;   // tokens per logits tile
+constexpr int kLE = 64;   // experts per logits tile
+constexpr int kLK = 32;   // K chunk
+
+template <int XT>
+__global__ void __launch_bounds__(256) row_norms_kernel(const void* x, int T, const float* w, int E, int H,
+                                                        float* xn, float* wn) {
+  const int gw = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (gw >= T + E) return;
+  float s = 0.f;
+  if (gw < T) {
+    for (int k = lane; k < H; k += 32) {
+      const float v = load_x<XT>(x, static_cast<size_t>(gw) * H + k);
+      s = fmaf(v, v, s);
+    }
+  } else {
+    const float* r = w + static_cast<size_t>(gw - T) * H;
+    for (int k = lane; k < H; k += 32) s = fmaf(r[k], r[k], s);
+  }
+  for (int off = 16; off; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+  // the fp32 sum of squares is within a relative 1e-3 of the exact one
+  const float nrm = sqrtf(s) * 1.001f;
+  if (lane == 0) {
+    if (gw < T)
+      xn[gw] = isfinite(nrm) ? nrm : INFINITY;
+    else
+      wn[gw - T] = isfinite(nrm) ? nrm : INFINITY;
+  }
+}
+
+template <int XT>
+__global__ void __launch_bounds__(256) logits_tiled_kernel(RouteArgs a, const float* xn, const float* wn) {
+  __shared__ __align__(16) float xs[kLK][kLT + 4];
+  __shared__ __align__(16) float ws[kLK][kLE + 4];
+  const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+  const int t0 = blockIdx.y * kLT, e0 = blockIdx.x * kLE;
+  const int T = a.T, E = a.E, H = a.H;
+  float hi[4][4], lo[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) hi[i][j] = lo[i][j] = 0.f;
+  for (int kc = 0; kc < H; kc += kLK) {
+    // 64 rows x 32 k of x and of w, transposed into [k][row]
+    for (int i = tid; i < kLT * kLK; i += 256) {
+      const int r = i / kLK, k = i - r * kLK;
+      xs[k][r] = (t0 + r < T) ? load_x<XT>(a.x, static_cast<size_t>(t0 + r) * H + kc + k) : 0.f;
+      ws[k][r] = (e0 + r < E) ? __ldg(a.w + static_cast<size_t>(e0 + r) * H + kc + k) : 0.f;
+    }
+    __syncthreads();
+    float p[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) p[i][j] = 0.f;
+#pragma unroll 8
+    for (int k = 0; k < kLK; ++k) {
+      const float4 xv = *reinterpret_cast<const float4*>(&xs[k][ty * 4]);
+      const float4 wv = *reinterpret_cast<const float4*>(&ws[k][tx * 4]);
+      const float xa[4] = {xv.x, xv.y, xv.z, xv.w}, wa[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) p[i][j] = fmaf(xa[i], wa[j], p[i][j]);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        float ns, es;
+        two_sum(hi[i][j], p[i][j], ns, es);
+        hi[i][j] = ns;
+        lo[i][j] = __fadd_rn(lo[i][j], es);
+      }
+    __syncthreads();
+  }
+  const size_t te = static_cast<size_t>(T) * E;
+  const double g32 = 32.0 * 0x1p-24 / (1.0 - 32.0 * 0x1p-24);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int t = t0 + ty * 4 + i;
+    if (t >= T) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int e = e0 + tx * 4 + j;
+      if (e >= E) continue;
+      const double b = a.bias ? static_cast<double>(a.bias[e]) : 0.0;
+      const double l = (static_cast<double>(hi[i][j]) + static_cast<double>(lo[i][j])) + b;
+      const double A = static_cast<double>(xn[t]) * static_cast<double>(wn[e]);
+      const double bnd = 1.01 * g32 * A + fabs(l) * 0x1p-51 + static_cast<double>(H + 1) * 0x1p-140;
+      const double wid = __dadd_ru(bnd, __dmul_ru(fabs(l), 0x1p-50));
+      const bool fin = isfinite(l) && isfinite(wid);
+      const size_t o = static_cast<size_t>(t) * E + e;
+      a.keys[o] = okey(l);
+      a.keys[te + o] = fin ? okey(__dsub_rd(l, wid)) : 0ull;
+      a.keys[2 * te + o] = fin ? okey(__dadd_ru(l, wid)) : ~0ull;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256) select_kernel(RouteArgs a, int* flags) {
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (t >= a.T) return;
+  const size_t te = static_cast<size_t>(a.T) * a.E, o = static_cast<size_t>(t) * a.E;
+  const TokenKeys K{a.keys + o, a.keys + te + o, a.keys + 2 * te + o};
+  int sel[16];
+  unsigned long long selk[16];
+  const bool ok = warp_select(K, a.E, a.k, sel, selk, true);
+  if (ok)
+    warp_write_selection(sel, selk, a.k, a.topk_idx + static_cast<size_t>(t) * a.k,
+                         a.topk_w + static_cast<size_t>(t) * a.k);
+  if (lane == 0) flags[t] = ok ? 0 : 1;
+}
+
+template <int XT>
+__global__ void __launch_bounds__(kRouteThreads) repair_kernel(RouteArgs a, const int* flags) {
+  const int t = blockIdx.x;
+  if (t >= a.T || __ldg(flags + t) == 0) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int E = a.E, H = a.H;
+  const size_t te = static_cast<size_t>(a.T) * E;
+  for (int ee = warp; ee < E; ee += kRouteWarps) {
+    double v;
+    const bool fin = warp_exact_logit<XT>(a.x, static_cast<size_t>(t) * H, a.w + static_cast<size_t>(ee) * H,
+                                          H, a.bias, ee, v);
+    if (lane == 0) {
+      if (!fin) atomicOr(a.err, MOE_DEVERR_NONFINITE);
+      const size_t o = static_cast<size_t>(t) * E + ee;
+      a.keys[o] = a.keys[te + o] = a.keys[2 * te + o] = okey(v);
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const size_t o = static_cast<size_t>(t) * E;
+    const TokenKeys K{a.keys + o, a.keys + te + o, a.keys + 2 * te + o};
+    int sel[16];
+    unsigned long long selk[16];
+    warp_select(K, E, a.k, sel, selk, false);
+    warp_write_selection(sel, selk, a.k, a.topk_idx + static_cast<size_t>(t) * a.k,
+                         a.topk_w + static_cast<size_t>(t) * a.k);
+    if (lane == 0) atomicAdd(a.repairs, 1ull);
+  }
+}
+
+// ---- multi-block plan: per-block counts, one scan, per-block stable scatter
+constexpr int kPB = 256;  // assignments per block
+
+__global__ void __launch_bounds__(kPB) plan_count_kernel(PlanArgs a, int* local) {
+  extern __shared__ int hist[];
+  const int E = a.E, A = a.T * a.k, b = blockIdx.x;
+  for (int e = threadIdx.x; e < E; e += kPB) hist[e] = 0;
+  __syncthreads();
+  const int i = b * kPB + threadIdx.x;
+  if (i < A) {
+    const int e = __ldg(a.idx + i);
+    if (e >= 0 && e < E)
+      atomicAdd(&hist[e], 1);
+    else
+      atomicOr(a.err, MOE_DEVERR_BADIDX);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += kPB) {
+    local[static_cast<size_t>(b) * E + e] = hist[e];
+    if (hist[e]) atomicAdd(a.plan.counts + e, hist[e]);
+  }
+}
+
+__global__ void __launch_bounds__(1024) plan_scan_kernel(PlanArgs a, int* local, int nb) {
+  extern __shared__ int sm[];
+  const int E = a.E;
+  int* cnt = sm;
+  int* cur = sm + E;
+  int* scratch = sm + 2 * E;
+  for (int e = threadIdx.x; e < E; e += 1024) {
+    cnt[e] = __ldcg(a.plan.counts + e);
+    cur[e] = cnt[e] > 0 ? 1 : 0;
+  }
+  __syncthreads();
+  const int nu = block_exclusive_scan<1024>(cur, E, scratch);
+  for (int e = threadIdx.x; e < E; e += 1024)
+    if (cnt[e] > 0) a.plan.uniq[cur[e]] = e;
+  if (threadIdx.x == 0) *a.plan.n_uniq = nu;
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += 1024) cur[e] = cnt[e];
+  __syncthreads();
+  const int total = block_exclusive_scan<1024>(cur, E, scratch);
+  for (int e = threadIdx.x; e < E; e += 1024) {
+    a.plan.offsets[e] = cur[e];
+    int run = cur[e];
+    for (int b = 0; b < nb; ++b) {
+      int* p = local + static_cast<size_t>(b) * E + e;
+      const int v = *p;
+      *p = run;
+      run += v;
+    }
+  }
+  if (threadIdx.x == 0) a.plan.offsets[E] = total;
+}
+
+__global__ void __launch_bounds__(kPB) plan_scatter_kernel(PlanArgs a, const int* local) {
+  extern __shared__ int wcount[];  // [8 warps][E]
+  const int E = a.E, A = a.T * a.k, b = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int i = tid; i < 8 * E; i += kPB) wcount[i] = 0;
+  __syncthreads();
+  const int i = b * kPB + tid;
+  const int e = i < A ? __ldg(a.idx + i) : -1;
+  const bool valid = e >= 0 && e < E;
+  const unsigned peers = __match_any_sync(0xffffffffu, valid ? e : -1 - lane);
+  const int rank = __popc(peers & ((1u << lane) - 1u));
+  if (valid && (__ffs(peers) - 1) == lane) wcount[warp * E + e] = __popc(peers);
+  __syncthreads();
+  if (valid) {
+    int pos = __ldg(local + static_cast<size_t>(b) * E + e) + rank;
+    for (int w2 = 0; w2 < warp; ++w2) pos += wcount[w2 * E + e];
+    a.plan.perm_tok[pos] = i / a.k;
+    a.plan.perm_rank[pos] = i % a.k;
+    a.plan.perm_w[pos] = __ldg(a.w + i);
+    a.plan.inv[i] = pos;
+  }
+}
+
+__global__ void admit_kernel(AdmitArgs A, moe_plan_t P, uint32_t* err) {
+  extern __shared__ unsigned char asm_smem[];
+  if (threadIdx.x < 32) admit_warp(A, P, asm_smem, err);
+}
+
+}  // namespace
+
+cudaError_t launch_route_large(const RouteArgs& a, float* norms, int* flags, cudaStream_t st) {
+  if (a.T < 1 || a.k > 16 || a.E > 1024 || a.H % kLK) return cudaErrorInvalidValue;
+  float* xn = norms;
+  float* wn = norms + a.T;
+  const int nrows = a.T + a.E;
+  if (a.xt == MOE_BF16)
+    row_norms_kernel<MOE_BF16><<<(nrows + 7) / 8, 256, 0, st>>>(a.x, a.T, a.w, a.E, a.H, xn, wn);
+  else
+    row_norms_kernel<MOE_F32><<<(nrows + 7) / 8, 256, 0, st>>>(a.x, a.T, a.w, a.E, a.H, xn, wn);
+  dim3 grid((a.E + kLE - 1) / kLE, (a.T + kLT - 1) / kLT);
+  if (a.xt == MOE_BF16)
+    logits_tiled_kernel<MOE_BF16><<<grid, 256, 0, st>>>(a, xn, wn);
+  else
+    logits_tiled_kernel<MOE_F32><<<grid, 256, 0, st>>>(a, xn, wn);
+  select_kernel<<<(a.T + 7) / 8, 256, 0, st>>>(a, flags);
+  if (a.xt == MOE_BF16)
+    repair_kernel<MOE_BF16><<<a.T, kRouteThreads, 0, st>>>(a, flags);
+  else
+    repair_kernel<MOE_F32><<<a.T, kRouteThreads, 0, st>>>(a, flags);
+  return cudaGetLastError();
+}
+
+int plan_blocks(int A) { return (A + kPB - 1) / kPB; }
+
+cudaError_t launch_plan_large(const PlanArgs& a, int* local, cudaStream_t st) {
+  const int A = a.T * a.k, nb = plan_blocks(A);
+  cudaError_t e = cudaMemsetAsync(a.plan.counts, 0, sizeof(int32_t) * a.E, st);
+  if (e != cudaSuccess) return e;
+  plan_count_kernel<<<nb, kPB, sizeof(int) * a.E, st>>>(a, local);
+  plan_scan_kernel<<<1, 1024, sizeof(int) * (2 * a.E + 33), st>>>(a, local, nb);
+  plan_scatter_kernel<<<nb, kPB, sizeof(int) * 8 * a.E, st>>>(a, local);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_admit(const AdmitArgs& A, const moe_plan_t& P, int max_units, uint32_t* err,
+                         cudaStream_t st) {
+  const size_t smem = admit_smem_bytes(A.E, A.S, max_units);
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(admit_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
+  admit_kernel<<<1, 32, smem, st>>>(A, P, err);
+  return cudaGetLastError();
+}
+
+}  // namespace moe
