@@ -293,6 +293,77 @@ def run_ours(args, rank, world, dev):
     return finish(args, w, world, value, elapsed_ms, e2e_value, kt, st0, st1, clk, extra), w
 
 
+def run_prefill(args, dev):
+    """The prefill workload: one 4096-token chunk (Zipf-skewed router bias),
+    every expert resident, repeated for the timed steps; tokens/s of the whole
+    layer step and TFLOP/s of the two grouped GEMMs (library CUDA events)."""
+    import torch
+    import bounded_expert_cache_gb300 as bec
+    w = W.WORKLOADS["prefill"]
+    T = args.prefill_tokens or w.tokens_per_step
+    E, k, H, I, Is = w.n_experts, w.top_k, w.hidden, w.inter, w.shared_inter
+    store = torch.empty((1, E, w.payload_bytes), dtype=torch.uint8, pin_memory=True)
+    W.fill_store(w, store.numpy())
+    ctx = bec.Context(1, E, k, H, I, Is, w.quant, E, w.policy, 3, 0, 262144, T, admit_on_device=1)
+    ctx.bind_store(store)
+    shared = torch.from_numpy(W.expert_payload(w, 0, E)).to(dev)
+    ctx.bind_shared(0, shared)
+    ctx.preload(0, list(range(E)))
+    Wr = torch.from_numpy(W.router_weights(w, 0)).to(dev)
+    bias = torch.from_numpy(W.router_bias(w, 0)).to(dev)
+    x = torch.from_numpy(W.activations(w, 0, T).view(np.int16)).view(torch.bfloat16).to(dev)
+    plan = bec.Plan(E, k, T, dev)
+    idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+    wt = torch.empty((T, k), dtype=torch.float32, device=dev)
+    y = torch.empty((T, H), dtype=torch.float32, device=dev)
+    steps = max(3, min(args.steps, 20))
+    for _ in range(3):
+        ctx.layer_forward(0, x, Wr, bias, idx, wt, plan, y)
+    ctx.check_device_errors()
+    stream = torch.cuda.current_stream(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    a.record(stream)
+    for _ in range(steps):
+        ctx.layer_forward(0, x, Wr, bias, idx, wt, plan, y)
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    step_ms = a.elapsed_time(b) / steps
+    ctx.kernel_times()
+    ctx.set_kernel_timing(True)
+    for _ in range(steps):
+        ctx.layer_forward(0, x, Wr, bias, idx, wt, plan, y)
+    kt = ctx.kernel_times()
+    ctx.set_kernel_timing(False)
+    ctx.check_device_errors()
+    counts = plan.counts.cpu().numpy()
+    ctx.close()
+    flops_gu = 2.0 * (T * k) * 2 * H * I + 2.0 * T * 2 * H * Is
+    flops_dn = 2.0 * (T * k) * H * I + 2.0 * T * H * Is
+    gu_ms, gu_n = kt["ffn_gateup"]
+    dn_ms, dn_n = kt["ffn_down"]
+    gemm_s = (gu_ms / gu_n + dn_ms / dn_n) / 1e3
+    tf = (flops_gu + flops_dn) / gemm_s / 1e12
+    pk = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
+        os.path.join(ROOT, "MEASURED_PEAKS.json")) else None
+    peak = float(pk["bf16_tflops"]) if pk else 1900.0
+    return {
+        "workload": f"prefill: hidden 2048, 256 experts top-8 + 1 shared, inter 512, Q8_0, {T} bf16 "
+                    "tokens, Zipf(1.1) router bias, all experts resident",
+        "tokens_per_s": round(T / (step_ms / 1e3), 1), "ms_per_step": round(step_ms, 4),
+        "steps": steps,
+        "active_experts": int((counts > 0).sum()), "max_expert_tokens": int(counts.max()),
+        "gemm_tflops": round(tf, 1),
+        "roofline": {"bound": "tensor", "kernel": "grouped dequant-GEMM gate/up + down (tcgen05)",
+                     "achieved": round(tf, 1), "peak": peak,
+                     "peak_source": "measured" if pk else "fallback", "unit": "TFLOP/s",
+                     "frac": round(tf / peak, 4), "algorithmic_gflop_per_step": round((flops_gu + flops_dn) / 1e9, 1)},
+        "kernels": {kname: {"ms": round(ms, 3), "launches": n,
+                            "avg_us": round(ms / n * 1e3, 2) if n else None}
+                    for kname, (ms, n) in kt.items()},
+    }
+
+
 def h2d_bandwidth(torch, dev):
     """Copy-engine bandwidth of a 1 GiB pinned host -> device copy (best of 3)."""
     src = torch.empty(1 << 30, dtype=torch.uint8).pin_memory()
@@ -382,6 +453,9 @@ def main():
     ap.add_argument("--skip-e2e", action="store_true", help="profiling: skip the host-buffer pass")
     ap.add_argument("--skip-cpu", action="store_true", help="profiling: skip the oracle baseline")
     ap.add_argument("--no-graph", action="store_true", help="launch the headline pass call by call")
+    ap.add_argument("--skip-prefill", action="store_true", help="skip the prefill workload pass")
+    ap.add_argument("--prefill-only", action="store_true", help="profiling: only the prefill pass")
+    ap.add_argument("--prefill-tokens", type=int, default=0, help="profiling: tokens of the prefill chunk")
     args = ap.parse_args()
     assert args.warmup >= 3
 
@@ -423,7 +497,12 @@ def main():
         torch.distributed.init_process_group("nccl")
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
+    if args.prefill_only:
+        print(json.dumps({"prefill": run_prefill(args, dev)}))
+        return
     out, w = run_ours(args, rank, world, dev)
+    if not args.skip_prefill:
+        out["prefill"] = run_prefill(args, dev)
     if rank == 0 and world == 1 and not args.skip_cpu:
         sec, layers = oracle_decode_sample(w, args.cpu_budget, w.n_layers)
         out["cpu_baseline"] = {

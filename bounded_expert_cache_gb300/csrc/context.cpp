@@ -245,9 +245,10 @@ extern "C" moe_status_t moe_create(const moe_config_t* cfg, moe_ctx_t** out) {
     ctx->prefill = true;
     const int64_t rows = static_cast<int64_t>(c.max_tokens) * (c.top_k + 1);
     ctx->ldh_p = static_cast<int>(round_up(std::max(c.inter, c.shared_inter), 64));
-    const int64_t mtiles = (rows + 127) / 128 + std::min<int64_t>(E, static_cast<int64_t>(c.max_tokens) * c.top_k) + 1;
-    ctx->max_items0 = static_cast<int>(mtiles * ((std::max(c.inter, c.shared_inter) + 127) / 128));
-    ctx->max_items1 = static_cast<int>(mtiles * ((c.hidden + 255) / 256));
+    const int64_t mtiles = (rows + moe::kPrefillTok - 1) / moe::kPrefillTok +
+                           std::min<int64_t>(E, static_cast<int64_t>(c.max_tokens) * c.top_k) + 1;
+    ctx->max_items0 = static_cast<int>(mtiles * ((std::max(c.inter, c.shared_inter) + 63) / 64));
+    ctx->max_items1 = static_cast<int>(mtiles * ((c.hidden + 127) / 128));
     CKC(cudaMalloc(&ctx->d_x16, sizeof(uint16_t) * rows * c.hidden));
     CKC(cudaMalloc(&ctx->d_hp, sizeof(uint16_t) * rows * ctx->ldh_p));
     CKC(cudaMalloc(&ctx->d_yp, sizeof(float) * rows * c.hidden));
@@ -698,8 +699,8 @@ extern "C" moe_status_t moe_expert_ffn(moe_ctx_t* ctx, int32_t layer, const void
     const moe_config_t& c = ctx->cfg;
     if (!ctx->prefill) return fail(ctx, MOE_ERR_ARG, "ffn: the prefill path needs max_tokens > 8");
     if (c.quant != MOE_Q8_0) return fail(ctx, MOE_ERR_ARG, "ffn: the prefill path reads Q8_0 experts");
-    if (c.hidden % 64 || c.inter % 64 || c.shared_inter % 64 || E > 1023)
-      return fail(ctx, MOE_ERR_ARG, "ffn: the prefill path needs H, I, I_s multiples of 64 and E <= 1023");
+    if (c.hidden % 128 || c.inter % 64 || c.shared_inter % 64 || E > 1023)
+      return fail(ctx, MOE_ERR_ARG, "ffn: the prefill path needs H % 128 == 0, I and I_s multiples of 64 and E <= 1023");
     moe::PrefillArgs p{};
     p.x = x;
     p.xt = xt;
@@ -727,6 +728,7 @@ extern "C" moe_status_t moe_expert_ffn(moe_ctx_t* ctx, int32_t layer, const void
     p.n_items1 = ctx->d_nitems + 1;
     p.max_items0 = ctx->max_items0;
     p.max_items1 = ctx->max_items1;
+    p.n_sm = ctx->num_sms;
     p.err = ctx->d_err;
     p.gen = ctx->d_gen + static_cast<size_t>(layer) * S;
     if (ctx->timing)

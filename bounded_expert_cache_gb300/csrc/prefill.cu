@@ -6,6 +6,8 @@
 // tokens' original positions. The combine adds, per token, the shared
 // expert's row and then its k routed rows in selection order, so the output
 // is independent of scheduling and of the cache state.
+#include <algorithm>
+
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -48,9 +50,10 @@ __global__ void __launch_bounds__(256) gather_kernel(const void* x, int T, int k
   }
 }
 
-// Work items of both GEMMs from the unit table: per unit, 128-row tiles times
-// weight-row tiles (128 gate+up rows, or 256 down rows); m varies fastest so
-// consecutive CTAs share a weight tile.
+// Work items of both GEMMs from the unit table: per unit, 192-token tiles
+// times weight tiles (64 gate rows with the same 64 up rows, or 128 down
+// rows); the weight tile varies fastest so that consecutive CTAs share a
+// token tile.
 __global__ void __launch_bounds__(1024) items_kernel(const int32_t* units, int I, int Is, int H,
                                                      int32_t* items0, int32_t* n0, int32_t* items1,
                                                      int32_t* n1) {
@@ -60,9 +63,9 @@ __global__ void __launch_bounds__(1024) items_kernel(const int32_t* units, int I
   int a = 0, b = 0, mt = 0, nt0 = 0, nt1 = 0;
   if (u < nu) {
     const int4 U = __ldg(reinterpret_cast<const int4*>(units + kUnitHeader) + u);
-    mt = (U.z + 127) / 128;
-    nt0 = ((U.x == -1 ? Is : I) + 127) / 128;
-    nt1 = (H + 255) / 256;
+    mt = (U.z + kPrefillTok - 1) / kPrefillTok;
+    nt0 = (U.x == -1 ? Is : I) / 64;
+    nt1 = H / 128;
     a = mt * nt0;
     b = mt * nt1;
   }
@@ -84,16 +87,20 @@ __global__ void __launch_bounds__(1024) items_kernel(const int32_t* units, int I
   __syncthreads();
   if (u < nu) {
     int o = c0[u];
-    for (int n = 0; n < nt0; ++n)
-      for (int m = 0; m < mt; ++m, ++o) reinterpret_cast<int4*>(items0)[o] = make_int4(u, m * 128, n * 128, 0);
+    for (int m = 0; m < mt; ++m)
+      for (int n = 0; n < nt0; ++n, ++o)
+        reinterpret_cast<int4*>(items0)[o] = make_int4(u, m * kPrefillTok, n * 64, 0);
     o = c1[u];
-    for (int n = 0; n < nt1; ++n)
-      for (int m = 0; m < mt; ++m, ++o) reinterpret_cast<int4*>(items1)[o] = make_int4(u, m * 128, n * 256, 0);
+    for (int m = 0; m < mt; ++m)
+      for (int n = 0; n < nt1; ++n, ++o)
+        reinterpret_cast<int4*>(items1)[o] = make_int4(u, m * kPrefillTok, n * 128, 0);
   }
 }
 
-__global__ void __launch_bounds__(256) combine_kernel(const float* yp, const int32_t* inv, int T, int k,
-                                                      int H, int has_shared, float* y) {
+// y[t] = shared row + sum over j in selection order of w[t,j] * row inv[t,j]
+// (the weight of expert-major row p is perm_w[p]).
+__global__ void __launch_bounds__(256) combine_kernel(const float* yp, const int32_t* inv, const float* w, int T,
+                                                      int k, int H, int has_shared, float* y) {
   const int t = blockIdx.x;
   const int A = T * k;
   for (int i = threadIdx.x * 4; i < H; i += 256 * 4) {
@@ -101,11 +108,12 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* yp, const int
                             : make_float4(0.f, 0.f, 0.f, 0.f);
     for (int j = 0; j < k; ++j) {
       const int p = __ldg(inv + t * k + j);
+      const float wj = __ldg(w + p);
       const float4 v = __ldg(reinterpret_cast<const float4*>(yp + static_cast<int64_t>(p) * H + i));
-      acc.x += v.x;
-      acc.y += v.y;
-      acc.z += v.z;
-      acc.w += v.w;
+      acc.x += wj * v.x;
+      acc.y += wj * v.y;
+      acc.z += wj * v.z;
+      acc.w += wj * v.w;
     }
     *reinterpret_cast<float4*>(y + static_cast<int64_t>(t) * H + i) = acc;
   }
@@ -122,11 +130,12 @@ cudaError_t encoder() {
   return cudaSuccess;
 }
 
-// 16-bit [rows][cols] operand, 64 x 128 boxes, 128-byte swizzle.
-cudaError_t map16(CUtensorMap* m, const void* base, CUtensorMapDataType t, int64_t rows, int64_t cols) {
+// 16-bit [rows][cols] token operand, 64 x box_rows boxes, 128-byte swizzle.
+cudaError_t map16(CUtensorMap* m, const void* base, CUtensorMapDataType t, int64_t rows, int64_t cols,
+                  int box_rows) {
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
-  cuuint32_t box[2] = {64, 128};
+  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
   cuuint32_t es[2] = {1, 1};
   CUresult r = g_encode(m, t, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -134,16 +143,21 @@ cudaError_t map16(CUtensorMap* m, const void* base, CUtensorMapDataType t, int64
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-// Q8_0 quant plane of one matrix in every slot: bytes x rows x slots.
-cudaError_t mapq(CUtensorMap* m, const void* base, int64_t kbytes, int64_t rows, int64_t slots,
-                 int64_t slot_stride, int box_rows) {
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kbytes), static_cast<cuuint64_t>(rows),
-                        static_cast<cuuint64_t>(slots)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(kbytes), static_cast<cuuint64_t>(slot_stride)};
-  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
-  cuuint32_t es[3] = {1, 1, 1};
-  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+// Q8_0 quant planes in every slot: bytes x rows x matrix x slot. The box is
+// 64 bytes x box_rows x n_mat: the gate/up GEMM reads the same rows of the
+// gate plane and of the up plane (mat_stride bytes further) in one copy.
+// The 64-byte swizzle lets the dequantising threads read one row each
+// without bank conflicts.
+cudaError_t mapq(CUtensorMap* m, const void* base, int64_t kbytes, int64_t rows, int64_t mat_stride, int n_mat,
+                 int64_t slots, int64_t slot_stride, int box_rows) {
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(kbytes), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(n_mat), static_cast<cuuint64_t>(slots)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(kbytes), static_cast<cuuint64_t>(mat_stride),
+                           static_cast<cuuint64_t>(slot_stride)};
+  cuuint32_t box[4] = {64, static_cast<cuuint32_t>(box_rows), static_cast<cuuint32_t>(n_mat), 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
@@ -166,21 +180,24 @@ cudaError_t prefill_ffn(const PrefillArgs& p, cudaStream_t st) {
   // 3. tensor maps (pointers are fixed per context and layer)
   GemmMaps m0{}, m1{};
   const int64_t S = p.S;
-  if ((e = map16(&m0.a, p.x16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, rows, p.H)) != cudaSuccess) return e;
-  if ((e = mapq(&m0.q0, p.pool + g.qoff[0], p.H, p.I, S, p.slot_stride, 128)) != cudaSuccess) return e;
-  if ((e = mapq(&m0.q1, p.pool + g.qoff[1], p.H, p.I, S, p.slot_stride, 128)) != cudaSuccess) return e;
-  if ((e = map16(&m1.a, p.h, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rows, p.ldh)) != cudaSuccess) return e;
-  if ((e = mapq(&m1.q0, p.pool + g.qoff[2], p.I, p.H, S, p.slot_stride, 256)) != cudaSuccess) return e;
-  m1.q1 = m1.q0;
+  const auto F16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16, BF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  if ((e = map16(&m0.b32, p.x16, F16, rows, p.H, 32)) != cudaSuccess) return e;
+  if ((e = map16(&m0.btile, p.x16, F16, rows, p.H, kPrefillTok)) != cudaSuccess) return e;
+  if ((e = map16(&m1.b32, p.h, BF16, rows, p.ldh, 32)) != cudaSuccess) return e;
+  if ((e = map16(&m1.btile, p.h, BF16, rows, p.ldh, kPrefillTok)) != cudaSuccess) return e;
+  if ((e = mapq(&m0.q, p.pool + g.qoff[0], p.H, p.I, g.qoff[1] - g.qoff[0], 2, S, p.slot_stride, 64)) != cudaSuccess)
+    return e;
+  if ((e = mapq(&m1.q, p.pool + g.qoff[2], p.I, p.H, g.qbytes[2], 1, S, p.slot_stride, 128)) != cudaSuccess) return e;
   if (p.shared) {
-    if ((e = mapq(&m0.sq0, p.shared + gs.qoff[0], p.H, p.Is, 1, gs.bytes, 128)) != cudaSuccess) return e;
-    if ((e = mapq(&m0.sq1, p.shared + gs.qoff[1], p.H, p.Is, 1, gs.bytes, 128)) != cudaSuccess) return e;
-    if ((e = mapq(&m1.sq0, p.shared + gs.qoff[2], p.Is, p.H, 1, gs.bytes, 256)) != cudaSuccess) return e;
+    if ((e = mapq(&m0.sq, p.shared + gs.qoff[0], p.H, p.Is, gs.qoff[1] - gs.qoff[0], 2, 1, gs.bytes, 64)) !=
+        cudaSuccess)
+      return e;
+    if ((e = mapq(&m1.sq, p.shared + gs.qoff[2], p.Is, p.H, gs.qbytes[2], 1, 1, gs.bytes, 128)) != cudaSuccess)
+      return e;
   } else {
-    m0.sq0 = m0.sq1 = m0.q0;
-    m1.sq0 = m1.q0;
+    m0.sq = m0.q;
+    m1.sq = m1.q;
   }
-  m1.sq1 = m1.sq0;
   GemmArgs a{};
   a.units = p.units;
   a.pool = p.pool;
@@ -206,21 +223,23 @@ cudaError_t prefill_ffn(const PrefillArgs& p, cudaStream_t st) {
   a.n_items = p.n_items0;
   a.kmax = p.H;
   a.stages = gemm_stages(a.kmax);
+  a.sc_bytes = gemm_scale_bytes(a.kmax);
   if (a.stages == 0) return cudaErrorInvalidValue;
   if (p.ev[0]) cudaEventRecord(p.ev[0], st);
-  if ((e = launch_gemm(0, m0, a, p.max_items0, st)) != cudaSuccess) return e;
+  if ((e = launch_gemm(0, m0, a, std::min(p.max_items0, p.n_sm), st)) != cudaSuccess) return e;
   if (p.ev[1]) cudaEventRecord(p.ev[1], st);
   // 5. down, weighted by the combine weights
   a.items = p.items1;
   a.n_items = p.n_items1;
   a.kmax = p.shared ? std::max(p.I, p.Is) : p.I;
   a.stages = gemm_stages(a.kmax);
+  a.sc_bytes = gemm_scale_bytes(a.kmax);
   if (a.stages == 0) return cudaErrorInvalidValue;
   if (p.ev[2]) cudaEventRecord(p.ev[2], st);
-  if ((e = launch_gemm(1, m1, a, p.max_items1, st)) != cudaSuccess) return e;
+  if ((e = launch_gemm(1, m1, a, std::min(p.max_items1, p.n_sm), st)) != cudaSuccess) return e;
   if (p.ev[3]) cudaEventRecord(p.ev[3], st);
   // 6. combine into the tokens' positions
-  combine_kernel<<<p.T, 256, 0, st>>>(p.yp, p.plan.inv, p.T, p.k, p.H, p.shared ? 1 : 0, p.y);
+  combine_kernel<<<p.T, 256, 0, st>>>(p.yp, p.plan.inv, p.plan.perm_w, p.T, p.k, p.H, p.shared ? 1 : 0, p.y);
   return cudaGetLastError();
 }
 

@@ -9,11 +9,14 @@
 
 namespace moe {
 
-// Tensor maps of one GEMM launch: the activation operand, the routed quant
-// planes (3-D: bytes, rows, slot) and the shared expert's quant planes
-// (3-D with one slot). q1/sq1 are the up planes (gate/up GEMM only).
+constexpr int kPrefillTok = 192;  // tokens per GEMM work item
+
+// Tensor maps of one GEMM launch: the token operand in 32-row boxes and in
+// whole-tile boxes, and the quant planes of the routed experts (4-D: bytes,
+// rows, matrix, slot; the gate/up GEMM takes the gate and up planes in one
+// box) and of the shared expert (one slot).
 struct GemmMaps {
-  CUtensorMap a, q0, q1, sq0, sq1;
+  CUtensorMap b32, btile, q, sq;
 };
 
 struct GemmArgs {
@@ -34,6 +37,7 @@ struct GemmArgs {
   const uint32_t* gen;      // [S] published slot generations (fail-closed check)
   int S;
   int stages, kmax;
+  int sc_bytes;             // shared memory per item-scale buffer
 };
 
 // One prefill FFN call: gather, both GEMMs, combine.
@@ -53,6 +57,7 @@ struct PrefillArgs {
   float* y;                 // [T][H]
   int32_t *items0, *n_items0, *items1, *n_items1;
   int max_items0, max_items1;
+  int n_sm;                 // persistent GEMM grid
   uint32_t* err;
   const uint32_t* gen;
   cudaEvent_t ev[4];        // optional timing around the two GEMMs
@@ -60,6 +65,7 @@ struct PrefillArgs {
 cudaError_t prefill_ffn(const PrefillArgs& p, cudaStream_t st);
 
 int gemm_stages(int K);
+int gemm_scale_bytes(int K);
 size_t gemm_smem_bytes(int stages, int K);
 cudaError_t launch_gemm(int phase, const GemmMaps& m, const GemmArgs& a, int grid, cudaStream_t st);
 

@@ -1075,43 +1075,108 @@ __global__ void __launch_bounds__(256) row_norms_kernel(const void* x, int T, co
   }
 }
 
+// One 64-token x 64-expert tile per 128-thread block; a thread owns 8 tokens
+// x 4 experts. K advances in chunks of 32 through a double-buffered,
+// transposed shared-memory stage; the next chunk's global loads are issued
+// before the current chunk's FMAs.
+constexpr int kLThreads = 128;
+constexpr int kLPad = kLT + 4;
+
 template <int XT>
-__global__ void __launch_bounds__(256) logits_tiled_kernel(RouteArgs a, const float* xn, const float* wn) {
-  __shared__ __align__(16) float xs[kLK][kLT + 4];
-  __shared__ __align__(16) float ws[kLK][kLE + 4];
+__device__ __forceinline__ void logits_fetch(const RouteArgs& a, int t0, int e0, int kc, float (&xv)[2][8],
+                                             float4 (&wv)[4]) {
+  const int tid = threadIdx.x;
+#pragma unroll
+  for (int rep = 0; rep < 2; ++rep) {
+    const int idx = tid + kLThreads * rep, r = idx & 63, part = idx >> 6;  // k = part*8 .. +7
+    const int t = t0 + r;
+    const size_t off = static_cast<size_t>(t) * a.H + kc + part * 8;
+    if (t >= a.T) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) xv[rep][j] = 0.f;
+    } else if (XT == MOE_BF16) {
+      const uint4 u = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.x) + off));
+      const uint32_t wds[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        xv[rep][2 * j] = __uint_as_float(wds[j] << 16);
+        xv[rep][2 * j + 1] = __uint_as_float(wds[j] & 0xFFFF0000u);
+      }
+    } else {
+      const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(a.x) + off);
+      const float4 p = __ldg(src), q = __ldg(src + 1);
+      xv[rep][0] = p.x, xv[rep][1] = p.y, xv[rep][2] = p.z, xv[rep][3] = p.w;
+      xv[rep][4] = q.x, xv[rep][5] = q.y, xv[rep][6] = q.z, xv[rep][7] = q.w;
+    }
+  }
+#pragma unroll
+  for (int rep = 0; rep < 4; ++rep) {
+    const int idx = tid + kLThreads * rep, r = idx & 63, q = idx >> 6;  // k = q*4 .. +3
+    const int e = e0 + r;
+    wv[rep] = e < a.E ? __ldg(reinterpret_cast<const float4*>(a.w + static_cast<size_t>(e) * a.H + kc + q * 4))
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+
+__device__ __forceinline__ void logits_stash(float (*xs)[kLPad], float (*ws)[kLPad], const float (&xv)[2][8],
+                                             const float4 (&wv)[4]) {
+  const int tid = threadIdx.x;
+#pragma unroll
+  for (int rep = 0; rep < 2; ++rep) {
+    const int idx = tid + kLThreads * rep, r = idx & 63, part = idx >> 6;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) xs[part * 8 + j][r] = xv[rep][j];
+  }
+#pragma unroll
+  for (int rep = 0; rep < 4; ++rep) {
+    const int idx = tid + kLThreads * rep, r = idx & 63, q = idx >> 6;
+    ws[q * 4 + 0][r] = wv[rep].x;
+    ws[q * 4 + 1][r] = wv[rep].y;
+    ws[q * 4 + 2][r] = wv[rep].z;
+    ws[q * 4 + 3][r] = wv[rep].w;
+  }
+}
+
+template <int XT>
+__global__ void __launch_bounds__(kLThreads) logits_tiled_kernel(RouteArgs a, const float* xn, const float* wn) {
+  __shared__ __align__(16) float xs[2][kLK][kLPad];
+  __shared__ __align__(16) float ws[2][kLK][kLPad];
   const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
   const int t0 = blockIdx.y * kLT, e0 = blockIdx.x * kLE;
   const int T = a.T, E = a.E, H = a.H;
-  float hi[4][4], lo[4][4];
+  float hi[8][4], lo[8][4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < 8; ++i)
 #pragma unroll
     for (int j = 0; j < 4; ++j) hi[i][j] = lo[i][j] = 0.f;
-  for (int kc = 0; kc < H; kc += kLK) {
-    // 64 rows x 32 k of x and of w, transposed into [k][row]
-    for (int i = tid; i < kLT * kLK; i += 256) {
-      const int r = i / kLK, k = i - r * kLK;
-      xs[k][r] = (t0 + r < T) ? load_x<XT>(a.x, static_cast<size_t>(t0 + r) * H + kc + k) : 0.f;
-      ws[k][r] = (e0 + r < E) ? __ldg(a.w + static_cast<size_t>(e0 + r) * H + kc + k) : 0.f;
-    }
-    __syncthreads();
-    float p[4][4];
+  float xv[2][8];
+  float4 wv[4];
+  logits_fetch<XT>(a, t0, e0, 0, xv, wv);
+  logits_stash(xs[0], ws[0], xv, wv);
+  __syncthreads();
+  const int nch = H / kLK;
+  for (int c = 0; c < nch; ++c) {
+    const int buf = c & 1;
+    if (c + 1 < nch) logits_fetch<XT>(a, t0, e0, (c + 1) * kLK, xv, wv);
+    float p[8][4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < 8; ++i)
 #pragma unroll
       for (int j = 0; j < 4; ++j) p[i][j] = 0.f;
-#pragma unroll 8
+#pragma unroll 4
     for (int k = 0; k < kLK; ++k) {
-      const float4 xv = *reinterpret_cast<const float4*>(&xs[k][ty * 4]);
-      const float4 wv = *reinterpret_cast<const float4*>(&ws[k][tx * 4]);
-      const float xa[4] = {xv.x, xv.y, xv.z, xv.w}, wa[4] = {wv.x, wv.y, wv.z, wv.w};
+      const float4 x0 = *reinterpret_cast<const float4*>(&xs[buf][k][ty * 8]);
+      const float4 x1 = *reinterpret_cast<const float4*>(&xs[buf][k][ty * 8 + 4]);
+      const float4 wq = *reinterpret_cast<const float4*>(&ws[buf][k][tx * 4]);
+      const float xa[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+      const float wa[4] = {wq.x, wq.y, wq.z, wq.w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+      for (int i = 0; i < 8; ++i)
 #pragma unroll
         for (int j = 0; j < 4; ++j) p[i][j] = fmaf(xa[i], wa[j], p[i][j]);
     }
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < 8; ++i)
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         float ns, es;
@@ -1119,13 +1184,14 @@ __global__ void __launch_bounds__(256) logits_tiled_kernel(RouteArgs a, const fl
         hi[i][j] = ns;
         lo[i][j] = __fadd_rn(lo[i][j], es);
       }
+    if (c + 1 < nch) logits_stash(xs[buf ^ 1], ws[buf ^ 1], xv, wv);
     __syncthreads();
   }
   const size_t te = static_cast<size_t>(T) * E;
   const double g32 = 32.0 * 0x1p-24 / (1.0 - 32.0 * 0x1p-24);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int t = t0 + ty * 4 + i;
+  for (int i = 0; i < 8; ++i) {
+    const int t = t0 + ty * 8 + i;
     if (t >= T) continue;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -1159,32 +1225,66 @@ __global__ void __launch_bounds__(256) select_kernel(RouteArgs a, int* flags) {
   if (lane == 0) flags[t] = ok ? 0 : 1;
 }
 
+// Exact repair of an uncertified token. Only the experts whose rank the bound
+// intervals leave open are recomputed: the candidates are the experts that
+// fewer than k others beat for certain (lower bound above their upper
+// bound); a candidate whose interval meets another candidate's is
+// recomputed exactly (its three keys collapse to the exact logit's). Every
+// other expert is either certainly outside the top k or certainly ordered
+// against each candidate, so selecting by the logit keys afterwards yields
+// the ranking of the exact logits, ties to the lower expert id.
 template <int XT>
 __global__ void __launch_bounds__(kRouteThreads) repair_kernel(RouteArgs a, const int* flags) {
+  __shared__ unsigned long long s_lo[1024], s_hi[1024];
+  __shared__ unsigned char s_cand[1024];
+  __shared__ int s_amb[1024];
+  __shared__ int s_namb;
   const int t = blockIdx.x;
   if (t >= a.T || __ldg(flags + t) == 0) return;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int E = a.E, H = a.H;
-  const size_t te = static_cast<size_t>(a.T) * E;
-  for (int ee = warp; ee < E; ee += kRouteWarps) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int E = a.E, H = a.H, k = a.k;
+  const size_t te = static_cast<size_t>(a.T) * E, o = static_cast<size_t>(t) * E;
+  for (int e = tid; e < E; e += kRouteThreads) {
+    s_lo[e] = __ldcg(a.keys + te + o + e);
+    s_hi[e] = __ldcg(a.keys + 2 * te + o + e);
+  }
+  if (tid == 0) s_namb = 0;
+  __syncthreads();
+  for (int e = tid; e < E; e += kRouteThreads) {
+    const unsigned long long h = s_hi[e];
+    int above = 0;
+    for (int j = 0; j < E; ++j) above += s_lo[j] > h ? 1 : 0;
+    s_cand[e] = above < k ? 1 : 0;
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += kRouteThreads) {
+    if (!s_cand[e]) continue;
+    const unsigned long long l = s_lo[e], h = s_hi[e];
+    bool meets = false;
+    for (int j = 0; j < E && !meets; ++j)
+      meets = j != e && s_cand[j] && !(l > s_hi[j] || s_lo[j] > h);
+    if (meets) s_amb[atomicAdd(&s_namb, 1)] = e;
+  }
+  __syncthreads();
+  const int namb = s_namb;
+  for (int i = warp; i < namb; i += kRouteWarps) {
+    const int ee = s_amb[i];
     double v;
     const bool fin = warp_exact_logit<XT>(a.x, static_cast<size_t>(t) * H, a.w + static_cast<size_t>(ee) * H,
                                           H, a.bias, ee, v);
     if (lane == 0) {
       if (!fin) atomicOr(a.err, MOE_DEVERR_NONFINITE);
-      const size_t o = static_cast<size_t>(t) * E + ee;
-      a.keys[o] = a.keys[te + o] = a.keys[2 * te + o] = okey(v);
+      a.keys[o + ee] = a.keys[te + o + ee] = a.keys[2 * te + o + ee] = okey(v);
     }
   }
   __syncthreads();
   if (warp == 0) {
-    const size_t o = static_cast<size_t>(t) * E;
     const TokenKeys K{a.keys + o, a.keys + te + o, a.keys + 2 * te + o};
     int sel[16];
     unsigned long long selk[16];
-    warp_select(K, E, a.k, sel, selk, false);
-    warp_write_selection(sel, selk, a.k, a.topk_idx + static_cast<size_t>(t) * a.k,
-                         a.topk_w + static_cast<size_t>(t) * a.k);
+    warp_select(K, E, k, sel, selk, false);
+    warp_write_selection(sel, selk, k, a.topk_idx + static_cast<size_t>(t) * k,
+                         a.topk_w + static_cast<size_t>(t) * k);
     if (lane == 0) atomicAdd(a.repairs, 1ull);
   }
 }
@@ -1285,9 +1385,9 @@ cudaError_t launch_route_large(const RouteArgs& a, float* norms, int* flags, cud
     row_norms_kernel<MOE_F32><<<(nrows + 7) / 8, 256, 0, st>>>(a.x, a.T, a.w, a.E, a.H, xn, wn);
   dim3 grid((a.E + kLE - 1) / kLE, (a.T + kLT - 1) / kLT);
   if (a.xt == MOE_BF16)
-    logits_tiled_kernel<MOE_BF16><<<grid, 256, 0, st>>>(a, xn, wn);
+    logits_tiled_kernel<MOE_BF16><<<grid, kLThreads, 0, st>>>(a, xn, wn);
   else
-    logits_tiled_kernel<MOE_F32><<<grid, 256, 0, st>>>(a, xn, wn);
+    logits_tiled_kernel<MOE_F32><<<grid, kLThreads, 0, st>>>(a, xn, wn);
   select_kernel<<<(a.T + 7) / 8, 256, 0, st>>>(a, flags);
   if (a.xt == MOE_BF16)
     repair_kernel<MOE_BF16><<<a.T, kRouteThreads, 0, st>>>(a, flags);
