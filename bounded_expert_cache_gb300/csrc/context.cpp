@@ -247,7 +247,7 @@ extern "C" moe_status_t moe_create(const moe_config_t* cfg, moe_ctx_t** out) {
     ctx->ldh_p = static_cast<int>(round_up(std::max(c.inter, c.shared_inter), 64));
     const int64_t mtiles = (rows + moe::kPrefillTok - 1) / moe::kPrefillTok +
                            std::min<int64_t>(E, static_cast<int64_t>(c.max_tokens) * c.top_k) + 1;
-    ctx->max_items0 = static_cast<int>(mtiles * ((std::max(c.inter, c.shared_inter) + 63) / 64));
+    ctx->max_items0 = static_cast<int>(mtiles * ((std::max(c.inter, c.shared_inter) + 127) / 128));
     ctx->max_items1 = static_cast<int>(mtiles * ((c.hidden + 127) / 128));
     CKC(cudaMalloc(&ctx->d_x16, sizeof(uint16_t) * rows * c.hidden));
     CKC(cudaMalloc(&ctx->d_hp, sizeof(uint16_t) * rows * ctx->ldh_p));

@@ -51,7 +51,7 @@ __global__ void __launch_bounds__(256) gather_kernel(const void* x, int T, int k
 }
 
 // Work items of both GEMMs from the unit table: per unit, 192-token tiles
-// times weight tiles (64 gate rows with the same 64 up rows, or 128 down
+// times weight tiles (128 gate rows with the same 128 up rows, or 128 down
 // rows); the weight tile varies fastest so that consecutive CTAs share a
 // token tile.
 __global__ void __launch_bounds__(1024) items_kernel(const int32_t* units, int I, int Is, int H,
@@ -64,7 +64,7 @@ __global__ void __launch_bounds__(1024) items_kernel(const int32_t* units, int I
   if (u < nu) {
     const int4 U = __ldg(reinterpret_cast<const int4*>(units + kUnitHeader) + u);
     mt = (U.z + kPrefillTok - 1) / kPrefillTok;
-    nt0 = (U.x == -1 ? Is : I) / 64;
+    nt0 = ((U.x == -1 ? Is : I) + 127) / 128;
     nt1 = H / 128;
     a = mt * nt0;
     b = mt * nt1;
@@ -89,7 +89,7 @@ __global__ void __launch_bounds__(1024) items_kernel(const int32_t* units, int I
     int o = c0[u];
     for (int m = 0; m < mt; ++m)
       for (int n = 0; n < nt0; ++n, ++o)
-        reinterpret_cast<int4*>(items0)[o] = make_int4(u, m * kPrefillTok, n * 64, 0);
+        reinterpret_cast<int4*>(items0)[o] = make_int4(u, m * kPrefillTok, n * 128, 0);
     o = c1[u];
     for (int m = 0; m < mt; ++m)
       for (int n = 0; n < nt1; ++n, ++o)
@@ -185,11 +185,11 @@ cudaError_t prefill_ffn(const PrefillArgs& p, cudaStream_t st) {
   if ((e = map16(&m0.btile, p.x16, F16, rows, p.H, kPrefillTok)) != cudaSuccess) return e;
   if ((e = map16(&m1.b32, p.h, BF16, rows, p.ldh, 32)) != cudaSuccess) return e;
   if ((e = map16(&m1.btile, p.h, BF16, rows, p.ldh, kPrefillTok)) != cudaSuccess) return e;
-  if ((e = mapq(&m0.q, p.pool + g.qoff[0], p.H, p.I, g.qoff[1] - g.qoff[0], 2, S, p.slot_stride, 64)) != cudaSuccess)
+  if ((e = mapq(&m0.q, p.pool + g.qoff[0], p.H, p.I, g.qoff[1] - g.qoff[0], 2, S, p.slot_stride, 128)) != cudaSuccess)
     return e;
   if ((e = mapq(&m1.q, p.pool + g.qoff[2], p.I, p.H, g.qbytes[2], 1, S, p.slot_stride, 128)) != cudaSuccess) return e;
   if (p.shared) {
-    if ((e = mapq(&m0.sq, p.shared + gs.qoff[0], p.H, p.Is, gs.qoff[1] - gs.qoff[0], 2, 1, gs.bytes, 64)) !=
+    if ((e = mapq(&m0.sq, p.shared + gs.qoff[0], p.H, p.Is, gs.qoff[1] - gs.qoff[0], 2, 1, gs.bytes, 128)) !=
         cudaSuccess)
       return e;
     if ((e = mapq(&m1.sq, p.shared + gs.qoff[2], p.Is, p.H, gs.qbytes[2], 1, 1, gs.bytes, 128)) != cudaSuccess)
@@ -221,9 +221,7 @@ cudaError_t prefill_ffn(const PrefillArgs& p, cudaStream_t st) {
   // 4. gate/up + SwiGLU
   a.items = p.items0;
   a.n_items = p.n_items0;
-  a.kmax = p.H;
-  a.stages = gemm_stages(a.kmax);
-  a.sc_bytes = gemm_scale_bytes(a.kmax);
+  a.stages = gemm_stages(0);
   if (a.stages == 0) return cudaErrorInvalidValue;
   if (p.ev[0]) cudaEventRecord(p.ev[0], st);
   if ((e = launch_gemm(0, m0, a, std::min(p.max_items0, p.n_sm), st)) != cudaSuccess) return e;
@@ -231,9 +229,7 @@ cudaError_t prefill_ffn(const PrefillArgs& p, cudaStream_t st) {
   // 5. down, weighted by the combine weights
   a.items = p.items1;
   a.n_items = p.n_items1;
-  a.kmax = p.shared ? std::max(p.I, p.Is) : p.I;
-  a.stages = gemm_stages(a.kmax);
-  a.sc_bytes = gemm_scale_bytes(a.kmax);
+  a.stages = gemm_stages(1);
   if (a.stages == 0) return cudaErrorInvalidValue;
   if (p.ev[2]) cudaEventRecord(p.ev[2], st);
   if ((e = launch_gemm(1, m1, a, std::min(p.max_items1, p.n_sm), st)) != cudaSuccess) return e;

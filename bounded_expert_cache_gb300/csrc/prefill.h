@@ -36,8 +36,7 @@ struct GemmArgs {
   uint32_t* err;
   const uint32_t* gen;      // [S] published slot generations (fail-closed check)
   int S;
-  int stages, kmax;
-  int sc_bytes;             // shared memory per item-scale buffer
+  int stages;
 };
 
 // One prefill FFN call: gather, both GEMMs, combine.
@@ -64,9 +63,8 @@ struct PrefillArgs {
 };
 cudaError_t prefill_ffn(const PrefillArgs& p, cudaStream_t st);
 
-int gemm_stages(int K);
-int gemm_scale_bytes(int K);
-size_t gemm_smem_bytes(int stages, int K);
+int gemm_stages(int phase);
+size_t gemm_smem_bytes(int phase, int stages);
 cudaError_t launch_gemm(int phase, const GemmMaps& m, const GemmArgs& a, int grid, cudaStream_t st);
 
 }  // namespace moe

@@ -11,31 +11,30 @@
 // activations (gathered once, fp16) and later its SwiGLU outputs h (bf16).
 // The weights are the MMA's A operand (M side) and the tokens its B operand
 // (N side), so a weight tile is dequantised once for up to 192 tokens:
-//   gate/up: D[128 x n] = [64 gate rows | the same 64 up rows] x X^T
-//            -> SwiGLU -> h[n tokens][64 columns]   (fp16 operands: x exact,
-//            d*q rounded to fp16)
-//   down:    D[128 x n] = [128 down rows] x h^T -> fp32 rows (bf16
-//            operands: h and d*q rounded to bf16; h may exceed the fp16
-//            range); the combine applies the routing weights
-// The dequantised A tile never touches shared memory: it is written to
+//   gate/up: G = Wg[128 rows] x X^T and U = Wu[the same rows] x X^T, two
+//            MMAs per K slice on one token tile -> SwiGLU in the epilogue
+//            -> h[n tokens][128 columns]  (fp16 operands: x exact, d*q
+//            rounded to fp16)
+//   down:    D = Wd[128 rows] x h^T -> fp32 rows (bf16 operands: h and d*q
+//            rounded to bf16; h may exceed the fp16 range); the combine
+//            applies the routing weights
+// The dequantised A tiles never touch shared memory: they are written to
 // tensor memory with tcgen05.st and the MMA reads A from there, so shared
-// memory holds only the TMA ring (token tile, raw Q8_0 rows, block scales).
+// memory holds only the TMA ring (token tile and raw Q8_0 rows).
 // A persistent CTA of 14 warps walks the work items (unit, token tile,
 // weight tile) of the launch:
 //   warp 0      TMA, two copies per stage: the token tile (64 K, 128-byte
 //               swizzle; one box for a whole tile, 32-row boxes for a
-//               partial one) and the raw Q8_0 rows of the weight tile
-//               (64-byte swizzle) addressed in the slot pool through a 4-D
-//               tensor map (bytes, rows, matrix, slot); once per item, a
-//               bulk copy of the tile's block scales into a double buffer
-//   warp 1      allocates TMEM (two 128-lane x 192-column fp32
-//               accumulators and four 32-column A stages) and issues
-//               tcgen05.mma (M 128, N <= 192, K 16, A from TMEM, B from a
-//               shared-memory descriptor)
-//   warps 2..9  dequantise one Q8_0 block (32 weights) of one row per stage
-//               each and store it to the A stage of their TMEM lane group
-//   warps 10-13 epilogue of one accumulator (tcgen05.ld) while the MMAs of
-//               the next item fill the other
+//               partial one) and the raw Q8_0 rows of the weight tile(s)
+//               (64-byte swizzle), addressed in the slot pool through a 4-D
+//               tensor map (bytes, rows, matrix, slot)
+//   warp 1      allocates TMEM and issues tcgen05.mma (M 128, N <= 192,
+//               K 16, A from TMEM, B from a shared-memory descriptor);
+//               gate/up: one accumulator pair (G, U); down: two
+//               accumulators so the epilogue overlaps the next item
+//   warps 2..9  dequantise (block scales prefetched into registers) and
+//               store to the A stage of their TMEM lane group
+//   warps 10-13 epilogue (tcgen05.ld)
 // Every wait is bounded; a wait that runs out sets an error bit and every
 // role leaves its loop; in-flight copies and MMAs are drained before TMEM
 // is released.
@@ -51,22 +50,33 @@ namespace {
 
 constexpr int kMaxStages = 8;
 constexpr int kTok = kPrefillTok;  // tokens per item (MMA N at most)
-constexpr int kWR = 128;           // weight rows per item (MMA M)
+constexpr int kWR = 128;           // weight rows per tile (MMA M)
 constexpr int kBK = 64;            // K per stage
-constexpr int kAStages = 4;        // A stages in TMEM (32 columns each)
-constexpr uint32_t kAcol0 = 2 * kTok;  // first A column (after two accumulators)
 constexpr int kThreadsG = 448;
 constexpr int kDqWarps = 8, kEpWarps = 4;
 constexpr int kEpTid0 = 64 + 32 * kDqWarps;   // first epilogue thread
 constexpr uint32_t kBBytes = kTok * kBK * 2;  // 24 KiB of tokens
-constexpr uint32_t kQBytes = kWR * kBK;       // 8 KiB raw int8
-constexpr uint32_t kStageBytes = kBBytes + kQBytes;
-constexpr uint32_t kEpiBytes = 16384;   // epilogue exchange + transpose
-constexpr int kGeoCap = 96;             // items per CTA kept in shared memory
-constexpr int kXP = 20;                 // floats per exchange row
-constexpr int kSP = 72;                 // bf16 per transpose row
-static_assert(kAcol0 + kAStages * 32 <= 512, "TMEM columns");
+constexpr uint32_t kAcc = 2 * kTok;           // TMEM columns of the accumulators
+constexpr int kGeoCap = 96;                   // items per CTA kept in shared memory
+constexpr int kSP = kWR + 8;                  // bf16 per transpose row (gate/up epilogue)
+constexpr int kPF = 4;                        // stages of block scales prefetched
 static_assert(kBBytes % 1024 == 0 && kTok % 32 == 0, "stage alignment");
+
+// Per-phase shape: weight tiles per item (gate + up, or down), raw quant
+// bytes per stage, A stages in TMEM (each tiles x 32 columns), accumulator
+// buffers.
+template <int PHASE> struct Shape {
+  static constexpr int kTiles = PHASE == 0 ? 2 : 1;
+  static constexpr uint32_t kQBytes = kTiles * kWR * kBK;
+  static constexpr uint32_t kStageBytes = kBBytes + kQBytes;
+  static constexpr int kAStages = PHASE == 0 ? 2 : 4;
+  static constexpr uint32_t kAStride = 32u * kTiles;  // TMEM columns per A stage
+  static constexpr int kAccBufs = PHASE == 0 ? 1 : 2;
+  static constexpr uint32_t kEpiBytes = PHASE == 0 ? 32u * kSP * 2 : 0u;
+  static_assert(kAcc + kAStages * kAStride <= 512, "TMEM columns");
+  static_assert(kStageBytes % 1024 == 0, "stage alignment");
+};
+
 constexpr long long kWaitCycles = 4000000000ll;  // about 2 s at the SM clock
 
 __device__ __forceinline__ uint32_t su32(const void* p) {
@@ -137,13 +147,6 @@ __device__ __forceinline__ void tma2d(uint32_t dst, const CUtensorMap* m, uint32
       "l"(m), "r"(bar), "r"(x), "r"(y)
       : "memory");
 }
-__device__ __forceinline__ void tma3d(uint32_t dst, const CUtensorMap* m, uint32_t bar, int x, int y, int z) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(
-          dst),
-      "l"(m), "r"(bar), "r"(x), "r"(y), "r"(z)
-      : "memory");
-}
 __device__ __forceinline__ void tma4d(uint32_t dst, const CUtensorMap* m, uint32_t bar, int x, int y, int z,
                                       int w) {
   asm volatile(
@@ -151,11 +154,6 @@ __device__ __forceinline__ void tma4d(uint32_t dst, const CUtensorMap* m, uint32
           dst),
       "l"(m), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w)
       : "memory");
-}
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-               "l"(src), "r"(bytes), "r"(bar)
-               : "memory");
 }
 // Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
 // 1024 bytes apart.
@@ -200,10 +198,6 @@ __device__ __forceinline__ uint4 lds128(uint32_t a) {
   uint4 v;
   asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
   return v;
-}
-__device__ __forceinline__ void sts128(uint32_t a, uint4 v) {
-  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-               : "memory");
 }
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
@@ -267,7 +261,7 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
 
 // Geometry of one work item, derived identically by every role.
 struct ItemGeo {
-  int m0, n0, slot, p0, ntok, K, shared, stale;
+  int m0, n0, slot, p0, ntok, K, nrows, flags;  // flags: 1 shared, 2 stale
 };
 
 template <int PHASE>
@@ -277,14 +271,18 @@ __device__ __forceinline__ ItemGeo item_geo(const GemmArgs& a, int bid) {
   g.m0 = t.y;
   g.n0 = t.z;
   const int4 U = __ldg(reinterpret_cast<const int4*>(a.units + kUnitHeader) + t.x);
-  g.shared = U.x == -1;
+  const bool shared = U.x == -1;
   g.slot = U.x >= 0 ? U.x : (U.x <= -2 ? -2 - U.x : 0);
-  g.p0 = g.shared ? a.rows_routed : U.y;
+  g.p0 = shared ? a.rows_routed : U.y;
   g.ntok = min(kTok, U.z - g.m0);
-  g.K = PHASE == 0 ? a.H : (g.shared ? a.Is : a.I);
+  g.K = PHASE == 0 ? a.H : (shared ? a.Is : a.I);
+  // weight rows of the tile inside the matrix (gate/up rows run to I or I_s)
+  g.nrows = PHASE == 0 ? min(kWR, (shared ? a.Is : a.I) - g.n0) : kWR;
   // fail closed: a routed expert is used only if its slot holds the
   // generation its page-table entry expects
-  g.stale = !g.shared && (g.slot >= a.S || (U.x >= 0 && __ldg(a.gen + g.slot) != static_cast<uint32_t>(U.w)));
+  const bool stale =
+      !shared && (g.slot >= a.S || (U.x >= 0 && __ldg(a.gen + g.slot) != static_cast<uint32_t>(U.w)));
+  g.flags = (shared ? 1 : 0) | (stale ? 2 : 0);
   return g;
 }
 
@@ -297,21 +295,41 @@ __device__ __forceinline__ ItemGeo geo_of(const GemmArgs& a, const ItemGeo* tabl
   return item_geo<PHASE>(a, blockIdx.x + i * gridDim.x);
 }
 
+// First item at or after i that is not stale (my_items if none).
+template <int PHASE>
+__device__ __forceinline__ int next_live(const GemmArgs& a, const ItemGeo* table, int i, int my_items) {
+  while (i < my_items && (geo_of<PHASE>(a, table, i).flags & 2)) ++i;
+  return i;
+}
+
+// Block-scale word (the two fp16 scales of one stage) of this thread's
+// weight row: gate/up: tile t is the gate (0) or up (1) plane; down: the
+// down plane. Rows past the matrix read as 0.
+template <int PHASE>
+__device__ __forceinline__ const uint32_t* scale_row(const GemmArgs& a, const ItemGeo& g, int t, int r) {
+  if (r >= g.nrows) return nullptr;
+  const uint8_t* wbase = (g.flags & 1) ? a.shared : a.pool + static_cast<int64_t>(g.slot) * a.slot_stride;
+  const int64_t* soff = (g.flags & 1) ? a.s_soff : a.r_soff;
+  const int64_t plane = PHASE == 0 ? soff[t] : soff[2];
+  return reinterpret_cast<const uint32_t*>(wbase + plane + static_cast<int64_t>(g.n0 + r) * (g.K / 16));
+}
+
 template <int PHASE>  // 0: gate/up + SwiGLU, 1: down
 __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constant__ CUtensorMap map_b32,
                                                             const __grid_constant__ CUtensorMap map_bt,
                                                             const __grid_constant__ CUtensorMap map_q,
                                                             const __grid_constant__ CUtensorMap map_sq,
                                                             GemmArgs a) {
+  using Sh = Shape<PHASE>;
+  constexpr int kAStages = Sh::kAStages;
   extern __shared__ unsigned char smraw[];
   unsigned char* sm =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
   // smem ring: full (TMA bytes), sfree (the MMA's commit + the 8 dequant
-  // warps); item scales: scf (bulk-copy bytes), sce (8 dequant warps); TMEM
-  // A ring: aready (8 dequant warps), afree (the MMA's commit);
-  // accumulators: accf (commit), acce (4 epilogue warps)
-  __shared__ uint64_t bar_full[kMaxStages], bar_sfree[kMaxStages], bar_scf[2], bar_sce[2];
-  __shared__ uint64_t bar_aready[kAStages], bar_afree[kAStages];
+  // warps); TMEM A ring: aready (8 dequant warps), afree (the MMA's
+  // commit); accumulators: accf (commit), acce (4 epilogue warps)
+  __shared__ uint64_t bar_full[kMaxStages], bar_sfree[kMaxStages];
+  __shared__ uint64_t bar_aready[4], bar_afree[4];
   __shared__ uint64_t bar_accf[2], bar_acce[2], bar_drain;
   __shared__ uint32_t tmem_holder;
   __shared__ int s_abort;
@@ -320,8 +338,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int kStages = a.stages;
   const uint32_t sbase = su32(sm);
-  const uint32_t sscale = sbase + static_cast<uint32_t>(kStages) * kStageBytes;  // 2 item-scale buffers
-  const uint32_t sepi = sscale + 2u * static_cast<uint32_t>(a.sc_bytes);
+  const uint32_t sepi = sbase + static_cast<uint32_t>(kStages) * Sh::kStageBytes;
   const int n_items = __ldg(a.n_items);
   const int my_items = blockIdx.x < n_items ? (n_items - 1 - blockIdx.x) / gridDim.x + 1 : 0;
   for (int i = tid; i < my_items && i < kGeoCap; i += kThreadsG)
@@ -331,10 +348,6 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
     for (int s = 0; s < kStages; ++s) {
       mbar_init(su32(&bar_full[s]), 1);
       mbar_init(su32(&bar_sfree[s]), 1 + kDqWarps);
-    }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(su32(&bar_scf[b]), 1);
-      mbar_init(su32(&bar_sce[b]), kDqWarps);
     }
     for (int j = 0; j < kAStages; ++j) {
       mbar_init(su32(&bar_aready[j]), kDqWarps);
@@ -358,93 +371,87 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
   const uint32_t tmem = tmem_holder;
 
   if (warp == 0) {
-    // ---------------- producer (one thread): per item the block scales of
-    // the weight tile (fp16 [rows][K/32]: gate rows then up rows, or the down
-    // rows) by bulk copy; per stage the token tile and the raw quant rows
+    // ---------------- producer (one thread): per stage the token tile and
+    // the raw quant rows (gate/up: rows [n0, n0+128) of the gate and of the
+    // up plane in one box; down: rows [n0, n0+128))
     if (lane == 0) {
-      uint32_t ring = 0, it = 0;
+      uint32_t ring = 0;
       RingPos rp;
       for (int i = 0; i < my_items && !*abort_flag; ++i) {
         const ItemGeo g = geo_of<PHASE>(a, s_geo, i);
-        if (g.stale) continue;
+        if (g.flags & 2) continue;
         const int nkb = g.K / kBK;
         const bool whole = g.ntok == kTok;
         const int nbox = (g.ntok + 31) / 32;
-        const uint32_t bytes = (whole ? kBBytes : static_cast<uint32_t>(nbox) * 4096u) + kQBytes;
-        const uint8_t* wbase = g.shared ? a.shared : a.pool + static_cast<int64_t>(g.slot) * a.slot_stride;
-        const int64_t* soff = g.shared ? a.s_soff : a.r_soff;
-        const int64_t pitch = g.K / 16;  // bytes per scale row
-        const uint32_t sb = it & 1u;
-        if (it >= 2 && !mbar_wait(su32(&bar_sce[sb]), ((it >> 1) & 1u) ^ 1u, abort_flag, a.err)) break;
-        const uint32_t sdst = sscale + sb * static_cast<uint32_t>(a.sc_bytes), scb = su32(&bar_scf[sb]);
-        mbar_expect_tx(scb, static_cast<uint32_t>(kWR * pitch));
-        if (PHASE == 0) {
-          bulk_g2s(sdst, wbase + soff[0] + g.n0 * pitch, static_cast<uint32_t>(64 * pitch), scb);
-          bulk_g2s(sdst + static_cast<uint32_t>(64 * pitch), wbase + soff[1] + g.n0 * pitch,
-                   static_cast<uint32_t>(64 * pitch), scb);
-        } else {
-          bulk_g2s(sdst, wbase + soff[2] + g.n0 * pitch, static_cast<uint32_t>(kWR * pitch), scb);
-        }
-        ++it;
-        const CUtensorMap* mq = g.shared ? &map_sq : &map_q;
-        const int zs = g.shared ? 0 : g.slot;
+        const uint32_t bytes = (whole ? kBBytes : static_cast<uint32_t>(nbox) * 4096u) + Sh::kQBytes;
+        const CUtensorMap* mq = (g.flags & 1) ? &map_sq : &map_q;
+        const int zs = (g.flags & 1) ? 0 : g.slot;
         bool ok = true;
         for (int kb = 0; kb < nkb; ++kb, ++ring, rp.next(kStages)) {
           const int s = rp.s;
           if (ring >= static_cast<uint32_t>(kStages) &&
               !(ok = mbar_wait(su32(&bar_sfree[s]), rp.ph ^ 1u, abort_flag, a.err)))
             break;
-          const uint32_t st = sbase + s * kStageBytes, fb = su32(&bar_full[s]);
+          const uint32_t st = sbase + s * Sh::kStageBytes, fb = su32(&bar_full[s]);
           mbar_expect_tx(fb, bytes);
           if (whole)
             tma2d(st, &map_bt, fb, kb * kBK, g.p0 + g.m0);
           else
             for (int bx = 0; bx < nbox; ++bx) tma2d(st + bx * 4096u, &map_b32, fb, kb * kBK, g.p0 + g.m0 + bx * 32);
-          // gate/up: rows [n0, n0+64) of the gate and of the up plane in one
-          // box; down: rows [n0, n0+128)
           tma4d(st + kBBytes, mq, fb, kb * kBK, g.n0, 0, zs);
         }
         if (!ok) break;
       }
-      // drain: the last copies into each stage and scale buffer complete
+      // drain: the last copies into each stage complete before exit
       const uint32_t n = ring < static_cast<uint32_t>(kStages) ? ring : static_cast<uint32_t>(kStages);
       for (uint32_t j = 0; j < n; ++j) {
         const uint32_t r = ring - 1 - j;
         mbar_drain(su32(&bar_full[r % kStages]), (r / kStages) & 1u, a.err);
       }
-      for (uint32_t j = 0; j < (it < 2u ? it : 2u); ++j) {
-        const uint32_t q = it - 1 - j;
-        mbar_drain(su32(&bar_scf[q & 1u]), (q >> 1) & 1u, a.err);
-      }
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer
+    // ---------------- MMA issuer. It waits only on aready: the dequantising
+    // warps arrive there after they observed the stage's full barrier, so the
+    // token tile of the stage has landed as well.
     if (lane == 0) {
       uint32_t ring = 0, acc_i = 0;
-      RingPos rp, ap;
+      int s = 0, j = 0;
+      uint32_t aph = 0;
       const uint32_t fmt = PHASE == 0 ? 0u : 1u;  // f16 : bf16
+      const uint64_t bd0 = sdesc(sbase);          // B descriptor of stage 0; + 16-byte units
       for (int i = 0; i < my_items && !*abort_flag; ++i) {
         const ItemGeo g = geo_of<PHASE>(a, s_geo, i);
-        if (g.stale) continue;
+        if (g.flags & 2) continue;
         const int nkb = g.K / kBK;
         const uint32_t n = static_cast<uint32_t>((g.ntok + 15) & ~15);
         const uint32_t idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | ((n >> 3) << 17) | ((kWR >> 4) << 24);
-        const uint32_t buf = acc_i & 1u, aph = (acc_i >> 1) & 1u;
-        if (acc_i >= 2 && !mbar_wait(su32(&bar_acce[buf]), aph ^ 1u, abort_flag, a.err)) break;
+        const uint32_t buf = Sh::kAccBufs == 2 ? (acc_i & 1u) : 0u;
+        const uint32_t cph = Sh::kAccBufs == 2 ? ((acc_i >> 1) & 1u) : (acc_i & 1u);
+        if (acc_i >= static_cast<uint32_t>(Sh::kAccBufs) &&
+            !mbar_wait(su32(&bar_acce[buf]), cph ^ 1u, abort_flag, a.err))
+          break;
         asm volatile("tcgen05.fence::after_thread_sync;");
         const uint32_t dt = tmem + buf * static_cast<uint32_t>(kTok);
         bool ok = true;
-        for (int kb = 0; kb < nkb; ++kb, ++ring, rp.next(kStages), ap.next(kAStages)) {
-          const int s = rp.s, j = ap.s;
-          if (!(ok = mbar_wait(su32(&bar_full[s]), rp.ph, abort_flag, a.err))) break;
-          if (!(ok = mbar_wait(su32(&bar_aready[j]), ap.ph, abort_flag, a.err))) break;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!(ok = mbar_wait(su32(&bar_aready[j]), aph, abort_flag, a.err))) break;
           asm volatile("tcgen05.fence::after_thread_sync;");
-          const uint32_t sb = sbase + s * kStageBytes, at = tmem + kAcol0 + 32u * j;
+          const uint64_t bd = bd0 + static_cast<uint64_t>((static_cast<uint32_t>(s) * Sh::kStageBytes) >> 4);
+          const uint32_t at = tmem + kAcc + Sh::kAStride * static_cast<uint32_t>(j);
+          const uint32_t acc0 = kb > 0 ? 1u : 0u;
 #pragma unroll
-          for (int k = 0; k < kBK / 16; ++k)
-            umma_ts(dt, at + 8 * k, sdesc(sb + 32 * k), idesc, (kb > 0 || k > 0) ? 1u : 0u);
+          for (int k = 0; k < kBK / 16; ++k) {
+            umma_ts(dt, at + 8 * k, bd + 2 * k, idesc, k > 0 ? 1u : acc0);
+            if (PHASE == 0) umma_ts(dt + kTok, at + 32 + 8 * k, bd + 2 * k, idesc, k > 0 ? 1u : acc0);  // up rows into U
+          }
           umma_commit(su32(&bar_sfree[s]));
           umma_commit(su32(&bar_afree[j]));
+          ++ring;
+          if (++s == kStages) s = 0;
+          if (++j == kAStages) {
+            j = 0;
+            aph ^= 1u;
+          }
         }
         if (!ok) break;
         umma_commit(su32(&bar_accf[buf]));
@@ -453,136 +460,166 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
       // drain: every MMA issued here has completed before TMEM is released
       umma_commit(su32(&bar_drain));
       mbar_drain(su32(&bar_drain), 0, a.err);
+      (void)ring;
     }
   } else if (warp < 2 + kDqWarps) {
     // ---------------- dequantisation: warp w owns TMEM lanes 32*(w%4) ..
-    // +31 (its weight rows) and one of the stage's two Q8_0 blocks
-    const int sp = warp & 3, half = (warp - 2) >> 2;
-    const int r = sp * 32 + lane;  // weight row of the tile
+    // +31; gate/up: warps 2..5 the gate tile, 6..9 the up tile, both blocks
+    // of a stage; down: one tile, warps 2..5 the first block, 6..9 the
+    // second. Block scales run kPF stages ahead in registers, across items.
+    const int sp = warp & 3, sub = (warp - 2) >> 2;
+    const int r = sp * 32 + lane;  // weight row within a tile
     const uint32_t lane_base = static_cast<uint32_t>(sp * 32) << 16;
     const uint32_t swz = static_cast<uint32_t>((r >> 1) & 3);  // 64-byte swizzle phase of row r
-    uint32_t ring = 0, it = 0;
+    const uint32_t qrow = kBBytes + static_cast<uint32_t>((PHASE == 0 ? sub * kWR : 0) + r) * kBK;
+    // prefetch cursor (item pi, stage pk)
+    int pi = next_live<PHASE>(a, s_geo, 0, my_items), pk = 0, pnkb = 1;
+    const uint32_t* prow = nullptr;
+    if (pi < my_items) {
+      const ItemGeo g = geo_of<PHASE>(a, s_geo, pi);
+      pnkb = g.K / kBK;
+      prow = scale_row<PHASE>(a, g, sub, r);
+    }
+    uint32_t sc[kPF];
+#pragma unroll
+    for (int u = 0; u < kPF; ++u) {
+      sc[u] = (pi < my_items && prow) ? __ldg(prow + pk) : 0u;
+      if (pi < my_items && ++pk == pnkb) {
+        pi = next_live<PHASE>(a, s_geo, pi + 1, my_items);
+        pk = 0;
+        if (pi < my_items) {
+          const ItemGeo g = geo_of<PHASE>(a, s_geo, pi);
+          pnkb = g.K / kBK;
+          prow = scale_row<PHASE>(a, g, sub, r);
+        }
+      }
+    }
+    // consumer cursor (item ci, stage kb)
+    int ci = next_live<PHASE>(a, s_geo, 0, my_items), kb = 0, nkb = 1;
+    if (ci < my_items) nkb = geo_of<PHASE>(a, s_geo, ci).K / kBK;
     RingPos rp, ap;
-    for (int i = 0; i < my_items && !*abort_flag; ++i) {
-      const ItemGeo g = geo_of<PHASE>(a, s_geo, i);
-      if (g.stale) continue;
-      const int nkb = g.K / kBK;
-      const uint32_t sb = it & 1u;
-      if (!mbar_wait(su32(&bar_scf[sb]), (it >> 1) & 1u, abort_flag, a.err)) break;
-      ++it;
-      // this row's block scales; block 2*kb + half in stage kb
-      const uint32_t srow = sscale + sb * static_cast<uint32_t>(a.sc_bytes) + r * (g.K / 16) + half * 2;
-      bool ok = true;
-      for (int kb = 0; kb < nkb; ++kb, ++ring, rp.next(kStages), ap.next(kAStages)) {
+    uint32_t ring = 0;
+    bool ok = true;
+    while (ci < my_items && ok && !*abort_flag) {
+#pragma unroll
+      for (int u = 0; u < kPF; ++u) {
+        if (ci >= my_items) break;
+        const uint32_t scw = sc[u];
+        sc[u] = (pi < my_items && prow) ? __ldg(prow + pk) : 0u;
+        if (pi < my_items && ++pk == pnkb) {
+          pi = next_live<PHASE>(a, s_geo, pi + 1, my_items);
+          pk = 0;
+          if (pi < my_items) {
+            const ItemGeo g = geo_of<PHASE>(a, s_geo, pi);
+            pnkb = g.K / kBK;
+            prow = scale_row<PHASE>(a, g, sub, r);
+          }
+        }
         const int s = rp.s, j = ap.s;
         if (!(ok = mbar_wait(su32(&bar_full[s]), rp.ph, abort_flag, a.err))) break;
-        const uint32_t sq = sbase + s * kStageBytes + kBBytes + r * kBK;
-        uint32_t h;
-        asm volatile("ld.shared.u16 %0, [%1];" : "=r"(h) : "r"(srow + kb * 4));
-        const uint4 raw0 = lds128(sq + (((2 * half) ^ swz) << 4));
-        const uint4 raw1 = lds128(sq + (((2 * half + 1) ^ swz) << 4));
-        uint32_t out[16];
-        {
-          uint4 o0, o1, o2, o3;
-          if (PHASE == 0) {
-            dq16_f16(raw0, h | (h << 16), o0, o1);
-            dq16_f16(raw1, h | (h << 16), o2, o3);
-          } else {
-            const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(h)));
-            dq16_bf16(raw0, d, o0, o1);
-            dq16_bf16(raw1, d, o2, o3);
+        const uint32_t sq = sbase + s * Sh::kStageBytes + qrow;
+        uint32_t out[32];
+        if (PHASE == 0) {
+          // both blocks of the stage: chunks 0,1 (scale lo) and 2,3 (scale hi)
+          const uint32_t lo = scw & 0xFFFFu, hi = scw >> 16;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const uint4 raw = lds128(sq + ((static_cast<uint32_t>(c) ^ swz) << 4));
+            const uint32_t h = c < 2 ? lo : hi;
+            uint4 o0, o1;
+            dq16_f16(raw, h | (h << 16), o0, o1);
+            out[8 * c] = o0.x, out[8 * c + 1] = o0.y, out[8 * c + 2] = o0.z, out[8 * c + 3] = o0.w;
+            out[8 * c + 4] = o1.x, out[8 * c + 5] = o1.y, out[8 * c + 6] = o1.z, out[8 * c + 7] = o1.w;
           }
-          out[0] = o0.x, out[1] = o0.y, out[2] = o0.z, out[3] = o0.w;
-          out[4] = o1.x, out[5] = o1.y, out[6] = o1.z, out[7] = o1.w;
-          out[8] = o2.x, out[9] = o2.y, out[10] = o2.z, out[11] = o2.w;
-          out[12] = o3.x, out[13] = o3.y, out[14] = o3.z, out[15] = o3.w;
+        } else {
+          const uint32_t h = sub ? (scw >> 16) : (scw & 0xFFFFu);
+          const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(h)));
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const uint4 raw = lds128(sq + ((static_cast<uint32_t>(2 * sub + c) ^ swz) << 4));
+            uint4 o0, o1;
+            dq16_bf16(raw, d, o0, o1);
+            out[8 * c] = o0.x, out[8 * c + 1] = o0.y, out[8 * c + 2] = o0.z, out[8 * c + 3] = o0.w;
+            out[8 * c + 4] = o1.x, out[8 * c + 5] = o1.y, out[8 * c + 6] = o1.z, out[8 * c + 7] = o1.w;
+          }
         }
-        // the stage's quant rows and scales have been read
+        // the stage's quant rows have been read
         __syncwarp();
         if (lane == 0) mbar_arrive(su32(&bar_sfree[s]));
         if (ring >= static_cast<uint32_t>(kAStages) &&
             !(ok = mbar_wait(su32(&bar_afree[j]), ap.ph ^ 1u, abort_flag, a.err)))
           break;
         asm volatile("tcgen05.fence::after_thread_sync;");
-        tmem_st16(tmem + lane_base + kAcol0 + 32u * j + 16u * half, out);
+        const uint32_t ta = tmem + lane_base + kAcc + Sh::kAStride * j;
+        if (PHASE == 0) {
+          tmem_st16(ta + 32u * sub, out);
+          tmem_st16(ta + 32u * sub + 16u, out + 16);
+        } else {
+          tmem_st16(ta + 16u * sub, out);
+        }
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         asm volatile("tcgen05.fence::before_thread_sync;");
         __syncwarp();
         if (lane == 0) mbar_arrive(su32(&bar_aready[j]));
+        ++ring;
+        rp.next(kStages);
+        ap.next(kAStages);
+        if (++kb == nkb) {
+          ci = next_live<PHASE>(a, s_geo, ci + 1, my_items);
+          kb = 0;
+          if (ci < my_items) nkb = geo_of<PHASE>(a, s_geo, ci).K / kBK;
+        }
       }
-      if (!ok) break;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(su32(&bar_sce[sb]));  // done with the item's scales
     }
   } else {
     // ---------------- epilogue: warp w reads TMEM lanes 32*(w%4) .. +31
     const int sp = warp & 3;
+    const int r = sp * 32 + lane;  // weight row within the tile
     const uint32_t lane_base = static_cast<uint32_t>(sp * 32) << 16;
     uint32_t acc_i = 0;
     for (int i = 0; i < my_items && !*abort_flag; ++i) {
       const ItemGeo g = geo_of<PHASE>(a, s_geo, i);
-      if (g.stale) {
+      if (g.flags & 2) {
         if (tid == kEpTid0) atomicOr(a.err, MOE_DEVERR_STALE);
         continue;
       }
-      const uint32_t buf = acc_i & 1u, aph = (acc_i >> 1) & 1u;
+      const uint32_t buf = Sh::kAccBufs == 2 ? (acc_i & 1u) : 0u;
+      const uint32_t aph = Sh::kAccBufs == 2 ? ((acc_i >> 1) & 1u) : (acc_i & 1u);
       if (!mbar_wait(su32(&bar_accf[buf]), aph, abort_flag, a.err)) break;
       asm volatile("tcgen05.fence::after_thread_sync;");
       const int nch = (g.ntok + 31) / 32;
       const uint32_t tb = tmem + lane_base + buf * static_cast<uint32_t>(kTok);
       const int64_t prow0 = static_cast<int64_t>(g.p0) + g.m0;
       if (PHASE == 0) {
-        // lanes 0..63 hold gate rows, 64..127 the same up rows; in each chunk
-        // of 32 tokens the gate warps finish tokens 0..15, the up warps 16..31
-        const bool gate = sp < 2;
-        const int rr = (sp & 1) * 32 + lane;  // h column within the tile
-        const uint32_t xg = sepi, xu = sepi + 64 * kXP * 4, sh = sepi + 2 * 64 * kXP * 4;
+        // lane r holds G and U of weight row n0 + r: h column n0 + r; each
+        // chunk of 32 tokens goes through a transpose buffer so that rows of
+        // h are written 16 bytes at a time
         const int et = tid - kEpTid0;  // 0..127
-        const uint32_t mine = (gate ? xg : xu) + rr * kXP * 4;
-        const uint32_t other = (gate ? xu : xg) + rr * kXP * 4;
-        const int tok0 = gate ? 0 : 16;
         for (int ch = 0; ch < nch; ++ch) {
-          uint32_t v[32];
-          tmem_ld32(tb + ch * 32, v);
-          uint32_t send[16];  // gate warps pass tokens 16..31, up warps 0..15
+          uint32_t gv[32], uv[32];
+          tmem_ld32(tb + ch * 32, gv);
+          tmem_ld32(tb + kTok + ch * 32, uv);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) send[j] = gate ? v[16 + j] : v[j];
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            sts128(mine + q * 16, make_uint4(send[4 * q], send[4 * q + 1], send[4 * q + 2], send[4 * q + 3]));
-          epi_sync();
-          float o[16];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const uint4 w = lds128(other + q * 16);
-            o[4 * q] = __uint_as_float(w.x);
-            o[4 * q + 1] = __uint_as_float(w.y);
-            o[4 * q + 2] = __uint_as_float(w.z);
-            o[4 * q + 3] = __uint_as_float(w.w);
-          }
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float gg = gate ? __uint_as_float(v[j]) : o[j];
-            const float uu = gate ? o[j] : __uint_as_float(v[16 + j]);
-            const __nv_bfloat16 hb = __float2bfloat16_rn(silu_mul(gg, uu));
-            asm volatile("st.shared.u16 [%0], %1;" ::"r"(sh + ((tok0 + j) * kSP + rr) * 2),
+          for (int j = 0; j < 32; ++j) {
+            const __nv_bfloat16 hb = __float2bfloat16_rn(silu_mul(__uint_as_float(gv[j]), __uint_as_float(uv[j])));
+            asm volatile("st.shared.u16 [%0], %1;" ::"r"(sepi + (j * kSP + r) * 2),
                          "h"(*reinterpret_cast<const unsigned short*>(&hb))
                          : "memory");
           }
           epi_sync();
-          // 32 tokens x 64 columns of bf16: 256 pieces of 16 bytes
+          // 32 tokens x 128 columns of bf16: 512 pieces of 16 bytes
 #pragma unroll
-          for (int rep = 0; rep < 2; ++rep) {
-            const int piece = et + 128 * rep, j = piece >> 3, part = piece & 7;
+          for (int rep = 0; rep < 4; ++rep) {
+            const int piece = et + 128 * rep, j = piece >> 4, part = piece & 15;
             const int tok = ch * 32 + j;
-            if (tok < g.ntok) {
-              const uint4 w = lds128(sh + (j * kSP + part * 8) * 2);
+            if (tok < g.ntok && part * 8 < g.nrows) {
+              const uint4 w = lds128(sepi + (j * kSP + part * 8) * 2);
               *reinterpret_cast<uint4*>(a.h + (prow0 + tok) * a.ldh + g.n0 + part * 8) = w;
             }
           }
+          epi_sync();
         }
       } else {
-        const int r = sp * 32 + lane;  // output column n0 + r
         for (int ch = 0; ch < nch; ++ch) {
           uint32_t v[32];
           tmem_ld32(tb + ch * 32, v);
@@ -604,27 +641,26 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
   if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512));
 }
 
+template <int PHASE>
+size_t smem_bytes(int stages) {
+  return static_cast<size_t>(stages) * Shape<PHASE>::kStageBytes + Shape<PHASE>::kEpiBytes + 1024;
+}
+
 }  // namespace
 
-// Shared memory of one item-scale buffer: 128 weight rows x K/32 fp16.
-int gemm_scale_bytes(int K) { return ((kWR * (K / 16)) + 1023) / 1024 * 1024; }
-
-// Pipeline stages that fit in shared memory beside the item-scale buffers
-// and the epilogue buffers.
-int gemm_stages(int K) {
+// Pipeline stages that fit in shared memory beside the epilogue buffer.
+int gemm_stages(int phase) {
   const size_t limit = 227 * 1024 - sizeof(ItemGeo) * kGeoCap - 512;  // static shared memory
-  const size_t fixed = 2 * static_cast<size_t>(gemm_scale_bytes(K)) + kEpiBytes + 1024;
-  const int n = static_cast<int>((limit - fixed) / kStageBytes);
+  const size_t fixed = phase == 0 ? smem_bytes<0>(0) : smem_bytes<1>(0);
+  const size_t per = phase == 0 ? Shape<0>::kStageBytes : Shape<1>::kStageBytes;
+  const int n = static_cast<int>((limit - fixed) / per);
   return n < 2 ? 0 : (n > kMaxStages ? kMaxStages : n);
 }
 
-size_t gemm_smem_bytes(int stages, int K) {
-  return static_cast<size_t>(stages) * kStageBytes + 2 * static_cast<size_t>(gemm_scale_bytes(K)) + kEpiBytes +
-         1024;
-}
+size_t gemm_smem_bytes(int phase, int stages) { return phase == 0 ? smem_bytes<0>(stages) : smem_bytes<1>(stages); }
 
 cudaError_t launch_gemm(int phase, const GemmMaps& m, const GemmArgs& a, int grid, cudaStream_t st) {
-  const int smem = static_cast<int>(gemm_smem_bytes(a.stages, a.kmax));
+  const int smem = static_cast<int>(gemm_smem_bytes(phase, a.stages));
   cudaError_t e;
   if (phase == 0) {
     e = cudaFuncSetAttribute(gemm_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
