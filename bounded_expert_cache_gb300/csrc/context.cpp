@@ -151,6 +151,7 @@ extern "C" void moe_destroy(moe_ctx_t* ctx) {
   cudaFree(ctx->d_plan_local);
   cudaFree(ctx->d_norms);
   cudaFree(ctx->d_flags);
+  cudaFree(ctx->d_lpart);
   cudaFreeHost(ctx->h_units);
   cudaFreeHost(ctx->h_pt);
   cudaFreeHost(ctx->h_ptgen);
@@ -259,6 +260,7 @@ extern "C" moe_status_t moe_create(const moe_config_t* cfg, moe_ctx_t** out) {
                    sizeof(int32_t) * moe::plan_blocks(c.max_tokens * c.top_k) * static_cast<int64_t>(E)));
     CKC(cudaMalloc(&ctx->d_norms, sizeof(float) * (c.max_tokens + E)));
     CKC(cudaMalloc(&ctx->d_flags, sizeof(int32_t) * c.max_tokens));
+    CKC(cudaMalloc(&ctx->d_lpart, sizeof(float2) * 4 * static_cast<size_t>(c.max_tokens) * E));
   }
   ctx->dev_admit = c.admit_on_device >= 1;
   ctx->read_through = c.admit_on_device == 2;
@@ -421,7 +423,7 @@ static moe_status_t route_impl(moe_ctx_t* ctx, int32_t layer, const void* x, int
     // and admission run as their own launches
     a.plan = moe_plan_t{};
     a.admit.enabled = 0;
-    CK(moe::launch_route_large(a, ctx->d_norms, ctx->d_flags, st));
+    CK(moe::launch_route_large(a, ctx->d_norms, ctx->d_flags, ctx->d_lpart, st));
   } else {
     CK(moe::launch_route(a, ctx->num_sms, st));
   }

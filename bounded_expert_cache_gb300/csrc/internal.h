@@ -113,7 +113,9 @@ struct PlanArgs {
 };
 cudaError_t launch_plan(const PlanArgs& a, cudaStream_t st);
 // Many-token routing (any T): norms [T + E] and flags [T] are scratch.
-cudaError_t launch_route_large(const RouteArgs& a, float* norms, int* flags, cudaStream_t st);
+// Many-token router; part holds up to 4 * T * E (hi, lo) pairs of split-K
+// partials.
+cudaError_t launch_route_large(const RouteArgs& a, float* norms, int* flags, float2* part, cudaStream_t st);
 // Multi-block plan for any T*k: local is scratch [plan_blocks(T*k)][E].
 int plan_blocks(int A);
 cudaError_t launch_plan_large(const PlanArgs& a, int* local, cudaStream_t st);
@@ -231,6 +233,7 @@ struct moe_ctx {
   int32_t* d_plan_local = nullptr;         // multi-block plan scratch
   float* d_norms = nullptr;                // many-token router scratch
   int32_t* d_flags = nullptr;
+  float2* d_lpart = nullptr;               // split-K logit partials [4][T][E]
   std::vector<cudaStream_t> streams;
   std::vector<cudaEvent_t> ev_stage;
   cudaEvent_t ev_compute = nullptr;

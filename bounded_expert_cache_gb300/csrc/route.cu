@@ -328,6 +328,163 @@ __device__ bool warp_select(const TokenKeys& K, int E, int k, int* sel, unsigned
   return warp_select_keys<32>(K, E, k, sel, selk, certify);
 }
 
+// ---- decode selection from keys staged in shared memory (l, lo, hi [E])
+// One warp round: the warp's best head by the high key word, then the low
+// word, then the lowest id (32-bit warp reductions; keys descending, ties
+// to the lower expert id). Returns the winning id (or -1) and its key.
+__device__ __forceinline__ int warp_round(bool has, unsigned long long v, int id, unsigned long long& key) {
+  const uint32_t h32 = has ? static_cast<uint32_t>(v >> 32) : 0u;
+  const uint32_t m1 = __reduce_max_sync(0xffffffffu, h32);
+  const bool c1 = has && h32 == m1;
+  const uint32_t m2 = __reduce_max_sync(0xffffffffu, c1 ? static_cast<uint32_t>(v) : 0u);
+  const bool c2 = c1 && static_cast<uint32_t>(v) == m2;
+  key = (static_cast<unsigned long long>(m1) << 32) | m2;
+  return static_cast<int>(__reduce_min_sync(0xffffffffu, c2 ? static_cast<unsigned>(id) : 0xffffffffu));
+}
+
+// Certification of a selection s_idx[k] (the same test as warp_select_keys):
+// the bound intervals of consecutive selections and of the k-th against
+// every other expert are disjoint. taken[e] marks the selected experts.
+__device__ bool warp_certify(const unsigned long long* slo, const unsigned long long* shi,
+                             const unsigned char* taken, const int* s_idx, int E, int k) {
+  const int lane = threadIdx.x & 31;
+  unsigned long long rest = 0ull;
+  bool any = false;
+#pragma unroll 1
+  for (int e = lane; e < E; e += 32) {
+    if (taken[e]) continue;
+    const unsigned long long h = shi[e];
+    rest = (!any || h > rest) ? h : rest;
+    any = true;
+  }
+  const uint32_t rh = __reduce_max_sync(0xffffffffu, any ? static_cast<uint32_t>(rest >> 32) : 0u);
+  const uint32_t rl =
+      __reduce_max_sync(0xffffffffu, any && static_cast<uint32_t>(rest >> 32) == rh ? static_cast<uint32_t>(rest) : 0u);
+  const bool any_rest = __any_sync(0xffffffffu, any);
+  const unsigned long long restmax = (static_cast<unsigned long long>(rh) << 32) | rl;
+  bool ok = true;
+  if (lane + 1 < k) ok = slo[s_idx[lane]] > shi[s_idx[lane + 1]];
+  if (lane == k - 1 && any_rest) ok = slo[s_idx[lane]] > restmax;
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Top-k of one token by one warp (E <= 256): every lane sorts its 8 keys in
+// registers once (odd-even transposition), then each round takes the best
+// head over the warp and the winning lane pops it. Writes s_idx/s_key and
+// marks taken[].
+__device__ void warp_select_heads(const unsigned long long* sl, int E, int k, int* s_idx,
+                                  unsigned long long* s_key, unsigned char* taken) {
+  const int lane = threadIdx.x & 31;
+  unsigned long long sv[8];
+  int sid[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int e = i * 32 + lane;
+    sv[i] = e < E ? sl[e] : 0ull;
+    sid[i] = e < E ? e : -1;
+  }
+#pragma unroll
+  for (int p = 0; p < 8; ++p) {
+#pragma unroll
+    for (int i = p & 1; i + 1 < 8; i += 2) {
+      const bool swap =
+          sid[i + 1] >= 0 && (sid[i] < 0 || sv[i + 1] > sv[i] || (sv[i + 1] == sv[i] && sid[i + 1] < sid[i]));
+      const unsigned long long x = sv[i], y = sv[i + 1];
+      const int ix = sid[i], iy = sid[i + 1];
+      sv[i] = swap ? y : x;
+      sv[i + 1] = swap ? x : y;
+      sid[i] = swap ? iy : ix;
+      sid[i + 1] = swap ? ix : iy;
+    }
+  }
+#pragma unroll 1
+  for (int r = 0; r < k; ++r) {
+    unsigned long long key;
+    const int mi = warp_round(sid[0] >= 0, sv[0], sid[0], key);
+    if (lane == 0) {
+      s_idx[r] = mi;
+      s_key[r] = key;
+      taken[mi] = 1;
+    }
+    const bool pop = sid[0] == mi;
+#pragma unroll
+    for (int i = 0; i < 7; ++i) {
+      sv[i] = pop ? sv[i + 1] : sv[i];
+      sid[i] = pop ? sid[i + 1] : sid[i];
+    }
+    sv[7] = pop ? 0ull : sv[7];
+    sid[7] = pop ? -1 : sid[7];
+  }
+  __syncwarp();
+}
+
+// Top-k (k <= 8) of one token by the whole block (E <= 256): warp w selects
+// the top k of experts 32w .. 32w+31 (one key per lane), then warp 0 merges
+// the 8k candidates (two per lane). Called by every thread of the block;
+// s_idx/s_key/taken are written by warp 0.
+__device__ void block_select_tournament(const unsigned long long* sl, int E, int k, int* cand_idx,
+                                        unsigned long long* cand_key, int* s_idx, unsigned long long* s_key,
+                                        unsigned char* taken) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  {
+    const int e = warp * 32 + lane;
+    const unsigned long long v = e < E ? sl[e] : 0ull;
+    bool has = e < E;
+#pragma unroll 1
+    for (int r = 0; r < k; ++r) {
+      unsigned long long key;
+      const int mi = warp_round(has, v, e, key);
+      if (lane == 0) {
+        cand_idx[warp * 8 + r] = mi;
+        cand_key[warp * 8 + r] = key;
+      }
+      if (e == mi) has = false;
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // candidates lane and lane + 32 (each warp's list is in order)
+    unsigned long long a = cand_key[lane], b = cand_key[lane + 32];
+    const int ia = (lane % 8) < k ? cand_idx[lane] : -1, ib = (lane % 8) < k ? cand_idx[lane + 32] : -1;
+    bool ha = ia >= 0, hb = ib >= 0;
+#pragma unroll 1
+    for (int r = 0; r < k; ++r) {
+      const bool useb = hb && (!ha || b > a || (b == a && ib < ia));
+      unsigned long long key;
+      const int mi = warp_round(ha || hb, useb ? b : a, useb ? ib : ia, key);
+      if (lane == 0) {
+        s_idx[r] = mi;
+        s_key[r] = key;
+        taken[mi] = 1;
+      }
+      if ((useb ? ib : ia) == mi && (ha || hb)) {
+        if (useb)
+          hb = false;
+        else
+          ha = false;
+      }
+    }
+    __syncwarp();
+  }
+}
+
+// Combine weights of a selection held in shared memory (same arithmetic and
+// order as warp_write_selection); also keeps the weights in shared memory.
+__device__ void fast_write_selection(const int* s_idx, const unsigned long long* s_key, int k, int32_t* idx,
+                                     float* w, float* s_w) {
+  const int lane = threadIdx.x & 31;
+  float z = 0.f;
+  if (lane < k) z = expf(static_cast<float>(okey_value(s_key[lane]) - okey_value(s_key[0])));
+  float sum = 0.f;
+  for (int j = 0; j < k; ++j) sum += __shfl_sync(0xffffffffu, z, j);  // fixed order
+  if (lane < k) {
+    const float wl = z / sum;
+    idx[lane] = s_idx[lane];
+    w[lane] = wl;
+    s_w[lane] = wl;
+  }
+}
+
 // Combine weights of a selection: softmax over the k selected logits, the
 // differences taken in fp64 and exponentiated in fp32.
 __device__ void warp_write_selection(const int* sel, const unsigned long long* selk, int k,
@@ -492,12 +649,48 @@ __host__ __device__ constexpr size_t admit_smem_bytes(int E, int S, int max_unit
          + 4 * static_cast<size_t>(max_units) * 2 + 16;  // union ids, their slots
 }
 
+// Inputs another warp of the block may have staged in shared memory before
+// the admission runs (the decode router's last block does so while it
+// selects): the slot state, the layer's page table, and the plan's union,
+// counts and offsets. Null pointers / false mean "read from global memory".
+struct AdmitStaged {
+  bool slots = false;        // last/owner/sgen already in the admission's smem
+  const int* pt = nullptr;   // [E] page table
+  int nu = 0;
+  const int* uniq = nullptr;  // [nu] union, ascending
+  const int* cnt = nullptr;   // [E] assignments per expert
+  const int* off = nullptr;   // [E] first expert-major assignment per expert
+  unsigned long long tick = 0, rng = 0;
+  bool have_tick = false;
+};
+
+// Stages the slot state and the page table of the layer into shared memory
+// (one warp); the admission smem layout starts with last[S], owner[S], sgen[S].
+__device__ void admit_stage(const AdmitArgs& A, unsigned char* smem, int* pt_s, unsigned long long* tick_rng) {
+  const int lane = threadIdx.x & 31;
+  const int S = A.S;
+  const DevCacheLayer c = A.c;
+  unsigned long long* s_last = reinterpret_cast<unsigned long long*>(smem);
+  int* s_owner = reinterpret_cast<int*>(s_last + S);
+  uint32_t* s_sgen = reinterpret_cast<uint32_t*>(s_owner + S);
+  for (int s = lane; s < S; s += 32) {
+    s_last[s] = __ldcg(c.last + s);
+    s_owner[s] = __ldcg(c.owner + s);
+    s_sgen[s] = __ldcg(c.sgen + s);
+  }
+  for (int e = lane; e < A.E; e += 32) pt_s[e] = __ldcg(c.pt + e);
+  if (lane == 0) {
+    tick_rng[0] = __ldcg(c.tick);
+    tick_rng[1] = __ldcg(c.rng);
+  }
+}
+
 __device__ void admit_warp(const AdmitArgs& A, const moe_plan_t& P, unsigned char* smem,
-                           uint32_t* err) {
+                           uint32_t* err, const AdmitStaged& st = AdmitStaged()) {
   const int lane = threadIdx.x & 31;
   const int E = A.E, S = A.S;
   const DevCacheLayer c = A.c;
-  const int nu = __ldcg(P.n_uniq);
+  const int nu = st.uniq ? st.nu : __ldcg(P.n_uniq);
   unsigned long long* s_last = reinterpret_cast<unsigned long long*>(smem);
   int* s_owner = reinterpret_cast<int*>(s_last + S);
   uint32_t* s_sgen = reinterpret_cast<uint32_t*>(s_owner + S);
@@ -506,16 +699,18 @@ __device__ void admit_warp(const AdmitArgs& A, const moe_plan_t& P, unsigned cha
   int* upt = uq + nu;
   const int nwords = (E + 31) / 32;
   for (int w = lane; w < nwords; w += 32) bm[w] = 0u;
-  for (int s = lane; s < S; s += 32) {
-    s_last[s] = __ldcg(c.last + s);
-    s_owner[s] = __ldcg(c.owner + s);
-    s_sgen[s] = __ldcg(c.sgen + s);
+  if (!st.slots) {
+    for (int s = lane; s < S; s += 32) {
+      s_last[s] = __ldcg(c.last + s);
+      s_owner[s] = __ldcg(c.owner + s);
+      s_sgen[s] = __ldcg(c.sgen + s);
+    }
   }
   __syncwarp();
   for (int u = lane; u < nu; u += 32) {
-    const int e = __ldcg(P.uniq + u);
+    const int e = st.uniq ? st.uniq[u] : __ldcg(P.uniq + u);
     uq[u] = e;
-    upt[u] = __ldcg(c.pt + e);
+    upt[u] = st.pt ? st.pt[e] : __ldcg(c.pt + e);
     atomicOr(&bm[e >> 5], 1u << (e & 31));
   }
   __syncwarp();
@@ -541,7 +736,7 @@ __device__ void admit_warp(const AdmitArgs& A, const moe_plan_t& P, unsigned cha
     }
     return;
   }
-  unsigned long long tick = __ldcg(c.tick);
+  unsigned long long tick = st.have_tick ? st.tick : __ldcg(c.tick);
   // hits in ascending id, consecutive ticks
   for (int u0 = 0; u0 < nu; u0 += 32) {
     const int u = u0 + lane;
@@ -552,7 +747,7 @@ __device__ void admit_warp(const AdmitArgs& A, const moe_plan_t& P, unsigned cha
   }
   __syncwarp();
   // misses in ascending id, one at a time
-  unsigned long long rng = __ldcg(c.rng);
+  unsigned long long rng = st.have_tick ? st.rng : __ldcg(c.rng);
   int nfill = 0, nevict = 0;
   for (int u = 0; u < nu; ++u) {
     if (upt[u] >= 0) continue;
@@ -632,7 +827,7 @@ __device__ void admit_warp(const AdmitArgs& A, const moe_plan_t& P, unsigned cha
     const int e = uq[u];
     const bool was_miss = upt[u] <= -2;
     const int slot = was_miss ? -2 - upt[u] : upt[u];
-    const int cnt = __ldcg(P.counts + e);
+    const int cnt = st.cnt ? st.cnt[e] : __ldcg(P.counts + e);
     assignments += cnt;
     c.pt[e] = slot;
     c.ptgen[e] = s_sgen[slot];
@@ -640,7 +835,7 @@ __device__ void admit_warp(const AdmitArgs& A, const moe_plan_t& P, unsigned cha
     int* U = A.units + kUnitHeader + kUnitInts * u;
     const bool filled = A.read_through && was_miss;
     U[0] = filled ? -2 - slot : slot;
-    U[1] = __ldcg(P.offsets + e);
+    U[1] = st.off ? st.off[e] : __ldcg(P.offsets + e);
     U[2] = cnt;
     U[3] = filled ? e : static_cast<int>(s_sgen[slot]);
   }
@@ -668,14 +863,15 @@ __device__ void admit_warp(const AdmitArgs& A, const moe_plan_t& P, unsigned cha
 // Expert-major plan of A <= 32 assignments by one warp (every decode step):
 // same outputs as plan_block. smem: counts[E], offsets[E].
 __device__ void plan_warp(const int32_t* idx, const float* w, int A, int k, int E,
-                          const moe_plan_t& P, int* smem, uint32_t* err) {
+                          const moe_plan_t& P, int* smem, uint32_t* err, int* uniq_s = nullptr,
+                          int* nu_s = nullptr) {
   const int lane = threadIdx.x & 31;
   int* cnt = smem;
   int* off = smem + E;
   for (int e = lane; e < E; e += 32) cnt[e] = 0;
   __syncwarp();
   const bool live = lane < A;
-  int e = live ? __ldcg(idx + lane) : -1;
+  int e = live ? idx[lane] : -1;  // global (written before) or shared memory
   const bool valid = live && e >= 0 && e < E;
   if (live && !valid) atomicOr(err, MOE_DEVERR_BADIDX);
   const unsigned peers = __match_any_sync(0xffffffffu, valid ? e : -1 - lane);
@@ -708,20 +904,24 @@ __device__ void plan_warp(const int32_t* idx, const float* w, int A, int k, int 
       off[ee] = rc;
       P.counts[ee] = c;
       P.offsets[ee] = rc;
-      if (c > 0) P.uniq[rn++] = ee;
+      if (c > 0) {
+        if (uniq_s) uniq_s[rn] = ee;
+        P.uniq[rn++] = ee;
+      }
       rc += c;
     }
   }
   if (lane == 31) {
     P.offsets[E] = ic;
     *P.n_uniq = in;
+    if (nu_s) *nu_s = in;
   }
   __syncwarp();
   if (valid) {
     const int pos = off[e] + rank;  // lanes are assignments in token order
     P.perm_tok[pos] = lane / k;
     P.perm_rank[pos] = lane % k;
-    P.perm_w[pos] = __ldcg(w + lane);
+    P.perm_w[pos] = w[lane];
     P.inv[lane] = pos;
   }
 }
@@ -730,6 +930,142 @@ constexpr int kPlanThreads = 256;
 
 size_t plan_smem_bytes(int E) {
   return sizeof(int) * (2 * E + (kPlanThreads / 32) * E + kPlanThreads / 32 + 1);
+}
+
+// ------------------------------------------------------------ decode tail
+// Shared-memory layout of the router's last block on the decode fast path
+// (T*k <= 32 assignments, E <= 256): admission scratch, the plan's counts and
+// offsets, the layer's page table, and the selection.
+struct FastTailLayout {
+  size_t admit, plan, pt, key, idx, w, uniq, tick, nu, cand, keys, taken, total;
+};
+__host__ __device__ constexpr size_t r16(size_t v) { return (v + 15) & ~size_t(15); }
+__host__ __device__ inline FastTailLayout fast_tail_layout(int T, int E, int S, int max_units, bool admit) {
+  FastTailLayout L{};
+  L.admit = 0;
+  L.plan = admit ? r16(admit_smem_bytes(E, S, max_units)) : 0;
+  L.pt = L.plan + r16(8 * static_cast<size_t>(E));
+  L.key = L.pt + r16(4 * static_cast<size_t>(E));
+  L.idx = L.key + 8 * 32;
+  L.w = L.idx + 4 * 32;
+  L.uniq = L.w + 4 * 32;
+  L.tick = L.uniq + 4 * 32;
+  L.nu = L.tick + 16;
+  L.cand = L.nu + 16;                                             // tournament: 64 ids, 64 keys
+  L.keys = L.cand + 4 * 64 + 8 * 64;                              // [3][T][E] u64
+  L.taken = L.keys + 24 * static_cast<size_t>(T) * E;             // [T][E] bytes
+  L.total = L.taken + r16(static_cast<size_t>(T) * E);
+  return L;
+}
+__host__ __device__ constexpr bool fast_tail_ok(int T, int k, int E) {
+  return T * k <= 32 && E <= 256 && T * E <= 2048;
+}
+
+// The decode fast path of the router's last block: warps 0..T-1 select the
+// tokens' experts (fast_select) while the last warp stages the layer's cache
+// state; uncertified tokens are repaired exactly (rare); then warp 0 plans
+// and admits from shared memory, so the tail costs one round of loads.
+template <int XT>
+__device__ void fast_tail(const RouteArgs& a, unsigned char* sm, int* s_flagged, int* s_nflag) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int T = a.T, E = a.E, H = a.H, k = a.k;
+  const bool adm = a.admit.enabled != 0;
+  const FastTailLayout L = fast_tail_layout(T, E, a.admit.S, min(E, T * k), adm);
+  unsigned char* s_admit = sm + L.admit;
+  int* s_plan = reinterpret_cast<int*>(sm + L.plan);
+  int* s_pt = reinterpret_cast<int*>(sm + L.pt);
+  unsigned long long* s_key = reinterpret_cast<unsigned long long*>(sm + L.key);
+  unsigned long long* s_keys = reinterpret_cast<unsigned long long*>(sm + L.keys);
+  unsigned char* s_taken = sm + L.taken;
+  int* s_idx = reinterpret_cast<int*>(sm + L.idx);
+  float* s_w = reinterpret_cast<float*>(sm + L.w);
+  int* s_uniq = reinterpret_cast<int*>(sm + L.uniq);
+  unsigned long long* s_tick = reinterpret_cast<unsigned long long*>(sm + L.tick);
+  int* s_nu = reinterpret_cast<int*>(sm + L.nu);
+  const size_t te = static_cast<size_t>(T) * E;
+  // the block stages every token's keys (one round of loads); the last warp
+  // stages the layer's cache state meanwhile
+  if (adm && warp == kRouteWarps - 1) admit_stage(a.admit, s_admit, s_pt, s_tick);
+  for (int i = tid; i < static_cast<int>(te); i += kRouteThreads) {
+    s_keys[i] = __ldcg(a.keys + i);
+    s_keys[te + i] = __ldcg(a.keys + te + i);
+    s_keys[2 * te + i] = __ldcg(a.keys + 2 * te + i);
+    s_taken[i] = 0;
+  }
+  __syncthreads();
+  if (T == 1 && k <= 8) {
+    // one token: tournament over the whole block
+    int* cand_idx = reinterpret_cast<int*>(sm + L.cand);
+    unsigned long long* cand_key = reinterpret_cast<unsigned long long*>(sm + L.cand + 4 * 64);
+    block_select_tournament(s_keys, E, k, cand_idx, cand_key, s_idx, s_key, s_taken);
+    if (warp == 0) {
+      const bool ok = warp_certify(s_keys + te, s_keys + 2 * te, s_taken, s_idx, E, k);
+      if (ok)
+        fast_write_selection(s_idx, s_key, k, a.topk_idx, a.topk_w, s_w);
+      else if (lane == 0)
+        s_flagged[atomicAdd(s_nflag, 1)] = 0;
+    }
+  } else {
+    for (int t = warp; t < T; t += kRouteWarps) {
+      const size_t o = static_cast<size_t>(t) * E;
+      warp_select_heads(s_keys + o, E, k, s_idx + t * k, s_key + t * k, s_taken + o);
+      const bool ok = warp_certify(s_keys + te + o, s_keys + 2 * te + o, s_taken + o, s_idx + t * k, E, k);
+      if (ok)
+        fast_write_selection(s_idx + t * k, s_key + t * k, k, a.topk_idx + t * k, a.topk_w + t * k, s_w + t * k);
+      else if (lane == 0)
+        s_flagged[atomicAdd(s_nflag, 1)] = t;
+    }
+  }
+  __syncthreads();
+  const int nflag = *s_nflag;
+  if (nflag) {
+    // exact logits of every expert of the uncertified tokens, then selection
+    // by the exact keys
+    for (int fi = 0; fi < nflag; ++fi) {
+      const int t = s_flagged[fi];
+      for (int ee = warp; ee < E; ee += kRouteWarps) {
+        double v;
+        const bool fin = warp_exact_logit<XT>(a.x, static_cast<size_t>(t) * H, a.w + static_cast<size_t>(ee) * H,
+                                              H, a.bias, ee, v);
+        if (lane == 0) {
+          if (!fin) atomicOr(a.err, MOE_DEVERR_NONFINITE);
+          const size_t o = static_cast<size_t>(t) * E + ee;
+          a.keys[o] = a.keys[te + o] = a.keys[2 * te + o] = okey(v);
+        }
+      }
+    }
+    __syncthreads();
+    for (int fi = warp; fi < nflag; fi += kRouteWarps) {
+      const int t = s_flagged[fi];
+      const size_t o = static_cast<size_t>(t) * E;
+      for (int e = lane; e < E; e += 32) {
+        s_keys[o + e] = __ldcg(a.keys + o + e);
+        s_taken[o + e] = 0;
+      }
+      __syncwarp();
+      warp_select_heads(s_keys + o, E, k, s_idx + t * k, s_key + t * k, s_taken + o);
+      fast_write_selection(s_idx + t * k, s_key + t * k, k, a.topk_idx + t * k, a.topk_w + t * k, s_w + t * k);
+      if (lane == 0) atomicAdd(a.repairs, 1ull);
+    }
+    __syncthreads();
+  }
+  if (warp == 0) {
+    plan_warp(s_idx, s_w, T * k, k, E, a.plan, s_plan, a.err, s_uniq, s_nu);
+    if (adm) {
+      __syncwarp();
+      AdmitStaged st;
+      st.slots = true;
+      st.pt = s_pt;
+      st.nu = *s_nu;
+      st.uniq = s_uniq;
+      st.cnt = s_plan;
+      st.off = s_plan + E;
+      st.tick = s_tick[0];
+      st.rng = s_tick[1];
+      st.have_tick = true;
+      admit_warp(a.admit, a.plan, s_admit, a.err, st);
+    }
+  }
 }
 
 // ------------------------------------------------------------ kernels
@@ -834,6 +1170,11 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a) {
   __threadfence();
   if (tid == 0) s_nflag = 0;
   __syncthreads();
+  if (a.plan.counts != nullptr && fast_tail_ok(T, a.k, E)) {
+    fast_tail<XT>(a, reinterpret_cast<unsigned char*>(dyn_smem), s_flagged, &s_nflag);
+    if (tid == 0) *a.ticket = 0u;
+    return;
+  }
   int sel[16];
   unsigned long long selk[16];
   const size_t te = static_cast<size_t>(T) * E;
@@ -906,6 +1247,8 @@ cudaError_t launch_route(const RouteArgs& a, int num_sms, cudaStream_t st) {
   size_t smem = a.plan.counts ? plan_smem_bytes(a.E) : 0;
   if (a.admit.enabled)
     smem = std::max(smem, admit_smem_bytes(a.E, a.admit.S, std::min(a.E, a.T * a.k)));
+  if (a.plan.counts && fast_tail_ok(a.T, a.k, a.E))
+    smem = std::max(smem, fast_tail_layout(a.T, a.E, a.admit.S, std::min(a.E, a.T * a.k), a.admit.enabled != 0).total);
   if (smem > 48 * 1024) {
     cudaError_t e = a.xt == MOE_BF16
         ? cudaFuncSetAttribute(route_kernel<MOE_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1037,8 +1380,8 @@ extern "C" moe_status_t moe_route_noalloc(const void* x, int32_t xt, int32_t T, 
 
 // ------------------------------------------------------------ many-token routing
 // Prefill chunks route thousands of tokens at once. Logits come from a tiled
-// fp32 GEMM that sums each 32-term chunk with plain FMAs and folds the chunk
-// sums into an error-free (hi, lo) pair; the chunk error is at most
+// fp32 GEMM (split along K) that sums each 32-term chunk with plain FMAs and
+// folds the chunk sums into an error-free (hi, lo) pair; the chunk error is at most
 // gamma_32 * sum|x w| <= gamma_32 * ||x|| * ||w|| (Cauchy-Schwarz), so the
 // same integer-key certification applies, and uncertified tokens are
 // recomputed exactly as in the few-token router.
@@ -1075,10 +1418,15 @@ __global__ void __launch_bounds__(256) row_norms_kernel(const void* x, int T, co
   }
 }
 
-// One 64-token x 64-expert tile per 128-thread block; a thread owns 8 tokens
-// x 4 experts. K advances in chunks of 32 through a double-buffered,
-// transposed shared-memory stage; the next chunk's global loads are issued
-// before the current chunk's FMAs.
+// Split-K logits: one 64-token x 64-expert tile and one of up to four
+// slices of K per 128-thread block. A thread owns 8 tokens x 4 experts; a
+// warp spans 8 token groups x 4 expert groups, so each of its shared loads
+// touches at most 128 bytes. K advances in chunks of 32 through a
+// double-buffered, transposed shared-memory stage (the next chunk's global
+// loads are issued before the current chunk's FMAs). Each chunk sum is
+// folded into an error-free (hi, lo) pair; the slice's pair goes to a
+// partial buffer and logits_keys_kernel folds the slices in slice order, so
+// the result does not depend on scheduling.
 constexpr int kLThreads = 128;
 constexpr int kLPad = kLT + 4;
 
@@ -1137,13 +1485,16 @@ __device__ __forceinline__ void logits_stash(float (*xs)[kLPad], float (*ws)[kLP
   }
 }
 
+// part: [slices][T][E] (hi, lo) pairs of the K slices
 template <int XT>
-__global__ void __launch_bounds__(kLThreads) logits_tiled_kernel(RouteArgs a, const float* xn, const float* wn) {
+__global__ void __launch_bounds__(kLThreads) logits_tiled_kernel(RouteArgs a, float2* part) {
   __shared__ __align__(16) float xs[2][kLK][kLPad];
   __shared__ __align__(16) float ws[2][kLK][kLPad];
-  const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int ty = lane & 7, tx = warp * 4 + (lane >> 3);  // tokens ty*8.., experts tx*4..
   const int t0 = blockIdx.y * kLT, e0 = blockIdx.x * kLE;
-  const int T = a.T, E = a.E, H = a.H;
+  const int T = a.T, E = a.E;
+  const int klen = a.H / gridDim.z, kbeg = blockIdx.z * klen;
   float hi[8][4], lo[8][4];
 #pragma unroll
   for (int i = 0; i < 8; ++i)
@@ -1151,13 +1502,13 @@ __global__ void __launch_bounds__(kLThreads) logits_tiled_kernel(RouteArgs a, co
     for (int j = 0; j < 4; ++j) hi[i][j] = lo[i][j] = 0.f;
   float xv[2][8];
   float4 wv[4];
-  logits_fetch<XT>(a, t0, e0, 0, xv, wv);
+  logits_fetch<XT>(a, t0, e0, kbeg, xv, wv);
   logits_stash(xs[0], ws[0], xv, wv);
   __syncthreads();
-  const int nch = H / kLK;
+  const int nch = klen / kLK;
   for (int c = 0; c < nch; ++c) {
     const int buf = c & 1;
-    if (c + 1 < nch) logits_fetch<XT>(a, t0, e0, (c + 1) * kLK, xv, wv);
+    if (c + 1 < nch) logits_fetch<XT>(a, t0, e0, kbeg + (c + 1) * kLK, xv, wv);
     float p[8][4];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
@@ -1167,9 +1518,9 @@ __global__ void __launch_bounds__(kLThreads) logits_tiled_kernel(RouteArgs a, co
     for (int k = 0; k < kLK; ++k) {
       const float4 x0 = *reinterpret_cast<const float4*>(&xs[buf][k][ty * 8]);
       const float4 x1 = *reinterpret_cast<const float4*>(&xs[buf][k][ty * 8 + 4]);
-      const float4 wq = *reinterpret_cast<const float4*>(&ws[buf][k][tx * 4]);
+      const float4 w4 = *reinterpret_cast<const float4*>(&ws[buf][k][tx * 4]);
       const float xa[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-      const float wa[4] = {wq.x, wq.y, wq.z, wq.w};
+      const float wa[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
       for (int i = 0; i < 8; ++i)
 #pragma unroll
@@ -1187,8 +1538,7 @@ __global__ void __launch_bounds__(kLThreads) logits_tiled_kernel(RouteArgs a, co
     if (c + 1 < nch) logits_stash(xs[buf ^ 1], ws[buf ^ 1], xv, wv);
     __syncthreads();
   }
-  const size_t te = static_cast<size_t>(T) * E;
-  const double g32 = 32.0 * 0x1p-24 / (1.0 - 32.0 * 0x1p-24);
+  float2* dst = part + static_cast<size_t>(blockIdx.z) * T * E;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int t = t0 + ty * 8 + i;
@@ -1196,19 +1546,43 @@ __global__ void __launch_bounds__(kLThreads) logits_tiled_kernel(RouteArgs a, co
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int e = e0 + tx * 4 + j;
-      if (e >= E) continue;
-      const double b = a.bias ? static_cast<double>(a.bias[e]) : 0.0;
-      const double l = (static_cast<double>(hi[i][j]) + static_cast<double>(lo[i][j])) + b;
-      const double A = static_cast<double>(xn[t]) * static_cast<double>(wn[e]);
-      const double bnd = 1.01 * g32 * A + fabs(l) * 0x1p-51 + static_cast<double>(H + 1) * 0x1p-140;
-      const double wid = __dadd_ru(bnd, __dmul_ru(fabs(l), 0x1p-50));
-      const bool fin = isfinite(l) && isfinite(wid);
-      const size_t o = static_cast<size_t>(t) * E + e;
-      a.keys[o] = okey(l);
-      a.keys[te + o] = fin ? okey(__dsub_rd(l, wid)) : 0ull;
-      a.keys[2 * te + o] = fin ? okey(__dadd_ru(l, wid)) : ~0ull;
+      if (e < E) dst[static_cast<size_t>(t) * E + e] = make_float2(hi[i][j], lo[i][j]);
     }
   }
+}
+
+// Folds the slices' (hi, lo) pairs in slice order and writes the logit keys
+// and the outward-rounded bound keys (one thread per token and expert). The
+// bound is formed in fp32 with every operation rounded up (an upper bound
+// of the fp64 expression gamma_32 * 1.01 * |x||w| + |l| (2^-51 + 2^-50) +
+// (H+1) 2^-126), so only the logit and the two interval ends use fp64.
+__global__ void __launch_bounds__(256) logits_keys_kernel(RouteArgs a, const float2* part, int slices,
+                                                          const float* xn, const float* wn) {
+  const size_t te = static_cast<size_t>(a.T) * a.E;
+  const int t = blockIdx.y, e = blockIdx.x * 256 + threadIdx.x;  // grid (ceil(E/256), T)
+  if (e >= a.E) return;
+  const size_t o = static_cast<size_t>(t) * a.E + e;
+  float2 v = __ldcs(part + o);
+  float hi = v.x, lo = v.y;
+  for (int z = 1; z < slices; ++z) {
+    v = __ldcs(part + z * te + o);
+    float ns, es;
+    two_sum(hi, v.x, ns, es);
+    hi = ns;
+    lo = __fadd_rn(__fadd_rn(lo, v.y), es);
+  }
+  const float bf = a.bias ? a.bias[e] : 0.f;
+  const double l = (static_cast<double>(hi) + static_cast<double>(lo)) + static_cast<double>(bf);
+  // 1.01 * gamma_32 rounded up; gamma_32 = 32u / (1 - 32u), u = 2^-24
+  const float c1 = 1.9314e-6f;
+  const float A = __fmul_ru(__ldg(xn + t), __ldg(wn + e));
+  const float absl = __fadd_ru(__fadd_ru(fabsf(hi), fabsf(lo)), fabsf(bf));
+  const float wid =
+      __fadd_ru(__fadd_ru(__fmul_ru(c1, A), __fmul_ru(absl, 0x1.8p-50f)), static_cast<float>(a.H + 1) * 0x1p-126f);
+  const bool fin = isfinite(l) && isfinite(wid);
+  a.keys[o] = okey(l);
+  a.keys[te + o] = fin ? okey(__dsub_rd(l, static_cast<double>(wid))) : 0ull;
+  a.keys[2 * te + o] = fin ? okey(__dadd_ru(l, static_cast<double>(wid))) : ~0ull;
 }
 
 __global__ void __launch_bounds__(256) select_kernel(RouteArgs a, int* flags) {
@@ -1374,8 +1748,9 @@ __global__ void admit_kernel(AdmitArgs A, moe_plan_t P, uint32_t* err) {
 
 }  // namespace
 
-cudaError_t launch_route_large(const RouteArgs& a, float* norms, int* flags, cudaStream_t st) {
+cudaError_t launch_route_large(const RouteArgs& a, float* norms, int* flags, float2* part, cudaStream_t st) {
   if (a.T < 1 || a.k > 16 || a.E > 1024 || a.H % kLK) return cudaErrorInvalidValue;
+  const int slices = a.H % (kLK * 4) == 0 ? 4 : (a.H % (kLK * 2) == 0 ? 2 : 1);
   float* xn = norms;
   float* wn = norms + a.T;
   const int nrows = a.T + a.E;
@@ -1383,11 +1758,12 @@ cudaError_t launch_route_large(const RouteArgs& a, float* norms, int* flags, cud
     row_norms_kernel<MOE_BF16><<<(nrows + 7) / 8, 256, 0, st>>>(a.x, a.T, a.w, a.E, a.H, xn, wn);
   else
     row_norms_kernel<MOE_F32><<<(nrows + 7) / 8, 256, 0, st>>>(a.x, a.T, a.w, a.E, a.H, xn, wn);
-  dim3 grid((a.E + kLE - 1) / kLE, (a.T + kLT - 1) / kLT);
+  dim3 grid((a.E + kLE - 1) / kLE, (a.T + kLT - 1) / kLT, slices);
   if (a.xt == MOE_BF16)
-    logits_tiled_kernel<MOE_BF16><<<grid, kLThreads, 0, st>>>(a, xn, wn);
+    logits_tiled_kernel<MOE_BF16><<<grid, kLThreads, 0, st>>>(a, part);
   else
-    logits_tiled_kernel<MOE_F32><<<grid, kLThreads, 0, st>>>(a, xn, wn);
+    logits_tiled_kernel<MOE_F32><<<grid, kLThreads, 0, st>>>(a, part);
+  logits_keys_kernel<<<dim3((a.E + 255) / 256, a.T), 256, 0, st>>>(a, part, slices, xn, wn);
   select_kernel<<<(a.T + 7) / 8, 256, 0, st>>>(a, flags);
   if (a.xt == MOE_BF16)
     repair_kernel<MOE_BF16><<<a.T, kRouteThreads, 0, st>>>(a, flags);
