@@ -36,6 +36,9 @@ import numpy as np  # noqa: E402
 import workloads as W  # noqa: E402
 
 WORKLOAD = "decode"
+# admission mode of the headline: 2 = on-device admission, misses read
+# through by the FFN kernels (1 = separate staging kernel, 0 = host)
+HEADLINE_MODE = 2
 METRIC = "MoE-layer tokens/s at 1 GB300; achieved HBM GB/s (decode) & TFLOP/s (prefill)"
 
 
@@ -163,7 +166,7 @@ def run_ours(args, rank, world, dev):
     x_pin = torch.from_numpy(x_host.view(np.int16)).view(torch.bfloat16).pin_memory()
     x_dev = x_pin.to(dev)
 
-    def make_ctx(device_admit=1):
+    def make_ctx(device_admit=HEADLINE_MODE):
         ctx = bec.Context(L, E, k, H, w.inter, w.shared_inter, w.quant, w.slots, w.policy, 3, 0,
                           262144, T, admit_on_device=device_admit)
         ctx.bind_store(store)
@@ -210,44 +213,53 @@ def run_ours(args, rank, world, dev):
         barrier()
         return max_over_ranks(ev0.elapsed_time(ev1))
 
-    # ---- pass 1 (headline): device-resident inputs, on-device admission, the
-    # 40-layer step replayed as one CUDA graph
-    ctx = make_ctx()
     x_step = torch.empty((L, T, H), dtype=torch.bfloat16, device=dev)
-    graph = None
-    if args.no_graph:
-        for s in range(args.warmup):
-            step(ctx, s)
-    else:
-        for s in range(args.warmup - 1):
-            step(ctx, s)
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
-            for l in range(L):
-                ctx.layer_forward(l, x_step[l], routers[l], None, idx, wt, plan, y[l])
 
-    def graph_step(s):
-        x_step.copy_(x_dev[:, s * T:(s + 1) * T], non_blocking=True)
-        graph.replay()
+    def graph_pass(mode, sample_clocks):
+        """Device-resident inputs, on-device admission, the 40-layer step
+        replayed as one CUDA graph; returns (ms, clocks, stats, used_graph)."""
+        ctx = make_ctx(mode)
+        graph = None
+        if args.no_graph:
+            for s in range(args.warmup):
+                step(ctx, s)
+        else:
+            for s in range(args.warmup - 1):
+                step(ctx, s)
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                for l in range(L):
+                    ctx.layer_forward(l, x_step[l], routers[l], None, idx, wt, plan, y[l])
 
-    if graph is not None:
-        graph_step(args.warmup - 1)  # the last warm-up step; its replay uploads the graph
-    torch.cuda.synchronize(dev)
-    ctx.check_device_errors()
+        def graph_step(s):
+            x_step.copy_(x_dev[:, s * T:(s + 1) * T], non_blocking=True)
+            graph.replay()
 
-    clocks = ClockSampler(dev.index if dev.index is not None else 0)
-    clocks.start()
-    elapsed_ms = timed(graph_step if graph is not None else (lambda s: step(ctx, s)))
-    clk = clocks.stop()
-    ctx.check_device_errors()
-    st_graph = ctx.stats()
-    used_graph = graph is not None
-    del graph
-    ctx.close()
+        if graph is not None:
+            graph_step(args.warmup - 1)  # the last warm-up step; its replay uploads the graph
+        torch.cuda.synchronize(dev)
+        ctx.check_device_errors()
+        clocks = ClockSampler(dev.index if dev.index is not None else 0) if sample_clocks else None
+        if clocks:
+            clocks.start()
+        ms = timed(graph_step if graph is not None else (lambda s: step(ctx, s)))
+        clk = clocks.stop() if clocks else None
+        ctx.check_device_errors()
+        st = ctx.stats()
+        used = graph is not None
+        del graph
+        ctx.close()
+        return ms, clk, st, used
+
+    # ---- pass 1 (headline): read-through misses (the FFN reads a missed
+    # expert from the pinned store over the host link and writes its slot)
+    elapsed_ms, clk, st_graph, used_graph = graph_pass(HEADLINE_MODE, True)
 
     # ---- pass 2: the same steps, launched call by call with library-side
-    # CUDA events around every kernel (roofline and kernel breakdown)
-    ctx = make_ctx()
+    # CUDA events around every kernel (roofline and kernel breakdown), with
+    # the misses staged by the separate staging kernel so that the FFN
+    # kernels read only HBM and the host-link copy is timed on its own
+    ctx = make_ctx(1)
     for s in range(args.warmup):
         step(ctx, s)
     ctx.check_device_errors()
@@ -268,16 +280,18 @@ def run_ours(args, rank, world, dev):
              "per_call_launch_tokens_per_s": round(tokens / (events_ms / 1e3), 2),
              "graph": used_graph}
     if not args.skip_e2e:
-        # pass 3: the other miss paths, call by call: admission and tile staging
-        # on the host (one sync per layer), and on-device admission with a
-        # separate staging kernel
-        for mode, key in ((0, "host_admission_tokens_per_s"), (2, "read_through_tokens_per_s")):
-            ctx = make_ctx(device_admit=mode)
-            for s in range(args.warmup):
-                step(ctx, s)
-            m_ms = timed(lambda s: step(ctx, s))
-            ctx.close()
-            extra[key] = round(tokens / (m_ms / 1e3), 2)
+        # pass 3: the other miss paths: on-device admission with a separate
+        # staging kernel (graph replay), and admission plus tile staging on
+        # the host with cudaMemcpyAsync on three streams (one sync per layer,
+        # call by call)
+        k_ms, _, _, _ = graph_pass(1, False)
+        extra["staging_kernel_tokens_per_s"] = round(tokens / (k_ms / 1e3), 2)
+        ctx = make_ctx(device_admit=0)
+        for s in range(args.warmup):
+            step(ctx, s)
+        m_ms = timed(lambda s: step(ctx, s))
+        ctx.close()
+        extra["host_admission_tokens_per_s"] = round(tokens / (m_ms / 1e3), 2)
     if args.skip_e2e:
         return finish(args, w, world, value, elapsed_ms, None, kt, st0, st1, clk, extra), w
     # ---- pass 4: end to end through host buffers, call by call
@@ -418,17 +432,23 @@ def finish(args, w, world, value, elapsed_ms, e2e_value, kt, st0, st1, clk, extr
         "kernels": {kname: {"ms": round(ms, 3), "launches": n,
                             "avg_us": round(ms / n * 1e3, 3) if n else None}
                     for kname, (ms, n) in kt.items()},
+        "kernels_pass": "call by call, misses staged by the staging kernel",
         "ffn_down": {"achieved_gbs": round(dn_gbs, 1) if dn_gbs else None,
                      "frac": round(dn_gbs / peak, 4) if dn_gbs else None, "bytes_per_launch": dn_bytes},
+        "host_link": {"kernel": "stage_copy (misses, pinned store -> slots)",
+                      "achieved": round(staged / (kt["stage_copy"][0] / 1e3) / 1e9, 1)
+                      if kt["stage_copy"][0] else None,
+                      "peak": extra.get("h2d_copy_engine_gbs"), "unit": "GB/s",
+                      "peak_source": "measured copy-engine bandwidth of a 1 GiB pinned copy"},
         "cache": {"hits": dh, "misses": dm,
                   "hit_rate": round(dh / max(1, dh + dm), 4),
                   "bytes_staged": staged,
                   "staging_gbs_avg_over_step": round(staged / (elapsed_ms / 1e3) / 1e9, 2),
                   "miss_bytes_per_step": round(staged / args.steps),
-                  "stage_copy_gbs": round(staged / (kt["stage_copy"][0] / 1e3) / 1e9, 1)
-                  if kt["stage_copy"][0] else None,
-                  "admission": "on device (router's last block); misses copied from the pinned "
-                               "store over the host link by a staging kernel, 32 KiB per CTA"},
+                  "admission": "on device (router's last block); a miss is read by the FFN kernels "
+                               "from the pinned store over the host link and written into its slot "
+                               "(read-through); the slot's generation is published once every tile "
+                               "of it has landed"},
         **extra,
         "gpu_launches": launches,
         "uncertified_repairs": st1["uncertified_repairs"] - st0["uncertified_repairs"],

@@ -849,6 +849,7 @@ extern "C" moe_status_t moe_layer_forward(moe_ctx_t* ctx, int32_t layer, const v
       sa.chunks_per_expert += sa.chunks[m];
     }
     sa.max_fills = std::min(ctx->max_fills, std::min(T * ctx->cfg.top_k, ctx->cfg.n_experts));
+    sa.grid = 4 * ctx->num_sms;
     if (ctx->timing) {
       moe_ctx::TimedLaunch r{MOE_KT_STAGE, timing_event(ctx), timing_event(ctx)};
       CK(cudaEventRecord(r.a, st));

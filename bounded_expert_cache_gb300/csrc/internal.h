@@ -144,6 +144,7 @@ struct StageArgs {
   int chunks[3];             // copy chunks per matrix
   int chunks_per_expert;
   int max_fills;
+  int grid;                  // persistent CTAs (a few per SM)
 };
 constexpr int64_t kStageChunkBytes = 32768;  // one CTA's copy: 256 threads x 8 x 16 B
 cudaError_t launch_stage_copy(const StageArgs& a, cudaStream_t st);

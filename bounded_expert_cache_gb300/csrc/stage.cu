@@ -8,11 +8,14 @@
 //
 // On GB300 the pinned store is reachable from the GPU over the coherent
 // host link, so the copy is a kernel: after on-device admission wrote the
-// fill list, one CTA per (fill, 32 KiB chunk) issues all its 16-byte loads at
-// once (eight per thread) and stores them; chunks never cross a matrix, and
+// fill list, a persistent grid walks the (fill, 32 KiB chunk) items; for
+// each, a CTA issues all its 16-byte loads at once (eight per thread) and
+// stores them; chunks never cross a matrix, and
 // the 256 KiB tiles of each matrix remain the accounting unit. The CTA that
 // lands a fill's last chunk publishes the slot's generation. No host round
 // trip sits between routing and the FFN.
+#include <algorithm>
+
 #include "internal.h"
 
 namespace moe {
@@ -24,46 +27,52 @@ constexpr int kCopyUnroll = 8;
 // Streaming load of the store through its device alias (host memory).
 __device__ __forceinline__ uint4 ld_host_stream(const uint4* p) { return __ldcs(p); }
 
+// Persistent: CTA b copies work items b, b + gridDim.x, ... of the
+// n_fills * chunks_per_expert items (item = fill * chunks_per_expert +
+// chunk), so the launch does not depend on how many misses the step has.
 __global__ void __launch_bounds__(kCopyThreads) stage_copy_kernel(StageArgs a) {
-  const int f = blockIdx.y;
   const int n = __ldcg(a.fills);
-  if (f >= n) return;
-  const int e = __ldcg(a.fills + 1 + 2 * f);
-  const int slot = __ldcg(a.fills + 2 + 2 * f);
-  // chunk -> (matrix, offset); chunks never cross a matrix
-  int j = blockIdx.x, m = 0;
-  while (m < 2 && j >= a.chunks[m]) {
-    j -= a.chunks[m];
-    ++m;
-  }
-  const int64_t off = a.mat_off[m] + static_cast<int64_t>(j) * kStageChunkBytes;
-  const int64_t len = min(kStageChunkBytes, a.mat_bytes[m] - static_cast<int64_t>(j) * kStageChunkBytes);
-  const uint4* src = reinterpret_cast<const uint4*>(a.store + static_cast<int64_t>(e) * a.payload + off);
-  uint4* dst = reinterpret_cast<uint4*>(a.pool + static_cast<int64_t>(slot) * a.slot_stride + off);
-  const int nv = static_cast<int>(len / 16);
-  uint4 v[kCopyUnroll];
+  const int cpe = a.chunks_per_expert;
+  const int items = n * cpe;
+  for (int w = blockIdx.x; w < items; w += gridDim.x) {
+    const int f = w / cpe;
+    const int e = __ldcg(a.fills + 1 + 2 * f);
+    const int slot = __ldcg(a.fills + 2 + 2 * f);
+    // chunk -> (matrix, offset); chunks never cross a matrix
+    int j = w - f * cpe, m = 0;
+    while (m < 2 && j >= a.chunks[m]) {
+      j -= a.chunks[m];
+      ++m;
+    }
+    const int64_t off = a.mat_off[m] + static_cast<int64_t>(j) * kStageChunkBytes;
+    const int64_t len = min(kStageChunkBytes, a.mat_bytes[m] - static_cast<int64_t>(j) * kStageChunkBytes);
+    const uint4* src = reinterpret_cast<const uint4*>(a.store + static_cast<int64_t>(e) * a.payload + off);
+    uint4* dst = reinterpret_cast<uint4*>(a.pool + static_cast<int64_t>(slot) * a.slot_stride + off);
+    const int nv = static_cast<int>(len / 16);
+    uint4 v[kCopyUnroll];
 #pragma unroll
-  for (int u = 0; u < kCopyUnroll; ++u) {
-    const int i = threadIdx.x + u * kCopyThreads;
-    if (i < nv) v[u] = ld_host_stream(src + i);
-  }
+    for (int u = 0; u < kCopyUnroll; ++u) {
+      const int i = threadIdx.x + u * kCopyThreads;
+      if (i < nv) v[u] = ld_host_stream(src + i);
+    }
 #pragma unroll
-  for (int u = 0; u < kCopyUnroll; ++u) {
-    const int i = threadIdx.x + u * kCopyThreads;
-    if (i < nv) dst[i] = v[u];
-  }
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    const unsigned prev = atomicAdd(a.done + f, 1u);
-    if (prev + 1 == static_cast<unsigned>(a.chunks_per_expert)) {
-      // every chunk of this fill has landed: publish the slot's generation
-      __threadfence();
-      a.gen[slot] = __ldcg(a.sgen + slot);
-      atomicAdd(reinterpret_cast<unsigned long long*>(a.stats + kStatTiles),
-                static_cast<unsigned long long>(a.tiles_per_expert));
-      atomicAdd(reinterpret_cast<unsigned long long*>(a.stats + kStatBytes),
-                static_cast<unsigned long long>(a.payload));
+    for (int u = 0; u < kCopyUnroll; ++u) {
+      const int i = threadIdx.x + u * kCopyThreads;
+      if (i < nv) dst[i] = v[u];
+    }
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      const unsigned prev = atomicAdd(a.done + f, 1u);
+      if (prev + 1 == static_cast<unsigned>(cpe)) {
+        // every chunk of this fill has landed: publish the slot's generation
+        __threadfence();
+        a.gen[slot] = __ldcg(a.sgen + slot);
+        atomicAdd(reinterpret_cast<unsigned long long*>(a.stats + kStatTiles),
+                  static_cast<unsigned long long>(a.tiles_per_expert));
+        atomicAdd(reinterpret_cast<unsigned long long*>(a.stats + kStatBytes),
+                  static_cast<unsigned long long>(a.payload));
+      }
     }
   }
 }
@@ -73,7 +82,7 @@ __global__ void __launch_bounds__(kCopyThreads) stage_copy_kernel(StageArgs a) {
 cudaError_t launch_stage_copy(const StageArgs& a, cudaStream_t st) {
   if (a.max_fills <= 0) return cudaSuccess;
   static_assert(kStageChunkBytes == 16 * kCopyThreads * kCopyUnroll, "one chunk per CTA");
-  dim3 grid(a.chunks_per_expert, a.max_fills);
+  const int grid = std::max(1, std::min(a.grid, a.chunks_per_expert * a.max_fills));
   stage_copy_kernel<<<grid, kCopyThreads, 0, st>>>(a);
   return cudaGetLastError();
 }
