@@ -253,7 +253,7 @@ def run_ours(args, rank, world, dev):
 
     # ---- pass 1 (headline): read-through misses (the FFN reads a missed
     # expert from the pinned store over the host link and writes its slot)
-    elapsed_ms, clk, st_graph, used_graph = graph_pass(HEADLINE_MODE, True)
+    elapsed_ms, clk, st_graph, used_graph = graph_pass(args.admission, True)
 
     # ---- pass 2: the same steps, launched call by call with library-side
     # CUDA events around every kernel (roofline and kernel breakdown), with
@@ -476,6 +476,8 @@ def main():
     ap.add_argument("--skip-prefill", action="store_true", help="skip the prefill workload pass")
     ap.add_argument("--prefill-only", action="store_true", help="profiling: only the prefill pass")
     ap.add_argument("--prefill-tokens", type=int, default=0, help="profiling: tokens of the prefill chunk")
+    ap.add_argument("--admission", type=int, default=HEADLINE_MODE, choices=[1, 2],
+                    help="profiling: miss path of the headline pass (2 read-through, 1 staging kernel)")
     args = ap.parse_args()
     assert args.warmup >= 3
 
