@@ -116,10 +116,14 @@ moe_status_t slots_step(moe_slots* s, const int32_t* uniq, int32_t n_uniq, const
   for (int32_t e : U) {
     if (s->pt[e] >= 0) s->last[s->pt[e]] = ++s->tick;
   }
+  // the misses are fixed before any fill: a resident expert of the union
+  // that a fill evicts (|U| > S) was still a hit of this step
+  std::vector<int32_t> M;
+  for (int32_t e : U)
+    if (s->pt[e] < 0) M.push_back(e);
   int32_t n_waves = 1;
   std::vector<int32_t> cand;
-  for (int32_t e : U) {
-    if (s->pt[e] >= 0) continue;
+  for (int32_t e : M) {
     ++s->tick;
     int32_t slot = lowest_free(s), victim = -1;
     if (slot < 0) {

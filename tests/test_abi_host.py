@@ -124,6 +124,37 @@ def test_slot_manager_waves_and_capacity(bec):
     assert r.read() == before
 
 
+def test_slot_manager_waves_over_many_steps_match_oracle(bec):
+    # LRU steps whose unions are larger than the slots, with residents of the
+    # union that a fill of the same step evicts: fills, page table,
+    # generations and counters follow the oracle's replay (the misses are
+    # the experts absent when the step starts), and the wave of a fill comes
+    # after the wave of the in-step expert it evicts
+    rng = np.random.default_rng(21)
+    for (E, S, lo, hi) in ((12, 4, 3, 11), (128, 44, 30, 128), (64, 20, 15, 64)):
+        s = bec.Slots(E, S, 0, 0, 0, 1)
+        ref = SlotCache(E, S, 0, seed=0, layer=0, payload_bytes=1)
+        for _ in range(40):
+            width = int(rng.integers(lo, hi + 1))
+            u = sorted(rng.choice(E, size=width, replace=False).tolist())
+            counts = [0] * E
+            for e in u:
+                counts[e] = int(rng.integers(1, 4))
+            r = ref.step(u, counts)
+            m = s.step(u, counts)
+            assert list(zip(m.expert, m.slot, m.victim)) == [tuple(f) for f in r["fills"]]
+            assert s.read() == (r["pt"], r["gen"])
+            assert (m.hits, m.misses) == (r["hits"], r["misses"])
+            wave_of = {e: 0 for e in u}
+            for e, v, wv in zip(m.expert, m.victim, m.wave):
+                assert wv == (wave_of[v] + 1 if v in wave_of else 0)
+                wave_of[e] = wv
+            assert m.n_waves == (max(m.wave) + 1 if m.wave else 1)
+        st, rs = s.stats(), ref.stats()
+        for key in ("hits", "misses", "evictions", "materialized_bytes"):
+            assert st[key] == rs[key], key
+
+
 def test_slot_manager_rejects_bad_union(bec):
     s = bec.Slots(8, 4, 0)
     with pytest.raises(bec.MoeError):
