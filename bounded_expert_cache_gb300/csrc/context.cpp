@@ -237,7 +237,9 @@ extern "C" moe_status_t moe_create(const moe_config_t* cfg, moe_ctx_t** out) {
   CKC(cudaHostAlloc(&ctx->h_err, sizeof(uint32_t), cudaHostAllocDefault));
   CKC(cudaHostAlloc(&ctx->h_union, sizeof(int32_t) * (2 * E + 2), cudaHostAllocDefault));
   ctx->max_units = std::min(E, c.max_tokens * c.top_k) + 1;
-  const size_t unit_ints = moe::kUnitHeader + moe::kUnitInts * static_cast<size_t>(ctx->max_units);
+  // room for one unit table and one fill list per compute wave (a wave
+  // holds at least one unit; fills <= units)
+  const size_t unit_ints = moe::kUnitHeader + 16 * static_cast<size_t>(ctx->max_units);
   CKC(cudaMalloc(&ctx->d_units, sizeof(int32_t) * unit_ints));
   CKC(cudaMemset(ctx->d_units, 0, sizeof(int32_t) * unit_ints));
   CKC(cudaHostAlloc(&ctx->h_units, sizeof(int32_t) * unit_ints, cudaHostAllocDefault));
@@ -496,15 +498,24 @@ static void publish_page_table_host(moe_ctx_t* ctx, int32_t layer) {
   (void)S;
 }
 
-extern "C" moe_status_t moe_cache_admit(moe_ctx_t* ctx, int32_t layer, const moe_plan_t* plan,
-                                        moe_miss_list_t* misses, moe_stream_t stream) {
-  if (!ctx) return MOE_ERR_ARG;
-  if (!valid_layer(ctx, layer)) return fail(ctx, MOE_ERR_ARG, "admit: bad layer");
-  if (!plan_ok(plan) || !misses) return fail(ctx, MOE_ERR_ARG, "admit: null pointer");
-  if (ctx->dev_admit)
-    return fail(ctx, MOE_ERR_STATE, "admit: this context admits on the device (moe_layer_forward)");
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const int E = ctx->cfg.n_experts;
+// Compute waves of one step: wave w's unit table sits at int offset off[w]
+// of the unit buffer and the list of its fills [n, (slot, generation) x n]
+// at offset pub[w]; fill i of the miss list leaves its slot at generation
+// fill_gen[i].
+struct WavePlan {
+  std::vector<int32_t> off, pub;
+  std::vector<uint32_t> fill_gen;
+};
+
+// Host admission of one step. With `waves` null a union larger than the
+// slots is refused; otherwise (the prefill path) the step may run in compute
+// waves, described by *waves. Each unit carries the slot and the generation it holds
+// during its wave: a slot can change hands inside the step, so they come
+// from replaying the fill list over the state before the step, not from the
+// final page table.
+static moe_status_t admit_host(moe_ctx_t* ctx, int32_t layer, const moe_plan_t* plan, moe_miss_list_t* misses,
+                               cudaStream_t st, WavePlan* waves) {
+  const int E = ctx->cfg.n_experts, S = ctx->cfg.slots_per_layer;
   int32_t* hu = ctx->h_union;
   CK(cudaMemcpyAsync(hu + 2 * E, plan->n_uniq, sizeof(int32_t), cudaMemcpyDeviceToHost, st));
   CK(cudaMemcpyAsync(hu, plan->uniq, sizeof(int32_t) * E, cudaMemcpyDeviceToHost, st));
@@ -512,60 +523,111 @@ extern "C" moe_status_t moe_cache_admit(moe_ctx_t* ctx, int32_t layer, const moe
   CK(cudaStreamSynchronize(st));
   const int32_t nu = hu[2 * E];
   if (nu < 0 || nu > E) return fail(ctx, MOE_ERR_STATE, "admit: plan holds no valid union");
-  if (nu > ctx->cfg.slots_per_layer)
+  if (nu > S && !waves)
     return fail(ctx, MOE_ERR_CAPACITY,
-                "admit: the step's union is larger than the slots; the decode path evaluates "
-                "a layer with all its experts resident");
-  moe_status_t s = moe::slots_step(ctx->slots[layer], hu, nu, hu + E, misses, &ctx->err);
+                "admit: the step's union is larger than the slots; only moe_layer_forward on the "
+                "prefill path (T > 8) runs such a step, in compute waves");
+  moe_slots* sl = ctx->slots[layer];
+  std::vector<int32_t> slot_of(E, -1), wave_of(E, 0);
+  std::vector<uint32_t> gen_of(E, 0u);
+  std::vector<uint32_t> g(moe::slots_gen(sl), moe::slots_gen(sl) + S);
+  for (int i = 0; i < nu; ++i) {
+    const int e = hu[i];
+    if (e < 0 || e >= E) return fail(ctx, MOE_ERR_STATE, "admit: union entry out of range");
+    slot_of[e] = moe::slots_pt(sl)[e];
+    if (slot_of[e] >= 0) gen_of[e] = g[slot_of[e]];
+  }
+  moe_status_t s = moe::slots_step(sl, hu, nu, hu + E, misses, &ctx->err);
   if (s != MOE_OK) return s;
+  if (waves) waves->fill_gen.assign(misses->n, 0u);
+  for (int i = 0; i < misses->n; ++i) {
+    const int e = misses->expert[i], slot = misses->slot[i];
+    slot_of[e] = slot;
+    gen_of[e] = ++g[slot];
+    wave_of[e] = misses->wave[i];
+    if (waves) waves->fill_gen[i] = gen_of[e];
+  }
   publish_page_table_host(ctx, layer);
   const size_t off = static_cast<size_t>(layer) * E;
   CK(cudaMemcpyAsync(ctx->d_pt + off, ctx->h_pt + off, sizeof(int32_t) * E, cudaMemcpyHostToDevice, st));
   CK(cudaMemcpyAsync(ctx->d_ptgen + off, ctx->h_ptgen + off, sizeof(uint32_t) * E,
                      cudaMemcpyHostToDevice, st));
-  // unit table of the step: routed experts in union order, then the shared one
-  const int32_t* pt = moe::slots_pt(ctx->slots[layer]);
-  const uint32_t* gen = moe::slots_gen(ctx->slots[layer]);
-  int32_t* ut = ctx->h_units;
-  int p0 = 0, nu_tab = 0;
+  // unit tables: per wave, its routed experts in union order; the shared
+  // expert runs in wave 0
   std::vector<int32_t> p0_of(E, 0);
+  int p0 = 0;
   for (int e = 0; e < E; ++e) {
     p0_of[e] = p0;
     p0 += hu[E + e];
   }
-  for (int i = 0; i < nu; ++i) {
-    const int e = hu[i];
-    int32_t* U = ut + moe::kUnitHeader + moe::kUnitInts * nu_tab++;
-    U[0] = pt[e];
-    U[1] = p0_of[e];
-    U[2] = hu[E + e];
-    U[3] = static_cast<int32_t>(gen[pt[e]]);
+  const int n_waves = std::max(1, misses->n_waves);
+  if (waves) {
+    waves->off.assign(n_waves, 0);
+    waves->pub.assign(n_waves, 0);
   }
-  if (ctx->cfg.shared_inter > 0) {
-    int32_t* U = ut + moe::kUnitHeader + moe::kUnitInts * nu_tab++;
-    U[0] = -1;
-    U[1] = -1;
-    U[2] = p0 / ctx->cfg.top_k;  // tokens of the step
-    U[3] = 0;
+  int32_t* ut = ctx->h_units;
+  int32_t at = 0;
+  for (int w = 0; w < n_waves; ++w) {
+    if (waves) waves->off[w] = at;
+    int32_t* tab = ut + at;
+    int n_tab = 0;
+    for (int i = 0; i < nu; ++i) {
+      const int e = hu[i];
+      if (wave_of[e] != w) continue;
+      int32_t* U = tab + moe::kUnitHeader + moe::kUnitInts * n_tab++;
+      U[0] = slot_of[e];
+      U[1] = p0_of[e];
+      U[2] = hu[E + e];
+      U[3] = static_cast<int32_t>(gen_of[e]);
+    }
+    if (w == 0 && ctx->cfg.shared_inter > 0) {
+      int32_t* U = tab + moe::kUnitHeader + moe::kUnitInts * n_tab++;
+      U[0] = -1;
+      U[1] = -1;
+      U[2] = p0 / ctx->cfg.top_k;  // tokens of the step
+      U[3] = 0;
+    }
+    tab[0] = n_tab;
+    at += moe::kUnitHeader + moe::kUnitInts * n_tab;
+    if (waves) {
+      waves->pub[w] = at;
+      int32_t* pl = ut + at;
+      int nf = 0;
+      for (int i = 0; i < misses->n; ++i) {
+        if (misses->wave[i] != w) continue;
+        pl[1 + 2 * nf] = misses->slot[i];
+        pl[2 + 2 * nf] = static_cast<int32_t>(waves->fill_gen[i]);
+        ++nf;
+      }
+      pl[0] = nf;
+      at += (1 + 2 * nf + 3) / 4 * 4;  // keep the next table 16-byte aligned
+    }
   }
-  ut[0] = nu_tab;
-  CK(cudaMemcpyAsync(ctx->d_units, ut, sizeof(int32_t) * (moe::kUnitHeader + moe::kUnitInts * nu_tab),
-                     cudaMemcpyHostToDevice, st));
+  CK(cudaMemcpyAsync(ctx->d_units, ut, sizeof(int32_t) * at, cudaMemcpyHostToDevice, st));
   return MOE_OK;
 }
 
-extern "C" moe_status_t moe_stage_tiles(moe_ctx_t* ctx, int32_t layer, const moe_miss_list_t* misses,
-                                        moe_stream_t compute_stream) {
+extern "C" moe_status_t moe_cache_admit(moe_ctx_t* ctx, int32_t layer, const moe_plan_t* plan,
+                                        moe_miss_list_t* misses, moe_stream_t stream) {
   if (!ctx) return MOE_ERR_ARG;
-  if (!valid_layer(ctx, layer) || !misses || misses->layer != layer)
-    return fail(ctx, MOE_ERR_ARG, "stage: bad layer or miss list");
-  if (misses->n > 0 && !ctx->store) return fail(ctx, MOE_ERR_STATE, "stage: no store bound");
+  if (!valid_layer(ctx, layer)) return fail(ctx, MOE_ERR_ARG, "admit: bad layer");
+  if (!plan_ok(plan) || !misses) return fail(ctx, MOE_ERR_ARG, "admit: null pointer");
   if (ctx->dev_admit)
-    return fail(ctx, MOE_ERR_STATE, "stage: this context stages on the device (moe_layer_forward)");
-  cudaStream_t cst = reinterpret_cast<cudaStream_t>(compute_stream);
+    return fail(ctx, MOE_ERR_STATE, "admit: this context admits on the device (moe_layer_forward)");
+  return admit_host(ctx, layer, plan, misses, reinterpret_cast<cudaStream_t>(stream), nullptr);
+}
+
+// Host->device copies of the fills of compute wave `wave` (all fills if
+// wave < 0), in tiles over the copy streams, after the compute enqueued so
+// far on `cst`; `cst` then waits for them. The slots' new generations are
+// published by the caller.
+static moe_status_t stage_fills(moe_ctx_t* ctx, int32_t layer, const moe_miss_list_t* misses, int wave,
+                                cudaStream_t cst) {
   const int E = ctx->cfg.n_experts, S = ctx->cfg.slots_per_layer;
   const int ns = static_cast<int>(ctx->streams.size());
-  if (misses->n == 0) return MOE_OK;
+  int n = 0;
+  for (int i = 0; i < misses->n; ++i) n += wave < 0 || misses->wave[i] == wave;
+  if (n == 0) return MOE_OK;
   // slots are overwritten only after the compute enqueued so far
   CK(cudaEventRecord(ctx->ev_compute, cst));
   for (int i = 0; i < ns; ++i) CK(cudaStreamWaitEvent(ctx->streams[i], ctx->ev_compute, 0));
@@ -574,6 +636,7 @@ extern "C" moe_status_t moe_stage_tiles(moe_ctx_t* ctx, int32_t layer, const moe
   int64_t issued = 0, bytes = 0;
   bool injected = false;
   for (int i = 0; i < misses->n && !injected; ++i) {
+    if (wave >= 0 && misses->wave[i] != wave) continue;
     const int e = misses->expert[i], slot = misses->slot[i];
     if (e < 0 || e >= E || slot < 0 || slot >= S) return fail(ctx, MOE_ERR_ARG, "stage: fill out of range");
     const uint8_t* src = ctx->store + (static_cast<size_t>(layer) * E + e) * g.bytes;
@@ -603,6 +666,25 @@ extern "C" moe_status_t moe_stage_tiles(moe_ctx_t* ctx, int32_t layer, const moe
     ctx->fail_after_tiles = -1;
     return fail(ctx, MOE_ERR_CUDA, "stage: injected copy failure (test hook); slots not published");
   }
+  if (ctx->fail_after_tiles >= 0) ctx->fail_after_tiles -= static_cast<int32_t>(issued);
+  return MOE_OK;
+}
+
+extern "C" moe_status_t moe_stage_tiles(moe_ctx_t* ctx, int32_t layer, const moe_miss_list_t* misses,
+                                        moe_stream_t compute_stream) {
+  if (!ctx) return MOE_ERR_ARG;
+  if (!valid_layer(ctx, layer) || !misses || misses->layer != layer)
+    return fail(ctx, MOE_ERR_ARG, "stage: bad layer or miss list");
+  if (misses->n > 0 && !ctx->store) return fail(ctx, MOE_ERR_STATE, "stage: no store bound");
+  if (ctx->dev_admit)
+    return fail(ctx, MOE_ERR_STATE, "stage: this context stages on the device (moe_layer_forward)");
+  if (misses->n_waves > 1)
+    return fail(ctx, MOE_ERR_STATE, "stage: a step in compute waves is staged by moe_layer_forward");
+  cudaStream_t cst = reinterpret_cast<cudaStream_t>(compute_stream);
+  const int S = ctx->cfg.slots_per_layer;
+  if (misses->n == 0) return MOE_OK;
+  moe_status_t s = stage_fills(ctx, layer, misses, -1, cst);
+  if (s != MOE_OK) return s;
   // publish the new generations of the filled slots
   const uint32_t* gen = moe::slots_gen(ctx->slots[layer]);
   uint32_t* hg = ctx->h_gen + static_cast<size_t>(layer) * S;
@@ -683,6 +765,62 @@ extern "C" moe_status_t moe_cache_preload(moe_ctx_t* ctx, int32_t layer, const i
   return MOE_OK;
 }
 
+// Checks and arguments of the prefill FFN over the unit table at d_units.
+static moe_status_t prefill_setup(moe_ctx_t* ctx, int32_t layer, const void* x, int32_t xt, int32_t T,
+                                  const moe_plan_t* plan, float* y, moe::PrefillArgs* out) {
+  const moe_config_t& c = ctx->cfg;
+  const int E = c.n_experts, S = c.slots_per_layer;
+  if (!ctx->prefill) return fail(ctx, MOE_ERR_ARG, "ffn: the prefill path needs max_tokens > 8");
+  if (c.quant != MOE_Q8_0) return fail(ctx, MOE_ERR_ARG, "ffn: the prefill path reads Q8_0 experts");
+  if (c.hidden % 128 || c.inter % 64 || c.shared_inter % 64 || E > 1023)
+    return fail(ctx, MOE_ERR_ARG, "ffn: the prefill path needs H % 128 == 0, I and I_s multiples of 64 and E <= 1023");
+  moe::PrefillArgs& p = *out;
+  p = moe::PrefillArgs{};
+  p.x = x;
+  p.xt = xt;
+  p.T = T;
+  p.k = c.top_k;
+  p.H = c.hidden;
+  p.I = c.inter;
+  p.Is = c.shared_inter;
+  p.S = S;
+  p.units = ctx->d_units;
+  p.plan = *plan;
+  p.pool = ctx->d_pool + static_cast<size_t>(layer) * S * ctx->slot_stride;
+  p.slot_stride = ctx->slot_stride;
+  p.shared = ctx->shared[layer];
+  p.g = ctx->geom;
+  p.gs = ctx->sgeom;
+  p.x16 = reinterpret_cast<__half*>(ctx->d_x16);
+  p.h = ctx->d_hp;
+  p.ldh = ctx->ldh_p;
+  p.yp = ctx->d_yp;
+  p.y = y;
+  p.items0 = ctx->d_items0;
+  p.items1 = ctx->d_items1;
+  p.n_items0 = ctx->d_nitems;
+  p.n_items1 = ctx->d_nitems + 1;
+  p.max_items0 = ctx->max_items0;
+  p.max_items1 = ctx->max_items1;
+  p.n_sm = ctx->num_sms;
+  p.err = ctx->d_err;
+  p.gen = ctx->d_gen + static_cast<size_t>(layer) * S;
+  return MOE_OK;
+}
+
+// Enqueues the parts p.parts of the prefill FFN (timed when enabled).
+static moe_status_t prefill_run(moe_ctx_t* ctx, moe::PrefillArgs& p, cudaStream_t st) {
+  const bool timed = ctx->timing && (p.parts & moe::kPartGemm);
+  for (int i = 0; i < 4; ++i) p.ev[i] = timed ? timing_event(ctx) : nullptr;
+  CK(moe::prefill_ffn(p, st));
+  if (timed) {
+    ctx->timed.push_back({MOE_KT_GATEUP, p.ev[0], p.ev[1]});
+    ctx->timed.push_back({MOE_KT_DOWN, p.ev[2], p.ev[3]});
+    if (ctx->timed.size() > 16384) CK(resolve_timing(ctx));
+  }
+  return MOE_OK;
+}
+
 // ------------------------------------------------------------ FFN
 extern "C" moe_status_t moe_expert_ffn(moe_ctx_t* ctx, int32_t layer, const void* x, int32_t xt,
                                        int32_t T, const moe_plan_t* plan, float* y, int32_t mode,
@@ -698,49 +836,11 @@ extern "C" moe_status_t moe_expert_ffn(moe_ctx_t* ctx, int32_t layer, const void
   if (mode == MOE_MODE_AUTO) mode = T <= 8 ? MOE_MODE_DECODE : MOE_MODE_PREFILL;
   const int E = ctx->cfg.n_experts, S = ctx->cfg.slots_per_layer;
   if (mode == MOE_MODE_PREFILL) {
-    const moe_config_t& c = ctx->cfg;
-    if (!ctx->prefill) return fail(ctx, MOE_ERR_ARG, "ffn: the prefill path needs max_tokens > 8");
-    if (c.quant != MOE_Q8_0) return fail(ctx, MOE_ERR_ARG, "ffn: the prefill path reads Q8_0 experts");
-    if (c.hidden % 128 || c.inter % 64 || c.shared_inter % 64 || E > 1023)
-      return fail(ctx, MOE_ERR_ARG, "ffn: the prefill path needs H % 128 == 0, I and I_s multiples of 64 and E <= 1023");
     moe::PrefillArgs p{};
-    p.x = x;
-    p.xt = xt;
-    p.T = T;
-    p.k = c.top_k;
-    p.H = c.hidden;
-    p.I = c.inter;
-    p.Is = c.shared_inter;
-    p.S = S;
-    p.units = ctx->d_units;
-    p.plan = *plan;
-    p.pool = ctx->d_pool + static_cast<size_t>(layer) * S * ctx->slot_stride;
-    p.slot_stride = ctx->slot_stride;
-    p.shared = ctx->shared[layer];
-    p.g = ctx->geom;
-    p.gs = ctx->sgeom;
-    p.x16 = reinterpret_cast<__half*>(ctx->d_x16);
-    p.h = ctx->d_hp;
-    p.ldh = ctx->ldh_p;
-    p.yp = ctx->d_yp;
-    p.y = y;
-    p.items0 = ctx->d_items0;
-    p.items1 = ctx->d_items1;
-    p.n_items0 = ctx->d_nitems;
-    p.n_items1 = ctx->d_nitems + 1;
-    p.max_items0 = ctx->max_items0;
-    p.max_items1 = ctx->max_items1;
-    p.n_sm = ctx->num_sms;
-    p.err = ctx->d_err;
-    p.gen = ctx->d_gen + static_cast<size_t>(layer) * S;
-    if (ctx->timing)
-      for (int i = 0; i < 4; ++i) p.ev[i] = timing_event(ctx);
-    CK(moe::prefill_ffn(p, reinterpret_cast<cudaStream_t>(stream)));
-    if (ctx->timing) {
-      ctx->timed.push_back({MOE_KT_GATEUP, p.ev[0], p.ev[1]});
-      ctx->timed.push_back({MOE_KT_DOWN, p.ev[2], p.ev[3]});
-    }
-    return MOE_OK;
+    moe_status_t s = prefill_setup(ctx, layer, x, xt, T, plan, y, &p);
+    if (s != MOE_OK) return s;
+    p.parts = moe::kPartAll;
+    return prefill_run(ctx, p, reinterpret_cast<cudaStream_t>(stream));
   }
   if (mode != MOE_MODE_DECODE || T > 8) return fail(ctx, MOE_ERR_ARG, "ffn: decode mode needs T <= 8");
   moe::FfnArgs a{};
@@ -869,11 +969,43 @@ extern "C" moe_status_t moe_layer_forward(moe_ctx_t* ctx, int32_t layer, const v
   }
   moe_miss_list_t local{};
   moe_miss_list_t* ml = misses ? misses : &local;
-  s = moe_cache_admit(ctx, layer, plan, ml, stream);
+  if (T <= 8) {
+    s = moe_cache_admit(ctx, layer, plan, ml, stream);
+    if (s != MOE_OK) return s;
+    s = moe_stage_tiles(ctx, layer, ml, stream);
+    if (s != MOE_OK) return s;
+    return moe_expert_ffn(ctx, layer, x, xt, T, plan, y, MOE_MODE_AUTO, stream);
+  }
+  // prefill: the step may run in compute waves
+  if (!ctx->store) return fail(ctx, MOE_ERR_STATE, "layer_forward: no store bound");
+  if (ctx->cfg.shared_inter > 0 && !ctx->shared[layer])
+    return fail(ctx, MOE_ERR_STATE, "layer_forward: shared expert of this layer not bound");
+  moe::PrefillArgs p{};
+  s = prefill_setup(ctx, layer, x, xt, T, plan, y, &p);
   if (s != MOE_OK) return s;
-  s = moe_stage_tiles(ctx, layer, ml, stream);
+  WavePlan wp;
+  s = admit_host(ctx, layer, plan, ml, st, &wp);
   if (s != MOE_OK) return s;
-  return moe_expert_ffn(ctx, layer, x, xt, T, plan, y, MOE_MODE_AUTO, stream);
+  const int S = ctx->cfg.slots_per_layer;
+  uint32_t* hg = ctx->h_gen + static_cast<size_t>(layer) * S;
+  p.parts = moe::kPartGather;
+  if ((s = prefill_run(ctx, p, st)) != MOE_OK) return s;
+  for (size_t w = 0; w < wp.off.size(); ++w) {
+    s = stage_fills(ctx, layer, ml, static_cast<int>(w), st);
+    if (s != MOE_OK) return s;
+    // the wave's slots hold their new payloads: publish their generations
+    // on the device (from the wave's unit table) and in the host mirror
+    p.parts = moe::kPartGemm;
+    p.units = ctx->d_units + wp.off[w];
+    p.publish_gen = ctx->d_gen + static_cast<size_t>(layer) * S;
+    p.publish_list = ctx->d_units + wp.pub[w];
+    if ((s = prefill_run(ctx, p, st)) != MOE_OK) return s;
+    for (int i = 0; i < ml->n; ++i)
+      if (ml->wave[i] == static_cast<int>(w)) hg[ml->slot[i]] = wp.fill_gen[i];
+  }
+  p.parts = moe::kPartCombine;
+  p.publish_gen = nullptr;
+  return prefill_run(ctx, p, st);
 }
 
 extern "C" moe_status_t moe_check_device_errors(moe_ctx_t* ctx, moe_stream_t stream) {

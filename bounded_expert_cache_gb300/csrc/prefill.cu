@@ -97,6 +97,15 @@ __global__ void __launch_bounds__(1024) items_kernel(const int32_t* units, int I
   }
 }
 
+// Publishes the new generations of one wave's fills once their copies are
+// complete (stream order): list = [n, (slot, generation) x n]. Hits are not
+// republished, so a slot whose earlier staging failed stays refused.
+__global__ void __launch_bounds__(256) publish_kernel(const int32_t* list, uint32_t* gen) {
+  const int n = __ldg(list);
+  for (int i = threadIdx.x; i < n; i += blockDim.x)
+    gen[__ldg(list + 1 + 2 * i)] = static_cast<uint32_t>(__ldg(list + 2 + 2 * i));
+}
+
 // y[t] = shared row + sum over j in selection order of w[t,j] * row inv[t,j]
 // (the weight of expert-major row p is perm_w[p]).
 __global__ void __launch_bounds__(256) combine_kernel(const float* yp, const int32_t* inv, const float* w, int T,
@@ -164,17 +173,13 @@ cudaError_t mapq(CUtensorMap* m, const void* base, int64_t kbytes, int64_t rows,
 
 }  // namespace
 
-cudaError_t prefill_ffn(const PrefillArgs& p, cudaStream_t st) {
-  cudaError_t e = encoder();
-  if (e != cudaSuccess) return e;
+// Work items, tensor maps and both GEMMs over the unit table p.units.
+static cudaError_t prefill_gemms(const PrefillArgs& p, cudaStream_t st) {
+  cudaError_t e = cudaSuccess;
   const int A = p.T * p.k, rows = A + p.T;
   const ExpertGeom& g = p.g;
   const ExpertGeom& gs = p.gs;
-  // 1. activations in expert-major order, fp16
-  if (p.xt == MOE_BF16)
-    gather_kernel<MOE_BF16><<<rows, 256, 0, st>>>(p.x, p.T, p.k, p.H, p.plan.perm_tok, p.x16);
-  else
-    gather_kernel<MOE_F32><<<rows, 256, 0, st>>>(p.x, p.T, p.k, p.H, p.plan.perm_tok, p.x16);
+  if (p.publish_gen) publish_kernel<<<1, 256, 0, st>>>(p.publish_list, p.publish_gen);
   // 2. work items
   items_kernel<<<1, 1024, 0, st>>>(p.units, p.I, p.Is, p.H, p.items0, p.n_items0, p.items1, p.n_items1);
   // 3. tensor maps (pointers are fixed per context and layer)
@@ -214,7 +219,6 @@ cudaError_t prefill_ffn(const PrefillArgs& p, cudaStream_t st) {
   a.h = p.h;
   a.ldh = p.ldh;
   a.yp = p.yp;
-  a.perm_w = p.plan.perm_w;
   a.err = p.err;
   a.gen = p.gen;
   a.S = p.S;
@@ -226,7 +230,7 @@ cudaError_t prefill_ffn(const PrefillArgs& p, cudaStream_t st) {
   if (p.ev[0]) cudaEventRecord(p.ev[0], st);
   if ((e = launch_gemm(0, m0, a, std::min(p.max_items0, p.n_sm), st)) != cudaSuccess) return e;
   if (p.ev[1]) cudaEventRecord(p.ev[1], st);
-  // 5. down, weighted by the combine weights
+  // 5. down (the combine applies the weights)
   a.items = p.items1;
   a.n_items = p.n_items1;
   a.stages = gemm_stages(1);
@@ -234,8 +238,26 @@ cudaError_t prefill_ffn(const PrefillArgs& p, cudaStream_t st) {
   if (p.ev[2]) cudaEventRecord(p.ev[2], st);
   if ((e = launch_gemm(1, m1, a, std::min(p.max_items1, p.n_sm), st)) != cudaSuccess) return e;
   if (p.ev[3]) cudaEventRecord(p.ev[3], st);
+  return cudaGetLastError();
+}
+
+cudaError_t prefill_ffn(const PrefillArgs& p, cudaStream_t st) {
+  cudaError_t e = encoder();
+  if (e != cudaSuccess) return e;
+  const int rows = p.T * p.k + p.T;
+  // 1. activations in expert-major order, fp16
+  if (p.parts & kPartGather) {
+    if (p.xt == MOE_BF16)
+      gather_kernel<MOE_BF16><<<rows, 256, 0, st>>>(p.x, p.T, p.k, p.H, p.plan.perm_tok, p.x16);
+    else
+      gather_kernel<MOE_F32><<<rows, 256, 0, st>>>(p.x, p.T, p.k, p.H, p.plan.perm_tok, p.x16);
+  }
+  if (p.parts & kPartGemm) {
+    if ((e = prefill_gemms(p, st)) != cudaSuccess) return e;
+  }
   // 6. combine into the tokens' positions
-  combine_kernel<<<p.T, 256, 0, st>>>(p.yp, p.plan.inv, p.plan.perm_w, p.T, p.k, p.H, p.shared ? 1 : 0, p.y);
+  if (p.parts & kPartCombine)
+    combine_kernel<<<p.T, 256, 0, st>>>(p.yp, p.plan.inv, p.plan.perm_w, p.T, p.k, p.H, p.shared ? 1 : 0, p.y);
   return cudaGetLastError();
 }
 

@@ -31,16 +31,22 @@ struct GemmArgs {
   int rows_routed;          // expert-major rows of routed assignments (T*k)
   uint16_t* h;              // bf16 [rows][ldh]
   int ldh;
-  float* yp;                // fp32 [rows][H], rows scaled by their combine weight
-  const float* perm_w;      // [T*k]
+  float* yp;                // fp32 [rows][H], unweighted expert outputs
   uint32_t* err;
   const uint32_t* gen;      // [S] published slot generations (fail-closed check)
   int S;
   int stages;
 };
 
-// One prefill FFN call: gather, both GEMMs, combine.
+// One prefill FFN call: gather, both GEMMs, combine. A step whose union is
+// larger than the slots runs as one gather, then the GEMMs once per compute
+// wave (each over that wave's unit table, after the wave's fills landed),
+// then one combine; `parts` selects the pieces of one call.
+enum { kPartGather = 1, kPartGemm = 2, kPartCombine = 4, kPartAll = 7 };
 struct PrefillArgs {
+  int parts;
+  uint32_t* publish_gen;    // non-null: first publish the fills of
+  const int32_t* publish_list;  // [n, (slot, generation) x n] to this array
   const void* x;
   int xt, T, k, H, I, Is, S;
   const int32_t* units;

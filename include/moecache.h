@@ -215,8 +215,10 @@ moe_status_t moe_plan_union(moe_ctx_t* ctx, const int32_t* topk_idx, const float
  * assigns slots, updates the host page table and enqueues its copy to the
  * device page table on stream. The miss list must be staged with
  * moe_stage_tiles before moe_expert_ffn reads the slots.
- * Errors: MOE_ERR_CAPACITY when the random policy has no unpinned victim;
- * the cache state is then unchanged. */
+ * Errors: MOE_ERR_CAPACITY when the random policy has no unpinned victim, or
+ * when the step's union is larger than the slots (such a step runs only
+ * inside moe_layer_forward, in compute waves); the cache state is then
+ * unchanged. */
 moe_status_t moe_cache_admit(moe_ctx_t* ctx, int32_t layer, const moe_plan_t* plan,
                              moe_miss_list_t* misses, moe_stream_t stream);
 
@@ -247,12 +249,23 @@ moe_status_t moe_stage_tiles(moe_ctx_t* ctx, int32_t layer, const moe_miss_list_
  * slot whose generation differs from the page table's is not read: the step
  * then fails closed (MOE_ERR_STALE from moe_check_device_errors) and y is
  * left unspecified. mode: MOE_MODE_DECODE (T <= 8, dequant-GEMV),
- * MOE_MODE_PREFILL (grouped GEMM; not built: MOE_ERR_ARG), AUTO picks. */
+ * MOE_MODE_PREFILL (Q8_0 only, contexts with max_tokens > 8: grouped
+ * dequant-GEMM on the tensor cores, H % 128 == 0, I and I_s multiples of
+ * 64), AUTO picks by T. */
 moe_status_t moe_expert_ffn(moe_ctx_t* ctx, int32_t layer, const void* x, int32_t xt, int32_t T,
                             const moe_plan_t* plan, float* y, int32_t mode, moe_stream_t stream);
 
 /* route -> plan -> admit -> stage -> ffn for one layer step (one host sync,
- * inside admit). misses may be NULL. */
+ * inside admit). misses may be NULL.
+ * Host admission, T > 8, LRU: a step whose union is larger than the slots
+ * runs in compute waves ([RT] §3.2 read as textbook LRU over the access
+ * sequence): a fill that evicts an expert of the same step belongs to the
+ * wave after that expert's. The activations are gathered once; per wave the
+ * wave's fills are staged (after the previous wave's GEMMs) and the grouped
+ * GEMMs run over the wave's experts; one combine follows. The output is the
+ * same, bit for bit, as with every expert resident. Decode (T <= 8) returns
+ * MOE_ERR_CAPACITY for such a step; on-device admission admits nothing and
+ * moe_check_device_errors reports MOE_ERR_CAPACITY. */
 moe_status_t moe_layer_forward(moe_ctx_t* ctx, int32_t layer, const void* x, int32_t xt,
                                int32_t T, const float* w_router, const float* bias,
                                int32_t* topk_idx, float* topk_w, const moe_plan_t* plan,
@@ -297,8 +310,9 @@ typedef enum {
 moe_status_t moe_set_kernel_timing(moe_ctx_t* ctx, int32_t enable);
 moe_status_t moe_get_kernel_times(moe_ctx_t* ctx, double* ms, int64_t* launches);
 
-/* Test hooks for fail-closed paths, all on the host side: make the next
- * moe_stage_tiles fail after `fail_after_tiles` tiles (-1 = off), or change
+/* Test hooks for fail-closed paths, all on the host side: make host staging
+ * (moe_stage_tiles, or a wave of moe_layer_forward) fail once
+ * `fail_after_tiles` more tiles have been issued (-1 = off), or change
  * the published generation of the slot holding a resident expert so that it
  * no longer matches the page-table entry. */
 moe_status_t moe_debug_fail_staging_after(moe_ctx_t* ctx, int32_t fail_after_tiles);

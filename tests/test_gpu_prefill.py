@@ -13,6 +13,8 @@ import torch
 import oracle
 import workloads as W
 
+from oracle.cache import SlotCache
+
 from gpu_common import (ExpertCache, bind_all, make_context, pinned_store, tolerance_ok, x_to_f64,
                         x_to_torch)
 
@@ -139,3 +141,103 @@ def test_prefill_transparency_bitwise(bec):
     c, ic, _ = _prefill(bec, w, 256, [5], device_admit=1, preload=False)
     assert np.array_equal(ia, ib) and np.array_equal(ia, ic)
     assert np.array_equal(a, b) and np.array_equal(a, c)
+
+
+def _check_waves(ml, union):
+    """The wave schedule is valid: a fill that evicts an expert of the same
+    step runs in a later wave than that expert, and n_waves covers them."""
+    wave_of = {e: 0 for e in union}
+    for e, v, wv in zip(ml.expert, ml.victim, ml.wave):
+        if v in wave_of:
+            assert wv > wave_of[v], (e, v, wv, wave_of[v])
+        wave_of[e] = wv
+    assert ml.n_waves == max(ml.wave) + 1
+
+
+def test_prefill_waves_union_larger_than_slots(bec):
+    # the long-prefill shapes with a cold 44-slot LRU cache: each chunk's
+    # union is larger than the slots, so the step runs in compute waves.
+    # Fills, page table, generations and counters match the oracle's replay;
+    # the output matches an all-resident context bit for bit and the oracle
+    # on sampled tokens.
+    w = W.WORKLOADS["wide_prefill"]
+    T, steps, E = 512, 2, w.n_experts
+    store = pinned_store(w, 1)
+    ctx = make_context(bec, w, 1, slots=w.slots, max_tokens=T, device_admit=0)
+    res = make_context(bec, w, 1, slots=E, max_tokens=T, device_admit=0)
+    keep = bind_all(ctx, w, 1, store) + bind_all(res, w, 1, store)
+    res.preload(0, list(range(E)))
+    cache = SlotCache(E, w.slots, w.policy, seed=0, layer=0, payload_bytes=w.payload_bytes)
+    experts = ExpertCache(w)
+    shared = experts.get(0, E) if w.shared_inter else None
+    Wr = W.router_weights(w, 0)
+    bias = W.router_bias(w, 0)
+    Wr_t = torch.from_numpy(Wr).cuda()
+    b_t = None if bias is None else torch.from_numpy(bias).cuda()
+    x = W.activations(w, 0, steps * T)
+    plan = bec.Plan(E, w.top_k, T)
+    idx = torch.empty((T, w.top_k), dtype=torch.int32, device="cuda")
+    wt = torch.empty((T, w.top_k), dtype=torch.float32, device="cuda")
+    y = torch.empty((T, w.hidden), dtype=torch.float32, device="cuda")
+    y_res = torch.empty_like(y)
+    for s in range(steps):
+        xs = x[s * T:(s + 1) * T]
+        xt = x_to_torch(w, xs)
+        ml = ctx.layer_forward(0, xt, Wr_t, b_t, idx, wt, plan, y)
+        ctx.check_device_errors()
+        ig = idx.cpu().numpy()
+        res.layer_forward(0, xt, Wr_t, b_t, idx, wt, plan, y_res)
+        res.check_device_errors()
+        x64 = x_to_f64(w, xs)
+        ridx, rw, _ = oracle.route(x64, Wr, bias, w.top_k)
+        assert np.array_equal(ig, ridx), s
+        rplan = oracle.plan_union(ridx, rw, E)
+        rec = cache.step(rplan["uniq"], rplan["counts"])
+        assert len(rplan["uniq"]) > w.slots and ml.n_waves > 1
+        assert list(zip(ml.expert, ml.slot, ml.victim)) == [tuple(f) for f in rec["fills"]], s
+        _check_waves(ml, set(int(e) for e in rplan["uniq"]))
+        pt, gen = ctx.read_page_table(0)
+        assert pt == rec["pt"] and gen == rec["gen"], s
+        assert torch.equal(y, y_res), s
+        yg = y.cpu().numpy().astype(np.float64)
+        sample = [0, 200, T - 1] if s == 0 else [77]
+        refs = [oracle.moe_layer(x64[t:t + 1], ridx[t:t + 1], rw[t:t + 1], lambda e: experts.get(0, e),
+                                 shared)[0] for t in sample]
+        ok, rel, mx = tolerance_ok(yg[sample], np.stack(refs))
+        assert ok, (s, rel, mx)
+    st, rs = ctx.stats(0), cache.stats()
+    for key in ("hits", "misses", "evictions", "materialized_bytes"):
+        assert st[key] == rs[key], (key, st[key], rs[key])
+    ctx.close()
+    res.close()
+    del keep
+
+
+def test_prefill_waves_failed_staging_fails_closed(bec):
+    # a copy failure inside a later wave: the call fails, the waves before it
+    # published their slots, and the experts whose payloads never landed are
+    # refused (stale generation) when the next step reads them
+    w = W.WORKLOADS["wide_prefill"]
+    T, E = 256, w.n_experts
+    store = pinned_store(w, 1)
+    ctx = make_context(bec, w, 1, slots=w.slots, max_tokens=T, device_admit=0)
+    keep = bind_all(ctx, w, 1, store)
+    Wr_t = torch.from_numpy(W.router_weights(w, 0)).cuda()
+    bias = W.router_bias(w, 0)
+    b_t = None if bias is None else torch.from_numpy(bias).cuda()
+    xt = x_to_torch(w, W.activations(w, 0, T))
+    plan = bec.Plan(E, w.top_k, T)
+    idx = torch.empty((T, w.top_k), dtype=torch.int32, device="cuda")
+    wt = torch.empty((T, w.top_k), dtype=torch.float32, device="cuda")
+    y = torch.empty((T, w.hidden), dtype=torch.float32, device="cuda")
+    tiles = len(oracle.tile_partition(w.hidden, w.inter, w.quant))
+    ctx.debug_fail_staging_after(w.slots * tiles + 3)  # inside wave 1 of a cold step
+    with pytest.raises(bec.MoeError):
+        ctx.layer_forward(0, xt, Wr_t, b_t, idx, wt, plan, y)
+    ctx.check_device_errors()  # nothing was read from an unpublished slot
+    ctx.layer_forward(0, xt, Wr_t, b_t, idx, wt, plan, y)
+    with pytest.raises(bec.MoeError) as ei:
+        ctx.check_device_errors()
+    assert ei.value.status == 4  # MOE_ERR_STALE
+    ctx.close()
+    del keep
