@@ -378,6 +378,81 @@ def run_prefill(args, dev):
     }
 
 
+def run_long_prefill(args, dev):
+    """The long-prefill workload: hidden 2816, 128 experts top-8 + 1 shared,
+    inter 704 (shared 2112), Q8_0; 32,768 tokens in 8 chunks of 4,096 through
+    a cold 44-slot LRU cache with host admission. Every chunk's union is
+    larger than the slots, so each chunk runs in compute waves with staging
+    on 3 copy streams between them. A pass starts from a cold cache (a new
+    context, created outside the timed region)."""
+    import torch
+    import bounded_expert_cache_gb300 as bec
+    w = W.WORKLOADS["wide_prefill"]
+    T, n_chunks = w.tokens_per_step, w.n_steps
+    E, k, H, I, Is, S = w.n_experts, w.top_k, w.hidden, w.inter, w.shared_inter, w.slots
+    store = torch.empty((1, E, w.payload_bytes), dtype=torch.uint8, pin_memory=True)
+    W.fill_store(w, store.numpy())
+    shared = torch.from_numpy(W.expert_payload(w, 0, E)).to(dev)
+    Wr = torch.from_numpy(W.router_weights(w, 0)).to(dev)
+    bias = W.router_bias(w, 0)
+    b_t = None if bias is None else torch.from_numpy(bias).to(dev)
+    x = torch.from_numpy(W.activations(w, 0, T * n_chunks).view(np.int16)).view(torch.bfloat16).to(dev)
+    plan = bec.Plan(E, k, T, dev)
+    idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+    wt = torch.empty((T, k), dtype=torch.float32, device=dev)
+    y = torch.empty((T, H), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def one_pass(timing=False):
+        ctx = bec.Context(1, E, k, H, I, Is, w.quant, S, w.policy, 3, 0, 262144, T, admit_on_device=0)
+        ctx.bind_store(store)
+        ctx.bind_shared(0, shared)
+        ctx.set_kernel_timing(timing)
+        waves = []
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for c in range(n_chunks):
+            ml = ctx.layer_forward(0, x[c * T:(c + 1) * T], Wr, b_t, idx, wt, plan, y)
+            waves.append(ml.n_waves)
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        ctx.check_device_errors()
+        kt = ctx.kernel_times() if timing else None
+        st = ctx.stats(0)
+        ctx.close()
+        return a.elapsed_time(b), waves, st, kt
+
+    one_pass()  # warm-up (module load, first-touch of the scratch)
+    passes = max(3, min(args.steps, 5))
+    times = []
+    for _ in range(passes):
+        ms, waves, st, _ = one_pass()
+        times.append(ms)
+    ms = statistics.median(times)
+    _, _, _, kt = one_pass(timing=True)
+    flops_gu = 2.0 * (T * k) * 2 * H * I + 2.0 * T * 2 * H * Is
+    flops_dn = 2.0 * (T * k) * H * I + 2.0 * T * H * Is
+    gemm_ms = kt["ffn_gateup"][0] + kt["ffn_down"][0]
+    tf = n_chunks * (flops_gu + flops_dn) / (gemm_ms / 1e3) / 1e12
+    staged = st["bytes_staged"]
+    h2d = h2d_bandwidth(torch, dev)
+    return {
+        "workload": f"long prefill: hidden {H}, {E} experts top-{k} + 1 shared, inter {I} (shared {Is}), "
+                    f"Q8_0, {n_chunks} chunks of {T} bf16 tokens, {S}-slot LRU cache from cold, host "
+                    f"admission, compute waves, staging on 3 copy streams",
+        "tokens_per_s": round(T * n_chunks / (ms / 1e3), 1), "ms_per_pass": round(ms, 3),
+        "passes": passes, "waves_per_chunk": waves,
+        "misses": st["misses"], "bytes_staged_per_pass": staged,
+        "staging_gb_per_s_over_pass": round(staged / (ms / 1e3) / 1e9, 1),
+        "h2d_copy_gb_per_s": h2d,
+        "staging_floor_ms": round(staged / (h2d * 1e9) * 1e3, 3),
+        "gemm_ms_per_pass": round(gemm_ms, 3),
+        "gemm_tflops": round(tf, 1),
+        "kernels": {kname: {"ms": round(kms, 3), "launches": n} for kname, (kms, n) in kt.items()},
+    }
+
+
 def h2d_bandwidth(torch, dev):
     """Copy-engine bandwidth of a 1 GiB pinned host -> device copy (best of 3)."""
     src = torch.empty(1 << 30, dtype=torch.uint8).pin_memory()
@@ -475,6 +550,8 @@ def main():
     ap.add_argument("--no-graph", action="store_true", help="launch the headline pass call by call")
     ap.add_argument("--skip-prefill", action="store_true", help="skip the prefill workload pass")
     ap.add_argument("--prefill-only", action="store_true", help="profiling: only the prefill pass")
+    ap.add_argument("--skip-long-prefill", action="store_true", help="skip the long-prefill (waves) pass")
+    ap.add_argument("--long-prefill-only", action="store_true", help="profiling: only the long-prefill pass")
     ap.add_argument("--prefill-tokens", type=int, default=0, help="profiling: tokens of the prefill chunk")
     ap.add_argument("--admission", type=int, default=HEADLINE_MODE, choices=[1, 2],
                     help="profiling: miss path of the headline pass (2 read-through, 1 staging kernel)")
@@ -522,9 +599,14 @@ def main():
     if args.prefill_only:
         print(json.dumps({"prefill": run_prefill(args, dev)}))
         return
+    if args.long_prefill_only:
+        print(json.dumps({"long_prefill": run_long_prefill(args, dev)}))
+        return
     out, w = run_ours(args, rank, world, dev)
     if not args.skip_prefill:
         out["prefill"] = run_prefill(args, dev)
+    if not args.skip_long_prefill:
+        out["long_prefill"] = run_long_prefill(args, dev)
     if rank == 0 and world == 1 and not args.skip_cpu:
         sec, layers = oracle_decode_sample(w, args.cpu_budget, w.n_layers)
         out["cpu_baseline"] = {

@@ -618,9 +618,13 @@ extern "C" moe_status_t moe_cache_admit(moe_ctx_t* ctx, int32_t layer, const moe
 }
 
 // Host->device copies of the fills of compute wave `wave` (all fills if
-// wave < 0), in tiles over the copy streams, after the compute enqueued so
-// far on `cst`; `cst` then waits for them. The slots' new generations are
-// published by the caller.
+// wave < 0), after the compute enqueued so far on `cst`; `cst` then waits
+// for them. The payload is cut into tiles of at most tile_bytes per matrix
+// (the accounting unit, and the point where the failure hook cuts); the
+// consecutive tiles of one fill go out as one copy, and fills rotate over
+// the copy streams: a copy costs microseconds of submission, which 256 KiB
+// copies would turn into the bound on the host link. The slots' new
+// generations are published by the caller.
 static moe_status_t stage_fills(moe_ctx_t* ctx, int32_t layer, const moe_miss_list_t* misses, int wave,
                                 cudaStream_t cst) {
   const int E = ctx->cfg.n_experts, S = ctx->cfg.slots_per_layer;
@@ -633,7 +637,7 @@ static moe_status_t stage_fills(moe_ctx_t* ctx, int32_t layer, const moe_miss_li
   for (int i = 0; i < ns; ++i) CK(cudaStreamWaitEvent(ctx->streams[i], ctx->ev_compute, 0));
   const moe::ExpertGeom& g = ctx->geom;
   const int64_t tile = ctx->cfg.tile_bytes;
-  int64_t issued = 0, bytes = 0;
+  int64_t issued = 0, bytes = 0, copies = 0;
   bool injected = false;
   for (int i = 0; i < misses->n && !injected; ++i) {
     if (wave >= 0 && misses->wave[i] != wave) continue;
@@ -641,6 +645,8 @@ static moe_status_t stage_fills(moe_ctx_t* ctx, int32_t layer, const moe_miss_li
     if (e < 0 || e >= E || slot < 0 || slot >= S) return fail(ctx, MOE_ERR_ARG, "stage: fill out of range");
     const uint8_t* src = ctx->store + (static_cast<size_t>(layer) * E + e) * g.bytes;
     uint8_t* dst = ctx->d_pool + (static_cast<size_t>(layer) * S + slot) * ctx->slot_stride;
+    cudaStream_t cs = ctx->streams[copies % ns];
+    int64_t run0 = 0, run_len = 0;  // pending run of consecutive tiles
     for (int m = 0; m < 3 && !injected; ++m) {
       const int64_t mo = g.qoff[m], mb = g.qbytes[m] + g.sbytes[m];
       for (int64_t o = 0; o < mb; o += tile) {
@@ -649,12 +655,19 @@ static moe_status_t stage_fills(moe_ctx_t* ctx, int32_t layer, const moe_miss_li
           break;
         }
         const int64_t len = std::min(tile, mb - o);
-        CK(cudaMemcpyAsync(dst + mo + o, src + mo + o, static_cast<size_t>(len), cudaMemcpyHostToDevice,
-                           ctx->streams[issued % ns]));
+        if (run_len > 0 && run0 + run_len != mo + o) {
+          CK(cudaMemcpyAsync(dst + run0, src + run0, static_cast<size_t>(run_len), cudaMemcpyHostToDevice, cs));
+          run_len = 0;
+        }
+        if (run_len == 0) run0 = mo + o;
+        run_len += len;
         ++issued;
         bytes += len;
       }
     }
+    if (run_len > 0)
+      CK(cudaMemcpyAsync(dst + run0, src + run0, static_cast<size_t>(run_len), cudaMemcpyHostToDevice, cs));
+    ++copies;
   }
   for (int i = 0; i < ns; ++i) {
     CK(cudaEventRecord(ctx->ev_stage[i], ctx->streams[i]));

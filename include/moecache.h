@@ -232,9 +232,11 @@ moe_status_t moe_cache_evict(moe_ctx_t* ctx, int32_t layer, int32_t expert);
 moe_status_t moe_cache_preload(moe_ctx_t* ctx, int32_t layer, const int32_t* experts, int32_t n);
 
 /* Miss staging ([NfE] §5.4): copy every fill of *misses from the bound
- * pinned store into its slot as tiles of at most tile_bytes (each matrix is
- * cut separately, the last tile partial), rotating over the context's
- * n_streams streams, then publish each slot's new generation. compute_stream
+ * pinned store into its slot. The payload is cut into tiles of at most
+ * tile_bytes (each matrix separately, the last tile partial): the unit of
+ * the tile counters and of the failure hook. The consecutive tiles of one
+ * fill are issued as one copy, and fills rotate over the context's
+ * n_streams streams. Then each slot's new generation is published. compute_stream
  * waits (cudaStreamWaitEvent) for all of it, so moe_expert_ffn enqueued on
  * compute_stream afterwards reads complete slots. Overwriting a slot waits
  * for the compute previously enqueued on compute_stream. */
