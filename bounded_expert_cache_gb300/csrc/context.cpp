@@ -841,6 +841,8 @@ extern "C" moe_status_t moe_expert_ffn(moe_ctx_t* ctx, int32_t layer, const void
   if (!ctx) return MOE_ERR_ARG;
   if (!valid_layer(ctx, layer)) return fail(ctx, MOE_ERR_ARG, "ffn: bad layer");
   if (!plan_ok(plan) || !x || !y) return fail(ctx, MOE_ERR_ARG, "ffn: null pointer");
+  if (reinterpret_cast<uintptr_t>(x) % 16 || reinterpret_cast<uintptr_t>(y) % 16)
+    return fail(ctx, MOE_ERR_ARG, "ffn: x and y must be 16-byte aligned");
   if (T < 1 || T > ctx->cfg.max_tokens) return fail(ctx, MOE_ERR_ARG, "ffn: T outside 1..max_tokens");
   if (xt != MOE_F32 && xt != MOE_BF16) return fail(ctx, MOE_ERR_ARG, "ffn: bad activation dtype");
   if (plan->capacity < T * ctx->cfg.top_k) return fail(ctx, MOE_ERR_ARG, "ffn: plan capacity < T*k");

@@ -27,6 +27,7 @@
 #include <cuda_fp16.h>
 
 #include "internal.h"
+#include "pdl.cuh"
 
 namespace moe {
 namespace {
@@ -196,10 +197,13 @@ __global__ void __launch_bounds__(kThreads) gateup_kernel(FfnArgs a) {
   extern __shared__ float xs[];  // [T][H] swizzled
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int H = a.H, T = a.T;
+  // x is the layer's input, complete once the router has passed its wait
   for (int i = tid; i < T * H; i += kThreads) {
     const int t = i / H, k = i - t * H;
     xs[t * H + swz(k)] = load_act<XT>(a.x, i);
   }
+  pdl_wait();
+  pdl_trigger();
   __syncthreads();
   const int n_units = __ldg(a.units);
   const int nu = n_units - (a.shared ? 1 : 0);  // routed units
@@ -329,6 +333,8 @@ __global__ void __launch_bounds__(kThreads) down_kernel(FfnArgs a) {
   const int ldh = a.ldh;
   float* hs = sm;                                   // [nrows][ldh] swizzled
   float* part = sm + static_cast<size_t>(nrows) * ldh;  // [items][2][TM]
+  pdl_wait();
+  pdl_trigger();
   for (int i = tid; i < nrows * ldh; i += kThreads) {
     const int p = i / ldh, k = i - p * ldh;
     hs[p * ldh + swz(k)] = __ldcg(a.h + i);
@@ -529,18 +535,16 @@ cudaError_t launch_tm(const FfnArgs& a, int num_sms, cudaStream_t st) {
   const int items1 = max_units * (std::max(a.I, a.Is) / kRowsPerItem);
   const int grid1 = std::max(1, std::min((items1 + kWarps - 1) / kWarps, num_sms * 2));
   if (a.ev[0]) cudaEventRecord(a.ev[0], st);
-  if (a.xt == MOE_BF16)
-    gateup_kernel<Q, TM, MOE_BF16><<<grid1, kThreads, smem1, st>>>(a);
-  else
-    gateup_kernel<Q, TM, MOE_F32><<<grid1, kThreads, smem1, st>>>(a);
-  err = cudaGetLastError();
+  err = a.xt == MOE_BF16 ? pdl_launch(gateup_kernel<Q, TM, MOE_BF16>, dim3(grid1), dim3(kThreads), smem1, st, a)
+                         : pdl_launch(gateup_kernel<Q, TM, MOE_F32>, dim3(grid1), dim3(kThreads), smem1, st, a);
+  if (err == cudaSuccess) err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   if (a.ev[1]) cudaEventRecord(a.ev[1], st);
   const int grid2 = (a.H + kDownRows - 1) / kDownRows;
   if (a.ev[2]) cudaEventRecord(a.ev[2], st);
-  down_kernel<Q, TM><<<grid2, kThreads, smem2, st>>>(a);
+  err = pdl_launch(down_kernel<Q, TM>, dim3(grid2), dim3(kThreads), smem2, st, a);
   if (a.ev[3]) cudaEventRecord(a.ev[3], st);
-  return cudaGetLastError();
+  return err != cudaSuccess ? err : cudaGetLastError();
 }
 
 template <int Q>

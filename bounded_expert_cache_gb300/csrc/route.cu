@@ -28,6 +28,7 @@
 #include <string>
 
 #include "internal.h"
+#include "pdl.cuh"
 
 namespace moe {
 namespace {
@@ -1081,6 +1082,12 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a) {
   const int H = a.H, E = a.E, T = a.T;
   const float* wrow = a.w + static_cast<size_t>(e) * H;
   const int nterm = 4 * ((H / 4 + kRouteThreads - 1) / kRouteThreads);  // terms per thread
+  // the router weights are constant: start this block's row before waiting
+  // for the kernels that produce x and reuse the scratch
+  for (int v = tid; v < (H >> 2); v += kRouteThreads)
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(reinterpret_cast<const float4*>(wrow) + v));
+  pdl_wait();
+  pdl_trigger();
 
   for (int t0 = 0; t0 < T; t0 += kRouteTB) {
     float s[kRouteTB], c[kRouteTB], ab[kRouteTB];
@@ -1257,11 +1264,10 @@ cudaError_t launch_route(const RouteArgs& a, int num_sms, cudaStream_t st) {
                                static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
-  if (a.xt == MOE_BF16)
-    route_kernel<MOE_BF16><<<a.E, kRouteThreads, smem, st>>>(a);
-  else
-    route_kernel<MOE_F32><<<a.E, kRouteThreads, smem, st>>>(a);
-  return cudaGetLastError();
+  const cudaError_t e = a.xt == MOE_BF16
+      ? pdl_launch(route_kernel<MOE_BF16>, dim3(a.E), dim3(kRouteThreads), smem, st, a)
+      : pdl_launch(route_kernel<MOE_F32>, dim3(a.E), dim3(kRouteThreads), smem, st, a);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_plan(const PlanArgs& a, cudaStream_t st) {

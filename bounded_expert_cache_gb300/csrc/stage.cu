@@ -17,6 +17,7 @@
 #include <algorithm>
 
 #include "internal.h"
+#include "pdl.cuh"
 
 namespace moe {
 namespace {
@@ -31,6 +32,8 @@ __device__ __forceinline__ uint4 ld_host_stream(const uint4* p) { return __ldcs(
 // n_fills * chunks_per_expert items (item = fill * chunks_per_expert +
 // chunk), so the launch does not depend on how many misses the step has.
 __global__ void __launch_bounds__(kCopyThreads) stage_copy_kernel(StageArgs a) {
+  pdl_wait();
+  pdl_trigger();
   const int n = __ldcg(a.fills);
   const int cpe = a.chunks_per_expert;
   const int items = n * cpe;
@@ -83,8 +86,8 @@ cudaError_t launch_stage_copy(const StageArgs& a, cudaStream_t st) {
   if (a.max_fills <= 0) return cudaSuccess;
   static_assert(kStageChunkBytes == 16 * kCopyThreads * kCopyUnroll, "one chunk per CTA");
   const int grid = std::max(1, std::min(a.grid, a.chunks_per_expert * a.max_fills));
-  stage_copy_kernel<<<grid, kCopyThreads, 0, st>>>(a);
-  return cudaGetLastError();
+  const cudaError_t e = pdl_launch(stage_copy_kernel, dim3(grid), dim3(kCopyThreads), 0, st, a);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace moe

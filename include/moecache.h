@@ -246,7 +246,8 @@ moe_status_t moe_stage_tiles(moe_ctx_t* ctx, int32_t layer, const moe_miss_list_
 /* Fused dequantise + SwiGLU expert FFN + shared expert + weighted combine
  * ([RT] §3.1, [NfE] §1, §5.5, §12). x: device [T,H]; plan from
  * moe_plan_union on this step; y: device fp32 [T,H], overwritten with
- * sum_j w[t,j] * FFN_{idx[t,j]}(x[t]) + FFN_shared(x[t]). Experts are read
+ * sum_j w[t,j] * FFN_{idx[t,j]}(x[t]) + FFN_shared(x[t]); x and y 16-byte
+ * aligned (else MOE_ERR_ARG). Experts are read
  * from their slots through the device page table; an absent expert or a
  * slot whose generation differs from the page table's is not read: the step
  * then fails closed (MOE_ERR_STALE from moe_check_device_errors) and y is
