@@ -85,16 +85,16 @@ __device__ __forceinline__ float ld_scale(const uint8_t* p) {
 __device__ __forceinline__ uint4 ld_host(const void* p) {
   return __ldcs(reinterpret_cast<const uint4*>(p));
 }
-__device__ __forceinline__ float ld_scale_host(const uint8_t* p) {
-  const unsigned short b = __ldcs(reinterpret_cast<const unsigned short*>(p));
-  return __half2float(__ushort_as_half(b));
+__device__ __forceinline__ unsigned short ld_scale_host_bits(const uint8_t* p) {
+  return __ldcs(reinterpret_cast<const unsigned short*>(p));
 }
 
-// Copy one row of fp16 scales (n of them) from a miss's source to its slot.
-__device__ __forceinline__ void copy_scale_row(const uint8_t* src, uint8_t* dst, int n, int lane) {
-  const unsigned short* s = reinterpret_cast<const unsigned short*>(src);
-  unsigned short* d = reinterpret_cast<unsigned short*>(dst);
-  for (int i = lane; i < n; i += 32) d[i] = __ldcs(s + i);
+// A miss's scales reach its slot from the loads the dot products make: the
+// lane whose chunk opens a 32-weight block (every Q4_0 chunk, even Q8_0
+// chunks) stores that block's fp16 scale, so no copy waits on its own load.
+template <int Q>
+__device__ __forceinline__ bool owns_scale(int c) {
+  return Q != MOE_Q8_0 || (c & 1) == 0;
 }
 
 // q (Q8_0 byte) -> float, exact: bits 0x4B0000uu = 2^23 + uu with uu = q + 128.
@@ -234,14 +234,6 @@ __global__ void __launch_bounds__(kThreads) gateup_kernel(FfnArgs a) {
         s[m * kRowsPerItem + r] = U.base + U.soff[m] + static_cast<int64_t>(r0 + r) * sc_row;
       }
     }
-    if (U.miss) {
-#pragma unroll
-      for (int r = 0; r < kRowsPerItem; ++r)
-#pragma unroll
-        for (int m = 0; m < 2; ++m)
-          copy_scale_row(s[m * kRowsPerItem + r], U.dst + U.soff[m] + static_cast<int64_t>(r0 + r) * sc_row,
-                         H / 32, lane);
-    }
     for (int m0 = 0; m0 < U.M; m0 += TM) {
       const int mcount = min(TM, U.M - m0);
       int tok[TM];
@@ -258,15 +250,21 @@ __global__ void __launch_bounds__(kThreads) gateup_kernel(FfnArgs a) {
         uint4 w[2 * kRowsPerItem];
         float d[2 * kRowsPerItem];
         if (U.miss) {
+          unsigned short sb[2 * kRowsPerItem];
 #pragma unroll
           for (int r = 0; r < 2 * kRowsPerItem; ++r) {
             w[r] = ld_host(q[r] + c * 16);
-            d[r] = ld_scale_host(s[r] + (Q == MOE_Q8_0 ? (c >> 1) : c) * 2);
+            sb[r] = ld_scale_host_bits(s[r] + (Q == MOE_Q8_0 ? (c >> 1) : c) * 2);
           }
+#pragma unroll
+          for (int r = 0; r < 2 * kRowsPerItem; ++r) d[r] = __half2float(__ushort_as_half(sb[r]));
           if (m0 == 0) {
 #pragma unroll
-            for (int r = 0; r < 2 * kRowsPerItem; ++r)
+            for (int r = 0; r < 2 * kRowsPerItem; ++r) {
               *reinterpret_cast<uint4*>(U.dst + (q[r] - U.base) + c * 16) = w[r];
+              if (owns_scale<Q>(c))
+                *reinterpret_cast<unsigned short*>(U.dst + (s[r] - U.base) + (Q == MOE_Q8_0 ? (c >> 1) : c) * 2) = sb[r];
+            }
           }
         } else {
 #pragma unroll
@@ -367,8 +365,6 @@ __global__ void __launch_bounds__(kThreads) down_kernel(FfnArgs a) {
         rv[r] = o < a.H;
         q[r] = U.base + U.qoff[2] + static_cast<int64_t>(rv[r] ? o : 0) * rowbytes;
         s[r] = U.base + U.soff[2] + static_cast<int64_t>(rv[r] ? o : 0) * sc_row;
-        if (U.miss && rv[r])
-          copy_scale_row(s[r], U.dst + (s[r] - U.base), K / 32, lane);
       }
       for (int m0 = 0; m0 < U.M; m0 += TM) {
         const int mcount = min(TM, U.M - m0);
@@ -402,11 +398,20 @@ __global__ void __launch_bounds__(kThreads) down_kernel(FfnArgs a) {
           uint4 w[kRowsPerItem];
           float d[kRowsPerItem];
           if (U.miss) {
+            unsigned short sb[kRowsPerItem];
 #pragma unroll
             for (int r = 0; r < kRowsPerItem; ++r) {
               w[r] = rv[r] ? ld_host(q[r] + c * 16) : make_uint4(0, 0, 0, 0);
-              d[r] = rv[r] ? ld_scale_host(s[r] + (Q == MOE_Q8_0 ? (c >> 1) : c) * 2) : 0.f;
-              if (rv[r] && m0 == 0) *reinterpret_cast<uint4*>(U.dst + (q[r] - U.base) + c * 16) = w[r];
+              sb[r] = rv[r] ? ld_scale_host_bits(s[r] + (Q == MOE_Q8_0 ? (c >> 1) : c) * 2) : 0;
+            }
+#pragma unroll
+            for (int r = 0; r < kRowsPerItem; ++r) {
+              d[r] = __half2float(__ushort_as_half(sb[r]));
+              if (rv[r] && m0 == 0) {
+                *reinterpret_cast<uint4*>(U.dst + (q[r] - U.base) + c * 16) = w[r];
+                if (owns_scale<Q>(c))
+                  *reinterpret_cast<unsigned short*>(U.dst + (s[r] - U.base) + (Q == MOE_Q8_0 ? (c >> 1) : c) * 2) = sb[r];
+              }
             }
           } else {
 #pragma unroll

@@ -226,6 +226,36 @@ def test_staged_slot_bytes_equal_store(bec):
         ctx.close()
 
 
+@pytest.mark.parametrize("device_admit", MODES)
+def test_resident_slots_hold_store_payloads(bec, device_admit):
+    # after decode steps with misses, every expert the page table marks
+    # resident holds exactly its store payload, however it was materialised
+    # (host copies, the staging kernel, or read-through by the FFN kernels)
+    w = W.with_changes(W.WORKLOADS["decode"], n_layers=1)
+    store = pinned_store(w, 1)
+    ctx = make_context(bec, w, 1, device_admit=device_admit)
+    keep = bind_all(ctx, w, 1, store)
+    T = w.tokens_per_step
+    plan = bec.Plan(w.n_experts, w.top_k, T)
+    idx = torch.empty((T, w.top_k), dtype=torch.int32, device="cuda")
+    wt = torch.empty((T, w.top_k), dtype=torch.float32, device="cuda")
+    y = torch.empty((T, w.hidden), dtype=torch.float32, device="cuda")
+    Wr = torch.from_numpy(W.router_weights(w, 0)).cuda()
+    x = W.activations(w, 0, 24 * T)
+    for s in range(24):
+        ctx.layer_forward(0, x_to_torch(w, x[s * T:(s + 1) * T]), Wr, None, idx, wt, plan, y)
+    ctx.check_device_errors()
+    assert ctx.stats(0)["misses"] > w.slots  # slots were refilled
+    pt, _ = ctx.read_page_table(0)
+    resident = [(e, s) for e, s in enumerate(pt) if s >= 0]
+    assert len(resident) == w.slots
+    for e, s in resident:
+        got = np.frombuffer(ctx.read_slot(0, s), dtype=np.uint8)
+        assert np.array_equal(got, store[0, e].numpy()), (device_admit, e, s)
+    ctx.close()
+    del keep
+
+
 @pytest.mark.parametrize("device_admit", [1, 2])
 def test_fail_closed_stale_generation_device_admission(bec, device_admit):
     w = W.with_changes(W.WORKLOADS["tiny"], n_steps=2)
