@@ -665,25 +665,41 @@ struct AdmitStaged {
   bool have_tick = false;
 };
 
-// Stages the slot state and the page table of the layer into shared memory
-// (one warp); the admission smem layout starts with last[S], owner[S], sgen[S].
-__device__ void admit_stage(const AdmitArgs& A, unsigned char* smem, int* pt_s, unsigned long long* tick_rng) {
-  const int lane = threadIdx.x & 31;
+// Asynchronous copies global -> shared (4 or 8 bytes, naturally aligned).
+__device__ __forceinline__ void cp_async4(void* smem, const void* gmem) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(static_cast<unsigned>(__cvta_generic_to_shared(smem))),
+               "l"(gmem)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async8(void* smem, const void* gmem) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(static_cast<unsigned>(__cvta_generic_to_shared(smem))),
+               "l"(gmem)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+// Every block of the decode router copies the layer's cache state (slot
+// state, page table, tick and generator state) into the admission area of
+// its shared memory when it starts; only the last block uses it, but the
+// copies are small and have landed by the time the tail needs them.
+__device__ void admit_stage_async(const AdmitArgs& A, unsigned char* smem, int* pt_s, unsigned long long* tick_rng) {
   const int S = A.S;
   const DevCacheLayer c = A.c;
   unsigned long long* s_last = reinterpret_cast<unsigned long long*>(smem);
   int* s_owner = reinterpret_cast<int*>(s_last + S);
   uint32_t* s_sgen = reinterpret_cast<uint32_t*>(s_owner + S);
-  for (int s = lane; s < S; s += 32) {
-    s_last[s] = __ldcg(c.last + s);
-    s_owner[s] = __ldcg(c.owner + s);
-    s_sgen[s] = __ldcg(c.sgen + s);
+  for (int i = threadIdx.x; i < S; i += blockDim.x) {
+    cp_async8(s_last + i, c.last + i);
+    cp_async4(s_owner + i, c.owner + i);
+    cp_async4(s_sgen + i, c.sgen + i);
   }
-  for (int e = lane; e < A.E; e += 32) pt_s[e] = __ldcg(c.pt + e);
-  if (lane == 0) {
-    tick_rng[0] = __ldcg(c.tick);
-    tick_rng[1] = __ldcg(c.rng);
+  for (int e = threadIdx.x; e < A.E; e += blockDim.x) cp_async4(pt_s + e, c.pt + e);
+  if (threadIdx.x == 0) {
+    cp_async8(tick_rng, c.tick);
+    cp_async8(tick_rng + 1, c.rng);
   }
+  cp_async_commit();
 }
 
 __device__ void admit_warp(const AdmitArgs& A, const moe_plan_t& P, unsigned char* smem,
@@ -938,9 +954,43 @@ size_t plan_smem_bytes(int E) {
 // (T*k <= 32 assignments, E <= 256): admission scratch, the plan's counts and
 // offsets, the layer's page table, and the selection.
 struct FastTailLayout {
-  size_t admit, plan, pt, key, idx, w, uniq, tick, nu, cand, keys, taken, total;
+  size_t admit, plan, pt, key, idx, w, uniq, tick, nu, cand, keys, taken, one, total;
 };
 __host__ __device__ constexpr size_t r16(size_t v) { return (v + 15) & ~size_t(15); }
+
+// Scratch of the one-token tail: candidate keys [E] and ids [E], per-warp
+// maxima and reductions, counters, the slots hit by the step [S] and the
+// slot of each miss.
+struct OneTokenScratch {
+  unsigned long long* ckey;   // [E]
+  int* cid;                   // [E]
+  unsigned long long* wrest;  // [kRouteWarps] largest upper bound outside the selection
+  uint32_t* wmax;             // [kRouteWarps]
+  int* cnt;                   // [8]: 0 candidates, 1 certified, 2 free slots
+  unsigned char* hit;         // [S]
+  int* mslot;                 // [32] slot of the r-th miss
+};
+__host__ __device__ constexpr size_t one_token_scratch_bytes(int E, int S) {
+  return 8 * static_cast<size_t>(E) + r16(4 * static_cast<size_t>(E)) + 8 * kRouteWarps + 4 * kRouteWarps +
+         32 + r16(static_cast<size_t>(S)) + 4 * 32;
+}
+__device__ inline OneTokenScratch one_token_scratch(unsigned char* p, int E, int S) {
+  OneTokenScratch o;
+  o.ckey = reinterpret_cast<unsigned long long*>(p);
+  p += 8 * static_cast<size_t>(E);
+  o.cid = reinterpret_cast<int*>(p);
+  p += r16(4 * static_cast<size_t>(E));
+  o.wrest = reinterpret_cast<unsigned long long*>(p);
+  p += 8 * kRouteWarps;
+  o.wmax = reinterpret_cast<uint32_t*>(p);
+  p += 4 * kRouteWarps;
+  o.cnt = reinterpret_cast<int*>(p);
+  p += 32;
+  o.hit = p;
+  p += r16(static_cast<size_t>(S));
+  o.mslot = reinterpret_cast<int*>(p);
+  return o;
+}
 __host__ __device__ inline FastTailLayout fast_tail_layout(int T, int E, int S, int max_units, bool admit) {
   FastTailLayout L{};
   L.admit = 0;
@@ -955,11 +1005,321 @@ __host__ __device__ inline FastTailLayout fast_tail_layout(int T, int E, int S, 
   L.cand = L.nu + 16;                                             // tournament: 64 ids, 64 keys
   L.keys = L.cand + 4 * 64 + 8 * 64;                              // [3][T][E] u64
   L.taken = L.keys + 24 * static_cast<size_t>(T) * E;             // [T][E] bytes
-  L.total = L.taken + r16(static_cast<size_t>(T) * E);
+  L.one = L.taken + r16(static_cast<size_t>(T) * E);                // one-token tail scratch
+  L.total = L.one + (T == 1 ? one_token_scratch_bytes(E, S) : 0);
   return L;
 }
 __host__ __device__ constexpr bool fast_tail_ok(int T, int k, int E) {
   return T * k <= 32 && E <= 256 && T * E <= 2048;
+}
+
+// One token (T == 1) on the whole block. Selection: experts whose high key
+// word reaches the smallest of the per-warp maxima (when at least k warps
+// hold experts, at least k experts do, so the top k are among them) are
+// ranked among themselves by (key descending, id ascending). If the
+// selection is certified, the weights, the plan and, for LRU, the
+// admission are computed in parallel: for one token the sequential rule
+// "a miss takes the lowest free slot, else the slot of oldest access" gives
+// the r-th miss (ascending id) the r-th free slot by index, and past the
+// free slots the untouched occupied slots in ascending (last access, slot)
+// order, since every slot the step touches gets a newer tick than any
+// earlier access. Returns false, having written nothing global, when the
+// selection is not certified.
+__device__ bool one_token_tail(const RouteArgs& a, unsigned char* sm, const FastTailLayout& L) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int E = a.E, k = a.k;
+  const bool adm = a.admit.enabled != 0;
+  const int S = a.admit.S;
+  const unsigned long long* sl = reinterpret_cast<const unsigned long long*>(sm + L.keys);
+  const unsigned long long* slo = sl + E;
+  const unsigned long long* shi = sl + 2 * E;
+  unsigned char* taken = sm + L.taken;
+  int* s_idx = reinterpret_cast<int*>(sm + L.idx);
+  unsigned long long* s_key = reinterpret_cast<unsigned long long*>(sm + L.key);
+  float* s_w = reinterpret_cast<float*>(sm + L.w);
+  int* s_plan = reinterpret_cast<int*>(sm + L.plan);
+  int* s_uniq = reinterpret_cast<int*>(sm + L.uniq);
+  int* s_nu = reinterpret_cast<int*>(sm + L.nu);
+  const int* s_pt = reinterpret_cast<const int*>(sm + L.pt);
+  const OneTokenScratch o = one_token_scratch(sm + L.one, E, S);
+  // ---- candidates
+  const bool live = tid < E;
+  const unsigned long long ke = live ? sl[tid] : 0ull;
+  const uint32_t he = static_cast<uint32_t>(ke >> 32);
+  const uint32_t wm = __reduce_max_sync(0xffffffffu, live ? he : 0u);
+  const int nwarps = (E + 31) / 32;
+  if (lane == 0) o.wmax[warp] = warp < nwarps ? wm : 0xffffffffu;
+  if (tid < 8) o.cnt[tid] = 0;
+  __syncthreads();
+  uint32_t t = 0u;
+  if (nwarps >= k) {
+    t = 0xffffffffu;
+    for (int w = 0; w < kRouteWarps; ++w) t = min(t, o.wmax[w]);
+  }
+  if (live && he >= t) {
+    const int c = atomicAdd(&o.cnt[0], 1);
+    o.ckey[c] = ke;
+    o.cid[c] = tid;
+  }
+  __syncthreads();
+  const int nc = o.cnt[0];
+  if (nc <= kRouteThreads / 2) {
+    // g threads per candidate (8, 4 or 2), each comparing against every g-th
+    const int lg = nc <= kRouteThreads / 8 ? 3 : (nc <= kRouteThreads / 4 ? 2 : 1);
+    const int g = 1 << lg;
+    const int i = tid >> lg, part = tid & (g - 1);
+    const bool ci = i < nc;
+    const unsigned long long ki = ci ? o.ckey[i] : 0ull;
+    const int ei = ci ? o.cid[i] : 0;
+    int r = 0;
+    if (ci) {
+      for (int j = part; j < nc; j += g) {
+        const unsigned long long kj = o.ckey[j];
+        const int ej = o.cid[j];
+        r += (kj > ki || (kj == ki && ej < ei)) ? 1 : 0;
+      }
+    }
+    for (int d = 1; d < g; d <<= 1) r += __shfl_xor_sync(0xffffffffu, r, d);
+    if (ci && part == 0 && r < k) {
+      s_idx[r] = ei;
+      s_key[r] = ki;
+      taken[ei] = 1;
+    }
+  } else {
+    for (int i = tid; i < nc; i += kRouteThreads) {
+      const unsigned long long ki = o.ckey[i];
+      const int ei = o.cid[i];
+      int r = 0;
+      for (int j = 0; j < nc; ++j) {
+        const unsigned long long kj = o.ckey[j];
+        const int ej = o.cid[j];
+        r += (kj > ki || (kj == ki && ej < ei)) ? 1 : 0;
+      }
+      if (r < k) {
+        s_idx[r] = ei;
+        s_key[r] = ki;
+        taken[ei] = 1;
+      }
+    }
+  }
+  __syncthreads();
+  // ---- certification: consecutive selections, and the k-th against the
+  // largest upper bound outside the selection
+  {
+    const bool out = live && !taken[tid];
+    const unsigned long long h = out ? shi[tid] : 0ull;
+    const uint32_t rh = __reduce_max_sync(0xffffffffu, out ? static_cast<uint32_t>(h >> 32) : 0u);
+    const uint32_t rl =
+        __reduce_max_sync(0xffffffffu, out && static_cast<uint32_t>(h >> 32) == rh ? static_cast<uint32_t>(h) : 0u);
+    const bool any = __any_sync(0xffffffffu, out);
+    if (lane == 0) o.wrest[warp] = any ? ((static_cast<unsigned long long>(rh) << 32) | rl) : 0ull;
+    if (lane == 0 && any) atomicOr(&o.cnt[3], 1);
+  }
+  __syncthreads();
+  if (warp == 0) {
+    unsigned long long rest = 0ull;
+    for (int w = 0; w < kRouteWarps; ++w) rest = o.wrest[w] > rest ? o.wrest[w] : rest;
+    const bool any_rest = o.cnt[3] != 0;
+    bool ok = true;
+    if (lane + 1 < k) ok = slo[s_idx[lane]] > shi[s_idx[lane + 1]];
+    if (lane == k - 1 && any_rest) ok = slo[s_idx[lane]] > rest;
+    ok = __all_sync(0xffffffffu, ok);
+    if (lane == 0) o.cnt[1] = ok ? 1 : 0;
+  }
+  __syncthreads();
+  if (!o.cnt[1]) return false;
+  const moe_plan_t& P = a.plan;
+  // ---- weights, permutation (warp 0) and the plan's per-expert arrays (all)
+  if (warp == 0) {
+    float z = 0.f;
+    int pos = 0;
+    if (lane < k) {
+      z = expf(static_cast<float>(okey_value(s_key[lane]) - okey_value(s_key[0])));
+      const int e = s_idx[lane];
+      for (int i = 0; i < k; ++i) pos += s_idx[i] < e ? 1 : 0;
+    }
+    float sum = 0.f;
+    for (int j = 0; j < k; ++j) sum += __shfl_sync(0xffffffffu, z, j);  // fixed order
+    if (lane < k) {
+      const float wl = z / sum;
+      const int e = s_idx[lane];
+      a.topk_idx[lane] = e;
+      a.topk_w[lane] = wl;
+      s_w[lane] = wl;
+      s_uniq[pos] = e;
+      P.uniq[pos] = e;
+      P.perm_tok[pos] = 0;
+      P.perm_rank[pos] = lane;
+      P.perm_w[pos] = wl;
+      P.inv[lane] = pos;
+    }
+    if (lane == 0) {
+      P.offsets[E] = k;
+      *P.n_uniq = k;
+      *s_nu = k;
+    }
+  }
+  if (live) {
+    int off = 0;
+    for (int i = 0; i < k; ++i) off += s_idx[i] < tid ? 1 : 0;
+    const int c = taken[tid];
+    P.counts[tid] = c;
+    P.offsets[tid] = off;
+    s_plan[tid] = c;
+    s_plan[E + tid] = off;
+  }
+  if (!adm || a.admit.policy != MOE_LRU) {
+    __syncthreads();  // the caller's admission (random policy) reads the plan from shared memory
+    return true;
+  }
+  // ---- LRU admission
+  const AdmitArgs& A = a.admit;
+  const DevCacheLayer c = A.c;
+  unsigned long long* s_last = reinterpret_cast<unsigned long long*>(sm + L.admit);
+  int* s_owner = reinterpret_cast<int*>(s_last + S);
+  uint32_t* s_sgen = reinterpret_cast<uint32_t*>(s_owner + S);
+  const unsigned long long tick0 = reinterpret_cast<const unsigned long long*>(sm + L.tick)[0];
+  if (k > S) {
+    if (tid == 0) {
+      atomicOr(a.err, MOE_DEVERR_CAPACITY);
+      A.units[0] = 0;
+      A.fills[0] = 0;
+    }
+    return true;
+  }
+  for (int i = tid; i < S; i += kRouteThreads) o.hit[i] = 0;
+  if (tid < 32) o.mslot[tid] = -1;
+  __syncthreads();
+  // selection j (warp 0, lane j): its slot before the step
+  int e_j = -1, slot_j = -1, hr = 0, mr = 0, nh = 0;
+  if (warp == 0) {
+    if (lane < k) {
+      e_j = s_idx[lane];
+      slot_j = s_pt[e_j];
+    }
+    const bool hit = lane < k && slot_j >= 0;
+    const unsigned hm = __ballot_sync(0xffffffffu, hit), mm = __ballot_sync(0xffffffffu, lane < k && !hit);
+    nh = __popc(hm);
+    for (int i = 0; i < k; ++i) {
+      const int ei = __shfl_sync(0xffffffffu, e_j, i);
+      if (ei < e_j) {
+        hr += (hm >> i) & 1u;
+        mr += (mm >> i) & 1u;
+      }
+    }
+    if (hit) o.hit[slot_j] = 1;
+  }
+  __syncwarp();
+  const int nm = k - nh;  // valid in warp 0
+  if (warp == 0) {
+    // the misses take the free slots in index order
+    int nfree = 0;
+    for (int s0 = 0; s0 < S; s0 += 32) {
+      const int s2 = s0 + lane;
+      const bool fr = s2 < S && s_owner[s2] < 0;
+      const unsigned fb = __ballot_sync(0xffffffffu, fr);
+      const int r = nfree + __popc(fb & ((1u << lane) - 1u));
+      if (fr && r < nm) o.mslot[r] = s2;
+      nfree += __popc(fb);
+    }
+    // then the untouched occupied slots, oldest access first (ties: lower slot)
+    unsigned chosen = 0u;  // bit j: slot lane + 32 j taken by an earlier round
+    for (int r = nfree; r < nm; ++r) {
+      unsigned long long best = ~0ull;
+      int bs = INT_MAX;
+      for (int j = 0; j * 32 < S; ++j) {
+        const int s2 = j * 32 + lane;
+        if (s2 < S && s_owner[s2] >= 0 && !o.hit[s2] && !((chosen >> j) & 1u)) {
+          const unsigned long long v = s_last[s2];
+          if (v < best) {
+            best = v;
+            bs = s2;
+          }
+        }
+      }
+      const uint32_t mh = __reduce_min_sync(0xffffffffu, static_cast<uint32_t>(best >> 32));
+      const bool c1 = static_cast<uint32_t>(best >> 32) == mh;
+      const uint32_t ml = __reduce_min_sync(0xffffffffu, c1 ? static_cast<uint32_t>(best) : 0xffffffffu);
+      const bool c2 = c1 && static_cast<uint32_t>(best) == ml;
+      const int win = static_cast<int>(__reduce_min_sync(0xffffffffu, c2 ? static_cast<unsigned>(bs) : 0xffffffffu));
+      if (lane == 0) o.mslot[r] = win < S ? win : -1;
+      if (win < S && (win & 31) == lane) chosen |= 1u << (win >> 5);
+    }
+    __syncwarp();
+    // every miss has a slot (guaranteed while the union fits the slots)
+    const bool bad = lane < k && slot_j < 0 && o.mslot[mr] < 0;
+    const bool any_bad = __any_sync(0xffffffffu, bad);
+    if (lane == 0) o.cnt[4] = any_bad ? 1 : 0;
+  }
+  __syncthreads();
+  if (o.cnt[4]) {
+    if (tid == 0) {
+      atomicOr(a.err, MOE_DEVERR_CAPACITY);
+      A.units[0] = 0;
+      A.fills[0] = 0;
+    }
+    return true;
+  }
+  if (warp == 0) {
+    int nevict = 0;
+    if (lane < k) {
+      const bool hit = slot_j >= 0;
+      int slot = slot_j;
+      if (!hit) {
+        slot = o.mslot[mr];
+        const int victim = s_owner[slot];
+        if (victim >= 0) {
+          c.pt[victim] = -1;  // victims are never in the union
+          nevict = 1;
+        }
+        s_owner[slot] = e_j;
+        s_sgen[slot] += 1u;
+        s_last[slot] = tick0 + nh + 1 + mr;
+        A.fills[1 + 2 * mr] = e_j;
+        A.fills[2 + 2 * mr] = slot;
+        A.done[mr] = 0u;
+      } else {
+        s_last[slot] = tick0 + 1 + hr;
+      }
+      const uint32_t g = s_sgen[slot];
+      c.pt[e_j] = slot;
+      c.ptgen[e_j] = g;
+      int pos = 0;
+      for (int i = 0; i < k; ++i) pos += s_idx[i] < e_j ? 1 : 0;
+      int* U = A.units + kUnitHeader + kUnitInts * pos;
+      const bool filled = A.read_through && !hit;
+      U[0] = filled ? -2 - slot : slot;
+      U[1] = pos;
+      U[2] = 1;
+      U[3] = filled ? e_j : static_cast<int>(g);
+    }
+    nevict = __reduce_add_sync(0xffffffffu, nevict);
+    if (lane == 0) {
+      if (A.has_shared) {
+        int* U = A.units + kUnitHeader + kUnitInts * k;
+        U[0] = -1;
+        U[1] = -1;
+        U[2] = 1;
+        U[3] = 0;
+      }
+      A.units[0] = k + (A.has_shared ? 1 : 0);
+      A.fills[0] = nm;
+      c.tick[0] = tick0 + k;
+      atomicAdd(reinterpret_cast<unsigned long long*>(c.stats + kStatSteps), 1ull);
+      atomicAdd(reinterpret_cast<unsigned long long*>(c.stats + kStatHits), static_cast<unsigned long long>(k - nm));
+      atomicAdd(reinterpret_cast<unsigned long long*>(c.stats + kStatMisses), static_cast<unsigned long long>(nm));
+      atomicAdd(reinterpret_cast<unsigned long long*>(c.stats + kStatEvictions), static_cast<unsigned long long>(nevict));
+      atomicAdd(reinterpret_cast<unsigned long long*>(c.stats + kStatMaterialized),
+                static_cast<unsigned long long>(nm) * static_cast<unsigned long long>(A.payload));
+    }
+  }
+  __syncthreads();
+  for (int s2 = tid; s2 < S; s2 += kRouteThreads) {
+    c.last[s2] = s_last[s2];
+    c.owner[s2] = s_owner[s2];
+    c.sgen[s2] = s_sgen[s2];
+  }
+  return true;
 }
 
 // The decode fast path of the router's last block: warps 0..T-1 select the
@@ -986,7 +1346,7 @@ __device__ void fast_tail(const RouteArgs& a, unsigned char* sm, int* s_flagged,
   const size_t te = static_cast<size_t>(T) * E;
   // the block stages every token's keys (one round of loads); the last warp
   // stages the layer's cache state meanwhile
-  if (adm && warp == kRouteWarps - 1) admit_stage(a.admit, s_admit, s_pt, s_tick);
+  if (adm) cp_async_wait_all();  // the cache state copied when the kernel started
   for (int i = tid; i < static_cast<int>(te); i += kRouteThreads) {
     s_keys[i] = __ldcg(a.keys + i);
     s_keys[te + i] = __ldcg(a.keys + te + i);
@@ -994,6 +1354,23 @@ __device__ void fast_tail(const RouteArgs& a, unsigned char* sm, int* s_flagged,
     s_taken[i] = 0;
   }
   __syncthreads();
+  if (T == 1 && one_token_tail(a, sm, L)) {
+    if (adm && a.admit.policy != MOE_LRU && warp == 0) {
+      AdmitStaged st;
+      st.slots = true;
+      st.pt = s_pt;
+      st.nu = *s_nu;
+      st.uniq = s_uniq;
+      st.cnt = s_plan;
+      st.off = s_plan + E;
+      st.tick = s_tick[0];
+      st.rng = s_tick[1];
+      st.have_tick = true;
+      __syncwarp();
+      admit_warp(a.admit, a.plan, s_admit, a.err, st);
+    }
+    return;
+  }
   if (T == 1 && k <= 8) {
     // one token: tournament over the whole block
     int* cand_idx = reinterpret_cast<int*>(sm + L.cand);
@@ -1086,6 +1463,15 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a) {
   // for the kernels that produce x and reuse the scratch
   for (int v = tid; v < (H >> 2); v += kRouteThreads)
     asm volatile("prefetch.global.L1 [%0];" ::"l"(reinterpret_cast<const float4*>(wrow) + v));
+  // the decode tail's cache state (not written by the kernels this launch may
+  // overlap): start copying it into shared memory now
+  const bool early_admit = a.admit.enabled && a.plan.counts != nullptr && fast_tail_ok(T, a.k, E);
+  if (early_admit) {
+    const FastTailLayout L = fast_tail_layout(T, E, a.admit.S, min(E, T * a.k), true);
+    unsigned char* sm = reinterpret_cast<unsigned char*>(dyn_smem);
+    admit_stage_async(a.admit, sm + L.admit, reinterpret_cast<int*>(sm + L.pt),
+                      reinterpret_cast<unsigned long long*>(sm + L.tick));
+  }
   pdl_wait();
   pdl_trigger();
 
@@ -1173,7 +1559,10 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a) {
   __threadfence();
   if (tid == 0) s_ticket = atomicAdd(a.ticket, 1u);
   __syncthreads();
-  if (s_ticket != gridDim.x - 1) return;
+  if (s_ticket != gridDim.x - 1) {
+    if (early_admit) cp_async_wait_all();
+    return;
+  }
   __threadfence();
   if (tid == 0) s_nflag = 0;
   __syncthreads();
