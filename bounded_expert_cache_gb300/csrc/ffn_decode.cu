@@ -20,10 +20,11 @@
 // and up matrices of one unit (a routed expert of the union, or the shared
 // expert), for every token routed to it; writes h = silu(g) * u in fp32 to
 // scratch, indexed by expert-major assignment (routed) or token (shared).
-// Phase 2 (down + combine): a block owns 8 output rows; warp items = (unit,
-// 2 rows); each item's partial sums (already weighted by the combine weight)
-// go to shared memory and are added in unit order, so the output does not
-// depend on scheduling and is identical whatever the cache state.
+// Phase 2 (down + combine): one block per SM owns an even run of output rows
+// (about H / SMs); warp items = (unit, 2 rows), loaded in batches; each
+// item's partial sums (already weighted by the combine weight) go to shared
+// memory and are added in unit order, so the output does not depend on
+// scheduling and is identical whatever the cache state.
 #include <cuda_fp16.h>
 
 #include "internal.h"
@@ -35,7 +36,6 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kRowsPerItem = 2;   // rows per warp item
-constexpr int kDownRows = 8;      // output rows per phase-2 block
 
 // Swizzled position of element k in an fp32 row whose length is a multiple
 // of 32: the four 16-byte quads of each 16-float chunk c are rotated by
@@ -97,42 +97,77 @@ __device__ __forceinline__ bool owns_scale(int c) {
   return Q != MOE_Q8_0 || (c & 1) == 0;
 }
 
-// q (Q8_0 byte) -> float, exact: bits 0x4B0000uu = 2^23 + uu with uu = q + 128.
-__device__ __forceinline__ float q8_to_f(uint32_t biased, int b) {
-  return __uint_as_float(__byte_perm(biased, 0x4B000000u, 0x7540u | b)) - 8388736.0f;
+// Packed pairs of fp32 (Blackwell's f32x2 add and FMA).
+__device__ __forceinline__ unsigned long long f2pack(uint32_t a, uint32_t b) {
+  unsigned long long v;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(v) : "r"(a), "r"(b));
+  return v;
 }
-// nibble n (0..15) in byte b of w -> n - 8, exact.
-__device__ __forceinline__ float q4_to_f(uint32_t nib, int b) {
-  return __uint_as_float(__byte_perm(nib, 0x4B000000u, 0x7540u | b)) - 8388616.0f;
+__device__ __forceinline__ unsigned long long f2packf(float a, float b) {
+  unsigned long long v;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(v) : "f"(a), "f"(b));
+  return v;
+}
+__device__ __forceinline__ float f2sum(unsigned long long v) {
+  float a, b;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+  return a + b;
+}
+__device__ __forceinline__ unsigned long long f2sub(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ unsigned long long f2fma(unsigned long long a, unsigned long long b, unsigned long long c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
 }
 
-// Dot of one 16-byte Q8_0 chunk (16 weights) with 16 activations.
+// Dot of one 16-byte Q8_0 chunk (16 weights) with 16 activations. A biased
+// byte u = q + 128 becomes the float 2^23 + u by one byte permute; a packed
+// subtraction of 2^23 + 128 leaves q exactly, two weights at a time, and
+// packed FMAs accumulate even and odd positions separately.
 __device__ __forceinline__ float dot_q8(const uint4 w, const float* x) {
   const uint32_t ws[4] = {w.x ^ 0x80808080u, w.y ^ 0x80808080u, w.z ^ 0x80808080u,
                           w.w ^ 0x80808080u};
-  float s = 0.f;
+  const unsigned long long bias = f2packf(8388736.0f, 8388736.0f);
+  unsigned long long s = 0ull;
 #pragma unroll
   for (int i = 0; i < 4; ++i)
 #pragma unroll
-    for (int b = 0; b < 4; ++b) s = fmaf(q8_to_f(ws[i], b), x[4 * i + b], s);
-  return s;
+    for (int h = 0; h < 2; ++h) {
+      const unsigned long long q = f2sub(f2pack(__byte_perm(ws[i], 0x4B000000u, 0x7540u | (2 * h)),
+                                                __byte_perm(ws[i], 0x4B000000u, 0x7540u | (2 * h + 1))),
+                                         bias);
+      s = f2fma(q, f2packf(x[4 * i + 2 * h], x[4 * i + 2 * h + 1]), s);
+    }
+  return f2sum(s);
 }
 
 // Dot of one 16-byte Q4_0 block (32 weights) with activations: xl for
-// elements 0..15 (low nibbles), xh for 16..31 (high nibbles).
+// elements 0..15 (low nibbles), xh for 16..31 (high nibbles); a nibble n
+// becomes 2^23 + n, and the packed subtraction of 2^23 + 8 leaves n - 8.
 __device__ __forceinline__ float dot_q4(const uint4 w, const float* xl, const float* xh) {
   const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-  float s = 0.f;
+  const unsigned long long bias = f2packf(8388616.0f, 8388616.0f);
+  unsigned long long s = 0ull;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const uint32_t lo = ws[i] & 0x0F0F0F0Fu, hi = (ws[i] >> 4) & 0x0F0F0F0Fu;
 #pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      s = fmaf(q4_to_f(lo, b), xl[4 * i + b], s);
-      s = fmaf(q4_to_f(hi, b), xh[4 * i + b], s);
+    for (int h = 0; h < 2; ++h) {
+      const unsigned long long ql = f2sub(f2pack(__byte_perm(lo, 0x4B000000u, 0x7540u | (2 * h)),
+                                                 __byte_perm(lo, 0x4B000000u, 0x7540u | (2 * h + 1))),
+                                          bias);
+      const unsigned long long qh = f2sub(f2pack(__byte_perm(hi, 0x4B000000u, 0x7540u | (2 * h)),
+                                                 __byte_perm(hi, 0x4B000000u, 0x7540u | (2 * h + 1))),
+                                          bias);
+      s = f2fma(ql, f2packf(xl[4 * i + 2 * h], xl[4 * i + 2 * h + 1]), s);
+      s = f2fma(qh, f2packf(xh[4 * i + 2 * h], xh[4 * i + 2 * h + 1]), s);
     }
   }
-  return s;
+  return f2sum(s);
 }
 
 struct UnitRef {
@@ -322,125 +357,242 @@ __global__ void __launch_bounds__(kThreads) gateup_kernel(FfnArgs a) {
 }
 
 // ------------------------------------------------------------ phase 2
+// One block per SM, 16 warps: block b owns output rows [b*rpb, b*rpb + rpb)
+// (rpb even, about H / SMs) of every unit. The prologue stages, in one round
+// of loads, the h rows (swizzled), the unit table (resolved) and the
+// permutation's tokens and weights; each warp then takes its items (unit,
+// row pair) in batches whose weight loads are all in flight at once.
+constexpr int kDownThreads = 512;
+constexpr int kDownWarps = kDownThreads / 32;
+
+struct DUnit {
+  const uint8_t* base;  // payload to read
+  uint8_t* dst;         // slot being filled (read-through miss) or nullptr
+  int M, p0, slot;      // slot: routed slot (S if refused), -1 shared
+  uint32_t egen;
+  int miss, pad;
+};
+
+// Shared-memory layout of the down kernel.
+struct DownSmem {
+  size_t part, perm, units, total;
+};
+__host__ __device__ inline DownSmem down_smem(int nrows, int ldh, int cap, int rpb, int TM, int A) {
+  DownSmem L{};
+  L.part = (static_cast<size_t>(nrows) * ldh * sizeof(float) + 15) & ~size_t(15);
+  L.perm = L.part + ((static_cast<size_t>(cap) * rpb * TM * sizeof(float) + 15) & ~size_t(15));
+  L.units = L.perm + ((static_cast<size_t>(A) * 8 + 15) & ~size_t(15));
+  L.total = L.units + sizeof(DUnit) * static_cast<size_t>(cap);
+  return L;
+}
+
+template <int TM>
+struct DownBatch {
+  static constexpr int B = TM == 1 ? 4 : (TM <= 4 ? 2 : 1);
+};
+
 template <int Q, int TM>
-__global__ void __launch_bounds__(kThreads) down_kernel(FfnArgs a) {
-  extern __shared__ float sm[];
+__global__ void __launch_bounds__(kDownThreads, 1) down_kernel(FfnArgs a, int rpb) {
+  extern __shared__ __align__(16) float sm[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int T = a.T, A = a.T * a.k;
   const int nrows = A + (a.shared ? T : 0);
   const int ldh = a.ldh;
-  float* hs = sm;                                   // [nrows][ldh] swizzled
-  float* part = sm + static_cast<size_t>(nrows) * ldh;  // [items][2][TM]
+  const int cap = min(a.E, A) + (a.shared ? 1 : 0);
+  const DownSmem L = down_smem(nrows, ldh, cap, rpb, TM, A);
+  float* hs = sm;                                                        // [nrows][ldh] swizzled
+  float* part = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(sm) + L.part);  // [units][rpb][TM]
+  int* ptok = reinterpret_cast<int*>(reinterpret_cast<unsigned char*>(sm) + L.perm);
+  float* pw = reinterpret_cast<float*>(ptok + A);
+  DUnit* su = reinterpret_cast<DUnit*>(reinterpret_cast<unsigned char*>(sm) + L.units);
   pdl_wait();
   pdl_trigger();
-  for (int i = tid; i < nrows * ldh; i += kThreads) {
-    const int p = i / ldh, k = i - p * ldh;
-    hs[p * ldh + swz(k)] = __ldcg(a.h + i);
+  const int units = __ldg(a.units);
+  // prologue, one round of loads: the unit table's capacity (entries past
+  // the count are never used), the permutation, the h rows
+  for (int u = tid; u < cap; u += kDownThreads) {
+    const UnitRef U = resolve_unit(a, u);
+    DUnit r;
+    r.base = U.base;
+    r.dst = U.miss ? U.dst : nullptr;
+    r.M = U.M;
+    r.p0 = U.p0;
+    r.slot = U.slot;
+    r.egen = U.egen;
+    r.miss = U.miss ? 1 : 0;
+    r.pad = 0;
+    su[u] = r;
+  }
+  for (int i = tid; i < A; i += kDownThreads) {
+    ptok[i] = __ldg(a.plan.perm_tok + i);
+    pw[i] = __ldg(a.plan.perm_w + i);
+  }
+  {
+    constexpr int kU = 8;
+    const int n = nrows * ldh;
+    for (int i0 = tid * 4; i0 < n; i0 += kDownThreads * 4 * kU) {
+      float4 v[kU];
+#pragma unroll
+      for (int j = 0; j < kU; ++j) {
+        const int i = i0 + j * kDownThreads * 4;
+        if (i < n) v[j] = __ldcg(reinterpret_cast<const float4*>(a.h + i));
+      }
+#pragma unroll
+      for (int j = 0; j < kU; ++j) {
+        const int i = i0 + j * kDownThreads * 4;
+        if (i < n) {
+          const int p = i / ldh, kk = i - p * ldh;
+          *reinterpret_cast<float4*>(hs + p * ldh + swz(kk)) = v[j];
+        }
+      }
+    }
   }
   __syncthreads();
-  const int units = __ldg(a.units);
-  const int o0 = blockIdx.x * kDownRows;
-  constexpr int kPairs = kDownRows / kRowsPerItem;
-  const int items = units * kPairs;
-  for (int it = warp; it < items; it += kWarps) {
-    const int u = it / kPairs, rp = it - u * kPairs;
-    const UnitRef U = resolve_unit(a, u);
-    const bool ok = unit_ok(a, U);
-    float acc[kRowsPerItem][TM];
+  const int o0 = blockIdx.x * rpb;
+  const int pairs = rpb / kRowsPerItem;
+  const int items = units * pairs;
+  constexpr int B = DownBatch<TM>::B;
+  for (int j0 = warp; j0 < items; j0 += kDownWarps * B) {
+    // the first chunk of every row of the batch, and the slots'
+    // generations, all in flight before the first is used
+    uint4 w[B][kRowsPerItem];
+    unsigned short sb[B][kRowsPerItem];
+    uint32_t gb[B];
 #pragma unroll
-    for (int r = 0; r < kRowsPerItem; ++r)
+    for (int b = 0; b < B; ++b) {
+      gb[b] = 0u;
 #pragma unroll
-      for (int m = 0; m < TM; ++m) acc[r][m] = 0.f;
-    {
-      const int K = U.p0 >= 0 ? a.I : a.Is;
+      for (int r = 0; r < kRowsPerItem; ++r) {
+        w[b][r] = make_uint4(0, 0, 0, 0);
+        sb[b][r] = 0;
+      }
+      const int it = j0 + b * kDownWarps;
+      if (it >= items) continue;
+      const int u = it / pairs, rp = it - u * pairs;
+      const DUnit U = su[u];
+      const bool routed = U.p0 >= 0;
+      gb[b] = (!U.miss && routed && U.slot < a.S) ? __ldg(a.gen + U.slot) : 0u;
+      const int K = routed ? a.I : a.Is;
+      const int rowbytes = Q == MOE_Q8_0 ? K : K / 2;
+      const int64_t qo = routed ? a.g.qoff[2] : a.gs.qoff[2];
+      const int64_t so = routed ? a.g.soff[2] : a.gs.soff[2];
+      if (lane < rowbytes / 16) {
+#pragma unroll
+        for (int r = 0; r < kRowsPerItem; ++r) {
+          const int o = o0 + rp * kRowsPerItem + r;
+          if (o >= a.H) continue;
+          const uint8_t* qp = U.base + qo + static_cast<int64_t>(o) * rowbytes + lane * 16;
+          const uint8_t* sp = U.base + so + static_cast<int64_t>(o) * (K / 16) + (Q == MOE_Q8_0 ? (lane >> 1) : lane) * 2;
+          if (U.miss) {
+            w[b][r] = ld_host(qp);
+            sb[b][r] = ld_scale_host_bits(sp);
+          } else {
+            w[b][r] = ldg_stream(qp);
+            sb[b][r] = __ldg(reinterpret_cast<const unsigned short*>(sp));
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < B; ++b) {
+      const int it = j0 + b * kDownWarps;
+      if (it >= items) break;
+      const int u = it / pairs, rp = it - u * pairs;
+      const DUnit U = su[u];
+      const bool routed = U.p0 >= 0;
+      const int K = routed ? a.I : a.Is;
       const int rowbytes = Q == MOE_Q8_0 ? K : K / 2;
       const int nch = rowbytes / 16;
       const int sc_row = (K / 32) * 2;
+      const int64_t qo = routed ? a.g.qoff[2] : a.gs.qoff[2];
+      const int64_t so = routed ? a.g.soff[2] : a.gs.soff[2];
+      const int mcount = U.M;  // <= T <= TM
+      int tok[TM], hrow[TM];
+      float wt[TM];
+#pragma unroll
+      for (int m = 0; m < TM; ++m) {
+        if (m < mcount) {
+          hrow[m] = routed ? U.p0 + m : A + m;
+          tok[m] = routed ? ptok[hrow[m]] : m;
+          wt[m] = routed ? pw[hrow[m]] : 1.0f;
+        } else {
+          hrow[m] = 0;
+          tok[m] = 0;
+          wt[m] = 0.f;
+        }
+      }
       const uint8_t* q[kRowsPerItem];
-      const uint8_t* s[kRowsPerItem];
+      const uint8_t* sp0[kRowsPerItem];
       bool rv[kRowsPerItem];
 #pragma unroll
       for (int r = 0; r < kRowsPerItem; ++r) {
         const int o = o0 + rp * kRowsPerItem + r;
         rv[r] = o < a.H;
-        q[r] = U.base + U.qoff[2] + static_cast<int64_t>(rv[r] ? o : 0) * rowbytes;
-        s[r] = U.base + U.soff[2] + static_cast<int64_t>(rv[r] ? o : 0) * sc_row;
+        q[r] = U.base + qo + static_cast<int64_t>(rv[r] ? o : 0) * rowbytes;
+        sp0[r] = U.base + so + static_cast<int64_t>(rv[r] ? o : 0) * sc_row;
       }
-      for (int m0 = 0; m0 < U.M; m0 += TM) {
-        const int mcount = min(TM, U.M - m0);
-        int tok[TM], hrow[TM];
-        float wt[TM];
+      float pm[kRowsPerItem][TM];
+#pragma unroll
+      for (int r = 0; r < kRowsPerItem; ++r)
+#pragma unroll
+        for (int m = 0; m < TM; ++m) pm[r][m] = 0.f;
+      for (int c = lane; c < nch; c += 32) {
+        uint4 wv[kRowsPerItem];
+        unsigned short sv[kRowsPerItem];
+        if (c == lane) {
+#pragma unroll
+          for (int r = 0; r < kRowsPerItem; ++r) {
+            wv[r] = w[b][r];
+            sv[r] = sb[b][r];
+          }
+        } else {
+#pragma unroll
+          for (int r = 0; r < kRowsPerItem; ++r) {
+            const uint8_t* qp = q[r] + c * 16;
+            const uint8_t* sp = sp0[r] + (Q == MOE_Q8_0 ? (c >> 1) : c) * 2;
+            wv[r] = !rv[r] ? make_uint4(0, 0, 0, 0) : (U.miss ? ld_host(qp) : ldg_stream(qp));
+            sv[r] = !rv[r] ? 0 : (U.miss ? ld_scale_host_bits(sp) : __ldg(reinterpret_cast<const unsigned short*>(sp)));
+          }
+        }
+        if (U.miss) {
+#pragma unroll
+          for (int r = 0; r < kRowsPerItem; ++r) {
+            if (!rv[r]) continue;
+            *reinterpret_cast<uint4*>(U.dst + (q[r] - U.base) + c * 16) = wv[r];
+            if (owns_scale<Q>(c))
+              *reinterpret_cast<unsigned short*>(U.dst + (sp0[r] - U.base) + (Q == MOE_Q8_0 ? (c >> 1) : c) * 2) = sv[r];
+          }
+        }
+        float dv[kRowsPerItem];
+#pragma unroll
+        for (int r = 0; r < kRowsPerItem; ++r) dv[r] = __half2float(__ushort_as_half(sv[r]));
 #pragma unroll
         for (int m = 0; m < TM; ++m) {
           if (m < mcount) {
-            if (U.p0 >= 0) {
-              hrow[m] = U.p0 + m0 + m;
-              tok[m] = __ldg(a.plan.perm_tok + hrow[m]);
-              wt[m] = __ldg(a.plan.perm_w + hrow[m]);
+            const float* hr = hs + hrow[m] * ldh;
+            if (Q == MOE_Q8_0) {
+              float hv[16];
+              load_chunk16(hr, c, hv);
+#pragma unroll
+              for (int r = 0; r < kRowsPerItem; ++r) pm[r][m] = fmaf(dv[r], dot_q8(wv[r], hv), pm[r][m]);
             } else {
-              hrow[m] = A + m0 + m;
-              tok[m] = m0 + m;
-              wt[m] = 1.0f;
-            }
-          } else {
-            hrow[m] = 0;
-            tok[m] = 0;
-            wt[m] = 0.f;
-          }
-        }
-        float pm[kRowsPerItem][TM];
+              float hl[16], hh[16];
+              load_chunk16(hr, 2 * c, hl);
+              load_chunk16(hr, 2 * c + 1, hh);
 #pragma unroll
-        for (int r = 0; r < kRowsPerItem; ++r)
-#pragma unroll
-          for (int m = 0; m < TM; ++m) pm[r][m] = 0.f;
-#pragma unroll 2
-        for (int c = lane; c < nch; c += 32) {
-          uint4 w[kRowsPerItem];
-          float d[kRowsPerItem];
-          if (U.miss) {
-            unsigned short sb[kRowsPerItem];
-#pragma unroll
-            for (int r = 0; r < kRowsPerItem; ++r) {
-              w[r] = rv[r] ? ld_host(q[r] + c * 16) : make_uint4(0, 0, 0, 0);
-              sb[r] = rv[r] ? ld_scale_host_bits(s[r] + (Q == MOE_Q8_0 ? (c >> 1) : c) * 2) : 0;
-            }
-#pragma unroll
-            for (int r = 0; r < kRowsPerItem; ++r) {
-              d[r] = __half2float(__ushort_as_half(sb[r]));
-              if (rv[r] && m0 == 0) {
-                *reinterpret_cast<uint4*>(U.dst + (q[r] - U.base) + c * 16) = w[r];
-                if (owns_scale<Q>(c))
-                  *reinterpret_cast<unsigned short*>(U.dst + (s[r] - U.base) + (Q == MOE_Q8_0 ? (c >> 1) : c) * 2) = sb[r];
-              }
-            }
-          } else {
-#pragma unroll
-            for (int r = 0; r < kRowsPerItem; ++r) {
-              w[r] = rv[r] ? ldg_stream(q[r] + c * 16) : make_uint4(0, 0, 0, 0);
-              d[r] = rv[r] ? ld_scale(s[r] + (Q == MOE_Q8_0 ? (c >> 1) : c) * 2) : 0.f;
-            }
-          }
-#pragma unroll
-          for (int m = 0; m < TM; ++m) {
-            if (m < mcount) {
-              const float* hr = hs + hrow[m] * ldh;
-              if (Q == MOE_Q8_0) {
-                float hv[16];
-                load_chunk16(hr, c, hv);
-#pragma unroll
-                for (int r = 0; r < kRowsPerItem; ++r) pm[r][m] = fmaf(d[r], dot_q8(w[r], hv), pm[r][m]);
-              } else {
-                float hl[16], hh[16];
-                load_chunk16(hr, 2 * c, hl);
-                load_chunk16(hr, 2 * c + 1, hh);
-#pragma unroll
-                for (int r = 0; r < kRowsPerItem; ++r)
-                  pm[r][m] = fmaf(d[r], dot_q4(w[r], hl, hh), pm[r][m]);
-              }
+              for (int r = 0; r < kRowsPerItem; ++r) pm[r][m] = fmaf(dv[r], dot_q4(wv[r], hl, hh), pm[r][m]);
             }
           }
         }
-        if (!ok) break;
+      }
+      // a slot that does not hold the expected generation is refused
+      const bool ok = U.miss ? true : (routed ? (U.slot < a.S && gb[b] == U.egen) : a.shared != nullptr);
+      float acc[kRowsPerItem][TM];
+#pragma unroll
+      for (int r = 0; r < kRowsPerItem; ++r)
+#pragma unroll
+        for (int t = 0; t < TM; ++t) acc[r][t] = 0.f;
+      if (ok) {
         // weight by the combine weight, accumulate per token (T <= TM)
 #pragma unroll
         for (int m = 0; m < TM; ++m) {
@@ -452,37 +604,31 @@ __global__ void __launch_bounds__(kThreads) down_kernel(FfnArgs a) {
                 for (int r = 0; r < kRowsPerItem; ++r) acc[r][t] = fmaf(wt[m], pm[r][m], acc[r][t]);
           }
         }
+      } else if (lane == 0) {
+        atomicOr(a.err, MOE_DEVERR_STALE);
       }
-    }
-    if (!ok) {
-      if (lane == 0) atomicOr(a.err, MOE_DEVERR_STALE);
 #pragma unroll
       for (int r = 0; r < kRowsPerItem; ++r)
 #pragma unroll
-        for (int m = 0; m < TM; ++m) acc[r][m] = 0.f;
-    }
+        for (int m = 0; m < TM; ++m)
 #pragma unroll
-    for (int r = 0; r < kRowsPerItem; ++r)
+          for (int off = 16; off; off >>= 1) acc[r][m] += __shfl_xor_sync(0xffffffffu, acc[r][m], off);
+      if (lane == 0) {
 #pragma unroll
-      for (int m = 0; m < TM; ++m)
+        for (int r = 0; r < kRowsPerItem; ++r)
 #pragma unroll
-        for (int off = 16; off; off >>= 1) acc[r][m] += __shfl_xor_sync(0xffffffffu, acc[r][m], off);
-    if (lane == 0) {
-#pragma unroll
-      for (int r = 0; r < kRowsPerItem; ++r)
-#pragma unroll
-        for (int m = 0; m < TM; ++m) part[(it * kRowsPerItem + r) * TM + m] = acc[r][m];
+          for (int m = 0; m < TM; ++m) part[(u * rpb + rp * kRowsPerItem + r) * TM + m] = acc[r][m];
+      }
     }
   }
   __syncthreads();
   // y[t][o] = sum over units in order
-  for (int i = tid; i < kDownRows * T; i += kThreads) {
+  for (int i = tid; i < rpb * T; i += kDownThreads) {
     const int r = i / T, t = i - r * T;
     const int o = o0 + r;
     if (o >= a.H) continue;
-    const int rp = r / kRowsPerItem, rr = r - rp * kRowsPerItem;
     float v = 0.f;
-    for (int u = 0; u < units; ++u) v += part[((u * kPairs + rp) * kRowsPerItem + rr) * TM + t];
+    for (int u = 0; u < units; ++u) v += part[(u * rpb + r) * TM + t];
     a.y[static_cast<int64_t>(t) * a.H + o] = v;
   }
   if (a.store) {
@@ -496,7 +642,7 @@ __global__ void __launch_bounds__(kThreads) down_kernel(FfnArgs a) {
     if (s_ticket == gridDim.x - 1) {
       __threadfence();
       int nmiss = 0;
-      for (int u = tid; u < units; u += kThreads) {
+      for (int u = tid; u < units; u += kDownThreads) {
         const int sl = __ldg(a.units + kUnitHeader + kUnitInts * u);
         if (sl <= -2 && -2 - sl < a.S) {
           a.gen[-2 - sl] = __ldcg(a.sgen + (-2 - sl));
@@ -521,8 +667,10 @@ cudaError_t launch_tm(const FfnArgs& a, int num_sms, cudaStream_t st) {
   const int A = a.T * a.k;
   const int nrows = A + (a.shared ? a.T : 0);
   const int max_units = std::min(a.E, A) + (a.shared ? 1 : 0);
-  const size_t smem2 = sizeof(float) * (static_cast<size_t>(nrows) * a.ldh +
-                                        static_cast<size_t>(max_units) * kDownRows * TM);
+  // down: one block per SM, an even number of output rows each
+  const int rpb = std::max(2, ((a.H + num_sms - 1) / num_sms + 1) & ~1);
+  const int grid2 = (a.H + rpb - 1) / rpb;
+  const size_t smem2 = down_smem(nrows, a.ldh, max_units, rpb, TM, A).total;
   if (smem1 > 220 * 1024 || smem2 > 220 * 1024) return cudaErrorInvalidValue;
   cudaError_t err;
   if (a.xt == MOE_BF16) {
@@ -545,9 +693,8 @@ cudaError_t launch_tm(const FfnArgs& a, int num_sms, cudaStream_t st) {
   if (err == cudaSuccess) err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   if (a.ev[1]) cudaEventRecord(a.ev[1], st);
-  const int grid2 = (a.H + kDownRows - 1) / kDownRows;
   if (a.ev[2]) cudaEventRecord(a.ev[2], st);
-  err = pdl_launch(down_kernel<Q, TM>, dim3(grid2), dim3(kThreads), smem2, st, a);
+  err = pdl_launch(down_kernel<Q, TM>, dim3(grid2), dim3(kDownThreads), smem2, st, a, rpb);
   if (a.ev[3]) cudaEventRecord(a.ev[3], st);
   return err != cudaSuccess ? err : cudaGetLastError();
 }
