@@ -2100,14 +2100,42 @@ __global__ void __launch_bounds__(1024) plan_scan_kernel(PlanArgs a, int* local,
   for (int e = threadIdx.x; e < E; e += 1024) cur[e] = cnt[e];
   __syncthreads();
   const int total = block_exclusive_scan<1024>(cur, E, scratch);
-  for (int e = threadIdx.x; e < E; e += 1024) {
-    a.plan.offsets[e] = cur[e];
+  for (int e = threadIdx.x; e < E; e += 1024) a.plan.offsets[e] = cur[e];
+  // each expert's per-block counts become per-block offsets: G threads per
+  // expert each take a run of blocks (loads batched ahead of the stores)
+  constexpr int kB = 8;
+  const int G = max(1, 1024 / E);
+  const int seg = (nb + G - 1) / G;
+  int* segsum = sm + 2 * E + 33;  // [G][E]
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < G * E; idx += 1024) {
+    const int e = idx % E, g = idx / E;
+    const int b0 = g * seg, b1 = min(nb, b0 + seg);
+    int sum = 0;
+    for (int b = b0; b < b1; b += kB) {
+      int v[kB];
+#pragma unroll
+      for (int j = 0; j < kB; ++j) v[j] = b + j < b1 ? __ldcg(local + static_cast<size_t>(b + j) * E + e) : 0;
+#pragma unroll
+      for (int j = 0; j < kB; ++j) sum += v[j];
+    }
+    segsum[g * E + e] = sum;
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < G * E; idx += 1024) {
+    const int e = idx % E, g = idx / E;
+    const int b0 = g * seg, b1 = min(nb, b0 + seg);
     int run = cur[e];
-    for (int b = 0; b < nb; ++b) {
-      int* p = local + static_cast<size_t>(b) * E + e;
-      const int v = *p;
-      *p = run;
-      run += v;
+    for (int g2 = 0; g2 < g; ++g2) run += segsum[g2 * E + e];
+    for (int b = b0; b < b1; b += kB) {
+      int v[kB];
+#pragma unroll
+      for (int j = 0; j < kB; ++j) v[j] = b + j < b1 ? __ldcg(local + static_cast<size_t>(b + j) * E + e) : 0;
+#pragma unroll
+      for (int j = 0; j < kB; ++j) {
+        if (b + j < b1) local[static_cast<size_t>(b + j) * E + e] = run;
+        run += v[j];
+      }
     }
   }
   if (threadIdx.x == 0) a.plan.offsets[E] = total;
@@ -2174,7 +2202,7 @@ cudaError_t launch_plan_large(const PlanArgs& a, int* local, cudaStream_t st) {
   cudaError_t e = cudaMemsetAsync(a.plan.counts, 0, sizeof(int32_t) * a.E, st);
   if (e != cudaSuccess) return e;
   plan_count_kernel<<<nb, kPB, sizeof(int) * a.E, st>>>(a, local);
-  plan_scan_kernel<<<1, 1024, sizeof(int) * (2 * a.E + 33), st>>>(a, local, nb);
+  plan_scan_kernel<<<1, 1024, sizeof(int) * (2 * a.E + 33 + std::max(a.E, 1024)), st>>>(a, local, nb);
   plan_scatter_kernel<<<nb, kPB, sizeof(int) * 8 * a.E, st>>>(a, local);
   return cudaGetLastError();
 }
