@@ -7,7 +7,7 @@ it fails if the library has not been built.
 """
 from . import _native
 from ._native import Q8_0, Q4_0, LRU, RANDOM, F32, BF16, MODE_AUTO, MODE_DECODE, MODE_PREFILL
-from .api import Context, Plan, Slots, Misses, MoeError, splitmix64
+from .api import Context, Plan, Slots, Misses, MoeError, splitmix64, static_budget
 
-__all__ = ["Context", "Plan", "Slots", "Misses", "MoeError", "splitmix64", "Q8_0", "Q4_0", "LRU",
+__all__ = ["Context", "Plan", "Slots", "Misses", "MoeError", "splitmix64", "static_budget", "Q8_0", "Q4_0", "LRU",
            "RANDOM", "F32", "BF16", "MODE_AUTO", "MODE_DECODE", "MODE_PREFILL"]

@@ -50,6 +50,12 @@ class Stats(C.Structure):
                 ("uncertified_repairs", C.c_int64)]
 
 
+class Budget(C.Structure):
+    _fields_ = [("common_bytes", C.c_int64), ("expert_bytes", C.c_int64), ("kv_bytes", C.c_int64),
+                ("overhead_bytes", C.c_int64), ("lower_bound", C.c_int64), ("footprint", C.c_int64),
+                ("slots_per_layer", C.c_int32), ("accepted", C.c_int32)]
+
+
 def _load():
     if not os.path.exists(_LIB_PATH):
         raise ImportError(
@@ -98,6 +104,8 @@ SIGNATURES = [
     ("moe_slots_read", _st, [_vp, C.POINTER(_i32), C.POINTER(C.c_uint32)]),
     ("moe_slots_stats", _st, [_vp, C.POINTER(Stats)]),
     ("moe_splitmix64_next", _u64, [C.POINTER(_u64)]),
+    ("moe_static_budget", _st, [_i32, _i32, C.c_int64, C.c_int64, C.c_int64, C.c_int64, C.c_int64, C.c_int64,
+                                C.c_int64, C.POINTER(Budget)]),
 ]
 
 for _name, _res, _args in SIGNATURES:

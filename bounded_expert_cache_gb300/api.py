@@ -248,6 +248,17 @@ class Slots:
         return {f: getattr(s, f) for f, _ in N.Stats._fields_}
 
 
+def static_budget(n_layers, n_experts, payload_bytes, cache_ppm, common_bytes=0, kv_bytes_per_token=0,
+                  context=0, overhead_bytes=0, target_bytes=0) -> dict:
+    """Static budget check before serving (moe_static_budget): the lower
+    bound C + E(p) + K(n), the footprint with the overhead, the slots per
+    layer and whether the row fits the target."""
+    b = N.Budget()
+    _check(lib.moe_static_budget(n_layers, n_experts, payload_bytes, cache_ppm, common_bytes,
+                                 kv_bytes_per_token, context, overhead_bytes, target_bytes, C.byref(b)))
+    return {f: getattr(b, f) for f, _ in N.Budget._fields_}
+
+
 def splitmix64(state: int, n: int) -> List[int]:
     s = C.c_uint64(state)
     return [lib.moe_splitmix64_next(C.byref(s)) for _ in range(n)]

@@ -350,6 +350,31 @@ moe_status_t moe_slots_stats(const moe_slots_t* s, moe_stats_t* out);
 /* Next output of SplitMix64 from state *state (advanced in place). */
 uint64_t moe_splitmix64_next(uint64_t* state);
 
+/* ---------------------------------------------------------------- budget
+ * Static budget check before serving ([MF] §IV-D): the lower bound
+ * L(p, n) = C + E(p) + K(n) of the footprint F(p, n) = L(p, n) + O, with C
+ * the resident common tensor bytes, E(p) the expert-cache budget at cache
+ * fraction p, K(n) the KV-cache bytes at context n and O the runtime
+ * overhead. A row whose lower bound exceeds the serving target is rejected
+ * (accepted = 0), which is a result, not an error. p is given in parts per
+ * million; E(p) = floor(p * layers * experts * payload_bytes); the slots of
+ * a layer are floor(p * experts); K(n) = kv_bytes_per_token * n. Host only,
+ * no CUDA call. Errors: MOE_ERR_ARG for a negative input, p above 10^6 or a
+ * byte count that overflows int64. */
+typedef struct {
+  int64_t common_bytes;    /* C */
+  int64_t expert_bytes;    /* E(p) */
+  int64_t kv_bytes;        /* K(n) */
+  int64_t overhead_bytes;  /* O */
+  int64_t lower_bound;     /* L(p, n) */
+  int64_t footprint;       /* F(p, n) */
+  int32_t slots_per_layer; /* floor(p * experts) */
+  int32_t accepted;        /* 1 if L(p, n) <= target_bytes */
+} moe_budget_t;
+moe_status_t moe_static_budget(int32_t n_layers, int32_t n_experts, int64_t payload_bytes, int64_t cache_ppm,
+                               int64_t common_bytes, int64_t kv_bytes_per_token, int64_t context,
+                               int64_t overhead_bytes, int64_t target_bytes, moe_budget_t* out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -38,6 +38,7 @@ from .route import router_logits, topk_select, combine_weights, route
 from .plan import plan_union
 from .splitmix import SplitMix64
 from .cache import SlotCache, CapacityError, LRU, RANDOM, slot_count
+from .budget import static_budget
 from .ffn import silu, expert_ffn, moe_layer
 from .tiles import tile_partition
 
