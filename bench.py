@@ -270,7 +270,9 @@ def run_ours(args, rank, world, dev):
 
     tokens = args.steps * T * world
     value = tokens / (elapsed_ms / 1e3)
-    extra = {"h2d_copy_engine_gbs": h2d_bandwidth(torch, dev),
+    policy_replay = replay_policies(bec, w, routers, x_dev, n_steps, dev) if rank == 0 else None
+    extra = {"policy_replay": policy_replay,
+             "h2d_copy_engine_gbs": h2d_bandwidth(torch, dev),
              "per_call_launch_tokens_per_s": round(tokens / (events_ms / 1e3), 2),
              "graph": used_graph}
     if not args.skip_e2e:
@@ -317,6 +319,52 @@ def run_ours(args, rank, world, dev):
     ctx.close()
     e2e_value = tokens / (e2e_ms / 1e3)
     return finish(args, w, world, value, elapsed_ms, e2e_value, kt, st0, st1, clk, extra), w
+
+
+def replay_policies(bec, w, routers, x_dev, n_steps, dev):
+    """The decode trace's routing (the library's router, bit-exact with the
+    oracle) replayed per layer under every cache policy on the host: LRU,
+    seeded random (seeds 0-4, mean), farthest next use (the offline bound)
+    and static working sets of 16 and 20 experts learned on the first
+    quarter of the steps."""
+    import torch
+    L, T, E, k = w.n_layers, w.tokens_per_step, w.n_experts, w.top_k
+    # routing only: one slot per layer keeps the context's pool small
+    ctx = bec.Context(L, E, k, w.hidden, w.inter, w.shared_inter, w.quant, 1, w.policy, 3, 0, 262144, T)
+    idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+    wt = torch.empty((T, k), dtype=torch.float32, device=dev)
+    traces = []
+    for l in range(L):
+        steps = []
+        for s in range(n_steps):
+            ctx.route(l, x_dev[l, s * T:(s + 1) * T], routers[l], None, idx, wt)
+            sel = idx.cpu().numpy().reshape(-1)
+            counts = [0] * E
+            for e in sel:
+                counts[int(e)] += 1
+            steps.append((sorted(set(int(e) for e in sel)), counts))
+        traces.append(steps)
+    ctx.close()
+    calib = n_steps // 4
+    runs = {"lru": [(bec.LRU, {})], "random_mean_5_seeds": [(bec.RANDOM, dict(seed=s)) for s in range(5)],
+            "farthest_next_use": [(bec.FARTHEST_NEXT_USE, {})],
+            "static_16": [(bec.STATIC_SET, dict(width=16, calib=calib))],
+            "static_20": [(bec.STATIC_SET, dict(width=20, calib=calib))]}
+    out = {}
+    for name, variants in runs.items():
+        hits = misses = 0
+        for policy, kw in variants:
+            for l in range(L):
+                r = bec.replay(policy, E, w.slots, traces[l], payload=w.payload_bytes, layer=l, **kw)
+                hits += r["hits"]
+                misses += r["misses"]
+        n = len(variants)
+        out[name] = {"hit_rate": round(hits / max(1, hits + misses), 4),
+                     "misses_per_step": round(misses / n / n_steps, 2),
+                     "miss_gb_per_step": round(misses / n / n_steps * w.payload_bytes / 1e9, 4)}
+    out["trace"] = (f"{L} layers x {n_steps} decode steps of the bench workload, {w.slots} slots per layer; "
+                    f"static sets learned on the first {calib} steps")
+    return out
 
 
 def run_prefill(args, dev):

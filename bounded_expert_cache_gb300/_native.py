@@ -16,7 +16,7 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_ARG", 2: "MOE_ERR_CUDA", 3: "MOE_ERR_CA
                 4: "MOE_ERR_STALE", 5: "MOE_ERR_TIMEOUT", 6: "MOE_ERR_UNCERTIFIED",
                 7: "MOE_ERR_STATE"}
 Q8_0, Q4_0 = 0, 1
-LRU, RANDOM = 0, 1
+LRU, RANDOM, FARTHEST_NEXT_USE, STATIC_SET = 0, 1, 2, 3
 F32, BF16 = 0, 1
 MODE_AUTO, MODE_DECODE, MODE_PREFILL = 0, 1, 2
 KERNEL_KINDS = ("route", "plan", "ffn_gateup", "ffn_down", "stage_copy")
@@ -104,6 +104,8 @@ SIGNATURES = [
     ("moe_slots_read", _st, [_vp, C.POINTER(_i32), C.POINTER(C.c_uint32)]),
     ("moe_slots_stats", _st, [_vp, C.POINTER(Stats)]),
     ("moe_splitmix64_next", _u64, [C.POINTER(_u64)]),
+    ("moe_replay", _st, [_i32, _i32, _i32, _u64, _i32, C.c_int64, _i32, _i32, _i32, C.POINTER(_i32),
+                         C.POINTER(_i32), C.POINTER(_i32), C.POINTER(Stats)]),
     ("moe_static_budget", _st, [_i32, _i32, C.c_int64, C.c_int64, C.c_int64, C.c_int64, C.c_int64, C.c_int64,
                                 C.c_int64, C.POINTER(Budget)]),
 ]

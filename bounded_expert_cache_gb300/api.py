@@ -248,6 +248,25 @@ class Slots:
         return {f: getattr(s, f) for f, _ in N.Stats._fields_}
 
 
+def replay(policy, n_experts, n_slots, steps, payload=0, seed=0, layer=0, width=0, calib=0) -> dict:
+    """Offline replay of one layer's steps (moe_replay); steps: a list of
+    (union, counts[E]) as for Slots.step. Returns the counters."""
+    offs, ex, cn = [0], [], []
+    for uniq, counts in steps:
+        for e in uniq:
+            ex.append(int(e))
+            cn.append(int(counts[int(e)]))
+        offs.append(len(ex))
+    n = len(steps)
+    o = (C.c_int32 * (n + 1))(*offs)
+    e_arr = (C.c_int32 * max(1, len(ex)))(*ex)
+    c_arr = (C.c_int32 * max(1, len(cn)))(*cn)
+    st = N.Stats()
+    _check(lib.moe_replay(policy, n_experts, n_slots, seed, layer, payload, width, calib, n, o, e_arr, c_arr,
+                          C.byref(st)))
+    return {f: getattr(st, f) for f, _ in N.Stats._fields_}
+
+
 def static_budget(n_layers, n_experts, payload_bytes, cache_ppm, common_bytes=0, kv_bytes_per_token=0,
                   context=0, overhead_bytes=0, target_bytes=0) -> dict:
     """Static budget check before serving (moe_static_budget): the lower

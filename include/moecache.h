@@ -61,7 +61,10 @@ typedef enum {
 } moe_status_t;
 
 typedef enum { MOE_Q8_0 = 0, MOE_Q4_0 = 1 } moe_quant_t;
-typedef enum { MOE_LRU = 0, MOE_RANDOM = 1 } moe_policy_t;
+/* Policies of a context: LRU and seeded random. The other two exist for
+ * offline replays only (moe_replay): farthest next use needs the future
+ * route trace, and the static working set is a fixed resident set. */
+typedef enum { MOE_LRU = 0, MOE_RANDOM = 1, MOE_FARTHEST_NEXT_USE = 2, MOE_STATIC_SET = 3 } moe_policy_t;
 typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype_t;
 typedef enum { MOE_MODE_AUTO = 0, MOE_MODE_DECODE = 1, MOE_MODE_PREFILL = 2 } moe_mode_t;
 
@@ -349,6 +352,29 @@ moe_status_t moe_slots_stats(const moe_slots_t* s, moe_stats_t* out);
 
 /* Next output of SplitMix64 from state *state (advanced in place). */
 uint64_t moe_splitmix64_next(uint64_t* state);
+
+/* ---------------------------------------------------------------- replay
+ * Offline replay of one layer's step sequence under a cache policy, for
+ * comparing policies on a fixed route trace ([RT] §2 farthest-next-use as
+ * the offline paging reference, §5.1 fixed replays; [NfE] §5.6, §7.4 a
+ * learned static working set). Step t's union is experts[offsets[t] ..
+ * offsets[t+1]) (distinct ids, any order) with counts[i] assignments of
+ * experts[i]; the union is pinned during its step. MOE_LRU and MOE_RANDOM
+ * behave as moe_slots_step (seed, layer). MOE_FARTHEST_NEXT_USE: a miss
+ * (ascending id after the hits) takes the lowest free slot, else evicts the
+ * resident expert outside the union whose next step of use is the farthest
+ * (never again is farthest; ties to the lower slot). MOE_STATIC_SET: the
+ * width experts with the most assignments over the first calib steps (ties
+ * to the lower id) are resident before the first step and never evicted;
+ * every other expert of a step is a miss that is not admitted. Fills *out
+ * (steps, hits = assignments - misses, misses, evictions, materialised =
+ * misses x payload_bytes). Host only. Errors: MOE_ERR_ARG for bad input,
+ * MOE_ERR_CAPACITY when a union exceeds the slots (random, farthest next
+ * use) or width exceeds them. */
+moe_status_t moe_replay(int32_t policy, int32_t n_experts, int32_t n_slots, uint64_t seed, int32_t layer,
+                        int64_t payload_bytes, int32_t width, int32_t calib, int32_t n_steps,
+                        const int32_t* offsets, const int32_t* experts, const int32_t* counts,
+                        moe_stats_t* out);
 
 /* ---------------------------------------------------------------- budget
  * Static budget check before serving ([MF] §IV-D): the lower bound

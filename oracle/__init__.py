@@ -39,6 +39,7 @@ from .plan import plan_union
 from .splitmix import SplitMix64
 from .cache import SlotCache, CapacityError, LRU, RANDOM, slot_count
 from .budget import static_budget
+from .replay import replay, static_set, FARTHEST_NEXT_USE, STATIC_SET
 from .ffn import silu, expert_ffn, moe_layer
 from .tiles import tile_partition
 
