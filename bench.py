@@ -36,9 +36,6 @@ import numpy as np  # noqa: E402
 import workloads as W  # noqa: E402
 
 WORKLOAD = "decode"
-# admission mode of the headline: 2 = on-device admission, misses read
-# through by the FFN kernels (1 = separate staging kernel, 0 = host)
-HEADLINE_MODE = 2
 METRIC = "MoE-layer tokens/s at 1 GB300; achieved HBM GB/s (decode) & TFLOP/s (prefill)"
 
 
@@ -166,7 +163,7 @@ def run_ours(args, rank, world, dev):
     x_pin = torch.from_numpy(x_host.view(np.int16)).view(torch.bfloat16).pin_memory()
     x_dev = x_pin.to(dev)
 
-    def make_ctx(device_admit=HEADLINE_MODE):
+    def make_ctx(device_admit):
         ctx = bec.Context(L, E, k, H, w.inter, w.shared_inter, w.quant, w.slots, w.policy, 3, 0,
                           262144, T, admit_on_device=device_admit)
         ctx.bind_store(store)
@@ -196,12 +193,13 @@ def run_ours(args, rank, world, dev):
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         return float(t.item())
 
-    def timed(fn):
-        """Run fn(s) for the timed steps between CUDA events; max over ranks."""
+    def timed(fn, n_timed=None):
+        """Run fn(s) for the timed steps (or the first n_timed of them)
+        between CUDA events; max over ranks."""
         ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         barrier()
         ev0.record(stream)
-        for s in range(args.warmup, n_steps):
+        for s in range(args.warmup, n_steps if n_timed is None else args.warmup + n_timed):
             fn(s)
         ev1.record(stream)
         barrier()
@@ -209,7 +207,7 @@ def run_ours(args, rank, world, dev):
 
     x_step = torch.empty((L, T, H), dtype=torch.bfloat16, device=dev)
 
-    def graph_pass(mode, sample_clocks):
+    def graph_pass(mode, sample_clocks, n_timed=None):
         """Device-resident inputs, on-device admission, the 40-layer step
         replayed as one CUDA graph; returns (ms, clocks, stats, used_graph)."""
         ctx = make_ctx(mode)
@@ -236,7 +234,7 @@ def run_ours(args, rank, world, dev):
         clocks = ClockSampler(dev.index if dev.index is not None else 0) if sample_clocks else None
         if clocks:
             clocks.start()
-        ms = timed(graph_step if graph is not None else (lambda s: step(ctx, s)))
+        ms = timed(graph_step if graph is not None else (lambda s: step(ctx, s)), n_timed)
         clk = clocks.stop() if clocks else None
         ctx.check_device_errors()
         st = ctx.stats()
@@ -245,9 +243,21 @@ def run_ours(args, rank, world, dev):
         ctx.close()
         return ms, clk, st, used
 
-    # ---- pass 1 (headline): read-through misses (the FFN reads a missed
-    # expert from the pinned store over the host link and writes its slot)
-    elapsed_ms, clk, st_graph, used_graph = graph_pass(args.admission, True)
+    # ---- the miss path of the headline: both on-device admission modes give
+    # bitwise the same outputs and counters; which is faster depends on the
+    # host link's state on this machine, so a short graph run of each picks it
+    # (unless --admission fixes it). 2: read-through (the FFN kernels read a
+    # missed expert from the pinned store and write its slot); 1: the
+    # staging kernel copies the misses before the FFN.
+    probe = None
+    mode = args.admission
+    if mode == 0:
+        n_probe = min(16, args.steps)
+        probe = {m: round(n_probe * T * world / (graph_pass(m, False, n_probe)[0] / 1e3), 2) for m in (2, 1)}
+        mode = max(probe, key=lambda m: probe[m])
+
+    # ---- pass 1 (headline)
+    elapsed_ms, clk, st_graph, used_graph = graph_pass(mode, True)
 
     # ---- pass 2: the same steps, launched call by call with library-side
     # CUDA events around every kernel (roofline and kernel breakdown), with
@@ -271,7 +281,10 @@ def run_ours(args, rank, world, dev):
     tokens = args.steps * T * world
     value = tokens / (elapsed_ms / 1e3)
     policy_replay = replay_policies(bec, w, routers, x_dev, n_steps, dev) if rank == 0 else None
-    extra = {"policy_replay": policy_replay,
+    extra = {"admission_mode": {2: "read-through", 1: "staging kernel"}[mode],
+             "admission_probe_tokens_per_s": None if probe is None else
+             {"read-through": probe[2], "staging kernel": probe[1]},
+             "policy_replay": policy_replay,
              "h2d_copy_engine_gbs": h2d_bandwidth(torch, dev),
              "per_call_launch_tokens_per_s": round(tokens / (events_ms / 1e3), 2),
              "graph": used_graph}
@@ -280,8 +293,10 @@ def run_ours(args, rank, world, dev):
         # staging kernel (graph replay), and admission plus tile staging on
         # the host with cudaMemcpyAsync on three streams (one sync per layer,
         # call by call)
-        k_ms, _, _, _ = graph_pass(1, False)
-        extra["staging_kernel_tokens_per_s"] = round(tokens / (k_ms / 1e3), 2)
+        other = 1 if mode == 2 else 2
+        k_ms, _, _, _ = graph_pass(other, False)
+        extra["staging_kernel_tokens_per_s"] = round(tokens / ((k_ms if other == 1 else elapsed_ms) / 1e3), 2)
+        extra["read_through_tokens_per_s"] = round(tokens / ((k_ms if other == 2 else elapsed_ms) / 1e3), 2)
         ctx = make_ctx(device_admit=0)
         for s in range(args.warmup):
             step(ctx, s)
@@ -289,7 +304,7 @@ def run_ours(args, rank, world, dev):
         ctx.close()
         extra["host_admission_tokens_per_s"] = round(tokens / (m_ms / 1e3), 2)
     if args.skip_e2e:
-        return finish(args, w, world, value, elapsed_ms, None, kt, st0, st1, clk, extra), w
+        return finish(args, w, world, value, elapsed_ms, None, kt, st0, st1, clk, extra, mode), w
     # ---- pass 4: end to end through host buffers: every step copies its 40
     # layers' inputs from pinned host memory, runs the step through the
     # public API (moe_layer_forward per layer, captured once as a CUDA graph
@@ -298,7 +313,7 @@ def run_ours(args, rank, world, dev):
     x_e2e = torch.empty((L, T, H), dtype=torch.bfloat16, device=dev)
     x_steps = x_pin.view(L, n_steps, T, H).transpose(0, 1).contiguous().pin_memory()  # [steps][L][T][H]
     y_host = torch.empty((L, T, H), dtype=torch.float32).pin_memory()
-    ctx = make_ctx()
+    ctx = make_ctx(mode)
     for s in range(args.warmup - 1):
         step(ctx, s)
     g = torch.cuda.CUDAGraph()
@@ -318,7 +333,7 @@ def run_ours(args, rank, world, dev):
     del g
     ctx.close()
     e2e_value = tokens / (e2e_ms / 1e3)
-    return finish(args, w, world, value, elapsed_ms, e2e_value, kt, st0, st1, clk, extra), w
+    return finish(args, w, world, value, elapsed_ms, e2e_value, kt, st0, st1, clk, extra, mode), w
 
 
 def replay_policies(bec, w, routers, x_dev, n_steps, dev):
@@ -529,7 +544,7 @@ def h2d_bandwidth(torch, dev):
     return round(best, 1)
 
 
-def finish(args, w, world, value, elapsed_ms, e2e_value, kt, st0, st1, clk, extra):
+def finish(args, w, world, value, elapsed_ms, e2e_value, kt, st0, st1, clk, extra, mode):
     L, T, E, k, H = w.n_layers, w.tokens_per_step, w.n_experts, w.top_k, w.hidden
     # roofline of the dominant kernel (ffn gate/up): algorithmic bytes per
     # launch = (k routed + 1 shared) units x (gate + up) Q8_0 matrices + x + h
@@ -580,10 +595,12 @@ def finish(args, w, world, value, elapsed_ms, e2e_value, kt, st0, st1, clk, extr
                   "bytes_staged": staged,
                   "staging_gbs_avg_over_step": round(staged / (elapsed_ms / 1e3) / 1e9, 2),
                   "miss_bytes_per_step": round(staged / args.steps),
-                  "admission": "on device (router's last block); a miss is read by the FFN kernels "
-                               "from the pinned store over the host link and written into its slot "
-                               "(read-through); the slot's generation is published once every tile "
-                               "of it has landed"},
+                  "admission": "on device (router's last block); " + (
+                      "a miss is read by the FFN kernels from the pinned store over the host link and "
+                      "written into its slot (read-through)" if mode == 2 else
+                      "the staging kernel copies the misses from the pinned store into their slots "
+                      "before the FFN") + "; the slot's generation is published once every tile of it "
+                      "has landed"},
         **extra,
         "gpu_launches": launches,
         "uncertified_repairs": st1["uncertified_repairs"] - st0["uncertified_repairs"],
@@ -613,8 +630,9 @@ def main():
     ap.add_argument("--skip-long-prefill", action="store_true", help="skip the long-prefill (waves) pass")
     ap.add_argument("--long-prefill-only", action="store_true", help="profiling: only the long-prefill pass")
     ap.add_argument("--prefill-tokens", type=int, default=0, help="profiling: tokens of the prefill chunk")
-    ap.add_argument("--admission", type=int, default=HEADLINE_MODE, choices=[1, 2],
-                    help="profiling: miss path of the headline pass (2 read-through, 1 staging kernel)")
+    ap.add_argument("--admission", type=int, default=0, choices=[0, 1, 2],
+                    help="miss path of the headline pass (0: the faster of a short run of each; "
+                         "2 read-through, 1 staging kernel)")
     args = ap.parse_args()
     assert args.warmup >= 3
 
