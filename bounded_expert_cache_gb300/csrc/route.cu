@@ -1013,6 +1013,150 @@ __host__ __device__ constexpr bool fast_tail_ok(int T, int k, int E) {
   return T * k <= 32 && E <= 256 && T * E <= 2048;
 }
 
+// LRU admission of one token's selection by one warp (the shared-memory
+// cache state copied when the router started): the r-th miss in ascending id
+// takes the r-th free slot by index, then the untouched occupied slots in
+// ascending (last access, slot) order. Sets o.cnt[4] if nothing was admitted
+// (the union does not fit); the slot state is written back by the caller.
+__device__ void one_token_admit_lru(const RouteArgs& a, unsigned char* sm, const FastTailLayout& L,
+                                    const OneTokenScratch& o) {
+  const int lane = threadIdx.x & 31;
+  const int k = a.k, S = a.admit.S;
+  const AdmitArgs& A = a.admit;
+  const DevCacheLayer c = A.c;
+  const int* s_idx = reinterpret_cast<const int*>(sm + L.idx);
+  const int* s_pt = reinterpret_cast<const int*>(sm + L.pt);
+  unsigned long long* s_last = reinterpret_cast<unsigned long long*>(sm + L.admit);
+  int* s_owner = reinterpret_cast<int*>(s_last + S);
+  uint32_t* s_sgen = reinterpret_cast<uint32_t*>(s_owner + S);
+  const unsigned long long tick0 = reinterpret_cast<const unsigned long long*>(sm + L.tick)[0];
+  if (k > S) {
+    if (lane == 0) {
+      atomicOr(a.err, MOE_DEVERR_CAPACITY);
+      A.units[0] = 0;
+      A.fills[0] = 0;
+      o.cnt[4] = 1;
+    }
+    return;
+  }
+  for (int i = lane; i < S; i += 32) o.hit[i] = 0;
+  o.mslot[lane] = -1;
+  __syncwarp();
+  // selection j (lane j): its slot before the step
+  int e_j = -1, slot_j = -1, hr = 0, mr = 0;
+  if (lane < k) {
+    e_j = s_idx[lane];
+    slot_j = s_pt[e_j];
+  }
+  const bool hit = lane < k && slot_j >= 0;
+  const unsigned hm = __ballot_sync(0xffffffffu, hit), mm = __ballot_sync(0xffffffffu, lane < k && !hit);
+  const int nh = __popc(hm), nm = k - nh;
+  for (int i = 0; i < k; ++i) {
+    const int ei = __shfl_sync(0xffffffffu, e_j, i);
+    if (ei < e_j) {
+      hr += (hm >> i) & 1u;
+      mr += (mm >> i) & 1u;
+    }
+  }
+  if (hit) o.hit[slot_j] = 1;
+  __syncwarp();
+  // the misses take the free slots in index order
+  int nfree = 0;
+  for (int s0 = 0; s0 < S; s0 += 32) {
+    const int s2 = s0 + lane;
+    const bool fr = s2 < S && s_owner[s2] < 0;
+    const unsigned fb = __ballot_sync(0xffffffffu, fr);
+    const int r = nfree + __popc(fb & ((1u << lane) - 1u));
+    if (fr && r < nm) o.mslot[r] = s2;
+    nfree += __popc(fb);
+  }
+  // then the untouched occupied slots, oldest access first (ties: lower slot)
+  unsigned chosen = 0u;  // bit j: slot lane + 32 j taken by an earlier round
+  for (int r = nfree; r < nm; ++r) {
+    unsigned long long best = ~0ull;
+    int bs = INT_MAX;
+    for (int j = 0; j * 32 < S; ++j) {
+      const int s2 = j * 32 + lane;
+      if (s2 < S && s_owner[s2] >= 0 && !o.hit[s2] && !((chosen >> j) & 1u)) {
+        const unsigned long long v = s_last[s2];
+        if (v < best) {
+          best = v;
+          bs = s2;
+        }
+      }
+    }
+    const uint32_t mh = __reduce_min_sync(0xffffffffu, static_cast<uint32_t>(best >> 32));
+    const bool c1 = static_cast<uint32_t>(best >> 32) == mh;
+    const uint32_t ml = __reduce_min_sync(0xffffffffu, c1 ? static_cast<uint32_t>(best) : 0xffffffffu);
+    const bool c2 = c1 && static_cast<uint32_t>(best) == ml;
+    const int win = static_cast<int>(__reduce_min_sync(0xffffffffu, c2 ? static_cast<unsigned>(bs) : 0xffffffffu));
+    if (lane == 0) o.mslot[r] = win < S ? win : -1;
+    if (win < S && (win & 31) == lane) chosen |= 1u << (win >> 5);
+  }
+  __syncwarp();
+  // every miss has a slot (guaranteed while the union fits the slots)
+  const bool bad = __any_sync(0xffffffffu, lane < k && !hit && o.mslot[mr] < 0);
+  if (bad) {
+    if (lane == 0) {
+      atomicOr(a.err, MOE_DEVERR_CAPACITY);
+      A.units[0] = 0;
+      A.fills[0] = 0;
+      o.cnt[4] = 1;
+    }
+    return;
+  }
+  int nevict = 0;
+  if (lane < k) {
+    int slot = slot_j;
+    if (!hit) {
+      slot = o.mslot[mr];
+      const int victim = s_owner[slot];
+      if (victim >= 0) {
+        c.pt[victim] = -1;  // victims are never in the union
+        nevict = 1;
+      }
+      s_owner[slot] = e_j;
+      s_sgen[slot] += 1u;
+      s_last[slot] = tick0 + nh + 1 + mr;
+      A.fills[1 + 2 * mr] = e_j;
+      A.fills[2 + 2 * mr] = slot;
+      A.done[mr] = 0u;
+    } else {
+      s_last[slot] = tick0 + 1 + hr;
+    }
+    const uint32_t g = s_sgen[slot];
+    c.pt[e_j] = slot;
+    c.ptgen[e_j] = g;
+    int pos = 0;
+    for (int i = 0; i < k; ++i) pos += s_idx[i] < e_j ? 1 : 0;
+    int* U = A.units + kUnitHeader + kUnitInts * pos;
+    const bool filled = A.read_through && !hit;
+    U[0] = filled ? -2 - slot : slot;
+    U[1] = pos;
+    U[2] = 1;
+    U[3] = filled ? e_j : static_cast<int>(g);
+  }
+  nevict = __reduce_add_sync(0xffffffffu, nevict);
+  if (lane == 0) {
+    if (A.has_shared) {
+      int* U = A.units + kUnitHeader + kUnitInts * k;
+      U[0] = -1;
+      U[1] = -1;
+      U[2] = 1;
+      U[3] = 0;
+    }
+    A.units[0] = k + (A.has_shared ? 1 : 0);
+    A.fills[0] = nm;
+    c.tick[0] = tick0 + k;
+    atomicAdd(reinterpret_cast<unsigned long long*>(c.stats + kStatSteps), 1ull);
+    atomicAdd(reinterpret_cast<unsigned long long*>(c.stats + kStatHits), static_cast<unsigned long long>(k - nm));
+    atomicAdd(reinterpret_cast<unsigned long long*>(c.stats + kStatMisses), static_cast<unsigned long long>(nm));
+    atomicAdd(reinterpret_cast<unsigned long long*>(c.stats + kStatEvictions), static_cast<unsigned long long>(nevict));
+    atomicAdd(reinterpret_cast<unsigned long long*>(c.stats + kStatMaterialized),
+              static_cast<unsigned long long>(nm) * static_cast<unsigned long long>(A.payload));
+  }
+}
+
 // One token (T == 1) on the whole block. Selection: experts whose high key
 // word reaches the smallest of the per-warp maxima (when at least k warps
 // hold experts, at least k experts do, so the top k are among them) are
@@ -1040,7 +1184,6 @@ __device__ bool one_token_tail(const RouteArgs& a, unsigned char* sm, const Fast
   int* s_plan = reinterpret_cast<int*>(sm + L.plan);
   int* s_uniq = reinterpret_cast<int*>(sm + L.uniq);
   int* s_nu = reinterpret_cast<int*>(sm + L.nu);
-  const int* s_pt = reinterpret_cast<const int*>(sm + L.pt);
   const OneTokenScratch o = one_token_scratch(sm + L.one, E, S);
   // ---- candidates
   const bool live = tid < E;
@@ -1129,7 +1272,10 @@ __device__ bool one_token_tail(const RouteArgs& a, unsigned char* sm, const Fast
   __syncthreads();
   if (!o.cnt[1]) return false;
   const moe_plan_t& P = a.plan;
-  // ---- weights, permutation (warp 0) and the plan's per-expert arrays (all)
+  const bool lru = adm && a.admit.policy == MOE_LRU;
+  // LRU admission needs only the selection and the page table before the
+  // step: warp 1 admits while warp 0 writes the weights and permutation and
+  // the other warps the plan's per-expert arrays
   if (warp == 0) {
     float z = 0.f;
     int pos = 0;
@@ -1158,162 +1304,28 @@ __device__ bool one_token_tail(const RouteArgs& a, unsigned char* sm, const Fast
       *P.n_uniq = k;
       *s_nu = k;
     }
+  } else if (warp == 1 && lru) {
+    one_token_admit_lru(a, sm, L, o);
   }
-  if (live) {
-    int off = 0;
-    for (int i = 0; i < k; ++i) off += s_idx[i] < tid ? 1 : 0;
-    const int c = taken[tid];
-    P.counts[tid] = c;
-    P.offsets[tid] = off;
-    s_plan[tid] = c;
-    s_plan[E + tid] = off;
-  }
-  if (!adm || a.admit.policy != MOE_LRU) {
-    __syncthreads();  // the caller's admission (random policy) reads the plan from shared memory
-    return true;
-  }
-  // ---- LRU admission
-  const AdmitArgs& A = a.admit;
-  const DevCacheLayer c = A.c;
-  unsigned long long* s_last = reinterpret_cast<unsigned long long*>(sm + L.admit);
-  int* s_owner = reinterpret_cast<int*>(s_last + S);
-  uint32_t* s_sgen = reinterpret_cast<uint32_t*>(s_owner + S);
-  const unsigned long long tick0 = reinterpret_cast<const unsigned long long*>(sm + L.tick)[0];
-  if (k > S) {
-    if (tid == 0) {
-      atomicOr(a.err, MOE_DEVERR_CAPACITY);
-      A.units[0] = 0;
-      A.fills[0] = 0;
-    }
-    return true;
-  }
-  for (int i = tid; i < S; i += kRouteThreads) o.hit[i] = 0;
-  if (tid < 32) o.mslot[tid] = -1;
-  __syncthreads();
-  // selection j (warp 0, lane j): its slot before the step
-  int e_j = -1, slot_j = -1, hr = 0, mr = 0, nh = 0;
-  if (warp == 0) {
-    if (lane < k) {
-      e_j = s_idx[lane];
-      slot_j = s_pt[e_j];
-    }
-    const bool hit = lane < k && slot_j >= 0;
-    const unsigned hm = __ballot_sync(0xffffffffu, hit), mm = __ballot_sync(0xffffffffu, lane < k && !hit);
-    nh = __popc(hm);
-    for (int i = 0; i < k; ++i) {
-      const int ei = __shfl_sync(0xffffffffu, e_j, i);
-      if (ei < e_j) {
-        hr += (hm >> i) & 1u;
-        mr += (mm >> i) & 1u;
-      }
-    }
-    if (hit) o.hit[slot_j] = 1;
-  }
-  __syncwarp();
-  const int nm = k - nh;  // valid in warp 0
-  if (warp == 0) {
-    // the misses take the free slots in index order
-    int nfree = 0;
-    for (int s0 = 0; s0 < S; s0 += 32) {
-      const int s2 = s0 + lane;
-      const bool fr = s2 < S && s_owner[s2] < 0;
-      const unsigned fb = __ballot_sync(0xffffffffu, fr);
-      const int r = nfree + __popc(fb & ((1u << lane) - 1u));
-      if (fr && r < nm) o.mslot[r] = s2;
-      nfree += __popc(fb);
-    }
-    // then the untouched occupied slots, oldest access first (ties: lower slot)
-    unsigned chosen = 0u;  // bit j: slot lane + 32 j taken by an earlier round
-    for (int r = nfree; r < nm; ++r) {
-      unsigned long long best = ~0ull;
-      int bs = INT_MAX;
-      for (int j = 0; j * 32 < S; ++j) {
-        const int s2 = j * 32 + lane;
-        if (s2 < S && s_owner[s2] >= 0 && !o.hit[s2] && !((chosen >> j) & 1u)) {
-          const unsigned long long v = s_last[s2];
-          if (v < best) {
-            best = v;
-            bs = s2;
-          }
-        }
-      }
-      const uint32_t mh = __reduce_min_sync(0xffffffffu, static_cast<uint32_t>(best >> 32));
-      const bool c1 = static_cast<uint32_t>(best >> 32) == mh;
-      const uint32_t ml = __reduce_min_sync(0xffffffffu, c1 ? static_cast<uint32_t>(best) : 0xffffffffu);
-      const bool c2 = c1 && static_cast<uint32_t>(best) == ml;
-      const int win = static_cast<int>(__reduce_min_sync(0xffffffffu, c2 ? static_cast<unsigned>(bs) : 0xffffffffu));
-      if (lane == 0) o.mslot[r] = win < S ? win : -1;
-      if (win < S && (win & 31) == lane) chosen |= 1u << (win >> 5);
-    }
-    __syncwarp();
-    // every miss has a slot (guaranteed while the union fits the slots)
-    const bool bad = lane < k && slot_j < 0 && o.mslot[mr] < 0;
-    const bool any_bad = __any_sync(0xffffffffu, bad);
-    if (lane == 0) o.cnt[4] = any_bad ? 1 : 0;
-  }
-  __syncthreads();
-  if (o.cnt[4]) {
-    if (tid == 0) {
-      atomicOr(a.err, MOE_DEVERR_CAPACITY);
-      A.units[0] = 0;
-      A.fills[0] = 0;
-    }
-    return true;
-  }
-  if (warp == 0) {
-    int nevict = 0;
-    if (lane < k) {
-      const bool hit = slot_j >= 0;
-      int slot = slot_j;
-      if (!hit) {
-        slot = o.mslot[mr];
-        const int victim = s_owner[slot];
-        if (victim >= 0) {
-          c.pt[victim] = -1;  // victims are never in the union
-          nevict = 1;
-        }
-        s_owner[slot] = e_j;
-        s_sgen[slot] += 1u;
-        s_last[slot] = tick0 + nh + 1 + mr;
-        A.fills[1 + 2 * mr] = e_j;
-        A.fills[2 + 2 * mr] = slot;
-        A.done[mr] = 0u;
-      } else {
-        s_last[slot] = tick0 + 1 + hr;
-      }
-      const uint32_t g = s_sgen[slot];
-      c.pt[e_j] = slot;
-      c.ptgen[e_j] = g;
-      int pos = 0;
-      for (int i = 0; i < k; ++i) pos += s_idx[i] < e_j ? 1 : 0;
-      int* U = A.units + kUnitHeader + kUnitInts * pos;
-      const bool filled = A.read_through && !hit;
-      U[0] = filled ? -2 - slot : slot;
-      U[1] = pos;
-      U[2] = 1;
-      U[3] = filled ? e_j : static_cast<int>(g);
-    }
-    nevict = __reduce_add_sync(0xffffffffu, nevict);
-    if (lane == 0) {
-      if (A.has_shared) {
-        int* U = A.units + kUnitHeader + kUnitInts * k;
-        U[0] = -1;
-        U[1] = -1;
-        U[2] = 1;
-        U[3] = 0;
-      }
-      A.units[0] = k + (A.has_shared ? 1 : 0);
-      A.fills[0] = nm;
-      c.tick[0] = tick0 + k;
-      atomicAdd(reinterpret_cast<unsigned long long*>(c.stats + kStatSteps), 1ull);
-      atomicAdd(reinterpret_cast<unsigned long long*>(c.stats + kStatHits), static_cast<unsigned long long>(k - nm));
-      atomicAdd(reinterpret_cast<unsigned long long*>(c.stats + kStatMisses), static_cast<unsigned long long>(nm));
-      atomicAdd(reinterpret_cast<unsigned long long*>(c.stats + kStatEvictions), static_cast<unsigned long long>(nevict));
-      atomicAdd(reinterpret_cast<unsigned long long*>(c.stats + kStatMaterialized),
-                static_cast<unsigned long long>(nm) * static_cast<unsigned long long>(A.payload));
+  {
+    const int busy = lru ? 64 : 32;  // threads of warp 0 (and 1)
+    for (int e = tid - busy; e >= 0 && e < E; e += kRouteThreads - busy) {
+      int off = 0;
+      for (int i = 0; i < k; ++i) off += s_idx[i] < e ? 1 : 0;
+      const int c = taken[e];
+      P.counts[e] = c;
+      P.offsets[e] = off;
+      s_plan[e] = c;
+      s_plan[E + e] = off;
     }
   }
-  __syncthreads();
+  __syncthreads();  // the caller's admission (random policy) reads the plan from shared memory
+  if (!lru || o.cnt[4]) return true;
+  // write back the layer's slot state
+  const DevCacheLayer c = a.admit.c;
+  const unsigned long long* s_last = reinterpret_cast<const unsigned long long*>(sm + L.admit);
+  const int* s_owner = reinterpret_cast<const int*>(s_last + S);
+  const uint32_t* s_sgen = reinterpret_cast<const uint32_t*>(s_owner + S);
   for (int s2 = tid; s2 < S; s2 += kRouteThreads) {
     c.last[s2] = s_last[s2];
     c.owner[s2] = s_owner[s2];
@@ -1882,7 +1894,7 @@ __device__ __forceinline__ void logits_stash(float (*xs)[kLPad], float (*ws)[kLP
 
 // part: [slices][T][E] (hi, lo) pairs of the K slices
 template <int XT>
-__global__ void __launch_bounds__(kLThreads) logits_tiled_kernel(RouteArgs a, float2* part) {
+__global__ void __launch_bounds__(kLThreads, 4) logits_tiled_kernel(RouteArgs a, float2* part) {
   __shared__ __align__(16) float xs[2][kLK][kLPad];
   __shared__ __align__(16) float ws[2][kLK][kLPad];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
