@@ -32,8 +32,8 @@ the byte counts printed on the pages. The routine ``moe_layer`` (fp64 FFN) is
 pinned by permutation-matrix closed forms; no page prints a worked output
 vector for synthetic inputs.
 """
-from .formats import (Q8_0, Q4_0, bf16_bits_to_f64, f16_bits_to_f64, payload_bytes,
-                      dequant_q8_0, dequant_q4_0, expert_matrices)
+from .formats import (Q8_0, Q4_0, I4_G64, bf16_bits_to_f64, f16_bits_to_f64, payload_bytes,
+                      dequant_q8_0, dequant_q4_0, dequant_i4_g64, expert_matrices)
 from .route import router_logits, topk_select, combine_weights, route
 from .plan import plan_union
 from .splitmix import SplitMix64

@@ -7,10 +7,16 @@ gate, up and down projections per expert):
 * Q8_0: x = d * q, q a signed byte;
 * Q4_0: x = d * (q - 8), q an unsigned nibble; byte j of a block holds
   element j (low nibble) and element j + 16 (high nibble).
+* I4_G64 (affine INT4, group size 64; Routide §3.1 stores gate, up and down
+  with scales and biases, BF16 quantisation metadata): x = s * q + b, q an
+  unsigned nibble, one bf16 scale s and one bf16 bias b per 64 weights; byte
+  j of a row holds element 2j (low nibble) and element 2j + 1 (high nibble).
+  At 36 B per 64 weights it is 4.5 bits per weight, as Q4_0.
 
 An expert's payload stores, for gate [I, H], up [I, H] and down [H, I] in that
 order, a quant plane (all rows, row-major) followed by a scale plane
-(fp16 [rows][K/32]). Blocks run along the input dimension K.
+(fp16 [rows][K/32]; for I4_G64 the (scale, bias) bf16 pairs [rows][K/64][2]).
+Blocks run along the input dimension K.
 """
 from __future__ import annotations
 
@@ -18,6 +24,7 @@ import numpy as np
 
 Q8_0 = 0
 Q4_0 = 1
+I4_G64 = 2
 
 
 def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
@@ -63,6 +70,21 @@ def dequant_q4_0(nib: np.ndarray, d_bits: np.ndarray) -> np.ndarray:
     return x.reshape(rows, k)
 
 
+def dequant_i4_g64(nib: np.ndarray, sb_bits: np.ndarray) -> np.ndarray:
+    """nib uint8 [rows, K/2], sb_bits uint16 [rows, K/64, 2] (bf16 scale,
+    bf16 bias) -> fp64 [rows, K], x = s*q + b; byte j holds elements 2j (low
+    nibble) and 2j+1 (high nibble)."""
+    rows, kh = nib.shape
+    k = 2 * kh
+    q = np.empty((rows, k), dtype=np.int64)
+    q[:, 0::2] = nib & 0x0F
+    q[:, 1::2] = nib >> 4
+    s = bf16_bits_to_f64(sb_bits[:, :, 0]).reshape(rows, k // 64)
+    b = bf16_bits_to_f64(sb_bits[:, :, 1]).reshape(rows, k // 64)
+    x = q.astype(np.float64).reshape(rows, k // 64, 64) * s[:, :, None] + b[:, :, None]
+    return x.reshape(rows, k)
+
+
 def _matrix(buf: np.ndarray, off: int, rows: int, k: int, quant: int):
     if quant == Q8_0:
         qn = rows * k
@@ -72,6 +94,9 @@ def _matrix(buf: np.ndarray, off: int, rows: int, k: int, quant: int):
         q = buf[off:off + qn].reshape(rows, k // 2)
     off += qn
     sn = rows * (k // 32) * 2
+    if quant == I4_G64:
+        sb = buf[off:off + sn].view("<u2").reshape(rows, k // 64, 2)
+        return dequant_i4_g64(q, sb), off + sn
     d = buf[off:off + sn].view("<u2").reshape(rows, k // 32)
     off += sn
     x = dequant_q8_0(q, d) if quant == Q8_0 else dequant_q4_0(q, d)

@@ -73,6 +73,53 @@ def test_q4_0_exhaustive_nibbles():
             assert x[blk, j + 16] == (v >> 4) - 8
 
 
+def test_i4_g64_nibble_order_scale_and_bias():
+    # byte j: element 2j in the low nibble, element 2j + 1 in the high one;
+    # x = s*q + b with one (s, b) per 64 weights
+    b = np.array([(j & 0xF) | ((15 - (j & 0xF)) << 4) for j in range(64)], dtype=np.uint8).reshape(1, 64)
+    # two groups: (s, b) = (1, 0) and (0.5, -2) as bf16 bits
+    sb = np.array([[[0x3F80, 0x0000], [0x3F00, 0xC000]]], dtype=np.uint16)
+    x = formats.dequant_i4_g64(b, sb).ravel()
+    for j in range(64):
+        lo, hi = j & 0xF, 15 - (j & 0xF)
+        s_, b_ = (1.0, 0.0) if j < 32 else (0.5, -2.0)
+        assert x[2 * j] == s_ * lo + b_ and x[2 * j + 1] == s_ * hi + b_
+
+
+def test_i4_g64_exhaustive_codes():
+    # every byte value, with an exactly representable scale and bias
+    b = np.arange(256, dtype=np.uint8).reshape(1, 256)  # 512 weights, 8 groups
+    s_bits, b_bits = 0x3E80, 0xBF40  # 0.25, -0.75
+    sb = np.tile(np.array([s_bits, b_bits], dtype=np.uint16), (1, 8, 1))
+    x = formats.dequant_i4_g64(b, sb).ravel()
+    for v in range(256):
+        assert x[2 * v] == 0.25 * (v & 15) - 0.75
+        assert x[2 * v + 1] == 0.25 * (v >> 4) - 0.75
+
+
+def test_i4_g64_expert_layout():
+    # quant plane then (scale, bias) plane per matrix; gate/up/down in order
+    H, I = 128, 64
+    parts = []
+    for m, (rows, k) in enumerate(((I, H), (I, H), (H, I))):
+        nib = np.full(rows * k // 2, (m + 1) | ((m + 2) << 4), dtype=np.uint8)
+        parts.append(nib)
+        sb = np.tile(np.array([0x3F80, [0x0000, 0x3F80, 0x4000][m]], dtype="<u2"), rows * (k // 64))
+        parts.append(sb.view(np.uint8))
+    p = np.concatenate(parts)
+    assert p.size == oracle.payload_bytes(H, I, oracle.I4_G64) == oracle.payload_bytes(H, I, oracle.Q4_0)
+    wg, wu, wd = oracle.expert_matrices(p, H, I, oracle.I4_G64)
+    for m, w in enumerate((wg, wu, wd)):
+        bias = [0.0, 1.0, 2.0][m]
+        assert np.all(w[:, 0::2] == (m + 1) + bias) and np.all(w[:, 1::2] == (m + 2) + bias)
+
+
+def test_i4_g64_payload_matches_routide():
+    # Routide §3.2: 540 MiB for 320 experts at hidden 2048, intermediate 512
+    # is 4.5 bits per weight: 36 B per 64 affine INT4 weights
+    assert oracle.payload_bytes(2048, 512, oracle.I4_G64) * 320 == 540 * 2**20
+
+
 def _hand_payload_q8(H, I):
     """Payload whose quant value at (matrix m, row r, col c) is
     (m*7 + r*3 + c) mod 101 - 50, with every scale of matrix m equal to 2^-m."""
@@ -119,17 +166,17 @@ def test_payload_bytes_match_pages(golden_dir):
 def test_workload_payload_sizes():
     from workloads import WORKLOADS
     want = {"tiny": 104448, "decode": 3342336, "mtp_decode": 1769472,
-            "prefill": 3342336, "wide_prefill": 6319104}
+            "prefill": 3342336, "wide_prefill": 6319104, "i4_decode": 1769472}
     for name, w in WORKLOADS.items():
         assert oracle.payload_bytes(w.hidden, w.inter, w.quant) == want[name]
         assert w.payload_bytes == want[name]
 
 
-@pytest.mark.parametrize("name", ["tiny", "mtp_decode"])
+@pytest.mark.parametrize("name", ["tiny", "mtp_decode", "i4_decode"])
 def test_generated_payload_ranges(name):
     from workloads import WORKLOADS, expert_payload
     w = WORKLOADS[name]
-    if name == "mtp_decode":
+    if name in ("mtp_decode", "i4_decode"):
         w = __import__("workloads").with_changes(w, hidden=256, inter=64)
     p = expert_payload(w, 0, 3)
     wg, wu, wd = oracle.expert_matrices(p, w.hidden, w.inter, w.quant)
@@ -144,6 +191,13 @@ def test_generated_payload_ranges(name):
         nib = p[:w.inter * w.hidden // 2]
         assert len(np.unique(nib & 15)) == 16 and len(np.unique(nib >> 4)) == 16
     off = w.inter * w.hidden if w.quant == oracle.Q8_0 else w.inter * w.hidden // 2
+    if w.quant == oracle.I4_G64:
+        sb = p[off:off + w.inter * w.hidden // 16].view("<u2").reshape(-1, 2)
+        sc, bi = oracle.bf16_bits_to_f64(sb[:, 0]), oracle.bf16_bits_to_f64(sb[:, 1])
+        # bf16 rounding: within 2^-8 relative of the drawn values
+        assert sc.min() >= 1e-3 * (1 - 2**-8) and sc.max() <= 2e-2 * (1 + 2**-8)
+        assert np.all(bi <= -6.9 * sc) and np.all(bi >= -8.1 * sc)
+        return
     d = oracle.f16_bits_to_f64(p[off:off + w.inter * w.hidden // 16].view("<u2"))
     assert d.min() >= 0.000999 and d.max() <= 0.02001
 

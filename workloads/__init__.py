@@ -16,11 +16,14 @@ decode         2048    256   8   512   512    Q8_0   1/step bf16 AR(1)      38
 mtp_decode     2048    256   8   512   512    Q4_0   4/step bf16 AR(1)      89
 prefill        2048    256   8   512   512    Q8_0   4096 bf16 N(0,1)+Zipf  256
 wide_prefill   2816    128   8   704   2112   Q8_0   32768 bf16 (8x4096)    44
+i4_decode      2048    256   8   512   512    I4_G64 1/step bf16 AR(1)      38
 =============  ======  ====  ==  ====  =====  =====  =====================  ====
 
 Router weights are fp32 N(0, 0.02). Q8_0 quants are uniform on [-127, 127];
 Q4_0 nibbles are uniform on [0, 15]; every 32-weight block carries an fp16
-scale drawn U[1e-3, 2e-2] and rounded to fp16. bf16 activations are drawn in
+scale drawn U[1e-3, 2e-2] and rounded to fp16. I4_G64 (affine INT4, groups
+of 64) nibbles are uniform on [0, 15]; each group's bf16 scale s is drawn
+U[1e-3, 2e-2] and its bf16 bias -s*U[7, 8], both rounded to bf16. bf16 activations are drawn in
 fp64 and rounded (fp64 -> fp32 -> bf16, round-to-nearest-even at each step).
 
 Expert payload layout ("split-plane"): for each matrix in the order gate
@@ -30,7 +33,10 @@ the input dimension K), a quant plane followed by a scale plane:
 * Q8_0 quant plane: int8 [rows][K]; Q4_0 quant plane: uint8 [rows][K/2], where
   byte j of each 32-block holds element j in its low nibble and element j+16
   in its high nibble (the GGUF convention);
-* scale plane: fp16 [rows][K/32], little-endian.
+* scale plane: fp16 [rows][K/32], little-endian; for I4_G64 (quant plane as
+  uint8 [rows][K/2] with element 2j in the low nibble of byte j and element
+  2j+1 in its high nibble) the plane holds (scale, bias) bf16 pairs
+  [rows][K/64][2], the same number of bytes.
 
 The bytes per expert equal the interleaved GGUF size (34 B per 32 weights for
 Q8_0, 18 B for Q4_0); only the order of the bytes differs.
@@ -50,6 +56,7 @@ import numpy as np
 
 Q8_0 = 0
 Q4_0 = 1
+I4_G64 = 2
 
 LRU = 0
 RANDOM = 1
@@ -119,6 +126,8 @@ WORKLOADS = {
                         preload=True),
     "wide_prefill": Workload("wide_prefill", 2816, 128, 8, 704, 2112, Q8_0,
                              "bf16", "normal", 4096, 1, 8, 44, LRU, seed=4),
+    "i4_decode": Workload("i4_decode", 2048, 256, 8, 512, 512, I4_G64, "bf16",
+                          "ar1", 1, 4, 24, 38, LRU, seed=5, rho=0.9),
 }
 
 
@@ -218,7 +227,18 @@ def expert_payload(w: Workload, layer: int, expert: int,
         _fill_quant(_rng(w.seed, layer, expert, _F_QUANT + m), out[off:off + qbytes], w.quant)
         off += qbytes
         nblk = rows * (k // 32)
-        d = _rng(w.seed, layer, expert, _F_SCALE + m).uniform(1e-3, 2e-2, nblk).astype(np.float16)
+        g = _rng(w.seed, layer, expert, _F_SCALE + m)
+        if w.quant == I4_G64:
+            ngrp = rows * (k // 64)
+            sc = g.uniform(1e-3, 2e-2, ngrp)
+            bi = -sc * g.uniform(7.0, 8.0, ngrp)
+            sb = np.empty((ngrp, 2), dtype=np.uint16)
+            sb[:, 0] = f64_to_bf16_bits(sc)
+            sb[:, 1] = f64_to_bf16_bits(bi)
+            out[off:off + 4 * ngrp] = sb.astype("<u2").view(np.uint8).ravel()
+            off += 4 * ngrp
+            continue
+        d = g.uniform(1e-3, 2e-2, nblk).astype(np.float16)
         out[off:off + 2 * nblk] = d.astype("<f2").view(np.uint8)
         off += 2 * nblk
     assert off == nbytes
