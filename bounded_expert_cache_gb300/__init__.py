@@ -6,10 +6,10 @@ The compute path is the in-tree CUDA library ``libmoecache.so`` (C ABI in
 it fails if the library has not been built.
 """
 from . import _native
-from ._native import (Q8_0, Q4_0, LRU, RANDOM, FARTHEST_NEXT_USE, STATIC_SET, F32, BF16, MODE_AUTO, MODE_DECODE,
+from ._native import (Q8_0, Q4_0, I4_G64, LRU, RANDOM, FARTHEST_NEXT_USE, STATIC_SET, F32, BF16, MODE_AUTO, MODE_DECODE,
                       MODE_PREFILL)
 from .api import Context, Plan, Slots, Misses, MoeError, splitmix64, static_budget, replay
 
 __all__ = ["Context", "Plan", "Slots", "Misses", "MoeError", "splitmix64", "static_budget", "replay",
-           "FARTHEST_NEXT_USE", "STATIC_SET", "Q8_0", "Q4_0", "LRU",
+           "FARTHEST_NEXT_USE", "STATIC_SET", "Q8_0", "Q4_0", "I4_G64", "LRU",
            "RANDOM", "F32", "BF16", "MODE_AUTO", "MODE_DECODE", "MODE_PREFILL"]

@@ -15,7 +15,7 @@ MOE_OK = 0
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_ARG", 2: "MOE_ERR_CUDA", 3: "MOE_ERR_CAPACITY",
                 4: "MOE_ERR_STALE", 5: "MOE_ERR_TIMEOUT", 6: "MOE_ERR_UNCERTIFIED",
                 7: "MOE_ERR_STATE"}
-Q8_0, Q4_0 = 0, 1
+Q8_0, Q4_0, I4_G64 = 0, 1, 2
 LRU, RANDOM, FARTHEST_NEXT_USE, STATIC_SET = 0, 1, 2, 3
 F32, BF16 = 0, 1
 MODE_AUTO, MODE_DECODE, MODE_PREFILL = 0, 1, 2

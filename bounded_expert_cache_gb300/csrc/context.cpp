@@ -176,7 +176,9 @@ extern "C" moe_status_t moe_create(const moe_config_t* cfg, moe_ctx_t** out) {
   else if (c.hidden < 32 || c.hidden % 32) why = "hidden not a positive multiple of 32";
   else if (c.inter < 32 || c.inter % 32) why = "inter not a positive multiple of 32";
   else if (c.shared_inter < 0 || c.shared_inter % 32) why = "shared_inter not a multiple of 32";
-  else if (c.quant != MOE_Q8_0 && c.quant != MOE_Q4_0) why = "unknown quant";
+  else if (c.quant != MOE_Q8_0 && c.quant != MOE_Q4_0 && c.quant != MOE_I4_G64) why = "unknown quant";
+  else if (c.quant == MOE_I4_G64 && (c.hidden % 64 || c.inter % 64 || c.shared_inter % 64))
+    why = "I4_G64 needs hidden, inter and shared_inter multiples of 64";
   else if (c.slots_per_layer < 1 || c.slots_per_layer > c.n_experts) why = "slots_per_layer outside 1..E";
   else if (c.policy != MOE_LRU && c.policy != MOE_RANDOM) why = "unknown policy";
   else if (c.n_streams < 1 || c.n_streams > 8) why = "n_streams outside 1..8";

@@ -76,25 +76,50 @@ __device__ __forceinline__ uint4 ldg_stream(const void* p) {
   return r;
 }
 
-__device__ __forceinline__ float ld_scale(const uint8_t* p) {
-  const unsigned short b = __ldg(reinterpret_cast<const unsigned short*>(p));
-  return __half2float(__ushort_as_half(b));
-}
-
 // Loads from a miss's source: the pinned store, read over the host link.
 __device__ __forceinline__ uint4 ld_host(const void* p) {
   return __ldcs(reinterpret_cast<const uint4*>(p));
 }
-__device__ __forceinline__ unsigned short ld_scale_host_bits(const uint8_t* p) {
-  return __ldcs(reinterpret_cast<const unsigned short*>(p));
-}
 
-// A miss's scales reach its slot from the loads the dot products make: the
-// lane whose chunk opens a 32-weight block (every Q4_0 chunk, even Q8_0
-// chunks) stores that block's fp16 scale, so no copy waits on its own load.
+// Block metadata of the 16-byte chunk c of a row: Q8_0 the fp16 scale of
+// its 32-weight block (chunks 2j and 2j+1 share one), Q4_0 the fp16 scale of
+// its block (one per chunk), I4_G64 the bf16 (scale, bias) pair of its
+// 64-weight group (chunks 2j and 2j+1), loaded as one 32-bit word.
 template <int Q>
-__device__ __forceinline__ bool owns_scale(int c) {
-  return Q != MOE_Q8_0 || (c & 1) == 0;
+__device__ __forceinline__ int meta_off(int c) {
+  return Q == MOE_Q4_0 ? 2 * c : (Q == MOE_Q8_0 ? 2 * (c >> 1) : 4 * (c >> 1));
+}
+template <int Q>
+__device__ __forceinline__ uint32_t ld_meta(const uint8_t* row, int c) {
+  const uint8_t* p = row + meta_off<Q>(c);
+  return Q == MOE_I4_G64 ? __ldg(reinterpret_cast<const uint32_t*>(p))
+                         : static_cast<uint32_t>(__ldg(reinterpret_cast<const unsigned short*>(p)));
+}
+template <int Q>
+__device__ __forceinline__ uint32_t ld_meta_host(const uint8_t* row, int c) {
+  const uint8_t* p = row + meta_off<Q>(c);
+  return Q == MOE_I4_G64 ? __ldcs(reinterpret_cast<const uint32_t*>(p))
+                         : static_cast<uint32_t>(__ldcs(reinterpret_cast<const unsigned short*>(p)));
+}
+// A miss's metadata reaches its slot from the loads the dot products make:
+// the lane whose chunk opens a block (every Q4_0 chunk, even chunks of the
+// others) stores it, so no copy waits on its own load.
+template <int Q>
+__device__ __forceinline__ void st_meta(uint8_t* row, int c, uint32_t v) {
+  if (Q != MOE_Q4_0 && (c & 1)) return;
+  uint8_t* p = row + meta_off<Q>(c);
+  if (Q == MOE_I4_G64)
+    *reinterpret_cast<uint32_t*>(p) = v;
+  else
+    *reinterpret_cast<unsigned short*>(p) = static_cast<unsigned short>(v);
+}
+template <int Q>
+__device__ __forceinline__ float meta_scale(uint32_t v) {
+  return Q == MOE_I4_G64 ? __uint_as_float(v << 16) : __half2float(__ushort_as_half(static_cast<unsigned short>(v)));
+}
+template <int Q>
+__device__ __forceinline__ float meta_bias(uint32_t v) {
+  return Q == MOE_I4_G64 ? __uint_as_float(v & 0xFFFF0000u) : 0.f;
 }
 
 // Packed pairs of fp32 (Blackwell's f32x2 add and FMA).
@@ -166,6 +191,41 @@ __device__ __forceinline__ float dot_q4(const uint4 w, const float* xl, const fl
       s = f2fma(ql, f2packf(xl[4 * i + 2 * h], xl[4 * i + 2 * h + 1]), s);
       s = f2fma(qh, f2packf(xh[4 * i + 2 * h], xh[4 * i + 2 * h + 1]), s);
     }
+  }
+  return f2sum(s);
+}
+
+// Dot of one 16-byte I4_G64 chunk (32 weights, half a group) with its
+// activations (xl elements 0..15, xh 16..31): byte j holds elements 2j (low
+// nibble) and 2j+1 (high nibble); a nibble n becomes 2^23 + n and the packed
+// subtraction of 2^23 leaves n. Returns sum(q * x); the caller adds
+// scale * that + bias * sum(x).
+__device__ __forceinline__ float dot_u4(const uint4 w, const float* xl, const float* xh) {
+  const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+  const unsigned long long bias = f2packf(8388608.0f, 8388608.0f);
+  unsigned long long s = 0ull;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t lo = ws[i] & 0x0F0F0F0Fu, hi = (ws[i] >> 4) & 0x0F0F0F0Fu;
+    const float* x8 = i < 2 ? xl + 8 * i : xh + 8 * (i - 2);
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const unsigned long long q = f2sub(f2pack(__byte_perm(lo, 0x4B000000u, 0x7540u | b),
+                                                __byte_perm(hi, 0x4B000000u, 0x7540u | b)),
+                                         bias);
+      s = f2fma(q, f2packf(x8[2 * b], x8[2 * b + 1]), s);
+    }
+  }
+  return f2sum(s);
+}
+
+__device__ __forceinline__ float sum32(const float* xl, const float* xh) {
+  unsigned long long s = 0ull;
+  const unsigned long long one = f2packf(1.0f, 1.0f);
+#pragma unroll
+  for (int j = 0; j < 16; j += 2) {
+    s = f2fma(f2packf(xl[j], xl[j + 1]), one, s);
+    s = f2fma(f2packf(xh[j], xh[j + 1]), one, s);
   }
   return f2sum(s);
 }
@@ -283,31 +343,30 @@ __global__ void __launch_bounds__(kThreads) gateup_kernel(FfnArgs a) {
 #pragma unroll 2
       for (int c = lane; c < nch; c += 32) {
         uint4 w[2 * kRowsPerItem];
-        float d[2 * kRowsPerItem];
+        uint32_t mb[2 * kRowsPerItem];
         if (U.miss) {
-          unsigned short sb[2 * kRowsPerItem];
 #pragma unroll
           for (int r = 0; r < 2 * kRowsPerItem; ++r) {
             w[r] = ld_host(q[r] + c * 16);
-            sb[r] = ld_scale_host_bits(s[r] + (Q == MOE_Q8_0 ? (c >> 1) : c) * 2);
+            mb[r] = ld_meta_host<Q>(s[r], c);
           }
-#pragma unroll
-          for (int r = 0; r < 2 * kRowsPerItem; ++r) d[r] = __half2float(__ushort_as_half(sb[r]));
           if (m0 == 0) {
 #pragma unroll
             for (int r = 0; r < 2 * kRowsPerItem; ++r) {
               *reinterpret_cast<uint4*>(U.dst + (q[r] - U.base) + c * 16) = w[r];
-              if (owns_scale<Q>(c))
-                *reinterpret_cast<unsigned short*>(U.dst + (s[r] - U.base) + (Q == MOE_Q8_0 ? (c >> 1) : c) * 2) = sb[r];
+              st_meta<Q>(U.dst + (s[r] - U.base), c, mb[r]);
             }
           }
         } else {
 #pragma unroll
           for (int r = 0; r < 2 * kRowsPerItem; ++r) {
             w[r] = ldg_stream(q[r] + c * 16);
-            d[r] = ld_scale(s[r] + (Q == MOE_Q8_0 ? (c >> 1) : c) * 2);
+            mb[r] = ld_meta<Q>(s[r], c);
           }
         }
+        float d[2 * kRowsPerItem];
+#pragma unroll
+        for (int r = 0; r < 2 * kRowsPerItem; ++r) d[r] = meta_scale<Q>(mb[r]);
 #pragma unroll
         for (int m = 0; m < TM; ++m) {
           if (m < mcount) {
@@ -318,13 +377,21 @@ __global__ void __launch_bounds__(kThreads) gateup_kernel(FfnArgs a) {
 #pragma unroll
               for (int r = 0; r < 2 * kRowsPerItem; ++r)
                 acc[r][m] = fmaf(d[r], dot_q8(w[r], xv), acc[r][m]);
-            } else {
+            } else if (Q == MOE_Q4_0) {
               float xl[16], xh[16];
               load_chunk16(xr, 2 * c, xl);
               load_chunk16(xr, 2 * c + 1, xh);
 #pragma unroll
               for (int r = 0; r < 2 * kRowsPerItem; ++r)
                 acc[r][m] = fmaf(d[r], dot_q4(w[r], xl, xh), acc[r][m]);
+            } else {
+              float xl[16], xh[16];
+              load_chunk16(xr, 2 * c, xl);
+              load_chunk16(xr, 2 * c + 1, xh);
+              const float xsum = sum32(xl, xh);
+#pragma unroll
+              for (int r = 0; r < 2 * kRowsPerItem; ++r)
+                acc[r][m] = fmaf(d[r], dot_u4(w[r], xl, xh), fmaf(meta_bias<Q>(mb[r]), xsum, acc[r][m]));
             }
           }
         }
@@ -456,7 +523,7 @@ __global__ void __launch_bounds__(kDownThreads, 1) down_kernel(FfnArgs a, int rp
     // the first chunk of every row of the batch, and the slots'
     // generations, all in flight before the first is used
     uint4 w[B][kRowsPerItem];
-    unsigned short sb[B][kRowsPerItem];
+    uint32_t sb[B][kRowsPerItem];
     uint32_t gb[B];
 #pragma unroll
     for (int b = 0; b < B; ++b) {
@@ -482,13 +549,13 @@ __global__ void __launch_bounds__(kDownThreads, 1) down_kernel(FfnArgs a, int rp
           const int o = o0 + rp * kRowsPerItem + r;
           if (o >= a.H) continue;
           const uint8_t* qp = U.base + qo + static_cast<int64_t>(o) * rowbytes + lane * 16;
-          const uint8_t* sp = U.base + so + static_cast<int64_t>(o) * (K / 16) + (Q == MOE_Q8_0 ? (lane >> 1) : lane) * 2;
+          const uint8_t* srow = U.base + so + static_cast<int64_t>(o) * (K / 16);
           if (U.miss) {
             w[b][r] = ld_host(qp);
-            sb[b][r] = ld_scale_host_bits(sp);
+            sb[b][r] = ld_meta_host<Q>(srow, lane);
           } else {
             w[b][r] = ldg_stream(qp);
-            sb[b][r] = __ldg(reinterpret_cast<const unsigned short*>(sp));
+            sb[b][r] = ld_meta<Q>(srow, lane);
           }
         }
       }
@@ -538,7 +605,7 @@ __global__ void __launch_bounds__(kDownThreads, 1) down_kernel(FfnArgs a, int rp
         for (int m = 0; m < TM; ++m) pm[r][m] = 0.f;
       for (int c = lane; c < nch; c += 32) {
         uint4 wv[kRowsPerItem];
-        unsigned short sv[kRowsPerItem];
+        uint32_t sv[kRowsPerItem];
         if (c == lane) {
 #pragma unroll
           for (int r = 0; r < kRowsPerItem; ++r) {
@@ -549,9 +616,8 @@ __global__ void __launch_bounds__(kDownThreads, 1) down_kernel(FfnArgs a, int rp
 #pragma unroll
           for (int r = 0; r < kRowsPerItem; ++r) {
             const uint8_t* qp = q[r] + c * 16;
-            const uint8_t* sp = sp0[r] + (Q == MOE_Q8_0 ? (c >> 1) : c) * 2;
             wv[r] = !rv[r] ? make_uint4(0, 0, 0, 0) : (U.miss ? ld_host(qp) : ldg_stream(qp));
-            sv[r] = !rv[r] ? 0 : (U.miss ? ld_scale_host_bits(sp) : __ldg(reinterpret_cast<const unsigned short*>(sp)));
+            sv[r] = !rv[r] ? 0u : (U.miss ? ld_meta_host<Q>(sp0[r], c) : ld_meta<Q>(sp0[r], c));
           }
         }
         if (U.miss) {
@@ -559,13 +625,12 @@ __global__ void __launch_bounds__(kDownThreads, 1) down_kernel(FfnArgs a, int rp
           for (int r = 0; r < kRowsPerItem; ++r) {
             if (!rv[r]) continue;
             *reinterpret_cast<uint4*>(U.dst + (q[r] - U.base) + c * 16) = wv[r];
-            if (owns_scale<Q>(c))
-              *reinterpret_cast<unsigned short*>(U.dst + (sp0[r] - U.base) + (Q == MOE_Q8_0 ? (c >> 1) : c) * 2) = sv[r];
+            st_meta<Q>(U.dst + (sp0[r] - U.base), c, sv[r]);
           }
         }
         float dv[kRowsPerItem];
 #pragma unroll
-        for (int r = 0; r < kRowsPerItem; ++r) dv[r] = __half2float(__ushort_as_half(sv[r]));
+        for (int r = 0; r < kRowsPerItem; ++r) dv[r] = meta_scale<Q>(sv[r]);
 #pragma unroll
         for (int m = 0; m < TM; ++m) {
           if (m < mcount) {
@@ -575,12 +640,20 @@ __global__ void __launch_bounds__(kDownThreads, 1) down_kernel(FfnArgs a, int rp
               load_chunk16(hr, c, hv);
 #pragma unroll
               for (int r = 0; r < kRowsPerItem; ++r) pm[r][m] = fmaf(dv[r], dot_q8(wv[r], hv), pm[r][m]);
-            } else {
+            } else if (Q == MOE_Q4_0) {
               float hl[16], hh[16];
               load_chunk16(hr, 2 * c, hl);
               load_chunk16(hr, 2 * c + 1, hh);
 #pragma unroll
               for (int r = 0; r < kRowsPerItem; ++r) pm[r][m] = fmaf(dv[r], dot_q4(wv[r], hl, hh), pm[r][m]);
+            } else {
+              float hl[16], hh[16];
+              load_chunk16(hr, 2 * c, hl);
+              load_chunk16(hr, 2 * c + 1, hh);
+              const float hsum = sum32(hl, hh);
+#pragma unroll
+              for (int r = 0; r < kRowsPerItem; ++r)
+                pm[r][m] = fmaf(dv[r], dot_u4(wv[r], hl, hh), fmaf(meta_bias<Q>(sv[r]), hsum, pm[r][m]));
             }
           }
         }
@@ -711,6 +784,7 @@ cudaError_t launch_q(const FfnArgs& a, int num_sms, cudaStream_t st) {
 cudaError_t launch_ffn_decode(const FfnArgs& a, int num_sms, cudaStream_t st) {
   if (a.T < 1 || a.T > 8) return cudaErrorInvalidValue;
   if (a.quant == MOE_Q8_0) return launch_q<MOE_Q8_0>(a, num_sms, st);
+  if (a.quant == MOE_I4_G64) return launch_q<MOE_I4_G64>(a, num_sms, st);
   return launch_q<MOE_Q4_0>(a, num_sms, st);
 }
 

@@ -34,7 +34,8 @@
  *     (Q8_0: int8 [rows][K]; Q4_0: uint8 [rows][K/2], byte j of a 32-block
  *     holds element j in its low nibble and element j+16 in its high nibble)
  *     followed by a little-endian fp16 scale plane [rows][K/32]. A weight is
- *     d*q (Q8_0) or d*(q-8) (Q4_0). All sizes K are multiples of 32.
+ *     d*q (Q8_0) or d*(q-8) (Q4_0). All sizes K are multiples of 32. The
+ *     affine INT4 format (MOE_I4_G64, below) keeps the same plane sizes.
  *   - A context is not thread-safe; use one per host thread.
  */
 #ifndef MOECACHE_H
@@ -60,7 +61,13 @@ typedef enum {
   MOE_ERR_STATE = 7        /* call order violated (e.g. no store bound) */
 } moe_status_t;
 
-typedef enum { MOE_Q8_0 = 0, MOE_Q4_0 = 1 } moe_quant_t;
+/* MOE_I4_G64: affine INT4 in groups of 64 along K ([RT] §3.1 gate/up/down
+ * with scales and biases, BF16 quantisation metadata): x = s*q + b, q an
+ * unsigned nibble, byte j of a row holding elements 2j (low nibble) and
+ * 2j+1 (high nibble); the metadata plane holds the bf16 (s, b) pairs
+ * [rows][K/64][2], as many bytes as a Q4_0 scale plane. Decode path only;
+ * every K a multiple of 64. */
+typedef enum { MOE_Q8_0 = 0, MOE_Q4_0 = 1, MOE_I4_G64 = 2 } moe_quant_t;
 /* Policies of a context: LRU and seeded random. The other two exist for
  * offline replays only (moe_replay): farthest next use needs the future
  * route trace, and the static working set is a fixed resident set. */

@@ -227,11 +227,23 @@ def test_staged_slot_bytes_equal_store(bec):
 
 
 @pytest.mark.parametrize("device_admit", MODES)
+def test_layer_affine_int4_trace(bec, device_admit):
+    # the decode shapes with affine INT4 group-64 experts: routing, page
+    # tables, counters and outputs against the oracle in every admission mode
+    w = W.with_changes(W.WORKLOADS["i4_decode"], n_layers=2, n_steps=12)
+    _run_trace(bec, w, 2, 12, {0, 5, 11}, device_admit=device_admit)
+
+
+@pytest.mark.parametrize("device_admit", MODES)
 def test_resident_slots_hold_store_payloads(bec, device_admit):
     # after decode steps with misses, every expert the page table marks
     # resident holds exactly its store payload, however it was materialised
     # (host copies, the staging kernel, or read-through by the FFN kernels)
-    w = W.with_changes(W.WORKLOADS["decode"], n_layers=1)
+    for name in ("decode", "i4_decode"):
+        _check_resident_payloads(bec, W.with_changes(W.WORKLOADS[name], n_layers=1), device_admit)
+
+
+def _check_resident_payloads(bec, w, device_admit):
     store = pinned_store(w, 1)
     ctx = make_context(bec, w, 1, device_admit=device_admit)
     keep = bind_all(ctx, w, 1, store)
