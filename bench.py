@@ -382,6 +382,67 @@ def replay_policies(bec, w, routers, x_dev, n_steps, dev):
     return out
 
 
+def run_int4_decode(args, dev, mode):
+    """The decode workload's shapes and trace recipe (40 layers, 1 token per
+    step, 15% cache, LRU) with affine INT4 group-64 experts (1.77 MB instead
+    of 3.34 MB per expert), graph-replayed with the headline's admission
+    mode; tokens/s and the miss bytes per step."""
+    import torch
+    import bounded_expert_cache_gb300 as bec
+    base = W.WORKLOADS["decode"]
+    n_steps = args.warmup + min(args.steps, 64)
+    w = W.with_changes(W.WORKLOADS["i4_decode"], n_layers=args.layers, n_steps=n_steps, slots=base.slots)
+    L, T, E, k, H = w.n_layers, w.tokens_per_step, w.n_experts, w.top_k, w.hidden
+    store = torch.empty((L, E, w.payload_bytes), dtype=torch.uint8, pin_memory=True)
+    W.fill_store(w, store.numpy())
+    shared = [torch.from_numpy(W.expert_payload(w, l, E)).to(dev) for l in range(L)]
+    routers = torch.stack([torch.from_numpy(W.router_weights(w, l)) for l in range(L)]).to(dev)
+    x_dev = torch.from_numpy(np.stack([W.activations(w, l, n_steps * T) for l in range(L)]).view(np.int16)) \
+        .view(torch.bfloat16).to(dev)
+    ctx = bec.Context(L, E, k, H, w.inter, w.shared_inter, w.quant, w.slots, w.policy, 3, 0, 262144, T,
+                      admit_on_device=mode)
+    ctx.bind_store(store)
+    for l in range(L):
+        ctx.bind_shared(l, shared[l])
+    plan = bec.Plan(E, k, T, dev)
+    idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+    wt = torch.empty((T, k), dtype=torch.float32, device=dev)
+    y = torch.empty((L, T, H), dtype=torch.float32, device=dev)
+    x_step = torch.empty((L, T, H), dtype=torch.bfloat16, device=dev)
+    for s in range(args.warmup - 1):
+        for l in range(L):
+            ctx.layer_forward(l, x_dev[l, s * T:(s + 1) * T], routers[l], None, idx, wt, plan, y[l])
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for l in range(L):
+            ctx.layer_forward(l, x_step[l], routers[l], None, idx, wt, plan, y[l])
+    x_step.copy_(x_dev[:, (args.warmup - 1) * T:args.warmup * T])
+    g.replay()
+    torch.cuda.synchronize(dev)
+    st0 = ctx.stats()
+    stream = torch.cuda.current_stream(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for s in range(args.warmup, n_steps):
+        x_step.copy_(x_dev[:, s * T:(s + 1) * T], non_blocking=True)
+        g.replay()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    ctx.check_device_errors()
+    st1 = ctx.stats()
+    del g
+    ctx.close()
+    steps = n_steps - args.warmup
+    ms = a.elapsed_time(b) / steps
+    misses = (st1["misses"] - st0["misses"]) / steps
+    return {"workload": f"decode shapes (hidden {H}, {E} experts top-{k} + 1 shared, inter {w.inter}), "
+                        f"affine INT4 group-64 experts, bf16, 1 token/step x {L} layers, {w.slots} slots LRU",
+            "admission": {2: "read-through", 1: "staging kernel"}[mode],
+            "tokens_per_s": round(T / (ms / 1e3), 2), "ms_per_step": round(ms, 4), "steps": steps,
+            "misses_per_step": round(misses, 2),
+            "miss_mb_per_step": round(misses * w.payload_bytes / 1e6, 2)}
+
+
 def run_prefill(args, dev):
     """The prefill workload: one 4096-token chunk (Zipf-skewed router bias),
     every expert resident, repeated for the timed steps; tokens/s of the whole
@@ -629,6 +690,8 @@ def main():
     ap.add_argument("--prefill-only", action="store_true", help="profiling: only the prefill pass")
     ap.add_argument("--skip-long-prefill", action="store_true", help="skip the long-prefill (waves) pass")
     ap.add_argument("--long-prefill-only", action="store_true", help="profiling: only the long-prefill pass")
+    ap.add_argument("--int4-decode-only", action="store_true",
+                    help="only the affine INT4 decode pass (--admission 1 or 2; 0 means read-through)")
     ap.add_argument("--prefill-tokens", type=int, default=0, help="profiling: tokens of the prefill chunk")
     ap.add_argument("--admission", type=int, default=0, choices=[0, 1, 2],
                     help="miss path of the headline pass (0: the faster of a short run of each; "
@@ -677,12 +740,17 @@ def main():
     if args.prefill_only:
         print(json.dumps({"prefill": run_prefill(args, dev)}))
         return
+    if args.int4_decode_only:
+        print(json.dumps({"int4_decode": run_int4_decode(args, dev, 1 if args.admission == 1 else 2)}))
+        return
     if args.long_prefill_only:
         print(json.dumps({"long_prefill": run_long_prefill(args, dev)}))
         return
     out, w = run_ours(args, rank, world, dev)
     if not args.skip_prefill:
         out["prefill"] = run_prefill(args, dev)
+    if not args.skip_prefill and world == 1:
+        out["int4_decode"] = run_int4_decode(args, dev, 2 if out.get("admission_mode") == "read-through" else 1)
     if not args.skip_long_prefill:
         out["long_prefill"] = run_long_prefill(args, dev)
     if rank == 0 and world == 1 and not args.skip_cpu:
