@@ -340,6 +340,20 @@ extern "C" moe_status_t moe_bind_store(moe_ctx_t* ctx, const void* store, size_t
       return fail(ctx, MOE_ERR_ARG, "moe_bind_store: store has no device mapping (on-device staging needs one)");
     dev = nullptr;
   }
+  if (dev) {
+    // touch every page once from the device (one load per page), so that no
+    // decode step pays the first-access cost of a page of the store
+    uint32_t* sink = nullptr;
+    e = cudaMalloc(&sink, sizeof(uint32_t));
+    if (e == cudaSuccess) e = moe::launch_touch_pages(static_cast<const uint8_t*>(dev), bytes, ctx->num_sms, sink,
+                                                      ctx->streams[0]);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(ctx->streams[0]);
+    if (sink) cudaFree(sink);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return fail(ctx, MOE_ERR_CUDA, std::string("moe_bind_store: ") + cudaGetErrorString(e));
+    }
+  }
   ctx->store = static_cast<const uint8_t*>(store);
   ctx->store_dev = static_cast<const uint8_t*>(dev);
   ctx->store_bytes = bytes;

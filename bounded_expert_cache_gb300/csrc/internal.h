@@ -148,6 +148,9 @@ struct StageArgs {
 };
 constexpr int64_t kStageChunkBytes = 32768;  // one CTA's copy: 256 threads x 8 x 16 B
 cudaError_t launch_stage_copy(const StageArgs& a, cudaStream_t st);
+// One load per kTouchPage bytes of a bound store (its device mapping), at bind time.
+constexpr size_t kTouchPage = 4096;
+cudaError_t launch_touch_pages(const uint8_t* dev_store, size_t bytes, int sms, uint32_t* sink, cudaStream_t st);
 
 // Arguments of the decode FFN launches.
 struct FfnArgs {

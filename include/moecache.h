@@ -164,8 +164,11 @@ int64_t moe_shared_payload_bytes(const moe_ctx_t* ctx);
 /* Bind the backing store of routed experts: PINNED host memory holding
  * payload [L][E] in split-plane layout, borrowed for the context's lifetime
  * ([MF] §IV-B split packs stand-in; [NfE] §3.4 pinned host memory).
+ * Binding reads one 32-bit word of every 4 KiB page of the store from the
+ * device and waits for it (about 0.1 s for 34 GB), so that the first miss
+ * on each page does not pay the device's first-access cost of host memory.
  * Errors: MOE_ERR_ARG if bytes != L*E*payload or the memory is not
- * page-locked. */
+ * page-locked; MOE_ERR_CUDA if that read fails. */
 moe_status_t moe_bind_store(moe_ctx_t* ctx, const void* pinned_host_store, size_t bytes);
 
 /* Bind the always-resident shared expert of a layer ([NfE] §1): a DEVICE
