@@ -178,6 +178,59 @@ def test_layer_mtp_decode_q4(bec, policy, seed, device_admit):
     _run_trace(bec, w, 1, 14, {0, 13}, policy=policy, seed=seed, device_admit=device_admit)
 
 
+@pytest.mark.parametrize("device_admit", [0, 2])
+@pytest.mark.parametrize("T", [2, 3, 5, 8])
+def test_layer_decode_token_counts(bec, T, device_admit):
+    # decode steps of 2..8 tokens: the FFN kernels' four- and eight-token
+    # groups, full (4, 8) and partial (2, 3, 5), with the union of up to T*k
+    # experts in the slots
+    w = W.with_changes(W.WORKLOADS["decode"], tokens_per_step=T, n_steps=6, slots=max(38, 8 * T))
+    _run_trace(bec, w, 1, 6, {0, 3, 5}, device_admit=device_admit)
+
+
+def test_calls_refuse_bad_token_counts(bec):
+    # T = 0 and T > max_tokens are refused before any launch; the context
+    # stays usable and the next valid step matches the oracle
+    w = W.with_changes(W.WORKLOADS["tiny"], n_steps=2)
+    T = w.tokens_per_step
+    store = pinned_store(w, 1)
+    ctx = make_context(bec, w, 1)
+    keep = bind_all(ctx, w, 1, store)
+    Wr = W.router_weights(w, 0)
+    Wr_t = torch.from_numpy(Wr).cuda()
+    plan = bec.Plan(w.n_experts, w.top_k, T)
+    x = W.activations(w, 0, 2 * T)
+    for bad in (0, T + 1):
+        xb = x_to_torch(w, np.resize(x, (bad, w.hidden)))
+        idx = torch.empty((max(bad, 1), w.top_k), dtype=torch.int32, device="cuda")
+        wt = torch.empty((max(bad, 1), w.top_k), dtype=torch.float32, device="cuda")
+        y = torch.empty((max(bad, 1), w.hidden), dtype=torch.float32, device="cuda")
+        with pytest.raises(bec.MoeError):
+            ctx.route(0, xb, Wr_t, None, idx, wt)
+        with pytest.raises(bec.MoeError):
+            ctx.layer_forward(0, xb, Wr_t, None, idx, wt, plan, y)
+    idx = torch.empty((T, w.top_k), dtype=torch.int32, device="cuda")
+    wt = torch.empty((T, w.top_k), dtype=torch.float32, device="cuda")
+    y = torch.empty((T, w.hidden), dtype=torch.float32, device="cuda")
+    xs = x[:T]
+    ctx.layer_forward(0, x_to_torch(w, xs), Wr_t, None, idx, wt, plan, y)
+    torch.cuda.synchronize()
+    ctx.check_device_errors()
+    x64 = x_to_f64(w, xs)
+    ridx, rw, _ = oracle.route(x64, Wr, None, w.top_k)
+    assert np.array_equal(idx.cpu().numpy(), ridx)
+    experts = ExpertCache(w)
+    ref = oracle.moe_layer(x64, ridx, rw, lambda e: experts.get(0, e),
+                           experts.get(0, w.n_experts) if w.shared_inter else None)
+    ok, rel, mx = tolerance_ok(y.cpu().numpy(), ref)
+    assert ok, (rel, mx)
+    st = ctx.stats(0)  # the refused calls counted nothing: one step from an empty cache
+    assert st["misses"] == len(set(ridx.ravel().tolist()))
+    assert st["hits"] + st["misses"] == T * w.top_k
+    ctx.close()
+    del keep
+
+
 @pytest.mark.parametrize("device_admit", [1, 2])
 def test_layer_decode_long_trace_device_admission(bec, device_admit):
     # the whole 128-step trace of one layer, cache state bit-exact every step
