@@ -141,6 +141,30 @@ def oracle_decode_sample(w: W.Workload, budget_s: float, max_layers: int):
     return spent / done * w.n_layers, done
 
 
+# ---------------------------------------------------------------- ranks
+# One process per GPU, each a replica of the whole step on its own inputs:
+# a barrier around the timed region, the slowest rank's time, and the
+# units of every rank over that time.
+def rank_barrier(world: int) -> None:
+    if world > 1:
+        import torch
+        torch.distributed.barrier()
+
+
+def max_over_ranks(v: float, world: int, device) -> float:
+    if world == 1:
+        return v
+    import torch
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, world: int, max_ms: float) -> float:
+    """Units all ranks processed per second of the slowest rank."""
+    return units_per_rank * world / (max_ms / 1e3)
+
+
 # ---------------------------------------------------------------- GPU arm
 def run_ours(args, rank, world, dev):
     import torch
@@ -182,16 +206,8 @@ def run_ours(args, rank, world, dev):
             ctx.layer_forward(l, x_dev[l, s * T:(s + 1) * T], routers[l], None, idx, wt, plan, y[l])
 
     def barrier():
-        if world > 1:
-            torch.distributed.barrier()
+        rank_barrier(world)
         torch.cuda.synchronize(dev)
-
-    def max_over_ranks(v: float) -> float:
-        if world == 1:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        return float(t.item())
 
     def timed(fn, n_timed=None):
         """Run fn(s) for the timed steps (or the first n_timed of them)
@@ -203,7 +219,7 @@ def run_ours(args, rank, world, dev):
             fn(s)
         ev1.record(stream)
         barrier()
-        return max_over_ranks(ev0.elapsed_time(ev1))
+        return max_over_ranks(ev0.elapsed_time(ev1), world, dev)
 
     x_step = torch.empty((L, T, H), dtype=torch.bfloat16, device=dev)
 
@@ -284,7 +300,7 @@ def run_ours(args, rank, world, dev):
     assert st1["misses"] - st0["misses"] == st_graph["misses"] - st0["misses"], "graph pass diverged"
 
     tokens = args.steps * T * world
-    value = tokens / (elapsed_ms / 1e3)
+    value = whole_job_rate(args.steps * T, world, elapsed_ms)
     policy_replay = replay_policies(bec, w, routers, x_dev, n_steps, dev) if rank == 0 else None
     extra = {"admission_mode": {2: "read-through", 1: "staging kernel"}[mode],
              "admission_probe_tokens_per_s": None if probe is None else
@@ -337,7 +353,7 @@ def run_ours(args, rank, world, dev):
     ctx.check_device_errors()
     del g
     ctx.close()
-    e2e_value = tokens / (e2e_ms / 1e3)
+    e2e_value = whole_job_rate(args.steps * T, world, e2e_ms)
     return finish(args, w, world, value, elapsed_ms, e2e_value, kt, st0, st1, clk, extra, mode), w
 
 
