@@ -115,6 +115,8 @@ extern "C" void moe_destroy(moe_ctx_t* ctx) {
   for (auto s : ctx->slots) moe_slots_destroy(s);
   for (auto e : ctx->ev_stage)
     if (e) cudaEventDestroy(e);
+  for (auto e : ctx->ev_stage_b)
+    if (e) cudaEventDestroy(e);
   for (auto& r : ctx->timed) {
     cudaEventDestroy(r.a);
     cudaEventDestroy(r.b);
@@ -241,7 +243,11 @@ extern "C" moe_status_t moe_create(const moe_config_t* cfg, moe_ctx_t** out) {
   ctx->max_units = std::min(E, c.max_tokens * c.top_k) + 1;
   // room for one unit table and one fill list per compute wave (a wave
   // holds at least one unit; fills <= units)
-  const size_t unit_ints = moe::kUnitHeader + 16 * static_cast<size_t>(ctx->max_units);
+  // a step's unit tables: at most 1.5 tables per unit (a wave is split only
+  // when it has two fills or more), each at most 8 ints of header and padding
+  // beyond 4 ints per unit and 2 per fill
+  const size_t unit_ints = moe::kUnitHeader + 32 * static_cast<size_t>(ctx->max_units);
+  ctx->unit_ints = unit_ints;
   CKC(cudaMalloc(&ctx->d_units, sizeof(int32_t) * unit_ints));
   CKC(cudaMemset(ctx->d_units, 0, sizeof(int32_t) * unit_ints));
   CKC(cudaHostAlloc(&ctx->h_units, sizeof(int32_t) * unit_ints, cudaHostAllocDefault));
@@ -293,9 +299,11 @@ extern "C" moe_status_t moe_create(const moe_config_t* cfg, moe_ctx_t** out) {
   }
   ctx->streams.assign(c.n_streams, nullptr);
   ctx->ev_stage.assign(c.n_streams, nullptr);
+  ctx->ev_stage_b.assign(c.n_streams, nullptr);
   for (int i = 0; i < c.n_streams; ++i) {
     CKC(cudaStreamCreateWithFlags(&ctx->streams[i], cudaStreamNonBlocking));
     CKC(cudaEventCreateWithFlags(&ctx->ev_stage[i], cudaEventDisableTiming));
+    CKC(cudaEventCreateWithFlags(&ctx->ev_stage_b[i], cudaEventDisableTiming));
   }
   CKC(cudaEventCreateWithFlags(&ctx->ev_compute, cudaEventDisableTiming));
   ctx->shared.assign(L, nullptr);
@@ -514,13 +522,19 @@ static void publish_page_table_host(moe_ctx_t* ctx, int32_t layer) {
   (void)S;
 }
 
-// Compute waves of one step: wave w's unit table sits at int offset off[w]
-// of the unit buffer and the list of its fills [n, (slot, generation) x n]
-// at offset pub[w]; fill i of the miss list leaves its slot at generation
-// fill_gen[i].
+// Compute waves of one step, each in two parts: part 0 holds the wave's
+// resident units and its first fills, part 1 its last fills (a quarter, at
+// least one, when the wave has two fills or more; else nothing). Part 0 is
+// computed while part 1's copies are still on the host link; a wave's fills
+// never evict its own units, so those copies touch no slot part 0 reads.
+// Part j of wave w has its unit table at int offset off[2w+j] of the unit
+// buffer and the list of its fills [n, (slot, generation) x n] at offset
+// pub[2w+j], with n_units[2w+j] units; fill i of the miss list belongs to
+// part part[i] and leaves its slot at generation fill_gen[i].
 struct WavePlan {
-  std::vector<int32_t> off, pub;
+  std::vector<int32_t> off, pub, n_units;
   std::vector<uint32_t> fill_gen;
+  std::vector<int8_t> part;
 };
 
 // Host admission of one step. With `waves` null a union larger than the
@@ -577,46 +591,71 @@ static moe_status_t admit_host(moe_ctx_t* ctx, int32_t layer, const moe_plan_t* 
     p0 += hu[E + e];
   }
   const int n_waves = std::max(1, misses->n_waves);
+  const int n_parts = waves ? 2 : 1;
+  // part of each expert (1: among the last fills of its wave)
+  std::vector<int8_t> part_of(E, 0);
   if (waves) {
-    waves->off.assign(n_waves, 0);
-    waves->pub.assign(n_waves, 0);
+    waves->off.assign(2 * n_waves, 0);
+    waves->pub.assign(2 * n_waves, 0);
+    waves->n_units.assign(2 * n_waves, 0);
+    waves->part.assign(misses->n, 0);
+    std::vector<int> nf_w(n_waves, 0), seen(n_waves, 0);
+    for (int i = 0; i < misses->n; ++i) ++nf_w[misses->wave[i]];
+    for (int i = 0; i < misses->n; ++i) {
+      const int w = misses->wave[i];
+      const int n_last = nf_w[w] >= 2 ? std::max(1, nf_w[w] / 4) : 0;
+      const int8_t pt = seen[w]++ >= nf_w[w] - n_last ? 1 : 0;
+      waves->part[i] = pt;
+      part_of[misses->expert[i]] = pt;
+    }
   }
   int32_t* ut = ctx->h_units;
-  int32_t at = 0;
+  size_t at = 0;
   for (int w = 0; w < n_waves; ++w) {
-    if (waves) waves->off[w] = at;
-    int32_t* tab = ut + at;
-    int n_tab = 0;
-    for (int i = 0; i < nu; ++i) {
-      const int e = hu[i];
-      if (wave_of[e] != w) continue;
-      int32_t* U = tab + moe::kUnitHeader + moe::kUnitInts * n_tab++;
-      U[0] = slot_of[e];
-      U[1] = p0_of[e];
-      U[2] = hu[E + e];
-      U[3] = static_cast<int32_t>(gen_of[e]);
-    }
-    if (w == 0 && ctx->cfg.shared_inter > 0) {
-      int32_t* U = tab + moe::kUnitHeader + moe::kUnitInts * n_tab++;
-      U[0] = -1;
-      U[1] = -1;
-      U[2] = p0 / ctx->cfg.top_k;  // tokens of the step
-      U[3] = 0;
-    }
-    tab[0] = n_tab;
-    at += moe::kUnitHeader + moe::kUnitInts * n_tab;
-    if (waves) {
-      waves->pub[w] = at;
-      int32_t* pl = ut + at;
-      int nf = 0;
-      for (int i = 0; i < misses->n; ++i) {
-        if (misses->wave[i] != w) continue;
-        pl[1 + 2 * nf] = misses->slot[i];
-        pl[2 + 2 * nf] = static_cast<int32_t>(waves->fill_gen[i]);
-        ++nf;
+    for (int pt = 0; pt < n_parts; ++pt) {
+      // size the table (and its fill list) before writing it
+      int need_units = (w == 0 && pt == 0 && ctx->cfg.shared_inter > 0) ? 1 : 0, need_fills = 0;
+      for (int i = 0; i < nu; ++i) need_units += wave_of[hu[i]] == w && part_of[hu[i]] == pt;
+      if (waves)
+        for (int i = 0; i < misses->n; ++i) need_fills += misses->wave[i] == w && waves->part[i] == pt;
+      const size_t need = moe::kUnitHeader + moe::kUnitInts * static_cast<size_t>(need_units) +
+                          (waves ? static_cast<size_t>((1 + 2 * need_fills + 3) / 4 * 4) : 0);
+      if (at + need > ctx->unit_ints) return fail(ctx, MOE_ERR_STATE, "admit: unit tables overflow their buffer");
+      if (waves) waves->off[n_parts * w + pt] = static_cast<int32_t>(at);
+      int32_t* tab = ut + at;
+      int n_tab = 0;
+      for (int i = 0; i < nu; ++i) {
+        const int e = hu[i];
+        if (wave_of[e] != w || part_of[e] != pt) continue;
+        int32_t* U = tab + moe::kUnitHeader + moe::kUnitInts * n_tab++;
+        U[0] = slot_of[e];
+        U[1] = p0_of[e];
+        U[2] = hu[E + e];
+        U[3] = static_cast<int32_t>(gen_of[e]);
       }
-      pl[0] = nf;
-      at += (1 + 2 * nf + 3) / 4 * 4;  // keep the next table 16-byte aligned
+      if (w == 0 && pt == 0 && ctx->cfg.shared_inter > 0) {
+        int32_t* U = tab + moe::kUnitHeader + moe::kUnitInts * n_tab++;
+        U[0] = -1;
+        U[1] = -1;
+        U[2] = p0 / ctx->cfg.top_k;  // tokens of the step
+        U[3] = 0;
+      }
+      tab[0] = n_tab;
+      at += moe::kUnitHeader + moe::kUnitInts * n_tab;
+      if (waves) {
+        waves->n_units[n_parts * w + pt] = n_tab;
+        waves->pub[n_parts * w + pt] = static_cast<int32_t>(at);
+        int32_t* pl = ut + at;
+        int nf = 0;
+        for (int i = 0; i < misses->n; ++i) {
+          if (misses->wave[i] != w || waves->part[i] != pt) continue;
+          pl[1 + 2 * nf] = misses->slot[i];
+          pl[2 + 2 * nf] = static_cast<int32_t>(waves->fill_gen[i]);
+          ++nf;
+        }
+        pl[0] = nf;
+        at += (1 + 2 * nf + 3) / 4 * 4;  // keep the next table 16-byte aligned
+      }
     }
   }
   CK(cudaMemcpyAsync(ctx->d_units, ut, sizeof(int32_t) * at, cudaMemcpyHostToDevice, st));
@@ -634,29 +673,38 @@ extern "C" moe_status_t moe_cache_admit(moe_ctx_t* ctx, int32_t layer, const moe
 }
 
 // Host->device copies of the fills of compute wave `wave` (all fills if
-// wave < 0), after the compute enqueued so far on `cst`; `cst` then waits
-// for them. The payload is cut into tiles of at most tile_bytes per matrix
+// wave < 0; with `part`, only fills i with part[i] == which), after the
+// compute enqueued so far on `cst` when `after_compute`; their completion is
+// recorded in `evs` (one event per copy stream), and `cst` waits for it when
+// `join`. *n_out (if given) receives the number of fills copied. The payload is cut into tiles of at most tile_bytes per matrix
 // (the accounting unit, and the point where the failure hook cuts); the
 // consecutive tiles of one fill go out as one copy, and fills rotate over
 // the copy streams: a copy costs microseconds of submission, which 256 KiB
 // copies would turn into the bound on the host link. The slots' new
 // generations are published by the caller.
 static moe_status_t stage_fills(moe_ctx_t* ctx, int32_t layer, const moe_miss_list_t* misses, int wave,
-                                cudaStream_t cst) {
+                                const int8_t* part, int which, cudaStream_t cst, bool after_compute,
+                                std::vector<cudaEvent_t>& evs, bool join, int* n_out = nullptr) {
   const int E = ctx->cfg.n_experts, S = ctx->cfg.slots_per_layer;
   const int ns = static_cast<int>(ctx->streams.size());
+  auto chosen = [&](int i) {
+    return (wave < 0 || misses->wave[i] == wave) && (!part || part[i] == which);
+  };
   int n = 0;
-  for (int i = 0; i < misses->n; ++i) n += wave < 0 || misses->wave[i] == wave;
+  for (int i = 0; i < misses->n; ++i) n += chosen(i);
+  if (n_out) *n_out = n;
   if (n == 0) return MOE_OK;
   // slots are overwritten only after the compute enqueued so far
-  CK(cudaEventRecord(ctx->ev_compute, cst));
-  for (int i = 0; i < ns; ++i) CK(cudaStreamWaitEvent(ctx->streams[i], ctx->ev_compute, 0));
+  if (after_compute) {
+    CK(cudaEventRecord(ctx->ev_compute, cst));
+    for (int i = 0; i < ns; ++i) CK(cudaStreamWaitEvent(ctx->streams[i], ctx->ev_compute, 0));
+  }
   const moe::ExpertGeom& g = ctx->geom;
   const int64_t tile = ctx->cfg.tile_bytes;
   int64_t issued = 0, bytes = 0, copies = 0;
   bool injected = false;
   for (int i = 0; i < misses->n && !injected; ++i) {
-    if (wave >= 0 && misses->wave[i] != wave) continue;
+    if (!chosen(i)) continue;
     const int e = misses->expert[i], slot = misses->slot[i];
     if (e < 0 || e >= E || slot < 0 || slot >= S) return fail(ctx, MOE_ERR_ARG, "stage: fill out of range");
     const uint8_t* src = ctx->store + (static_cast<size_t>(layer) * E + e) * g.bytes;
@@ -686,8 +734,8 @@ static moe_status_t stage_fills(moe_ctx_t* ctx, int32_t layer, const moe_miss_li
     ++copies;
   }
   for (int i = 0; i < ns; ++i) {
-    CK(cudaEventRecord(ctx->ev_stage[i], ctx->streams[i]));
-    CK(cudaStreamWaitEvent(cst, ctx->ev_stage[i], 0));
+    CK(cudaEventRecord(evs[i], ctx->streams[i]));
+    if (join) CK(cudaStreamWaitEvent(cst, evs[i], 0));
   }
   ctx->tiles_staged[layer] += issued;
   ctx->bytes_staged[layer] += bytes;
@@ -712,7 +760,7 @@ extern "C" moe_status_t moe_stage_tiles(moe_ctx_t* ctx, int32_t layer, const moe
   cudaStream_t cst = reinterpret_cast<cudaStream_t>(compute_stream);
   const int S = ctx->cfg.slots_per_layer;
   if (misses->n == 0) return MOE_OK;
-  moe_status_t s = stage_fills(ctx, layer, misses, -1, cst);
+  moe_status_t s = stage_fills(ctx, layer, misses, -1, nullptr, 0, cst, true, ctx->ev_stage, true);
   if (s != MOE_OK) return s;
   // publish the new generations of the filled slots
   const uint32_t* gen = moe::slots_gen(ctx->slots[layer]);
@@ -1021,18 +1069,31 @@ extern "C" moe_status_t moe_layer_forward(moe_ctx_t* ctx, int32_t layer, const v
   uint32_t* hg = ctx->h_gen + static_cast<size_t>(layer) * S;
   p.parts = moe::kPartGather;
   if ((s = prefill_run(ctx, p, st)) != MOE_OK) return s;
-  for (size_t w = 0; w < wp.off.size(); ++w) {
-    s = stage_fills(ctx, layer, ml, static_cast<int>(w), st);
+  const int n_waves = static_cast<int>(wp.off.size()) / 2;
+  for (int w = 0; w < n_waves; ++w) {
+    // both parts' copies go out now (part 1's behind part 0's on the same
+    // streams, with no new wait on the compute): part 0 is computed while
+    // part 1 is still on the host link
+    int nf[2] = {0, 0};
+    s = stage_fills(ctx, layer, ml, w, wp.part.data(), 0, st, true, ctx->ev_stage, false, &nf[0]);
     if (s != MOE_OK) return s;
-    // the wave's slots hold their new payloads: publish their generations
-    // on the device (from the wave's unit table) and in the host mirror
-    p.parts = moe::kPartGemm;
-    p.units = ctx->d_units + wp.off[w];
-    p.publish_gen = ctx->d_gen + static_cast<size_t>(layer) * S;
-    p.publish_list = ctx->d_units + wp.pub[w];
-    if ((s = prefill_run(ctx, p, st)) != MOE_OK) return s;
-    for (int i = 0; i < ml->n; ++i)
-      if (ml->wave[i] == static_cast<int>(w)) hg[ml->slot[i]] = wp.fill_gen[i];
+    s = stage_fills(ctx, layer, ml, w, wp.part.data(), 1, st, false, ctx->ev_stage_b, false, &nf[1]);
+    if (s != MOE_OK) return s;
+    for (int pt = 0; pt < 2; ++pt) {
+      const int sw = 2 * w + pt;
+      if (wp.n_units[sw] == 0) continue;
+      if (nf[pt] > 0)
+        for (auto e : pt == 0 ? ctx->ev_stage : ctx->ev_stage_b) CK(cudaStreamWaitEvent(st, e, 0));
+      // the part's slots hold their new payloads: publish their generations
+      // on the device (from the part's fill list) and in the host mirror
+      p.parts = moe::kPartGemm;
+      p.units = ctx->d_units + wp.off[sw];
+      p.publish_gen = ctx->d_gen + static_cast<size_t>(layer) * S;
+      p.publish_list = ctx->d_units + wp.pub[sw];
+      if ((s = prefill_run(ctx, p, st)) != MOE_OK) return s;
+      for (int i = 0; i < ml->n; ++i)
+        if (ml->wave[i] == w && wp.part[i] == pt) hg[ml->slot[i]] = wp.fill_gen[i];
+    }
   }
   p.parts = moe::kPartCombine;
   p.publish_gen = nullptr;

@@ -239,8 +239,9 @@ struct moe_ctx {
   int32_t* d_flags = nullptr;
   float2* d_lpart = nullptr;               // split-K logit partials [4][T][E]
   std::vector<cudaStream_t> streams;
-  std::vector<cudaEvent_t> ev_stage;
+  std::vector<cudaEvent_t> ev_stage, ev_stage_b;  // copies of a wave's two parts
   cudaEvent_t ev_compute = nullptr;
+  size_t unit_ints = 0;  // capacity of the unit-table buffer
   int32_t fail_after_tiles = -1;
   // kernel timing
   struct TimedLaunch {
