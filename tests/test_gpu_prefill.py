@@ -213,10 +213,13 @@ def test_prefill_waves_union_larger_than_slots(bec):
     del keep
 
 
-def test_prefill_waves_failed_staging_fails_closed(bec):
-    # a copy failure inside a later wave: the call fails, the waves before it
-    # published their slots, and the experts whose payloads never landed are
-    # refused (stale generation) when the next step reads them
+@pytest.mark.parametrize("fills_before", ["wave1", "wave0_last_part"])
+def test_prefill_waves_failed_staging_fails_closed(bec, fills_before):
+    # a copy failure inside a later wave, or inside the last part of the
+    # first wave (a wave's last quarter of fills, copied while its first
+    # part would compute): the call fails, only waves whose copies all
+    # landed publish their slots, and the experts whose payloads never landed
+    # are refused (stale generation) when the next step reads them
     w = W.WORKLOADS["wide_prefill"]
     T, E = 256, w.n_experts
     store = pinned_store(w, 1)
@@ -231,7 +234,9 @@ def test_prefill_waves_failed_staging_fails_closed(bec):
     wt = torch.empty((T, w.top_k), dtype=torch.float32, device="cuda")
     y = torch.empty((T, w.hidden), dtype=torch.float32, device="cuda")
     tiles = len(oracle.tile_partition(w.hidden, w.inter, w.quant))
-    ctx.debug_fail_staging_after(w.slots * tiles + 3)  # inside wave 1 of a cold step
+    # a cold step's wave 0 fills all 44 slots: 33 fills in its first part, 11 in its last
+    first_part = w.slots - max(1, w.slots // 4)
+    ctx.debug_fail_staging_after((w.slots if fills_before == "wave1" else first_part) * tiles + 3)
     with pytest.raises(bec.MoeError):
         ctx.layer_forward(0, xt, Wr_t, b_t, idx, wt, plan, y)
     ctx.check_device_errors()  # nothing was read from an unpublished slot
