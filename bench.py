@@ -711,6 +711,7 @@ def main():
     ap.add_argument("--prefill-only", action="store_true", help="profiling: only the prefill pass")
     ap.add_argument("--skip-long-prefill", action="store_true", help="skip the long-prefill (waves) pass")
     ap.add_argument("--long-prefill-only", action="store_true", help="profiling: only the long-prefill pass")
+    ap.add_argument("--skip-int4", action="store_true", help="skip the affine INT4 decode pass")
     ap.add_argument("--int4-decode-only", action="store_true",
                     help="only the affine INT4 decode pass (--admission 1 or 2; 0 means read-through)")
     ap.add_argument("--prefill-tokens", type=int, default=0, help="profiling: tokens of the prefill chunk")
@@ -770,7 +771,7 @@ def main():
     out, w = run_ours(args, rank, world, dev)
     if not args.skip_prefill:
         out["prefill"] = run_prefill(args, dev)
-    if not args.skip_prefill and world == 1:
+    if not args.skip_int4 and world == 1:
         out["int4_decode"] = run_int4_decode(args, dev, 2 if out.get("admission_mode") == "read-through" else 1)
     if not args.skip_long_prefill:
         out["long_prefill"] = run_long_prefill(args, dev)
