@@ -278,7 +278,10 @@ moe_status_t moe_expert_ffn(moe_ctx_t* ctx, int32_t layer, const void* x, int32_
  * sequence): a fill that evicts an expert of the same step belongs to the
  * wave after that expert's. The activations are gathered once; per wave the
  * wave's fills are staged (after the previous wave's GEMMs) and the grouped
- * GEMMs run over the wave's experts; one combine follows. The output is the
+ * GEMMs run over the wave's experts, in two parts: the resident experts and
+ * first fills, then the last quarter of the fills, whose copies overlap the
+ * first part's GEMMs (a wave's fills never evict its own experts). A copy
+ * failure leaves the whole wave unpublished. One combine follows. The output is the
  * same, bit for bit, as with every expert resident. Decode (T <= 8) returns
  * MOE_ERR_CAPACITY for such a step; on-device admission admits nothing and
  * moe_check_device_errors reports MOE_ERR_CAPACITY. */
