@@ -188,6 +188,33 @@ def test_layer_decode_token_counts(bec, T, device_admit):
     _run_trace(bec, w, 1, 6, {0, 3, 5}, device_admit=device_admit)
 
 
+@pytest.mark.parametrize("device_admit", [0, 2])
+@pytest.mark.parametrize("T", [1, 4])
+def test_layer_at_maximum_experts_and_top_k(bec, T, device_admit):
+    # the ABI's limits, 1,024 experts and top-16: the router's general
+    # selection path (more than 256 experts), its block planner (more than 32
+    # assignments at T = 4) and the admission warp reading the cache state
+    w = W.with_changes(W.WORKLOADS["tiny"], n_experts=1024, top_k=16, tokens_per_step=T, n_steps=3,
+                       slots=max(32, 16 * T))
+    _run_trace(bec, w, 1, 3, {0, 2}, device_admit=device_admit)
+
+
+def test_route_many_tokens_at_maximum_experts_and_top_k(bec):
+    # the many-token router (T > 64: tiled logits, key folding, selection,
+    # exact repair) at 1,024 experts and top-16
+    w = W.with_changes(W.WORKLOADS["tiny"], n_experts=1024, top_k=16, tokens_per_step=100, n_steps=1,
+                       slots=1024)
+    T = w.tokens_per_step
+    ctx = make_context(bec, w, 1, max_tokens=T)
+    Wr = W.router_weights(w, 0)
+    x = W.activations(w, 0, T)
+    idx, wt = _route_gpu(bec, ctx, 0, x_to_torch(w, x), torch.from_numpy(Wr).cuda(), None, w.top_k)
+    ridx, rw, _ = oracle.route(x_to_f64(w, x), Wr, None, w.top_k)
+    assert np.array_equal(idx, ridx)
+    assert np.allclose(wt, rw, rtol=1e-5, atol=1e-7)
+    ctx.close()
+
+
 def test_calls_refuse_bad_token_counts(bec):
     # T = 0 and T > max_tokens are refused before any launch; the context
     # stays usable and the next valid step matches the oracle
