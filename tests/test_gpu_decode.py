@@ -215,6 +215,46 @@ def test_route_many_tokens_at_maximum_experts_and_top_k(bec):
     ctx.close()
 
 
+@pytest.mark.parametrize("T", [1, 4, 100])
+def test_route_reports_non_finite_input(bec, T):
+    # a NaN in one token's activations leaves its routing undefined: the
+    # router reports MOE_ERR_UNCERTIFIED (a decode step with on-device
+    # admission through the last block's tail, or the many-token router)
+    # and the next clean call matches the oracle
+    w = W.with_changes(W.WORKLOADS["tiny"], tokens_per_step=T, n_steps=2)
+    decode = T <= 8
+    ctx = make_context(bec, w, 1, max_tokens=T, device_admit=2 if decode else 0)
+    keep = bind_all(ctx, w, 1, pinned_store(w, 1)) if decode else None
+    Wr = W.router_weights(w, 0)
+    Wr_t = torch.from_numpy(Wr).cuda()
+    x = W.activations(w, 0, 2 * T)
+    bad = x[:T].copy()
+    bad[0, 5] = np.nan
+    idx = torch.empty((T, w.top_k), dtype=torch.int32, device="cuda")
+    wt = torch.empty((T, w.top_k), dtype=torch.float32, device="cuda")
+    plan = bec.Plan(w.n_experts, w.top_k, T)
+    y = torch.empty((T, w.hidden), dtype=torch.float32, device="cuda")
+
+    def call(xs):
+        if decode:
+            ctx.layer_forward(0, x_to_torch(w, xs), Wr_t, None, idx, wt, plan, y)
+        else:
+            ctx.route(0, x_to_torch(w, xs), Wr_t, None, idx, wt)
+
+    call(bad)
+    with pytest.raises(bec.MoeError) as ei:
+        ctx.check_device_errors()
+    assert ei.value.status == 6  # MOE_ERR_UNCERTIFIED
+    good = x[T:]
+    call(good)
+    ctx.check_device_errors()
+    ridx, rw, _ = oracle.route(x_to_f64(w, good), Wr, None, w.top_k)
+    assert np.array_equal(idx.cpu().numpy(), ridx)
+    assert np.allclose(wt.cpu().numpy(), rw, rtol=1e-5, atol=1e-7)
+    ctx.close()
+    del keep
+
+
 def test_calls_refuse_bad_token_counts(bec):
     # T = 0 and T > max_tokens are refused before any launch; the context
     # stays usable and the next valid step matches the oracle
