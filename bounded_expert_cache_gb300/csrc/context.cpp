@@ -1077,7 +1077,8 @@ extern "C" moe_status_t moe_layer_forward(moe_ctx_t* ctx, int32_t layer, const v
     int nf[2] = {0, 0};
     s = stage_fills(ctx, layer, ml, w, wp.part.data(), 0, st, true, ctx->ev_stage, false, &nf[0]);
     if (s != MOE_OK) return s;
-    s = stage_fills(ctx, layer, ml, w, wp.part.data(), 1, st, false, ctx->ev_stage_b, false, &nf[1]);
+    // (part 1 waits for the compute itself if part 0 copied nothing)
+    s = stage_fills(ctx, layer, ml, w, wp.part.data(), 1, st, nf[0] == 0, ctx->ev_stage_b, false, &nf[1]);
     if (s != MOE_OK) return s;
     for (int pt = 0; pt < 2; ++pt) {
       const int sw = 2 * w + pt;
