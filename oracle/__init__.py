@@ -26,9 +26,12 @@ Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s ``cpu_baseline``
 leg may import this package. It shares no code with the CUDA path and never
 consumes its outputs.
 
-Pins: every function here is checked in ``tests/test_oracle_pins.py`` against
-closed forms, brute force, an independent implementation of textbook LRU and
-the byte counts printed on the pages. The routine ``moe_layer`` (fp64 FFN) is
+Pins: every function here is checked in ``tests/test_oracle_formats.py``,
+``test_oracle_route.py``, ``test_oracle_ffn.py``, ``test_oracle_cache.py``,
+``test_oracle_replay.py``, ``test_oracle_budget.py`` and
+``test_oracle_trace.py`` against closed forms, brute force, an independent
+implementation of textbook LRU, hand-worked replays and the byte counts
+printed on the pages. The routine ``moe_layer`` (fp64 FFN) is
 pinned by permutation-matrix closed forms; no page prints a worked output
 vector for synthetic inputs.
 """
