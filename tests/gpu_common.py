@@ -69,3 +69,26 @@ def bind_all(ctx, w: W.Workload, layers: int, store: torch.Tensor):
             ctx.bind_shared(l, p)
             shared.append(p)
     return shared
+
+
+def _route_rows(args):
+    x64, wr, bias, k = args
+    idx, w, _ = oracle.route(x64, wr, bias, k)
+    return idx, w
+
+
+def oracle_route_rows(x64: np.ndarray, wr: np.ndarray, bias, k: int, rows, workers: int = 0):
+    """Oracle routing of the given token rows, split over a pool of worker
+    processes started with ``spawn`` (a forked child of a process that has
+    used the GPU can hang). Returns (idx [n,k], weights [n,k]) in row order."""
+    import multiprocessing as mp
+    import os
+    rows = list(rows)
+    n = len(rows)
+    workers = workers or max(1, min(16, (os.cpu_count() or 1), n // 32))
+    if workers <= 1 or n < 64:
+        return _route_rows((x64[rows], wr, bias, k))
+    parts = np.array_split(np.asarray(rows), workers)
+    with mp.get_context("spawn").Pool(workers) as pool:
+        res = pool.map(_route_rows, [(x64[p], wr, bias, k) for p in parts])
+    return np.concatenate([r[0] for r in res]), np.concatenate([r[1] for r in res])

@@ -15,8 +15,8 @@ import workloads as W
 
 from oracle.cache import SlotCache
 
-from gpu_common import (ExpertCache, bind_all, make_context, pinned_store, tolerance_ok, x_to_f64,
-                        x_to_torch)
+from gpu_common import (ExpertCache, bind_all, make_context, oracle_route_rows, pinned_store,
+                        tolerance_ok, x_to_f64, x_to_torch)
 
 pytestmark = pytest.mark.gpu
 
@@ -120,10 +120,61 @@ def test_prefill_chunk_sampled(bec):
     _prefill(bec, w, 512, [0, 1, 7, 100, 255, 256, 400, 511])
 
 
-def test_prefill_full_chunk_4096_sampled(bec):
-    # the full 4096-token Zipf-skewed chunk, checked on sampled tokens
+def test_prefill_full_chunk_4096_every_expert(bec):
+    # the full 4096-token Zipf-skewed chunk: routing of all 4,096 tokens and
+    # the expert-major plan bit-exact; the output within the bar on, for
+    # every active expert, its first token, the first token of its last
+    # 192-token tile and its last token (so every expert's partial tile is
+    # read), plus every token of one heavy tile
     w = W.WORKLOADS["prefill"]
-    _prefill(bec, w, 4096, [0, 1000, 2047, 3333, 4095])
+    T, E, k = 4096, w.n_experts, w.top_k
+    store = pinned_store(w, 1)
+    ctx = make_context(bec, w, 1, slots=E, max_tokens=T, device_admit=1)
+    keep = bind_all(ctx, w, 1, store)
+    ctx.preload(0, list(range(E)))
+    Wr = W.router_weights(w, 0)
+    bias = W.router_bias(w, 0)
+    x = W.activations(w, 0, T)
+    plan = bec.Plan(E, k, T)
+    idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    wt = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    y = torch.empty((T, w.hidden), dtype=torch.float32, device="cuda")
+    ctx.layer_forward(0, x_to_torch(w, x), torch.from_numpy(Wr).cuda(), torch.from_numpy(bias).cuda(),
+                      idx, wt, plan, y)
+    ctx.check_device_errors()
+    yg = y.cpu().numpy().astype(np.float64)
+    x64 = x_to_f64(w, x)
+    ridx, rw = oracle_route_rows(x64, Wr, bias, k, range(T))
+    assert np.array_equal(idx.cpu().numpy(), ridx)
+    assert np.allclose(wt.cpu().numpy(), rw, rtol=1e-5, atol=1e-7)
+    rplan = oracle.plan_union(ridx, rw, E)
+    nu = int(plan.n_uniq.item())
+    assert plan.uniq[:nu].cpu().numpy().tolist() == rplan["uniq"].tolist()
+    for key in ("counts", "offsets"):
+        assert np.array_equal(getattr(plan, key).cpu().numpy(), rplan[key]), key
+    for key in ("perm_tok", "perm_rank", "inv"):
+        assert np.array_equal(getattr(plan, key)[:T * k].cpu().numpy(), rplan[key]), key
+    tile = 192  # tokens per GEMM tile
+    sample = set()
+    for e in rplan["uniq"].tolist():
+        toks = rplan["perm_tok"][rplan["offsets"][e]:rplan["offsets"][e + 1]]
+        sample.update((int(toks[0]), int(toks[(len(toks) - 1) // tile * tile]), int(toks[-1])))
+    heavy = int(np.argmax(rplan["counts"]))
+    toks = rplan["perm_tok"][rplan["offsets"][heavy]:rplan["offsets"][heavy + 1]]
+    sample.update(int(t) for t in toks[tile:2 * tile])
+    sample = sorted(sample)
+    assert len(rplan["uniq"]) > 100 and len(sample) > 300
+    experts = ExpertCache(w)
+    shared = experts.get(0, E)
+    refs = [oracle.moe_layer(x64[t:t + 1], ridx[t:t + 1], rw[t:t + 1], lambda e: experts.get(0, e),
+                             shared)[0] for t in sample]
+    ok, rel, mx = tolerance_ok(yg[sample], np.stack(refs))
+    assert ok, (rel, mx)
+    for t, ref in zip(sample, refs):  # every sampled token on its own
+        ok, rel, mx = tolerance_ok(yg[t:t + 1], ref[None])
+        assert ok, (t, rel, mx)
+    ctx.close()
+    del keep
 
 
 def test_prefill_wide_shapes(bec):
@@ -246,3 +297,4 @@ def test_prefill_waves_failed_staging_fails_closed(bec, fills_before):
     assert ei.value.status == 4  # MOE_ERR_STALE
     ctx.close()
     del keep
+
