@@ -96,6 +96,7 @@ SIGNATURES = [
     ("moe_get_kernel_times", _st, [_vp, C.POINTER(C.c_double), C.POINTER(_i64)]),
     ("moe_debug_fail_staging_after", _st, [_vp, _i32]),
     ("moe_debug_corrupt_generation", _st, [_vp, _i32, _i32]),
+    ("moe_debug_prefill_wait_timeout", _st, [_vp, _i64, _i32]),
     ("moe_slots_create", _st, [_i32, _i32, _i32, _u64, _i32, _i64, C.POINTER(_vp)]),
     ("moe_slots_destroy", None, [_vp]),
     ("moe_slots_step", _st, [_vp, C.POINTER(_i32), _i32, C.POINTER(_i32), C.POINTER(MissList)]),

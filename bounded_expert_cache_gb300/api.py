@@ -199,6 +199,9 @@ class Context:
     def debug_corrupt_generation(self, layer, expert):
         self._ck(lib.moe_debug_corrupt_generation(self.h, layer, expert))
 
+    def debug_prefill_wait_timeout(self, wait_cycles: int, skip_ring: int):
+        self._ck(lib.moe_debug_prefill_wait_timeout(self.h, wait_cycles, skip_ring))
+
 
 def _misses(ml: N.MissList) -> Misses:
     n = ml.n

@@ -888,6 +888,14 @@ static moe_status_t prefill_setup(moe_ctx_t* ctx, int32_t layer, const void* x, 
 // Enqueues the parts p.parts of the prefill FFN (timed when enabled).
 static moe_status_t prefill_run(moe_ctx_t* ctx, moe::PrefillArgs& p, cudaStream_t st) {
   const bool timed = ctx->timing && (p.parts & moe::kPartGemm);
+  p.wait_cycles = 0;
+  p.skip_ring = -1;
+  if ((p.parts & moe::kPartGemm) && ctx->dbg_skip_ring >= 0) {  // one-shot test hook
+    p.wait_cycles = ctx->dbg_wait_cycles;
+    p.skip_ring = ctx->dbg_skip_ring;
+    ctx->dbg_wait_cycles = 0;
+    ctx->dbg_skip_ring = -1;
+  }
   for (int i = 0; i < 4; ++i) p.ev[i] = timed ? timing_event(ctx) : nullptr;
   CK(moe::prefill_ffn(p, st));
   if (timed) {
@@ -1208,6 +1216,15 @@ extern "C" moe_status_t moe_debug_corrupt_generation(moe_ctx_t* ctx, int32_t lay
   CK(cudaMemcpy(&g, ctx->d_gen + layer * S + slot, sizeof(uint32_t), cudaMemcpyDeviceToHost));
   g += 0x10000u;
   CK(cudaMemcpy(ctx->d_gen + layer * S + slot, &g, sizeof(uint32_t), cudaMemcpyHostToDevice));
+  return MOE_OK;
+}
+
+extern "C" moe_status_t moe_debug_prefill_wait_timeout(moe_ctx_t* ctx, int64_t wait_cycles, int32_t skip_ring) {
+  if (!ctx) return MOE_ERR_ARG;
+  if (skip_ring < -1 || wait_cycles < 0)
+    return fail(ctx, MOE_ERR_ARG, "debug_prefill_wait_timeout: bad arguments");
+  ctx->dbg_skip_ring = skip_ring;
+  ctx->dbg_wait_cycles = skip_ring >= 0 ? wait_cycles : 0;
   return MOE_OK;
 }
 

@@ -242,6 +242,8 @@ struct moe_ctx {
   std::vector<cudaEvent_t> ev_stage, ev_stage_b;  // copies of a wave's two parts
   cudaEvent_t ev_compute = nullptr;
   size_t unit_ints = 0;  // capacity of the unit-table buffer
+  long long dbg_wait_cycles = 0;  // test hook of the next prefill gate/up GEMM
+  int32_t dbg_skip_ring = -1;
   int32_t fail_after_tiles = -1;
   // kernel timing
   struct TimedLaunch {

@@ -225,6 +225,8 @@ static cudaError_t prefill_gemms(const PrefillArgs& p, cudaStream_t st) {
   // 4. gate/up + SwiGLU
   a.items = p.items0;
   a.n_items = p.n_items0;
+  a.wait_cycles = p.wait_cycles > 0 ? p.wait_cycles : kPrefillWaitCycles;
+  a.skip_ring = p.skip_ring;
   a.stages = gemm_stages(0);
   if (a.stages == 0) return cudaErrorInvalidValue;
   if (p.ev[0]) cudaEventRecord(p.ev[0], st);
@@ -233,6 +235,8 @@ static cudaError_t prefill_gemms(const PrefillArgs& p, cudaStream_t st) {
   // 5. down (the combine applies the weights)
   a.items = p.items1;
   a.n_items = p.n_items1;
+  a.wait_cycles = kPrefillWaitCycles;
+  a.skip_ring = -1;
   a.stages = gemm_stages(1);
   if (a.stages == 0) return cudaErrorInvalidValue;
   if (p.ev[2]) cudaEventRecord(p.ev[2], st);

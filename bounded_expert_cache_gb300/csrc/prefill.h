@@ -10,6 +10,7 @@
 namespace moe {
 
 constexpr int kPrefillTok = 192;  // tokens per GEMM work item
+constexpr long long kPrefillWaitCycles = 4000000000ll;  // about 2 s at the SM clock
 
 // Tensor maps of one GEMM launch: the token operand in 32-row boxes and in
 // whole-tile boxes, and the quant planes of the routed experts (4-D: bytes,
@@ -36,6 +37,10 @@ struct GemmArgs {
   const uint32_t* gen;      // [S] published slot generations (fail-closed check)
   int S;
   int stages;
+  long long wait_cycles;    // limit of every mbarrier wait (SM clock cycles)
+  int skip_ring;            // test hook: CTA 0's producer issues no copy for
+                            // this ring index (-1: off), so the consumers'
+                            // wait on it runs out
 };
 
 // One prefill FFN call: gather, both GEMMs, combine. A step whose union is
@@ -66,6 +71,8 @@ struct PrefillArgs {
   uint32_t* err;
   const uint32_t* gen;
   cudaEvent_t ev[4];        // optional timing around the two GEMMs
+  long long wait_cycles;    // 0: the default limit of the GEMMs' waits (about 2 s)
+  int skip_ring;            // test hook of the gate/up GEMM (see GemmArgs), -1: off
 };
 cudaError_t prefill_ffn(const PrefillArgs& p, cudaStream_t st);
 

@@ -77,7 +77,6 @@ template <int PHASE> struct Shape {
   static_assert(kStageBytes % 1024 == 0, "stage alignment");
 };
 
-constexpr long long kWaitCycles = 4000000000ll;  // about 2 s at the SM clock
 
 __device__ __forceinline__ uint32_t su32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -100,11 +99,12 @@ __device__ __forceinline__ bool mbar_try(uint32_t b, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Bounded wait on a phase of an mbarrier. False if it ran out (about 2 s;
-// this raises the CTA's abort flag) or if another role has aborted. The
-// clock and the flag are read once per 16 probes.
+// Bounded wait on a phase of an mbarrier. False if it ran out (after
+// `limit` SM cycles, about 2 s unless a test shortens it; this raises the
+// CTA's abort flag) or if another role has aborted. The clock and the flag
+// are read once per 16 probes.
 __device__ __forceinline__ bool mbar_wait(uint32_t b, uint32_t parity, volatile int* abort_flag,
-                                          uint32_t* err) {
+                                          uint32_t* err, long long limit) {
   if (mbar_try(b, parity)) return true;
   const long long t0 = clock64();
   while (true) {
@@ -112,7 +112,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t b, uint32_t parity, volatile 
     for (int i = 0; i < 16; ++i)
       if (mbar_try(b, parity)) return true;
     if (*abort_flag) return false;
-    if (clock64() - t0 > kWaitCycles) {
+    if (clock64() - t0 > limit) {
       *abort_flag = 1;
       atomicOr(err, MOE_DEVERR_TIMEOUT);
       return false;
@@ -131,10 +131,10 @@ struct RingPos {
   }
 };
 // Bounded wait that ignores the abort flag (draining before exit).
-__device__ __forceinline__ void mbar_drain(uint32_t b, uint32_t parity, uint32_t* err) {
+__device__ __forceinline__ void mbar_drain(uint32_t b, uint32_t parity, uint32_t* err, long long limit) {
   const long long t0 = clock64();
   while (!mbar_try(b, parity)) {
-    if (clock64() - t0 > kWaitCycles) {
+    if (clock64() - t0 > limit) {
       atomicOr(err, MOE_DEVERR_TIMEOUT);
       return;
     }
@@ -390,8 +390,9 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
         for (int kb = 0; kb < nkb; ++kb, ++ring, rp.next(kStages)) {
           const int s = rp.s;
           if (ring >= static_cast<uint32_t>(kStages) &&
-              !(ok = mbar_wait(su32(&bar_sfree[s]), rp.ph ^ 1u, abort_flag, a.err)))
+              !(ok = mbar_wait(su32(&bar_sfree[s]), rp.ph ^ 1u, abort_flag, a.err, a.wait_cycles)))
             break;
+          if (static_cast<int>(ring) == a.skip_ring && blockIdx.x == 0) continue;  // test hook: nothing issued
           const uint32_t st = sbase + s * Sh::kStageBytes, fb = su32(&bar_full[s]);
           mbar_expect_tx(fb, bytes);
           if (whole)
@@ -406,7 +407,8 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
       const uint32_t n = ring < static_cast<uint32_t>(kStages) ? ring : static_cast<uint32_t>(kStages);
       for (uint32_t j = 0; j < n; ++j) {
         const uint32_t r = ring - 1 - j;
-        mbar_drain(su32(&bar_full[r % kStages]), (r / kStages) & 1u, a.err);
+        if (static_cast<int>(r) == a.skip_ring && blockIdx.x == 0) continue;  // no copy in flight
+        mbar_drain(su32(&bar_full[r % kStages]), (r / kStages) & 1u, a.err, a.wait_cycles);
       }
     }
   } else if (warp == 1) {
@@ -428,13 +430,13 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
         const uint32_t buf = Sh::kAccBufs == 2 ? (acc_i & 1u) : 0u;
         const uint32_t cph = Sh::kAccBufs == 2 ? ((acc_i >> 1) & 1u) : (acc_i & 1u);
         if (acc_i >= static_cast<uint32_t>(Sh::kAccBufs) &&
-            !mbar_wait(su32(&bar_acce[buf]), cph ^ 1u, abort_flag, a.err))
+            !mbar_wait(su32(&bar_acce[buf]), cph ^ 1u, abort_flag, a.err, a.wait_cycles))
           break;
         asm volatile("tcgen05.fence::after_thread_sync;");
         const uint32_t dt = tmem + buf * static_cast<uint32_t>(kTok);
         bool ok = true;
         for (int kb = 0; kb < nkb; ++kb) {
-          if (!(ok = mbar_wait(su32(&bar_aready[j]), aph, abort_flag, a.err))) break;
+          if (!(ok = mbar_wait(su32(&bar_aready[j]), aph, abort_flag, a.err, a.wait_cycles))) break;
           asm volatile("tcgen05.fence::after_thread_sync;");
           const uint64_t bd = bd0 + static_cast<uint64_t>((static_cast<uint32_t>(s) * Sh::kStageBytes) >> 4);
           const uint32_t at = tmem + kAcc + Sh::kAStride * static_cast<uint32_t>(j);
@@ -459,7 +461,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
       }
       // drain: every MMA issued here has completed before TMEM is released
       umma_commit(su32(&bar_drain));
-      mbar_drain(su32(&bar_drain), 0, a.err);
+      mbar_drain(su32(&bar_drain), 0, a.err, a.wait_cycles);
       (void)ring;
     }
   } else if (warp < 2 + kDqWarps) {
@@ -516,7 +518,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
           }
         }
         const int s = rp.s, j = ap.s;
-        if (!(ok = mbar_wait(su32(&bar_full[s]), rp.ph, abort_flag, a.err))) break;
+        if (!(ok = mbar_wait(su32(&bar_full[s]), rp.ph, abort_flag, a.err, a.wait_cycles))) break;
         const uint32_t sq = sbase + s * Sh::kStageBytes + qrow;
         uint32_t out[32];
         if (PHASE == 0) {
@@ -547,7 +549,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
         __syncwarp();
         if (lane == 0) mbar_arrive(su32(&bar_sfree[s]));
         if (ring >= static_cast<uint32_t>(kAStages) &&
-            !(ok = mbar_wait(su32(&bar_afree[j]), ap.ph ^ 1u, abort_flag, a.err)))
+            !(ok = mbar_wait(su32(&bar_afree[j]), ap.ph ^ 1u, abort_flag, a.err, a.wait_cycles)))
           break;
         asm volatile("tcgen05.fence::after_thread_sync;");
         const uint32_t ta = tmem + lane_base + kAcc + Sh::kAStride * j;
@@ -576,8 +578,12 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
     const int sp = warp & 3;
     const int r = sp * 32 + lane;  // weight row within the tile
     const uint32_t lane_base = static_cast<uint32_t>(sp * 32) << 16;
+    // The four epilogue warps meet at named barriers inside an item, so they
+    // decide together whether to take it: by its accumulator barrier alone
+    // (a completed phase is seen by all of them), never by the abort flag,
+    // which one warp could read before and another after it was raised.
     uint32_t acc_i = 0;
-    for (int i = 0; i < my_items && !*abort_flag; ++i) {
+    for (int i = 0; i < my_items; ++i) {
       const ItemGeo g = geo_of<PHASE>(a, s_geo, i);
       if (g.flags & 2) {
         if (tid == kEpTid0) atomicOr(a.err, MOE_DEVERR_STALE);
@@ -585,7 +591,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
       }
       const uint32_t buf = Sh::kAccBufs == 2 ? (acc_i & 1u) : 0u;
       const uint32_t aph = Sh::kAccBufs == 2 ? ((acc_i >> 1) & 1u) : (acc_i & 1u);
-      if (!mbar_wait(su32(&bar_accf[buf]), aph, abort_flag, a.err)) break;
+      if (!mbar_wait(su32(&bar_accf[buf]), aph, abort_flag, a.err, a.wait_cycles)) break;
       asm volatile("tcgen05.fence::after_thread_sync;");
       const int nch = (g.ntok + 31) / 32;
       const uint32_t tb = tmem + lane_base + buf * static_cast<uint32_t>(kTok);

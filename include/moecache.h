@@ -207,7 +207,9 @@ moe_status_t moe_route(moe_ctx_t* ctx, int32_t layer, const void* x, int32_t xt,
  * moe_last_error(NULL) and launches nothing.
  * The first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before any stream
- * capture. No call allocates (no cudaMalloc, cudaFree or allocating library
+ * capture. The address is then kept per device ordinal for the life of the
+ * process: after cudaDeviceReset on that device it no longer names the
+ * array, so do not call this entry point on a device that has been reset. No call allocates (no cudaMalloc, cudaFree or allocating library
  * routine). Every call shares the one array: it clears its counters on the
  * stream before the launch, and calls whose kernels overlap on the GPU (on
  * different streams, or from several threads) race on it — serialise them.
@@ -336,6 +338,18 @@ moe_status_t moe_get_kernel_times(moe_ctx_t* ctx, double* ms, int64_t* launches)
  * no longer matches the page-table entry. */
 moe_status_t moe_debug_fail_staging_after(moe_ctx_t* ctx, int32_t fail_after_tiles);
 moe_status_t moe_debug_corrupt_generation(moe_ctx_t* ctx, int32_t layer, int32_t expert);
+
+/* Test hook of the device's bounded waits ([NfE] §3.2 fail closed on a
+ * deadline): the next prefill gate/up GEMM of this context (one launch; the
+ * hook then clears itself) limits each of its mbarrier waits to
+ * wait_cycles SM clock cycles (0: the default, about 2 s) and its first CTA
+ * issues no copy for ring stage skip_ring (-1: off), so that no copy is in
+ * flight for that stage and the consumers' wait on it runs out. The kernel
+ * then raises its abort flag, drains the copies and MMAs it did issue,
+ * frees its tensor memory and returns; moe_check_device_errors reports
+ * MOE_ERR_TIMEOUT and the context stays usable. Host side only: no wait is
+ * removed and nothing faults. */
+moe_status_t moe_debug_prefill_wait_timeout(moe_ctx_t* ctx, int64_t wait_cycles, int32_t skip_ring);
 
 /* ---------------------------------------------------------------- slot manager
  * The host-side policy of the cache on its own (no CUDA calls): the same

@@ -298,3 +298,41 @@ def test_prefill_waves_failed_staging_fails_closed(bec, fills_before):
     ctx.close()
     del keep
 
+
+def test_prefill_gemm_wait_runs_out_and_context_recovers(bec):
+    # a bounded device wait that runs out, without a fault: the first CTA of
+    # the next gate/up GEMM issues no copy for its first ring stage and every
+    # wait is limited to ~1 ms, so its consumers' wait on that stage expires.
+    # The kernel drains what it issued and returns; the call reports
+    # MOE_ERR_TIMEOUT, and the next step on the same context matches the
+    # oracle.
+    w = W.with_changes(W.WORKLOADS["tiny"], n_steps=32)
+    T = 64
+    store = pinned_store(w, 1)
+    ctx = make_context(bec, w, 1, slots=w.n_experts, max_tokens=T, device_admit=1)
+    keep = bind_all(ctx, w, 1, store)
+    ctx.preload(0, list(range(w.n_experts)))
+    Wr = W.router_weights(w, 0)
+    Wr_t = torch.from_numpy(Wr).cuda()
+    x = W.activations(w, 0, 2 * T)
+    plan = bec.Plan(w.n_experts, w.top_k, T)
+    idx = torch.empty((T, w.top_k), dtype=torch.int32, device="cuda")
+    wt = torch.empty((T, w.top_k), dtype=torch.float32, device="cuda")
+    y = torch.empty((T, w.hidden), dtype=torch.float32, device="cuda")
+    ctx.debug_prefill_wait_timeout(2_000_000, 0)
+    ctx.layer_forward(0, x_to_torch(w, x[:T]), Wr_t, None, idx, wt, plan, y)
+    with pytest.raises(bec.MoeError) as ei:
+        ctx.check_device_errors()
+    assert ei.value.status == 5  # MOE_ERR_TIMEOUT
+    good = x[T:]
+    ctx.layer_forward(0, x_to_torch(w, good), Wr_t, None, idx, wt, plan, y)
+    ctx.check_device_errors()
+    x64 = x_to_f64(w, good)
+    ridx, rw, _ = oracle.route(x64, Wr, None, w.top_k)
+    assert np.array_equal(idx.cpu().numpy(), ridx)
+    experts = ExpertCache(w)
+    ref = oracle.moe_layer(x64, ridx, rw, lambda e: experts.get(0, e), None)
+    ok, rel, mx = tolerance_ok(y.cpu().numpy(), ref)
+    assert ok, (rel, mx)
+    ctx.close()
+    del keep
