@@ -14,7 +14,8 @@ pages:
   tiles, device page table with sentinel entries), §5.5 (merge into the
   original output positions);
 * "Paging the Experts" (Routide, arxiv 2609.29032v1), §3.1 (gate/up/down
-  projections), §3.2 (byte-budgeted cache, entries pinned per layer),
+  projections), §3.2 (byte-budgeted cache, entries pinned per layer), §3.3
+  and §5.2 (confidence-gated prefetch, useful and wasted loads),
   §4.1/§5.1 (LRU versus seeded random eviction on fixed route replays),
   §4.2 (materialised bytes = demand misses x payload).
 
@@ -40,7 +41,9 @@ from .formats import (Q8_0, Q4_0, I4_G64, bf16_bits_to_f64, f16_bits_to_f64, pay
 from .route import router_logits, topk_select, combine_weights, route
 from .plan import plan_union
 from .splitmix import SplitMix64
-from .cache import SlotCache, CapacityError, LRU, RANDOM, slot_count
+from .cache import (SlotCache, CapacityError, LRU, RANDOM, PREFETCH_REFRESH, PREFETCH_PRESERVE,
+                    slot_count)
+from .prefetch import prediction as prefetch_prediction
 from .budget import static_budget
 from .replay import replay, static_set, FARTHEST_NEXT_USE, STATIC_SET
 from .ffn import silu, expert_ffn, moe_layer

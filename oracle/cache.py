@@ -39,6 +39,13 @@ from .splitmix import SplitMix64, layer_seed
 LRU = 0
 RANDOM = 1
 
+# Prefetch modes ("Paging the Experts" §3.3): an absent predicted expert is
+# loaded in both; a resident one is either touched like a hit
+# (resident-refresh: the check updates its recency) or only recorded
+# (preserve-resident: the cache state does not change).
+PREFETCH_REFRESH = 1
+PREFETCH_PRESERVE = 2
+
 
 class CapacityError(RuntimeError):
     pass
@@ -66,6 +73,12 @@ class SlotCache:
         self.misses = 0
         self.evictions = 0
         self.materialized_bytes = 0
+        # speculative loads are counted apart from demand ("Paging the
+        # Experts" §4.2): loads, useful / wasted (the next step's union holds
+        # the loaded expert / does not), resident probes that refreshed
+        # recency or changed nothing, and the bytes the loads moved
+        self.pending = -1
+        self.pf = dict(loads=0, useful=0, wasted=0, refreshes=0, probes=0, bytes=0)
 
     # -- helpers
     def _fill(self, e: int, s: int) -> None:
@@ -73,6 +86,19 @@ class SlotCache:
         self.pt[e] = s
         self.gen[s] += 1
         self.last[s] = self.tick
+
+    def _take_slot(self, current: set) -> Tuple[int, int]:
+        """Slot for a new fill: the lowest free one, else the policy's
+        victim (evicted here). Returns (slot, evicted expert or -1)."""
+        free = [s for s in range(self.S) if self.owner[s] < 0]
+        if free:
+            return free[0], -1
+        s = self._victim_slot(current)
+        victim = self.owner[s]
+        self.pt[victim] = -1
+        self.owner[s] = -1
+        self.evictions += 1
+        return s, victim
 
     def _victim_slot(self, current: set) -> int:
         if self.policy == LRU:
@@ -88,6 +114,9 @@ class SlotCache:
         experts have ``counts[e]`` assignments. Returns the step record."""
         U = sorted(int(e) for e in uniq)
         current = set(U)
+        if self.pending >= 0:  # the last speculative load meets its step
+            self.pf["useful" if self.pending in current else "wasted"] += 1
+            self.pending = -1
         hit_e = [e for e in U if self.pt[e] >= 0]
         miss_e = [e for e in U if self.pt[e] < 0]
         for e in hit_e:
@@ -96,15 +125,7 @@ class SlotCache:
         fills: List[Tuple[int, int, int]] = []  # (expert, slot, evicted expert or -1)
         for e in miss_e:
             self.tick += 1
-            free = [s for s in range(self.S) if self.owner[s] < 0]
-            if free:
-                s, victim = free[0], -1
-            else:
-                s = self._victim_slot(current)
-                victim = self.owner[s]
-                self.pt[victim] = -1
-                self.owner[s] = -1
-                self.evictions += 1
+            s, victim = self._take_slot(current)
             self._fill(e, s)
             fills.append((e, s, victim))
         n_assign = sum(int(counts[e]) for e in U)
@@ -114,6 +135,31 @@ class SlotCache:
         self.materialized_bytes += len(miss_e) * self.payload
         return dict(hits=hits, misses=len(miss_e), fills=fills,
                     pt=list(self.pt), gen=list(self.gen))
+
+    def prefetch(self, e: int, mode: int) -> dict:
+        """Speculative access to expert ``e`` before a step ("Paging the
+        Experts" §3.3): routing and arithmetic are unchanged, only the cache
+        is. If ``e`` is absent it is loaded like a miss, with nothing pinned
+        (the lowest free slot, else the policy's victim), one tick; if it is
+        resident, PREFETCH_REFRESH touches it as a hit would (one tick) and
+        PREFETCH_PRESERVE records the probe and changes nothing. Returns
+        dict(action="load"|"refresh"|"probe", slot, victim)."""
+        e = int(e)
+        if self.pt[e] >= 0:
+            if mode == PREFETCH_REFRESH:
+                self.tick += 1
+                self.last[self.pt[e]] = self.tick
+                self.pf["refreshes"] += 1
+                return dict(action="refresh", slot=self.pt[e], victim=-1)
+            self.pf["probes"] += 1
+            return dict(action="probe", slot=self.pt[e], victim=-1)
+        self.tick += 1
+        s, victim = self._take_slot(set())
+        self._fill(e, s)
+        self.pending = e
+        self.pf["loads"] += 1
+        self.pf["bytes"] += self.payload
+        return dict(action="load", slot=s, victim=victim)
 
     def preload(self, experts: Sequence[int]) -> None:
         """Fill slots with ``experts`` (ascending) before the first step; not
@@ -139,3 +185,6 @@ class SlotCache:
     def stats(self) -> dict:
         return dict(hits=self.hits, misses=self.misses, evictions=self.evictions,
                     materialized_bytes=self.materialized_bytes)
+
+    def prefetch_stats(self) -> dict:
+        return dict(self.pf)

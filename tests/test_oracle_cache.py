@@ -208,3 +208,42 @@ def test_tile_partition(golden_dir):
             a, b = line.split()[:2]
             vals[a] = float(b)
     assert vals["nanite_tile_gb"] * 1e9 / vals["nanite_tiles"] < vals["nanite_tile_bytes"]
+
+
+def test_prefetch_loads_useful_wasted_hand_worked():
+    # "Paging the Experts" §3.3/§5.2: speculative loads, counted apart from
+    # demand misses (§4.2) as useful when the next step uses them. Hand-worked
+    # LRU replay, 2 slots, payload 100 B:
+    #   step {0,1,2} (larger than the slots): 0 -> s0 (t1), 1 -> s1 (t2),
+    #        2 evicts 0 from s0 (t3)
+    #   prefetch 0: absent -> load, evicts 1 from s1 (oldest, t2) at t4
+    #   step {0,3}: 0 was the load -> useful; hit 0 (t5); 3 evicts 2 from s0 (t3) at t6
+    #   prefetch 4: absent -> load, evicts 0 from s1 (t5) at t7
+    #   step {3,5}: 4 unused -> wasted; hit 3 (t8); 5 evicts 4 from s1 (t7) at t9
+    #   prefetch 5 (preserve): resident -> probe; prefetch 3 (refresh): touch s0 at t10
+    from oracle.cache import PREFETCH_PRESERVE, PREFETCH_REFRESH
+    c = SlotCache(6, 2, LRU, payload_bytes=100)
+    c.step([0, 1, 2], [1, 1, 1, 0, 0, 0])
+    assert c.prefetch(0, PREFETCH_REFRESH) == dict(action="load", slot=1, victim=1)
+    r = c.step([0, 3], [1, 0, 0, 1, 0, 0])
+    assert (r["hits"], r["misses"], r["fills"]) == (1, 1, [(3, 0, 2)])
+    assert c.prefetch(4, PREFETCH_PRESERVE) == dict(action="load", slot=1, victim=0)
+    r = c.step([3, 5], [0, 0, 0, 1, 0, 1])
+    assert (r["hits"], r["misses"], r["fills"]) == (1, 1, [(5, 1, 4)])
+    assert c.prefetch(5, PREFETCH_PRESERVE) == dict(action="probe", slot=1, victim=-1)
+    assert c.prefetch(3, PREFETCH_REFRESH) == dict(action="refresh", slot=0, victim=-1)
+    assert c.last == [10, 9] and c.tick == 10
+    assert c.pt == [-1, -1, -1, 0, -1, 1] and c.gen == [3, 4]
+    assert c.stats() == dict(hits=2, misses=5, evictions=5, materialized_bytes=500)
+    assert c.prefetch_stats() == dict(loads=2, useful=1, wasted=1, refreshes=1, probes=1, bytes=200)
+
+
+def test_prefetch_random_policy_draws_over_every_slot():
+    # nothing is pinned before a step: the random victim of a speculative
+    # load is cand[next() mod n] over all slots; SplitMix64 (seed 0, layer 0)
+    # first output 0xE220A8397B1DCDAF is odd -> slot 1 of 2
+    from oracle.cache import PREFETCH_PRESERVE
+    c = SlotCache(6, 2, RANDOM, seed=0, layer=0)
+    c.step([0, 1], [1, 1, 0, 0, 0, 0])
+    assert c.prefetch(5, PREFETCH_PRESERVE) == dict(action="load", slot=1, victim=1)
+    assert c.pt == [0, -1, -1, -1, -1, 1]
