@@ -19,6 +19,8 @@ Q8_0, Q4_0, I4_G64 = 0, 1, 2
 LRU, RANDOM, FARTHEST_NEXT_USE, STATIC_SET = 0, 1, 2, 3
 F32, BF16 = 0, 1
 MODE_AUTO, MODE_DECODE, MODE_PREFILL = 0, 1, 2
+PREFETCH_OFF, PREFETCH_REFRESH, PREFETCH_PRESERVE = 0, 1, 2
+PREFETCH_ACTIONS = ("probe", "refresh", "load")
 KERNEL_KINDS = ("route", "plan", "ffn_gateup", "ffn_down", "stage_copy")
 
 
@@ -47,7 +49,10 @@ class Stats(C.Structure):
     _fields_ = [("steps", C.c_int64), ("hits", C.c_int64), ("misses", C.c_int64),
                 ("evictions", C.c_int64), ("materialized_bytes", C.c_int64),
                 ("tiles_staged", C.c_int64), ("bytes_staged", C.c_int64),
-                ("uncertified_repairs", C.c_int64)]
+                ("uncertified_repairs", C.c_int64), ("prefetch_loads", C.c_int64),
+                ("prefetch_useful", C.c_int64), ("prefetch_wasted", C.c_int64),
+                ("prefetch_refreshes", C.c_int64), ("prefetch_probes", C.c_int64),
+                ("prefetch_bytes", C.c_int64)]
 
 
 class Budget(C.Structure):
@@ -88,6 +93,7 @@ SIGNATURES = [
     ("moe_expert_ffn", _st, [_vp, _i32, _vp, _i32, _i32, C.POINTER(PlanT), _vp, _i32, _vp]),
     ("moe_layer_forward", _st, [_vp, _i32, _vp, _i32, _i32, _vp, _vp, _vp, _vp, C.POINTER(PlanT),
                                 _vp, C.POINTER(MissList), _vp]),
+    ("moe_set_prefetch", _st, [_vp, _i32, C.c_float]),
     ("moe_check_device_errors", _st, [_vp, _vp]),
     ("moe_get_stats", _st, [_vp, _i32, C.POINTER(Stats)]),
     ("moe_read_page_table", _st, [_vp, _i32, C.POINTER(_i32), C.POINTER(C.c_uint32)]),
@@ -100,6 +106,7 @@ SIGNATURES = [
     ("moe_slots_create", _st, [_i32, _i32, _i32, _u64, _i32, _i64, C.POINTER(_vp)]),
     ("moe_slots_destroy", None, [_vp]),
     ("moe_slots_step", _st, [_vp, C.POINTER(_i32), _i32, C.POINTER(_i32), C.POINTER(MissList)]),
+    ("moe_slots_prefetch", _st, [_vp, _i32, _i32, C.POINTER(_i32), C.POINTER(MissList)]),
     ("moe_slots_preload", _st, [_vp, C.POINTER(_i32), _i32]),
     ("moe_slots_evict", _st, [_vp, _i32]),
     ("moe_slots_read", _st, [_vp, C.POINTER(_i32), C.POINTER(C.c_uint32)]),

@@ -193,6 +193,10 @@ class Context:
         self._ck(lib.moe_get_kernel_times(self.h, ms, n))
         return {k: (ms[i], n[i]) for i, k in enumerate(N.KERNEL_KINDS)}
 
+    def set_prefetch(self, mode: int, threshold: float = 0.2):
+        """Confidence-gated prefetch before every layer step (host admission)."""
+        self._ck(lib.moe_set_prefetch(self.h, mode, threshold))
+
     def debug_fail_staging_after(self, n_tiles: int):
         self._ck(lib.moe_debug_fail_staging_after(self.h, n_tiles))
 
@@ -231,6 +235,16 @@ class Slots:
         ml = N.MissList()
         _check(lib.moe_slots_step(self.h, u, len(uniq), cnt, C.byref(ml)))
         return _misses(ml)
+
+    def prefetch(self, expert, mode):
+        """Speculative access before the next step: returns (action, fill)
+        with action "probe", "refresh" or "load" and fill (expert, slot,
+        victim) of a load, else None."""
+        act = C.c_int32()
+        ml = N.MissList()
+        _check(lib.moe_slots_prefetch(self.h, expert, mode, C.byref(act), C.byref(ml)))
+        fill = (ml.expert[0], ml.slot[0], ml.victim[0]) if ml.n else None
+        return N.PREFETCH_ACTIONS[act.value], fill
 
     def preload(self, experts):
         arr = (C.c_int32 * max(1, len(experts)))(*experts)

@@ -16,6 +16,7 @@
 // writes gen only after every tile of the step has landed, so a kernel that
 // runs without the staging (or after a failed one) sees gen != pt_gen and
 // reads nothing from that slot.
+#include <algorithm>
 #include <cstdio>
 #include <cstring>
 
@@ -116,6 +117,8 @@ extern "C" void moe_destroy(moe_ctx_t* ctx) {
   for (auto e : ctx->ev_stage)
     if (e) cudaEventDestroy(e);
   for (auto e : ctx->ev_stage_b)
+    if (e) cudaEventDestroy(e);
+  for (auto e : ctx->ev_prefetch)
     if (e) cudaEventDestroy(e);
   for (auto& r : ctx->timed) {
     cudaEventDestroy(r.a);
@@ -239,7 +242,9 @@ extern "C" moe_status_t moe_create(const moe_config_t* cfg, moe_ctx_t** out) {
   CKC(cudaMalloc(&ctx->d_err, sizeof(uint32_t)));
   CKC(cudaMemset(ctx->d_err, 0, sizeof(uint32_t)));
   CKC(cudaHostAlloc(&ctx->h_err, sizeof(uint32_t), cudaHostAllocDefault));
-  CKC(cudaHostAlloc(&ctx->h_union, sizeof(int32_t) * (2 * E + 2), cudaHostAllocDefault));
+  // uniq [E], counts [E], n_uniq, spare, then the prefetch prediction of the
+  // step (expert, weight bits)
+  CKC(cudaHostAlloc(&ctx->h_union, sizeof(int32_t) * (2 * E + 4), cudaHostAllocDefault));
   ctx->max_units = std::min(E, c.max_tokens * c.top_k) + 1;
   // room for one unit table and one fill list per compute wave (a wave
   // holds at least one unit; fills <= units)
@@ -300,11 +305,14 @@ extern "C" moe_status_t moe_create(const moe_config_t* cfg, moe_ctx_t** out) {
   ctx->streams.assign(c.n_streams, nullptr);
   ctx->ev_stage.assign(c.n_streams, nullptr);
   ctx->ev_stage_b.assign(c.n_streams, nullptr);
+  ctx->ev_prefetch.assign(c.n_streams, nullptr);
   for (int i = 0; i < c.n_streams; ++i) {
     CKC(cudaStreamCreateWithFlags(&ctx->streams[i], cudaStreamNonBlocking));
     CKC(cudaEventCreateWithFlags(&ctx->ev_stage[i], cudaEventDisableTiming));
     CKC(cudaEventCreateWithFlags(&ctx->ev_stage_b[i], cudaEventDisableTiming));
+    CKC(cudaEventCreateWithFlags(&ctx->ev_prefetch[i], cudaEventDisableTiming));
   }
+  ctx->pred.assign(L, -1);
   CKC(cudaEventCreateWithFlags(&ctx->ev_compute, cudaEventDisableTiming));
   ctx->shared.assign(L, nullptr);
   ctx->tiles_staged.assign(L, 0);
@@ -1048,17 +1056,67 @@ extern "C" moe_status_t moe_layer_forward(moe_ctx_t* ctx, int32_t layer, const v
     }
     return moe_expert_ffn(ctx, layer, x, xt, T, plan, y, MOE_MODE_AUTO, stream);
   }
+  // confidence-gated prefetch of the layer's prediction from its previous
+  // step: a load goes out on the staging streams now, overlapping this
+  // step's routing and admission
+  int pf_slot = -1;
+  uint32_t pf_gen = 0;
+  if (ctx->prefetch_mode != MOE_PREFETCH_OFF && ctx->pred[layer] >= 0) {
+    if (!ctx->store) return fail(ctx, MOE_ERR_STATE, "layer_forward: no store bound");
+    int32_t action = 0;
+    moe_miss_list_t fl{};
+    moe_status_t ps = moe::slots_prefetch(ctx->slots[layer], ctx->pred[layer], ctx->prefetch_mode, &action, &fl,
+                                          &ctx->err);
+    ctx->pred[layer] = -1;
+    if (ps != MOE_OK) return ps;
+    if (action == MOE_PREFETCH_LOADED) {
+      ps = stage_fills(ctx, layer, &fl, -1, nullptr, 0, st, true, ctx->ev_prefetch, false);
+      if (ps != MOE_OK) return ps;
+      pf_slot = fl.slot[0];
+      pf_gen = moe::slots_gen(ctx->slots[layer])[pf_slot];
+    }
+  }
   moe_status_t s = route_impl(ctx, layer, x, xt, T, w_router, bias, topk_idx, topk_w, plan, st);
   if (s != MOE_OK) return s;
   if (T > 64) {
     s = moe_plan_union(ctx, topk_idx, topk_w, T, plan, stream);
     if (s != MOE_OK) return s;
   }
+  const int E_ = ctx->cfg.n_experts, k_ = ctx->cfg.top_k;
+  int32_t* hpred = ctx->h_union + 2 * E_ + 2;
+  if (ctx->prefetch_mode != MOE_PREFETCH_OFF) {
+    // the next step's prediction: the last token's rank-0 expert and weight
+    // (read back with the union, before the admission's synchronisation)
+    CK(cudaMemcpyAsync(hpred, topk_idx + static_cast<size_t>(T - 1) * k_, sizeof(int32_t),
+                       cudaMemcpyDeviceToHost, st));
+    CK(cudaMemcpyAsync(hpred + 1, topk_w + static_cast<size_t>(T - 1) * k_, sizeof(float),
+                       cudaMemcpyDeviceToHost, st));
+  }
+  // after the admission: record the prediction; the prefetched slot's
+  // generation is published once its copy has landed (before any copy or
+  // compute of this step that could touch or read that slot)
+  auto after_admit = [&]() -> moe_status_t {
+    if (ctx->prefetch_mode != MOE_PREFETCH_OFF) {
+      float wgt;
+      std::memcpy(&wgt, hpred + 1, sizeof(float));
+      ctx->pred[layer] = (hpred[0] >= 0 && hpred[0] < E_ && wgt >= ctx->prefetch_threshold) ? hpred[0] : -1;
+    }
+    if (pf_slot >= 0) {
+      const int S_ = ctx->cfg.slots_per_layer;
+      for (auto e : ctx->ev_prefetch) CK(cudaStreamWaitEvent(st, e, 0));
+      // (the host mirror may change again within this call, in a later
+      // compute wave, before a copy from it would run)
+      ctx->h_gen[static_cast<size_t>(layer) * S_ + pf_slot] = pf_gen;
+      CK(moe::launch_set_word(ctx->d_gen + static_cast<size_t>(layer) * S_ + pf_slot, pf_gen, st));
+    }
+    return MOE_OK;
+  };
   moe_miss_list_t local{};
   moe_miss_list_t* ml = misses ? misses : &local;
   if (T <= 8) {
     s = moe_cache_admit(ctx, layer, plan, ml, stream);
     if (s != MOE_OK) return s;
+    if ((s = after_admit()) != MOE_OK) return s;
     s = moe_stage_tiles(ctx, layer, ml, stream);
     if (s != MOE_OK) return s;
     return moe_expert_ffn(ctx, layer, x, xt, T, plan, y, MOE_MODE_AUTO, stream);
@@ -1073,6 +1131,7 @@ extern "C" moe_status_t moe_layer_forward(moe_ctx_t* ctx, int32_t layer, const v
   WavePlan wp;
   s = admit_host(ctx, layer, plan, ml, st, &wp);
   if (s != MOE_OK) return s;
+  if ((s = after_admit()) != MOE_OK) return s;
   const int S = ctx->cfg.slots_per_layer;
   uint32_t* hg = ctx->h_gen + static_cast<size_t>(layer) * S;
   p.parts = moe::kPartGather;
@@ -1162,6 +1221,12 @@ extern "C" moe_status_t moe_get_stats(const moe_ctx_t* cctx, int32_t layer, moe_
     t.tiles_staged += ctx->tiles_staged[l];
     t.bytes_staged += ctx->bytes_staged[l];
     t.uncertified_repairs += static_cast<int64_t>(rep[l]);
+    t.prefetch_loads += s.prefetch_loads;
+    t.prefetch_useful += s.prefetch_useful;
+    t.prefetch_wasted += s.prefetch_wasted;
+    t.prefetch_refreshes += s.prefetch_refreshes;
+    t.prefetch_probes += s.prefetch_probes;
+    t.prefetch_bytes += s.prefetch_bytes;
   }
   *out = t;
   return MOE_OK;
@@ -1216,6 +1281,19 @@ extern "C" moe_status_t moe_debug_corrupt_generation(moe_ctx_t* ctx, int32_t lay
   CK(cudaMemcpy(&g, ctx->d_gen + layer * S + slot, sizeof(uint32_t), cudaMemcpyDeviceToHost));
   g += 0x10000u;
   CK(cudaMemcpy(ctx->d_gen + layer * S + slot, &g, sizeof(uint32_t), cudaMemcpyHostToDevice));
+  return MOE_OK;
+}
+
+extern "C" moe_status_t moe_set_prefetch(moe_ctx_t* ctx, int32_t mode, float threshold) {
+  if (!ctx) return MOE_ERR_ARG;
+  if (mode != MOE_PREFETCH_OFF && mode != MOE_PREFETCH_REFRESH && mode != MOE_PREFETCH_PRESERVE)
+    return fail(ctx, MOE_ERR_ARG, "set_prefetch: bad mode");
+  if (!(threshold >= 0.f && threshold <= 1.f)) return fail(ctx, MOE_ERR_ARG, "set_prefetch: threshold outside [0, 1]");
+  if (ctx->dev_admit && mode != MOE_PREFETCH_OFF)
+    return fail(ctx, MOE_ERR_STATE, "set_prefetch: prefetch runs with host admission only");
+  ctx->prefetch_mode = mode;
+  ctx->prefetch_threshold = threshold;
+  std::fill(ctx->pred.begin(), ctx->pred.end(), -1);
   return MOE_OK;
 }
 

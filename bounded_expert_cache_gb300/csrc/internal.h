@@ -30,6 +30,8 @@ moe_status_t slots_preload(moe_slots* s, const int32_t* experts, int32_t n,
                            std::vector<int32_t>* filled, std::vector<int32_t>* filled_slots,
                            std::string* err);
 moe_status_t slots_evict(moe_slots* s, int32_t e, std::string* err);
+moe_status_t slots_prefetch(moe_slots* s, int32_t e, int32_t mode, int32_t* action, moe_miss_list_t* fill,
+                            std::string* err);
 const int32_t* slots_pt(const moe_slots* s);
 const int32_t* slots_owner(const moe_slots* s);
 const uint64_t* slots_last(const moe_slots* s);
@@ -148,6 +150,7 @@ struct StageArgs {
 };
 constexpr int64_t kStageChunkBytes = 32768;  // one CTA's copy: 256 threads x 8 x 16 B
 cudaError_t launch_stage_copy(const StageArgs& a, cudaStream_t st);
+cudaError_t launch_set_word(uint32_t* dst, uint32_t v, cudaStream_t st);
 // One load per kTouchPage bytes of a bound store (its device mapping), at bind time.
 constexpr size_t kTouchPage = 4096;
 cudaError_t launch_touch_pages(const uint8_t* dev_store, size_t bytes, int sms, uint32_t* sink, cudaStream_t st);
@@ -178,6 +181,20 @@ struct FfnArgs {
   cudaEvent_t ev[4];          // optional timing events around gate/up and down
 };
 cudaError_t launch_ffn_decode(const FfnArgs& a, int num_sms, cudaStream_t st);
+
+// The fused decode FFN (one persistent cooperative launch): its counters
+// (zero between launches; the kernel clears them) and launch shape.
+struct FusedLaunch {
+  unsigned int* sync;   // [2 + max_units + max_units * max_tiles]
+  int max_units;        // unit-table capacity (the last counter is the shared expert's)
+  int max_tiles;        // tiles of one down plane
+  int64_t tile_bytes;   // staging tile
+  long long wait_cycles;
+  int grid;             // CTAs (one per SM)
+  bool pdl;             // with programmatic stream serialisation
+};
+cudaError_t launch_ffn_decode_fused(const FfnArgs& a, const FusedLaunch& fl, cudaStream_t st);
+constexpr long long kFusedWaitCycles = 4000000000ll;  // about 2 s at the SM clock
 
 }  // namespace moe
 
@@ -242,6 +259,10 @@ struct moe_ctx {
   std::vector<cudaEvent_t> ev_stage, ev_stage_b;  // copies of a wave's two parts
   cudaEvent_t ev_compute = nullptr;
   size_t unit_ints = 0;  // capacity of the unit-table buffer
+  int32_t prefetch_mode = 0;      // moe_prefetch_mode_t (host admission only)
+  float prefetch_threshold = 0.2f;
+  std::vector<int32_t> pred;      // [L] expert to prefetch before the layer's next step, or -1
+  std::vector<cudaEvent_t> ev_prefetch;  // the prefetch copy, one per staging stream
   long long dbg_wait_cycles = 0;  // test hook of the next prefill gate/up GEMM
   int32_t dbg_skip_ring = -1;
   int32_t fail_after_tiles = -1;

@@ -18,6 +18,15 @@
 // the same step; such a fill is assigned to the compute wave after the one
 // of the expert it evicts, so a slot is overwritten only after the compute
 // that reads it.
+//
+// Prefetch ("Paging the Experts" §3.3): before a step, a predicted expert
+// that is absent is loaded like a miss with nothing pinned (one tick, the
+// lowest free slot, else the policy's victim over every slot); a resident
+// one is touched like a hit (resident refresh) or only recorded
+// (preserve-resident). The next step counts the load useful if its union
+// holds the expert, else wasted; speculative bytes are counted apart from
+// the demand misses' (§4.2).
+#include <algorithm>
 #include <cstring>
 #include <string>
 #include <vector>
@@ -48,6 +57,7 @@ struct moe_slots {
   std::vector<int32_t> f_expert, f_slot, f_victim, f_wave;
   std::vector<int32_t> wave_of;   // per expert, for the current step
   std::vector<uint8_t> in_step;   // per expert, member of the current union
+  int32_t pending = -1;           // expert of the last speculative load, until its step
   moe_stats_t stats{};
 };
 
@@ -75,6 +85,23 @@ static int32_t lowest_free(const moe_slots* s) {
   for (int32_t i = 0; i < s->S; ++i)
     if (s->owner[i] < 0) return i;
   return -1;
+}
+
+// Slot of the policy's victim when no slot is free: LRU the oldest access;
+// random cand[next() mod n] over the slots whose expert is not in the
+// current union (in_step), listed by slot index.
+static int32_t victim_slot(moe_slots* s, std::vector<int32_t>& cand) {
+  if (s->policy == MOE_LRU) {
+    int32_t slot = 0;
+    for (int32_t i = 1; i < s->S; ++i)
+      if (s->last[i] < s->last[slot]) slot = i;
+    return slot;
+  }
+  cand.clear();
+  for (int32_t i = 0; i < s->S; ++i)
+    if (!s->in_step[s->owner[i]]) cand.push_back(i);
+  uint64_t r = moe_splitmix64_next(&s->rng);
+  return cand[r % cand.size()];
 }
 
 moe_status_t slots_step(moe_slots* s, const int32_t* uniq, int32_t n_uniq, const int32_t* counts,
@@ -105,6 +132,11 @@ moe_status_t slots_step(moe_slots* s, const int32_t* uniq, int32_t n_uniq, const
       return MOE_ERR_CAPACITY;
     }
   }
+  if (s->pending >= 0) {  // the last speculative load meets its step
+    const bool used = std::binary_search(U.begin(), U.end(), s->pending);
+    (used ? s->stats.prefetch_useful : s->stats.prefetch_wasted)++;
+    s->pending = -1;
+  }
   for (int32_t e : U) {
     s->in_step[e] = 1;
     s->wave_of[e] = 0;
@@ -127,17 +159,7 @@ moe_status_t slots_step(moe_slots* s, const int32_t* uniq, int32_t n_uniq, const
     ++s->tick;
     int32_t slot = lowest_free(s), victim = -1;
     if (slot < 0) {
-      if (s->policy == MOE_LRU) {
-        slot = 0;
-        for (int32_t i = 1; i < s->S; ++i)
-          if (s->last[i] < s->last[slot]) slot = i;
-      } else {
-        cand.clear();
-        for (int32_t i = 0; i < s->S; ++i)
-          if (!s->in_step[s->owner[i]]) cand.push_back(i);
-        uint64_t r = moe_splitmix64_next(&s->rng);
-        slot = cand[r % cand.size()];
-      }
+      slot = victim_slot(s, cand);
       victim = s->owner[slot];
       s->pt[victim] = -1;
       s->owner[slot] = -1;
@@ -174,6 +196,61 @@ moe_status_t slots_step(moe_slots* s, const int32_t* uniq, int32_t n_uniq, const
   out->hits = hits;
   out->misses = n_miss;
   out->layer = s->layer;
+  return MOE_OK;
+}
+
+moe_status_t slots_prefetch(moe_slots* s, int32_t e, int32_t mode, int32_t* action, moe_miss_list_t* fill,
+                            std::string* err) {
+  if (e < 0 || e >= s->E || (mode != MOE_PREFETCH_REFRESH && mode != MOE_PREFETCH_PRESERVE)) {
+    *err = "prefetch: bad expert or mode";
+    return MOE_ERR_ARG;
+  }
+  s->f_expert.clear();
+  s->f_slot.clear();
+  s->f_victim.clear();
+  s->f_wave.clear();
+  *fill = moe_miss_list_t{};
+  fill->layer = s->layer;
+  fill->n_waves = 1;
+  const int32_t at = s->pt[e];
+  if (at >= 0) {
+    if (mode == MOE_PREFETCH_REFRESH) {
+      s->last[at] = ++s->tick;
+      s->stats.prefetch_refreshes++;
+      *action = MOE_PREFETCH_REFRESHED;
+    } else {
+      s->stats.prefetch_probes++;
+      *action = MOE_PREFETCH_PROBED;
+    }
+    return MOE_OK;
+  }
+  ++s->tick;
+  std::vector<int32_t> cand;
+  int32_t slot = lowest_free(s), victim = -1;
+  if (slot < 0) {  // nothing is pinned outside a step
+    slot = victim_slot(s, cand);
+    victim = s->owner[slot];
+    s->pt[victim] = -1;
+    s->owner[slot] = -1;
+    s->stats.evictions++;
+  }
+  s->owner[slot] = e;
+  s->pt[e] = slot;
+  s->gen[slot]++;
+  s->last[slot] = s->tick;
+  s->pending = e;
+  s->stats.prefetch_loads++;
+  s->stats.prefetch_bytes += s->payload;
+  s->f_expert.push_back(e);
+  s->f_slot.push_back(slot);
+  s->f_victim.push_back(victim);
+  s->f_wave.push_back(0);
+  fill->n = 1;
+  fill->expert = s->f_expert.data();
+  fill->slot = s->f_slot.data();
+  fill->victim = s->f_victim.data();
+  fill->wave = s->f_wave.data();
+  *action = MOE_PREFETCH_LOADED;
   return MOE_OK;
 }
 
@@ -251,6 +328,12 @@ extern "C" moe_status_t moe_slots_step(moe_slots_t* s, const int32_t* uniq, int3
                                        const int32_t* counts, moe_miss_list_t* out) {
   if (!s || !out) return MOE_ERR_ARG;
   return moe::slots_step(s, uniq, n_uniq, counts, out, &g_slots_err);
+}
+
+extern "C" moe_status_t moe_slots_prefetch(moe_slots_t* s, int32_t expert, int32_t mode, int32_t* action,
+                                           moe_miss_list_t* fill) {
+  if (!s || !action || !fill) return MOE_ERR_ARG;
+  return moe::slots_prefetch(s, expert, mode, action, fill, &g_slots_err);
 }
 
 extern "C" moe_status_t moe_slots_preload(moe_slots_t* s, const int32_t* experts, int32_t n) {

@@ -92,7 +92,16 @@ __global__ void __launch_bounds__(256) touch_pages_kernel(const uint8_t* p, size
   if (acc == 0x9e3779b9u) *sink = acc;
 }
 
+// One 32-bit store, its value taken when the launch is enqueued (a copy
+// from host memory would read the source only when it runs).
+__global__ void set_word_kernel(uint32_t* dst, uint32_t v) { *dst = v; }
+
 }  // namespace
+
+cudaError_t launch_set_word(uint32_t* dst, uint32_t v, cudaStream_t st) {
+  set_word_kernel<<<1, 1, 0, st>>>(dst, v);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_touch_pages(const uint8_t* dev_store, size_t bytes, int sms, uint32_t* sink, cudaStream_t st) {
   if (bytes < 4) return cudaSuccess;

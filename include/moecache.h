@@ -136,7 +136,22 @@ typedef struct {
   int64_t tiles_staged;        /* copy tiles issued by moe_stage_tiles */
   int64_t bytes_staged;        /* bytes copied by moe_stage_tiles */
   int64_t uncertified_repairs; /* tokens whose top-k needed exact logits */
+  /* Confidence-gated prefetch ([RT] §3.3, §5.2), counted apart from the
+   * demand counters above ([RT] §4.2): */
+  int64_t prefetch_loads;      /* absent predicted experts loaded before their step */
+  int64_t prefetch_useful;     /* loads whose next step's union held the expert */
+  int64_t prefetch_wasted;     /* loads whose next step's union did not */
+  int64_t prefetch_refreshes;  /* resident predictions touched like a hit */
+  int64_t prefetch_probes;     /* resident predictions recorded, state unchanged */
+  int64_t prefetch_bytes;      /* loads x payload */
 } moe_stats_t;
+
+/* Prefetch modes ([RT] §3.3): an absent predicted expert is loaded in both;
+ * a resident one is touched like a hit (RESIDENT_REFRESH: the check
+ * updates its recency) or only recorded (PRESERVE: no state change). */
+typedef enum { MOE_PREFETCH_OFF = 0, MOE_PREFETCH_REFRESH = 1, MOE_PREFETCH_PRESERVE = 2 } moe_prefetch_mode_t;
+/* What one prefetch did. */
+typedef enum { MOE_PREFETCH_PROBED = 0, MOE_PREFETCH_REFRESHED = 1, MOE_PREFETCH_LOADED = 2 } moe_prefetch_action_t;
 
 typedef struct moe_ctx moe_ctx_t;
 typedef struct moe_slots moe_slots_t;
@@ -292,6 +307,21 @@ moe_status_t moe_layer_forward(moe_ctx_t* ctx, int32_t layer, const void* x, int
                                int32_t* topk_idx, float* topk_w, const moe_plan_t* plan,
                                float* y, moe_miss_list_t* misses, moe_stream_t stream);
 
+/* Confidence-gated prefetch ([RT] §3.3; the page applies it during
+ * prefill): with mode != MOE_PREFETCH_OFF, every moe_layer_forward of this
+ * context first prefetches the layer's prediction from its previous step,
+ * namely the rank-0 expert of that step's last token when its combine
+ * weight is >= threshold (0.20 on the page). An absent expert is loaded
+ * into a slot chosen as for a miss with nothing pinned (the lowest free
+ * slot, else the policy's victim); its copy goes out on the staging streams
+ * before the step's routing, so it overlaps the routing and the host
+ * admission, and its generation is published once it has landed. Routing
+ * and outputs do not change (cache transparency); hits, misses and victims
+ * may. Counted in moe_stats_t.prefetch_*. Host admission only
+ * (admit_on_device = 0): MOE_ERR_STATE otherwise; MOE_ERR_ARG for a bad
+ * mode or a threshold outside [0, 1]. Clears every layer's prediction. */
+moe_status_t moe_set_prefetch(moe_ctx_t* ctx, int32_t mode, float threshold);
+
 /* Synchronise stream and report device-side failures recorded since the
  * last check (stale page-table entries, timed-out waits); clears them. */
 moe_status_t moe_check_device_errors(moe_ctx_t* ctx, moe_stream_t stream);
@@ -371,6 +401,14 @@ void moe_slots_destroy(moe_slots_t* s);
  * candidate. */
 moe_status_t moe_slots_step(moe_slots_t* s, const int32_t* uniq, int32_t n_uniq,
                             const int32_t* counts, moe_miss_list_t* out);
+/* Prefetch one expert before the next step ([RT] §3.3): mode
+ * MOE_PREFETCH_REFRESH or MOE_PREFETCH_PRESERVE (see moe_set_prefetch).
+ * *action receives a moe_prefetch_action_t; *fill the load (n = 1: expert,
+ * slot, evicted expert or -1) or nothing (n = 0), arrays owned by s and
+ * valid until the next call. The next moe_slots_step counts a load useful
+ * or wasted. */
+moe_status_t moe_slots_prefetch(moe_slots_t* s, int32_t expert, int32_t mode, int32_t* action,
+                                moe_miss_list_t* fill);
 moe_status_t moe_slots_preload(moe_slots_t* s, const int32_t* experts, int32_t n);
 moe_status_t moe_slots_evict(moe_slots_t* s, int32_t expert);
 /* pt [E] (slot or -1) and gen [S]; either may be NULL. */

@@ -178,3 +178,39 @@ def test_create_validates_config_without_gpu(bec):
         st = N.lib.moe_create(C.byref(cfg), C.byref(h))
         assert st == 1 and not h.value
         assert b"moe_create" in N.lib.moe_last_error(None)
+
+
+@pytest.mark.parametrize("policy", [0, 1])
+@pytest.mark.parametrize("mode", [1, 2])
+def test_slot_manager_prefetch_matches_oracle(bec, policy, mode):
+    # speculative accesses between steps ("Paging the Experts" §3.3): the
+    # ABI's loads, refreshes, probes, victims and useful/wasted counts equal
+    # the oracle's on random traces; a predicted expert is sometimes resident,
+    # sometimes absent (also when a union larger than the slots evicted it)
+    rng = np.random.default_rng(40 + 2 * policy + mode)
+    for (E, S, width) in ((16, 8, 3), (64, 12, 10), (32, 6, 9 if policy == 0 else 4)):
+        ref = SlotCache(E, S, policy, seed=5, layer=3, payload_bytes=77)
+        s = bec.Slots(E, S, policy, 5, 3, 77)
+        for _ in range(120):
+            if rng.random() < 0.7:
+                e = int(rng.integers(E))
+                r = ref.prefetch(e, mode)
+                act, fill = s.prefetch(e, mode)
+                assert act == r["action"]
+                if act == "load":
+                    assert fill == (e, r["slot"], r["victim"])
+            u = sorted(rng.choice(E, size=width, replace=False).tolist())
+            counts = [0] * E
+            for e in u:
+                counts[e] = int(rng.integers(1, 4))
+            r = ref.step(u, counts)
+            m = s.step(u, counts)
+            assert (m.hits, m.misses) == (r["hits"], r["misses"])
+            assert list(zip(m.expert, m.slot, m.victim)) == [tuple(f) for f in r["fills"]]
+            assert s.read() == (r["pt"], r["gen"])
+        st, rs, pf = s.stats(), ref.stats(), ref.prefetch_stats()
+        for key in ("hits", "misses", "evictions", "materialized_bytes"):
+            assert st[key] == rs[key], key
+        for key in ("loads", "useful", "wasted", "refreshes", "probes", "bytes"):
+            assert st["prefetch_" + key] == pf[key], key
+        assert pf["loads"] > 0 and pf["refreshes" if mode == 1 else "probes"] > 0

@@ -12,8 +12,8 @@ import oracle
 import workloads as W
 from oracle.cache import SlotCache
 
-from gpu_common import (ExpertCache, bind_all, make_context, pinned_store, tolerance_ok, x_to_f64,
-                        x_to_torch)
+from gpu_common import (ExpertCache, bind_all, make_context, oracle_route_rows, pinned_store,
+                        tolerance_ok, x_to_f64, x_to_torch)
 
 pytestmark = pytest.mark.gpu
 
@@ -98,8 +98,22 @@ def test_plan_matches_oracle(bec):
         ctx.close()
 
 
+_ROUTES = {}
+
+
+def _oracle_routes(w, layer, x64, Wr, bias):
+    """The oracle's routing of every token of a layer's trace (per token, so
+    the rows of one step are the step's routing), computed once per
+    workload and layer."""
+    key = (w, layer, x64.shape[0])
+    if key not in _ROUTES:
+        _ROUTES[key] = oracle_route_rows(x64, Wr, bias, w.top_k, range(x64.shape[0]))
+    return _ROUTES[key]
+
+
 def _run_trace(bec, w, layers, steps, ffn_steps, policy=None, seed=0, tile_bytes=262144,
-               slots=None, preload=False, check_every_step=True, device_admit=False):
+               slots=None, preload=False, check_every_step=True, device_admit=False, stats_out=None,
+               prefetch=0):
     """Run layer_forward for every (step, layer) on the GPU and replay the
     same trace in the oracle; compare bit-exact state each step and outputs on
     ffn_steps. Returns the GPU outputs {(layer, step): y}."""
@@ -110,6 +124,8 @@ def _run_trace(bec, w, layers, steps, ffn_steps, policy=None, seed=0, tile_bytes
     ctx = make_context(bec, w, layers, policy=pol, slots=S, seed=seed, tile_bytes=tile_bytes,
                        device_admit=device_admit)
     keep = bind_all(ctx, w, layers, store)
+    if prefetch:
+        ctx.set_prefetch(prefetch)
     experts = ExpertCache(w)
     plan = bec.Plan(w.n_experts, w.top_k, T)
     idx_t = torch.empty((T, w.top_k), dtype=torch.int32, device="cuda")
@@ -122,11 +138,13 @@ def _run_trace(bec, w, layers, steps, ffn_steps, policy=None, seed=0, tile_bytes
         Wr_t = torch.from_numpy(Wr).cuda()
         b_t = None if bias is None else torch.from_numpy(bias).cuda()
         x = W.activations(w, l, steps * T)
+        all_idx, all_w = _oracle_routes(w, l, x_to_f64(w, x), Wr, bias)
         cache = SlotCache(w.n_experts, S, pol, seed=seed, layer=l, payload_bytes=w.payload_bytes)
         if preload:
             ctx.preload(l, list(range(w.n_experts)))
             cache.preload(range(w.n_experts))
         shared = experts.get(l, w.n_experts) if w.shared_inter else None
+        pred = None
         for s in range(steps):
             xs = x[s * T:(s + 1) * T]
             ctx.layer_forward(l, x_to_torch(w, xs), Wr_t, b_t, idx_t, wt_t, plan, y_t)
@@ -134,9 +152,16 @@ def _run_trace(bec, w, layers, steps, ffn_steps, policy=None, seed=0, tile_bytes
             y = y_t.cpu().numpy().copy()
             outs[(l, s)] = y
             x64 = x_to_f64(w, xs)
-            ridx, rw, _ = oracle.route(x64, Wr, bias, w.top_k)
+            ridx, rw = all_idx[s * T:(s + 1) * T], all_w[s * T:(s + 1) * T]
             rplan = oracle.plan_union(ridx, rw, w.n_experts)
+            if prefetch and pred is not None:
+                cache.prefetch(pred, prefetch)
             rec = cache.step(rplan["uniq"], rplan["counts"])
+            if prefetch:
+                # the decision is taken on fp32 weights on the device: it
+                # must not sit on the threshold
+                assert abs(rw[-1, 0] - 0.2) > 1e-5, (l, s)
+                pred = oracle.prefetch_prediction(ridx, rw)
             assert np.array_equal(idx_t.cpu().numpy(), ridx), (l, s)
             if check_every_step or s == steps - 1:
                 pt, gen = ctx.read_page_table(l)
@@ -151,6 +176,12 @@ def _run_trace(bec, w, layers, steps, ffn_steps, policy=None, seed=0, tile_bytes
         rs = cache.stats()
         for key in ("hits", "misses", "evictions", "materialized_bytes"):
             assert st[key] == rs[key], (l, key, st[key], rs[key])
+        if prefetch:
+            for key, v in cache.prefetch_stats().items():
+                assert st["prefetch_" + key] == v, (l, key, st["prefetch_" + key], v)
+            rs = dict(rs, **{"prefetch_" + key: v for key, v in cache.prefetch_stats().items()})
+        if stats_out is not None:
+            stats_out.append(rs)
     ctx.close()
     del keep
     return outs
@@ -176,6 +207,33 @@ def test_layer_decode_full_size(bec, device_admit):
 def test_layer_mtp_decode_q4(bec, policy, seed, device_admit):
     w = W.with_changes(W.WORKLOADS["mtp_decode"], slots=40)  # >= T*k, small enough to evict
     _run_trace(bec, w, 1, 14, {0, 13}, policy=policy, seed=seed, device_admit=device_admit)
+
+
+@pytest.mark.parametrize("policy,seed,device_admit", [(0, 0, 0), (0, 0, 2), (1, 0, 1), (1, 3, 2)])
+def test_layer_mtp_decode_at_its_configuration(bec, policy, seed, device_admit):
+    # the MTP-batched decode workload as measured: Q4_0 experts, 4 tokens per
+    # step through their expert-major union, 89 slots per layer (35% of 256),
+    # LRU and seeded random; 4 layers x 32 steps with page tables,
+    # generations and counters bit-exact every step and outputs on three steps
+    w = W.with_changes(W.WORKLOADS["mtp_decode"], n_layers=4, n_steps=32)
+    assert w.slots == 89 and w.tokens_per_step == 4
+    stats = []
+    _run_trace(bec, w, 4, 32, {0, 15, 31}, policy=policy, seed=seed, device_admit=device_admit,
+               stats_out=stats)
+    assert sum(r["evictions"] for r in stats) > 0  # the slots were full and refilled
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+def test_layer_decode_trace_with_prefetch(bec, mode):
+    # confidence-gated prefetch with host admission on one-token steps (the
+    # page's serial steps): before each step the previous step's top expert
+    # (weight >= 0.20) is refreshed (mode 1) or probed (mode 2). Page tables,
+    # generations and counters, prefetch counters included, bit-exact with
+    # the oracle's replay; outputs within the bar on three steps
+    w = W.with_changes(W.WORKLOADS["decode"], n_layers=2)
+    stats = []
+    _run_trace(bec, w, 2, 40, {0, 20, 39}, prefetch=mode, stats_out=stats)
+    assert sum(r["prefetch_refreshes" if mode == 1 else "prefetch_probes"] for r in stats) > 10
 
 
 @pytest.mark.parametrize("device_admit", [0, 2])

@@ -336,3 +336,68 @@ def test_prefill_gemm_wait_runs_out_and_context_recovers(bec):
     assert ok, (rel, mx)
     ctx.close()
     del keep
+
+
+def test_prefill_waves_with_prefetch(bec):
+    # confidence-gated prefetch ("Paging the Experts" §3.3, during prefill)
+    # on the long-prefill shapes with a cold 44-slot LRU cache: each chunk's
+    # union is larger than the slots, so its later waves can evict the
+    # previous chunk's predicted expert, which the next chunk then loads
+    # speculatively before its routing. Fills, page tables, generations,
+    # demand and prefetch counters match the oracle's replay; the output is
+    # bit for bit the all-resident context's.
+    w = W.WORKLOADS["wide_prefill"]
+    T, steps, E = 256, 4, w.n_experts
+    store = pinned_store(w, 1)
+    ctx = make_context(bec, w, 1, slots=w.slots, max_tokens=T, device_admit=0)
+    res = make_context(bec, w, 1, slots=E, max_tokens=T, device_admit=0)
+    keep = bind_all(ctx, w, 1, store) + bind_all(res, w, 1, store)
+    res.preload(0, list(range(E)))
+    ctx.set_prefetch(bec.PREFETCH_REFRESH)
+    cache = SlotCache(E, w.slots, w.policy, seed=0, layer=0, payload_bytes=w.payload_bytes)
+    experts = ExpertCache(w)
+    shared = experts.get(0, E)
+    Wr = W.router_weights(w, 0)
+    Wr_t = torch.from_numpy(Wr).cuda()
+    x = W.activations(w, 0, steps * T)
+    x64 = x_to_f64(w, x)
+    all_idx, all_w = oracle_route_rows(x64, Wr, None, w.top_k, range(steps * T))
+    plan = bec.Plan(E, w.top_k, T)
+    idx = torch.empty((T, w.top_k), dtype=torch.int32, device="cuda")
+    wt = torch.empty((T, w.top_k), dtype=torch.float32, device="cuda")
+    y = torch.empty((T, w.hidden), dtype=torch.float32, device="cuda")
+    y_res = torch.empty_like(y)
+    pred, actions = None, []
+    for s in range(steps):
+        xt = x_to_torch(w, x[s * T:(s + 1) * T])
+        ml = ctx.layer_forward(0, xt, Wr_t, None, idx, wt, plan, y)
+        ctx.check_device_errors()
+        res.layer_forward(0, xt, Wr_t, None, idx, wt, plan, y_res)
+        res.check_device_errors()
+        ridx, rw = all_idx[s * T:(s + 1) * T], all_w[s * T:(s + 1) * T]
+        assert np.array_equal(idx.cpu().numpy(), ridx), s
+        rplan = oracle.plan_union(ridx, rw, E)
+        if pred is not None:
+            actions.append(cache.prefetch(pred, oracle.PREFETCH_REFRESH)["action"])
+        rec = cache.step(rplan["uniq"], rplan["counts"])
+        assert abs(rw[-1, 0] - 0.2) > 1e-5, s  # the fp32 decision is well posed
+        pred = oracle.prefetch_prediction(ridx, rw)
+        assert list(zip(ml.expert, ml.slot, ml.victim)) == [tuple(f) for f in rec["fills"]], s
+        pt, gen = ctx.read_page_table(0)
+        assert pt == rec["pt"] and gen == rec["gen"], s
+        assert torch.equal(y, y_res), s
+        yg = y.cpu().numpy().astype(np.float64)
+        sample = [0, T // 2, T - 1]
+        refs = [oracle.moe_layer(x64[s * T + t:s * T + t + 1], ridx[t:t + 1], rw[t:t + 1],
+                                 lambda e: experts.get(0, e), shared)[0] for t in sample]
+        ok, rel, mx = tolerance_ok(yg[sample], np.stack(refs))
+        assert ok, (s, rel, mx)
+    assert "load" in actions  # a prediction evicted by a later wave was loaded
+    st, rs, pf = ctx.stats(0), cache.stats(), cache.prefetch_stats()
+    for key in ("hits", "misses", "evictions", "materialized_bytes"):
+        assert st[key] == rs[key], (key, st[key], rs[key])
+    for key, v in pf.items():
+        assert st["prefetch_" + key] == v, (key, st["prefetch_" + key], v)
+    ctx.close()
+    res.close()
+    del keep
