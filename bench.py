@@ -187,9 +187,9 @@ def run_ours(args, rank, world, dev):
     x_pin = torch.from_numpy(x_host.view(np.int16)).view(torch.bfloat16).pin_memory()
     x_dev = x_pin.to(dev)
 
-    def make_ctx(device_admit):
+    def make_ctx(device_admit, decode_ffn=0):
         ctx = bec.Context(L, E, k, H, w.inter, w.shared_inter, w.quant, w.slots, w.policy, 3, 0,
-                          262144, T, admit_on_device=device_admit)
+                          262144, T, admit_on_device=device_admit, decode_ffn=decode_ffn)
         ctx.bind_store(store)
         for l in range(L):
             ctx.bind_shared(l, shared[l])
@@ -223,10 +223,10 @@ def run_ours(args, rank, world, dev):
 
     x_step = torch.empty((L, T, H), dtype=torch.bfloat16, device=dev)
 
-    def graph_pass(mode, sample_clocks, n_timed=None):
+    def graph_pass(mode, sample_clocks, n_timed=None, decode_ffn=0):
         """Device-resident inputs, on-device admission, the 40-layer step
         replayed as one CUDA graph; returns (ms, clocks, stats, used_graph)."""
-        ctx = make_ctx(mode)
+        ctx = make_ctx(mode, decode_ffn)
         graph = None
         if args.no_graph:
             for s in range(args.warmup):
@@ -288,6 +288,57 @@ def run_ours(args, rank, world, dev):
     clk = clocks.stop()
     elapsed_ms = statistics.median(reps)
 
+    # ---- all-hit pass: every step of a layer repeats that layer's first
+    # token, so after the first step every expert access hits; the 40 layers
+    # read 1.3 GB per step, so each layer's experts have left L2 before the
+    # layer comes round again. Graph-replayed: the route + FFN chain of a
+    # layer step at the speed of HBM, with no host-link traffic
+    def all_hit_pass(decode_ffn=0):
+        ctx = make_ctx(1, decode_ffn)
+        x_fix = x_dev[:, 0:T].contiguous()
+        for _ in range(2):
+            for l in range(L):
+                ctx.layer_forward(l, x_fix[l], routers[l], None, idx, wt, plan, y[l])
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for l in range(L):
+                ctx.layer_forward(l, x_fix[l], routers[l], None, idx, wt, plan, y[l])
+        g.replay()
+        torch.cuda.synchronize(dev)
+        st_a = ctx.stats()
+        n_rep = max(8, min(args.steps, 32))
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(n_rep):
+            g.replay()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        ctx.check_device_errors()
+        st_b = ctx.stats()
+        del g
+        ctx.close()
+        assert st_b["misses"] == st_a["misses"], "the all-hit pass missed"
+        return ev0.elapsed_time(ev1) / n_rep
+
+    ah_ms = statistics.median(all_hit_pass() for _ in range(3))
+
+    # ---- the decode FFN as one persistent launch with tile-granular staging
+    # of the read-through misses' down planes (decode_ffn = 1): the
+    # headline's miss path, the all-hit pass and its kernel time
+    fz_ms = statistics.median(graph_pass(mode, False, decode_ffn=1)[0] for _ in range(2))
+    fz_ah_ms = statistics.median(all_hit_pass(1) for _ in range(2))
+    ctx = make_ctx(1, 1)
+    for s in range(args.warmup):
+        step(ctx, s)
+    ctx.kernel_times()
+    ctx.set_kernel_timing(True)
+    for s in range(args.warmup, n_steps):
+        step(ctx, s)
+    fz_kt = ctx.kernel_times()
+    ctx.set_kernel_timing(False)
+    ctx.check_device_errors()
+    ctx.close()
+
     # ---- pass 2: the same steps, launched call by call with library-side
     # CUDA events around every kernel (roofline and kernel breakdown), with
     # the misses staged by the separate staging kernel so that the FFN
@@ -318,6 +369,19 @@ def run_ours(args, rank, world, dev):
              "policy_replay": policy_replay,
              "h2d_copy_engine_gbs": h2d_bandwidth(torch, dev),
              "per_call_launch_tokens_per_s": round(tokens / (events_ms / 1e3), 2),
+             "decode_ffn_persistent": {
+                 "what": "the decode FFN as one persistent cooperative launch per layer step, a read-through "
+                         "miss's down plane copied into its slot in 256 KiB tiles with ready counters (opt-in "
+                         "decode_ffn = 1; the headline uses the two-launch FFN)",
+                 "tokens_per_s": round(T / (fz_ms / args.steps / 1e3), 2),
+                 "all_hit_tokens_per_s": round(T / (fz_ah_ms / 1e3), 2),
+                 "ffn_us_staged": round(fz_kt["ffn_decode"][0] / max(1, fz_kt["ffn_decode"][1]) * 1e3, 3)},
+             "all_hit": {"what": "graph replay of a 40-layer step whose every expert access hits (each layer "
+                                 "repeats its first token); weights read from HBM, no host-link traffic",
+                         "tokens_per_s": round(T / (ah_ms / 1e3), 2), "ms_per_step": round(ah_ms, 4),
+                         "us_per_layer_step": round(ah_ms * 1e3 / L, 3),
+                         "hbm_gbs": round((min(k * T, E) + 1) * w.payload_bytes / (ah_ms / L / 1e3) / 1e9
+                                          + E * H * 4 / (ah_ms / L / 1e3) / 1e9, 1)},
              "graph": used_graph,
              "repeats": {"n": len(reps), "what": "the K timed steps from a fresh context, each repetition "
                                                  "timed on its own; value = the median",
@@ -554,8 +618,10 @@ def run_mtp_decode(args, dev, mode):
     rows = T * k + T
     gu_bytes = sum((u + 1) * 2 * mat + T * H * 2 + rows * I * 4 for u in timed_u) / len(timed_u)
     gu_ms, gu_n = kt["ffn_gateup"]
+    dn_ms, dn_n = kt["ffn_down"]
     peak, peak_kind = peaks()
     gu_gbs = gu_bytes / (gu_ms / gu_n / 1e3) / 1e9 if gu_n else None
+    rt_ms, rt_n = kt["route"]
     all_u = [len(st[0]) for tr in traces for st in tr]
     assign = L * n_steps * T * k
     return {
@@ -574,6 +640,8 @@ def run_mtp_decode(args, dev, mode):
                      "unit": "GB/s", "frac": round(gu_gbs / peak, 4) if gu_gbs else None,
                      "bytes_per_launch": round(gu_bytes),
                      "avg_launch_us": round(gu_ms / gu_n * 1e3, 3) if gu_n else None},
+        "layer_step_us_staged": round((rt_ms / rt_n + gu_ms / gu_n + dn_ms / dn_n) * 1e3, 2)
+        if gu_n and rt_n and dn_n else None,
         "kernels": {kname: {"ms": round(kms, 3), "launches": n, "avg_us": round(kms / n * 1e3, 3) if n else None}
                     for kname, (kms, n) in kt.items()},
         "policy_replay": replay_policies(bec, w, traces, n_steps, static=False),
@@ -889,9 +957,12 @@ def finish(args, w, world, value, elapsed_ms, e2e_value, kt, st0, st1, clk, extr
     dn_bytes = units * mat + units * T * w.inter * 4 + T * H * 4
     gu_ms, gu_n = kt["ffn_gateup"]
     dn_ms, dn_n = kt["ffn_down"]
+    rt_ms, rt_n = kt["route"]
     peak, peak_kind = peaks()
     gu_gbs = gu_bytes / (gu_ms / gu_n / 1e3) / 1e9 if gu_n else None
     dn_gbs = dn_bytes / (dn_ms / dn_n / 1e3) / 1e9 if dn_n else None
+    rt_bytes = E * H * 4 + T * H * 2
+    layer_us = (rt_ms / rt_n + gu_ms / gu_n + dn_ms / dn_n) * 1e3 if gu_n and rt_n and dn_n else None
     launches = sum(n for _, n in kt.values())
     dh = st1["hits"] - st0["hits"]
     dm = st1["misses"] - st0["misses"]
@@ -914,12 +985,18 @@ def finish(args, w, world, value, elapsed_ms, e2e_value, kt, st0, st1, clk, extr
                      "traffic": recorded_traffic("ffn_decode.cu", "ffn_gateup_decode"),
                      "bytes_per_launch": gu_bytes,
                      "avg_launch_us": round(gu_ms / gu_n * 1e3, 3) if gu_n else None},
+        "ffn_down": {"achieved_gbs": round(dn_gbs, 1) if dn_gbs else None,
+                     "frac": round(dn_gbs / peak, 4) if dn_gbs else None, "bytes_per_launch": dn_bytes},
+        "layer_step_staged": {"what": "route + gate/up + down launched call by call with events around each "
+                                      "kernel (launch gaps included), misses staged by the staging kernel",
+                              "route_plus_ffn_us": round(layer_us, 3) if layer_us else None,
+                              "bytes": gu_bytes + dn_bytes + rt_bytes,
+                              "hbm_frac": round((gu_bytes + dn_bytes + rt_bytes) / (layer_us * 1e-6) / 1e9 / peak,
+                                                4) if layer_us else None},
         "kernels": {kname: {"ms": round(ms, 3), "launches": n,
                             "avg_us": round(ms / n * 1e3, 3) if n else None}
                     for kname, (ms, n) in kt.items()},
         "kernels_pass": "call by call, misses staged by the staging kernel",
-        "ffn_down": {"achieved_gbs": round(dn_gbs, 1) if dn_gbs else None,
-                     "frac": round(dn_gbs / peak, 4) if dn_gbs else None, "bytes_per_launch": dn_bytes},
         "host_link": {"kernel": "stage_copy (misses, pinned store -> slots)",
                       "achieved": round(staged / (kt["stage_copy"][0] / 1e3) / 1e9, 1)
                       if kt["stage_copy"][0] else None,

@@ -21,7 +21,7 @@ F32, BF16 = 0, 1
 MODE_AUTO, MODE_DECODE, MODE_PREFILL = 0, 1, 2
 PREFETCH_OFF, PREFETCH_REFRESH, PREFETCH_PRESERVE = 0, 1, 2
 PREFETCH_ACTIONS = ("probe", "refresh", "load")
-KERNEL_KINDS = ("route", "plan", "ffn_gateup", "ffn_down", "stage_copy")
+KERNEL_KINDS = ("route", "plan", "ffn_gateup", "ffn_down", "stage_copy", "ffn_decode")
 
 
 class Config(C.Structure):
@@ -29,7 +29,7 @@ class Config(C.Structure):
                 ("hidden", C.c_int32), ("inter", C.c_int32), ("shared_inter", C.c_int32),
                 ("quant", C.c_int32), ("slots_per_layer", C.c_int32), ("policy", C.c_int32),
                 ("n_streams", C.c_int32), ("seed", C.c_uint64), ("tile_bytes", C.c_int64),
-                ("max_tokens", C.c_int32), ("admit_on_device", C.c_int32)]
+                ("max_tokens", C.c_int32), ("admit_on_device", C.c_int32), ("decode_ffn", C.c_int32)]
 
 
 class PlanT(C.Structure):

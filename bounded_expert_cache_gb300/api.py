@@ -86,10 +86,10 @@ class Context:
 
     def __init__(self, n_layers, n_experts, top_k, hidden, inter, shared_inter=0, quant=N.Q8_0,
                  slots_per_layer=None, policy=N.LRU, n_streams=3, seed=0, tile_bytes=262144,
-                 max_tokens=8, admit_on_device=0):
+                 max_tokens=8, admit_on_device=0, decode_ffn=0):
         self.cfg = N.Config(n_layers, n_experts, top_k, hidden, inter, shared_inter, quant,
                             slots_per_layer or n_experts, policy, n_streams, seed, tile_bytes,
-                            max_tokens, int(admit_on_device))
+                            max_tokens, int(admit_on_device), int(decode_ffn))
         h = C.c_void_p()
         _check(lib.moe_create(C.byref(self.cfg), C.byref(h)), None)
         self.h = h

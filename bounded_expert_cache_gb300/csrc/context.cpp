@@ -147,6 +147,7 @@ extern "C" void moe_destroy(moe_ctx_t* ctx) {
   cudaFree(ctx->d_fills);
   cudaFree(ctx->d_done);
   cudaFree(ctx->d_ffn_ticket);
+  cudaFree(ctx->d_fsync);
   cudaFree(ctx->d_x16);
   cudaFree(ctx->d_hp);
   cudaFree(ctx->d_yp);
@@ -190,6 +191,7 @@ extern "C" moe_status_t moe_create(const moe_config_t* cfg, moe_ctx_t** out) {
   else if (c.tile_bytes < 16 || c.tile_bytes % 16) why = "tile_bytes not a positive multiple of 16";
   else if (c.max_tokens < 1) why = "max_tokens < 1";
   else if (c.admit_on_device < 0 || c.admit_on_device > 2) why = "admit_on_device must be 0, 1 or 2";
+  else if (c.decode_ffn < 0 || c.decode_ffn > 1) why = "decode_ffn must be 0 or 1";
   if (!why.empty()) {
     g_create_err = "moe_create: " + why;
     return MOE_ERR_ARG;
@@ -281,6 +283,16 @@ extern "C" moe_status_t moe_create(const moe_config_t* cfg, moe_ctx_t** out) {
   ctx->read_through = c.admit_on_device == 2;
   CKC(cudaMalloc(&ctx->d_ffn_ticket, sizeof(unsigned int)));
   CKC(cudaMemset(ctx->d_ffn_ticket, 0, sizeof(unsigned int)));
+  {
+    // counters of the fused decode FFN: end ticket, abort flag, gate/up
+    // items done, one per tile of each unit's down plane
+    ctx->fused_units = std::min(E, std::min(c.max_tokens, 8) * c.top_k) + 1;
+    const int64_t dn = ctx->geom.qbytes[2] + ctx->geom.sbytes[2];
+    ctx->fused_tiles = static_cast<int>((dn + c.tile_bytes - 1) / c.tile_bytes);
+    const size_t n = 3 + static_cast<size_t>(ctx->fused_units) * ctx->fused_tiles;
+    CKC(cudaMalloc(&ctx->d_fsync, sizeof(unsigned int) * n));
+    CKC(cudaMemset(ctx->d_fsync, 0, sizeof(unsigned int) * n));
+  }
   if (ctx->dev_admit) {
     ctx->max_fills = std::min(E, c.max_tokens * c.top_k);
     CKC(cudaMalloc(&ctx->d_owner, sizeof(int32_t) * L * S));
@@ -973,13 +985,34 @@ extern "C" moe_status_t moe_expert_ffn(moe_ctx_t* ctx, int32_t layer, const void
   a.ldh = ctx->ldh;
   a.y = y;
   a.err = ctx->d_err;
-  if (ctx->timing) {
-    for (int i = 0; i < 4; ++i) a.ev[i] = timing_event(ctx);
+  if (ctx->cfg.decode_ffn == 0) {
+    // two launches: gate/up + SwiGLU, then down + combine
+    if (ctx->timing) {
+      for (int i = 0; i < 4; ++i) a.ev[i] = timing_event(ctx);
+    }
+    CK(moe::launch_ffn_decode(a, ctx->num_sms, reinterpret_cast<cudaStream_t>(stream)));
+    if (ctx->timing) {
+      ctx->timed.push_back({MOE_KT_GATEUP, a.ev[0], a.ev[1]});
+      ctx->timed.push_back({MOE_KT_DOWN, a.ev[2], a.ev[3]});
+      if (ctx->timed.size() > 16384) CK(resolve_timing(ctx));
+    }
+    return MOE_OK;
   }
-  CK(moe::launch_ffn_decode(a, ctx->num_sms, reinterpret_cast<cudaStream_t>(stream)));
   if (ctx->timing) {
-    ctx->timed.push_back({MOE_KT_GATEUP, a.ev[0], a.ev[1]});
-    ctx->timed.push_back({MOE_KT_DOWN, a.ev[2], a.ev[3]});
+    for (int i = 0; i < 2; ++i) a.ev[i] = timing_event(ctx);
+  }
+  // one persistent launch: gate/up, down and the misses' down-plane tiles
+  moe::FusedLaunch fl{};
+  fl.sync = ctx->d_fsync;
+  fl.max_units = ctx->fused_units;
+  fl.max_tiles = ctx->fused_tiles;
+  fl.tile_bytes = ctx->cfg.tile_bytes;
+  fl.wait_cycles = moe::kFusedWaitCycles;
+  fl.grid = ctx->num_sms;
+  fl.pdl = true;
+  CK(moe::launch_ffn_decode_fused(a, fl, reinterpret_cast<cudaStream_t>(stream)));
+  if (ctx->timing) {
+    ctx->timed.push_back({MOE_KT_FFN, a.ev[0], a.ev[1]});
     if (ctx->timed.size() > 16384) CK(resolve_timing(ctx));
   }
   return MOE_OK;

@@ -185,8 +185,8 @@ cudaError_t launch_ffn_decode(const FfnArgs& a, int num_sms, cudaStream_t st);
 // The fused decode FFN (one persistent cooperative launch): its counters
 // (zero between launches; the kernel clears them) and launch shape.
 struct FusedLaunch {
-  unsigned int* sync;   // [2 + max_units + max_units * max_tiles]
-  int max_units;        // unit-table capacity (the last counter is the shared expert's)
+  unsigned int* sync;   // [3 + max_units * max_tiles]
+  int max_units;        // unit-table capacity
   int max_tiles;        // tiles of one down plane
   int64_t tile_bytes;   // staging tile
   long long wait_cycles;
@@ -242,6 +242,8 @@ struct moe_ctx {
   int32_t max_fills = 0;
   bool read_through = false;              // misses materialised by the FFN
   unsigned int* d_ffn_ticket = nullptr;
+  unsigned int* d_fsync = nullptr;        // counters of the fused decode FFN
+  int fused_units = 0, fused_tiles = 0;
   // prefill path (max_tokens > 8)
   bool prefill = false;
   uint16_t* d_x16 = nullptr;               // fp16 [rows][H]

@@ -96,6 +96,12 @@ typedef struct {
                                  kernel over the host link, no host sync;
                               2: admission on the GPU, misses materialised by
                                  the FFN while it reads them from the store */
+  int32_t decode_ffn;      /* decode FFN (T <= 8): 0: two launches, gate/up
+                                 then down (the default); 1: one persistent
+                                 cooperative launch in which a read-through
+                                 miss's down plane is copied into its slot in
+                                 staging tiles, each with a ready counter that
+                                 the down rows it holds wait on (bounded) */
 } moe_config_t;
 
 /* Expert-major plan ([NfE] §5.3, §5.5). Device arrays owned by the caller.
@@ -346,17 +352,19 @@ moe_status_t moe_read_slot(moe_ctx_t* ctx, int32_t layer, int32_t slot, void* ho
 /* Kernel timing (tracing aid). While enabled, the context records CUDA
  * events on the launching stream around every kernel it launches.
  * moe_get_kernel_times synchronises those events and returns, per kind
- * (route incl. fused plan and on-device admission, standalone plan, FFN
- * gate/up, FFN down, on-device staging copy), the
- * summed device milliseconds and the launch count since the last call, then
- * resets them. Either output may be NULL. */
+ * (route incl. fused plan and on-device admission, standalone plan, prefill
+ * FFN gate/up, prefill FFN down, on-device staging copy, decode FFN: gate/up,
+ * down and the misses' tiles in one launch), the summed device milliseconds
+ * and the launch count since the last call, then resets them. Either output
+ * may be NULL. */
 typedef enum {
   MOE_KT_ROUTE = 0,
   MOE_KT_PLAN = 1,
   MOE_KT_GATEUP = 2,
   MOE_KT_DOWN = 3,
   MOE_KT_STAGE = 4,
-  MOE_KT_COUNT = 5
+  MOE_KT_FFN = 5,
+  MOE_KT_COUNT = 6
 } moe_kernel_kind_t;
 moe_status_t moe_set_kernel_timing(moe_ctx_t* ctx, int32_t enable);
 moe_status_t moe_get_kernel_times(moe_ctx_t* ctx, double* ms, int64_t* launches);

@@ -53,10 +53,11 @@ class ExpertCache:
 
 
 def make_context(bec, w: W.Workload, layers: int, policy=None, slots=None, seed=0,
-                 tile_bytes=262144, max_tokens=None, device_admit=False):
+                 tile_bytes=262144, max_tokens=None, device_admit=False, decode_ffn=0):
     ctx = bec.Context(layers, w.n_experts, w.top_k, w.hidden, w.inter, w.shared_inter, w.quant,
                       slots or w.slots, w.policy if policy is None else policy, 3, seed,
-                      tile_bytes, max_tokens or w.tokens_per_step, admit_on_device=device_admit)
+                      tile_bytes, max_tokens or w.tokens_per_step, admit_on_device=device_admit,
+                      decode_ffn=decode_ffn)
     return ctx
 
 

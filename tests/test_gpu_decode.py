@@ -113,7 +113,7 @@ def _oracle_routes(w, layer, x64, Wr, bias):
 
 def _run_trace(bec, w, layers, steps, ffn_steps, policy=None, seed=0, tile_bytes=262144,
                slots=None, preload=False, check_every_step=True, device_admit=False, stats_out=None,
-               prefetch=0):
+               prefetch=0, decode_ffn=0):
     """Run layer_forward for every (step, layer) on the GPU and replay the
     same trace in the oracle; compare bit-exact state each step and outputs on
     ffn_steps. Returns the GPU outputs {(layer, step): y}."""
@@ -122,7 +122,7 @@ def _run_trace(bec, w, layers, steps, ffn_steps, policy=None, seed=0, tile_bytes
     pol = w.policy if policy is None else policy
     S = slots or w.slots
     ctx = make_context(bec, w, layers, policy=pol, slots=S, seed=seed, tile_bytes=tile_bytes,
-                       device_admit=device_admit)
+                       device_admit=device_admit, decode_ffn=decode_ffn)
     keep = bind_all(ctx, w, layers, store)
     if prefetch:
         ctx.set_prefetch(prefetch)
@@ -221,6 +221,29 @@ def test_layer_mtp_decode_at_its_configuration(bec, policy, seed, device_admit):
     _run_trace(bec, w, 4, 32, {0, 15, 31}, policy=policy, seed=seed, device_admit=device_admit,
                stats_out=stats)
     assert sum(r["evictions"] for r in stats) > 0  # the slots were full and refilled
+
+
+# The decode FFN as one persistent launch with the tile-granular staging of a
+# read-through miss's down plane (decode_ffn = 1): the same parity bar, in
+# every admission mode, at one, four (MTP, Q4_0) and eight tokens, with small
+# staging tiles (many ready counters per down plane) and the affine INT4
+# format; outputs bitwise equal to the two-launch path.
+@pytest.mark.parametrize("device_admit", MODES)
+def test_fused_decode_ffn_trace(bec, device_admit):
+    w = W.WORKLOADS["decode"]
+    _run_trace(bec, w, 2, 24, {0, 5, 23}, device_admit=device_admit, decode_ffn=1)
+
+
+@pytest.mark.parametrize("name,T,tile", [("mtp_decode", 4, 262144), ("decode", 8, 16000), ("decode", 1, 4096),
+                                         ("i4_decode", 1, 262144), ("tiny", 4, 8192)])
+def test_fused_decode_ffn_shapes_and_tiles(bec, name, T, tile):
+    base = W.WORKLOADS[name]
+    w = W.with_changes(base, tokens_per_step=T, n_layers=1, n_steps=10,
+                       slots=min(base.n_experts, max(base.slots, base.top_k * T)))
+    a = _run_trace(bec, w, 1, 10, {0, 9}, device_admit=2, tile_bytes=tile, decode_ffn=1)
+    b = _run_trace(bec, w, 1, 10, set(), device_admit=2, tile_bytes=tile, check_every_step=False)
+    for key in a:
+        assert np.array_equal(a[key], b[key]), key
 
 
 @pytest.mark.parametrize("mode", [1, 2])
@@ -446,11 +469,12 @@ def _check_resident_payloads(bec, w, device_admit):
     del keep
 
 
+@pytest.mark.parametrize("decode_ffn", [0, 1])
 @pytest.mark.parametrize("device_admit", [1, 2])
-def test_fail_closed_stale_generation_device_admission(bec, device_admit):
+def test_fail_closed_stale_generation_device_admission(bec, device_admit, decode_ffn):
     w = W.with_changes(W.WORKLOADS["tiny"], n_steps=2)
     store = pinned_store(w, 1)
-    ctx = make_context(bec, w, 1, device_admit=device_admit)
+    ctx = make_context(bec, w, 1, device_admit=device_admit, decode_ffn=decode_ffn)
     bind_all(ctx, w, 1, store)
     plan = bec.Plan(w.n_experts, w.top_k, 4)
     x = x_to_torch(w, W.activations(w, 0, 4))
