@@ -187,9 +187,10 @@ def run_ours(args, rank, world, dev):
     x_pin = torch.from_numpy(x_host.view(np.int16)).view(torch.bfloat16).pin_memory()
     x_dev = x_pin.to(dev)
 
-    def make_ctx(device_admit, decode_ffn=0):
+    def make_ctx(device_admit, decode_ffn=None):
         ctx = bec.Context(L, E, k, H, w.inter, w.shared_inter, w.quant, w.slots, w.policy, 3, 0,
-                          262144, T, admit_on_device=device_admit, decode_ffn=decode_ffn)
+                          262144, T, admit_on_device=device_admit,
+                          decode_ffn=args.decode_ffn if decode_ffn is None else decode_ffn)
         ctx.bind_store(store)
         for l in range(L):
             ctx.bind_shared(l, shared[l])
@@ -223,7 +224,7 @@ def run_ours(args, rank, world, dev):
 
     x_step = torch.empty((L, T, H), dtype=torch.bfloat16, device=dev)
 
-    def graph_pass(mode, sample_clocks, n_timed=None, decode_ffn=0):
+    def graph_pass(mode, sample_clocks, n_timed=None, decode_ffn=None):
         """Device-resident inputs, on-device admission, the 40-layer step
         replayed as one CUDA graph; returns (ms, clocks, stats, used_graph)."""
         ctx = make_ctx(mode, decode_ffn)
@@ -293,7 +294,7 @@ def run_ours(args, rank, world, dev):
     # read 1.3 GB per step, so each layer's experts have left L2 before the
     # layer comes round again. Graph-replayed: the route + FFN chain of a
     # layer step at the speed of HBM, with no host-link traffic
-    def all_hit_pass(decode_ffn=0):
+    def all_hit_pass(decode_ffn=None):
         ctx = make_ctx(1, decode_ffn)
         x_fix = x_dev[:, 0:T].contiguous()
         for _ in range(2):
@@ -320,24 +321,25 @@ def run_ours(args, rank, world, dev):
         assert st_b["misses"] == st_a["misses"], "the all-hit pass missed"
         return ev0.elapsed_time(ev1) / n_rep
 
-    ah_ms = statistics.median(all_hit_pass() for _ in range(3))
-
-    # ---- the decode FFN as one persistent launch with tile-granular staging
-    # of the read-through misses' down planes (decode_ffn = 1): the
-    # headline's miss path, the all-hit pass and its kernel time
-    fz_ms = statistics.median(graph_pass(mode, False, decode_ffn=1)[0] for _ in range(2))
-    fz_ah_ms = statistics.median(all_hit_pass(1) for _ in range(2))
-    ctx = make_ctx(1, 1)
-    for s in range(args.warmup):
-        step(ctx, s)
-    ctx.kernel_times()
-    ctx.set_kernel_timing(True)
-    for s in range(args.warmup, n_steps):
-        step(ctx, s)
-    fz_kt = ctx.kernel_times()
-    ctx.set_kernel_timing(False)
-    ctx.check_device_errors()
-    ctx.close()
+    ah_ms = fz_ms = fz_ah_ms = fz_kt = None
+    if not args.skip_extra:
+        ah_ms = statistics.median(all_hit_pass() for _ in range(3))
+        # ---- the decode FFN as one persistent launch with tile-granular
+        # staging of the read-through misses' down planes (decode_ffn = 1):
+        # the headline's miss path, the all-hit pass and its kernel time
+        fz_ms = statistics.median(graph_pass(mode, False, decode_ffn=1)[0] for _ in range(2))
+        fz_ah_ms = statistics.median(all_hit_pass(1) for _ in range(2))
+        ctx = make_ctx(1, 1)
+        for s in range(args.warmup):
+            step(ctx, s)
+        ctx.kernel_times()
+        ctx.set_kernel_timing(True)
+        for s in range(args.warmup, n_steps):
+            step(ctx, s)
+        fz_kt = ctx.kernel_times()
+        ctx.set_kernel_timing(False)
+        ctx.check_device_errors()
+        ctx.close()
 
     # ---- pass 2: the same steps, launched call by call with library-side
     # CUDA events around every kernel (roofline and kernel breakdown), with
@@ -369,14 +371,14 @@ def run_ours(args, rank, world, dev):
              "policy_replay": policy_replay,
              "h2d_copy_engine_gbs": h2d_bandwidth(torch, dev),
              "per_call_launch_tokens_per_s": round(tokens / (events_ms / 1e3), 2),
-             "decode_ffn_persistent": {
+             "decode_ffn_persistent": None if fz_ms is None else {
                  "what": "the decode FFN as one persistent cooperative launch per layer step, a read-through "
                          "miss's down plane copied into its slot in 256 KiB tiles with ready counters (opt-in "
                          "decode_ffn = 1; the headline uses the two-launch FFN)",
                  "tokens_per_s": round(T / (fz_ms / args.steps / 1e3), 2),
                  "all_hit_tokens_per_s": round(T / (fz_ah_ms / 1e3), 2),
                  "ffn_us_staged": round(fz_kt["ffn_decode"][0] / max(1, fz_kt["ffn_decode"][1]) * 1e3, 3)},
-             "all_hit": {"what": "graph replay of a 40-layer step whose every expert access hits (each layer "
+             "all_hit": None if ah_ms is None else {"what": "graph replay of a 40-layer step whose every expert access hits (each layer "
                                  "repeats its first token); weights read from HBM, no host-link traffic",
                          "tokens_per_s": round(T / (ah_ms / 1e3), 2), "ms_per_step": round(ah_ms, 4),
                          "us_per_layer_step": round(ah_ms * 1e3 / L, 3),
@@ -1048,6 +1050,10 @@ def main():
     ap.add_argument("--int4-decode-only", action="store_true",
                     help="only the affine INT4 decode pass (--admission 1 or 2; 0 means read-through)")
     ap.add_argument("--prefill-tokens", type=int, default=0, help="profiling: tokens of the prefill chunk")
+    ap.add_argument("--skip-extra", action="store_true",
+                    help="profiling: skip the all-hit and persistent-FFN passes of the decode workload")
+    ap.add_argument("--decode-ffn", type=int, default=0, choices=[0, 1],
+                    help="decode FFN of the headline passes (0 two launches, 1 one persistent launch)")
     ap.add_argument("--repeats", type=int, default=5,
                     help="repetitions of the timed headline and end-to-end passes (median reported)")
     ap.add_argument("--admission", type=int, default=0, choices=[0, 1, 2],
