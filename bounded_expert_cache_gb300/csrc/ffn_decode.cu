@@ -16,10 +16,11 @@
 // Each 16- or 32-weight chunk is dotted in fp32 and scaled once by its fp16
 // block scale.
 //
-// Phase 1 (gate/up): one warp item = (unit, 2 rows): rows r, r+1 of the gate
-// and up matrices of one unit (a routed expert of the union, or the shared
-// expert), for every token routed to it; writes h = silu(g) * u in fp32 to
-// scratch, indexed by expert-major assignment (routed) or token (shared).
+// Phase 1 (gate/up): one warp item = (unit, rows): row r (one token) or rows
+// r, r+1 (several tokens) of the gate and up matrices of one unit (a routed
+// expert of the union, or the shared expert), for every token routed to it;
+// writes h = silu(g) * u in fp32 to scratch, indexed by expert-major
+// assignment (routed) or token (shared).
 // Phase 2 (down + combine): one block per SM owns an even run of output rows
 // (about H / SMs); warp items = (unit, 2 rows), loaded in batches; each
 // item's partial sums (already weighted by the combine weight) go to shared
@@ -287,13 +288,24 @@ __device__ __forceinline__ bool unit_ok(const FfnArgs& a, const UnitRef& U) {
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 
 // ------------------------------------------------------------ phase 1
-// Two blocks per SM for four-token groups (at most 128 registers a thread,
-// a few spilled): 29.5 against 32.4 us a launch on the MTP-batched workload.
+// Rows per gate/up warp item and blocks per SM the launch asks for. One
+// token: one gate and one up row per item, four blocks per SM (64
+// registers a thread, a few spilled): twice the warps of two-row items, 13.6
+// against 16.6 us a launch on the decode workload (16.0 at three blocks per
+// SM). Four-token groups: two rows, two blocks per SM (at most 128
+// registers, a few spilled): 29.5 against 32.4 us on the MTP-batched
+// workload. Eight-token groups: two rows, as many blocks as fit.
+template <int TM>
+struct GateupRows {
+  static constexpr int R = TM == 1 ? 1 : 2;
+  static constexpr int kMinBlocks = TM == 1 ? 4 : (TM == 4 ? 2 : 1);
+};
 template <int Q, int TM, int XT>
-__global__ void __launch_bounds__(kThreads, TM == 4 ? 2 : 1) gateup_kernel(FfnArgs a) {
+__global__ void __launch_bounds__(kThreads, GateupRows<TM>::kMinBlocks) gateup_kernel(FfnArgs a) {
   extern __shared__ float xs[];  // [T][H] swizzled
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int H = a.H, T = a.T;
+  constexpr int RG = GateupRows<TM>::R;  // gate rows (and as many up rows) per warp item
   // x is the layer's input, complete once the router has passed its wait
   for (int i = tid; i < T * H; i += kThreads) {
     const int t = i / H, k = i - t * H;
@@ -304,8 +316,8 @@ __global__ void __launch_bounds__(kThreads, TM == 4 ? 2 : 1) gateup_kernel(FfnAr
   __syncthreads();
   const int n_units = __ldg(a.units);
   const int nu = n_units - (a.shared ? 1 : 0);  // routed units
-  const int per_routed = a.I / kRowsPerItem;
-  const int per_shared = a.shared ? a.Is / kRowsPerItem : 0;
+  const int per_routed = a.I / RG;
+  const int per_shared = a.shared ? a.Is / RG : 0;
   const int items = nu * per_routed + per_shared;
   const int rowbytes = Q == MOE_Q8_0 ? H : H / 2;
   const int nch = rowbytes / 16;
@@ -314,21 +326,21 @@ __global__ void __launch_bounds__(kThreads, TM == 4 ? 2 : 1) gateup_kernel(FfnAr
     int u, r0;
     if (it < nu * per_routed) {
       u = it / per_routed;
-      r0 = (it - u * per_routed) * kRowsPerItem;
+      r0 = (it - u * per_routed) * RG;
     } else {
       u = nu;
-      r0 = (it - nu * per_routed) * kRowsPerItem;
+      r0 = (it - nu * per_routed) * RG;
     }
     const UnitRef U = resolve_unit(a, u);
     const bool ok = unit_ok(a, U);
-    const uint8_t* q[2 * kRowsPerItem];
-    const uint8_t* s[2 * kRowsPerItem];
+    const uint8_t* q[2 * RG];
+    const uint8_t* s[2 * RG];
 #pragma unroll
-    for (int r = 0; r < kRowsPerItem; ++r) {
+    for (int r = 0; r < RG; ++r) {
 #pragma unroll
       for (int m = 0; m < 2; ++m) {
-        q[m * kRowsPerItem + r] = U.base + U.qoff[m] + static_cast<int64_t>(r0 + r) * rowbytes;
-        s[m * kRowsPerItem + r] = U.base + U.soff[m] + static_cast<int64_t>(r0 + r) * sc_row;
+        q[m * RG + r] = U.base + U.qoff[m] + static_cast<int64_t>(r0 + r) * rowbytes;
+        s[m * RG + r] = U.base + U.soff[m] + static_cast<int64_t>(r0 + r) * sc_row;
       }
     }
     for (int m0 = 0; m0 < U.M; m0 += TM) {
@@ -337,38 +349,38 @@ __global__ void __launch_bounds__(kThreads, TM == 4 ? 2 : 1) gateup_kernel(FfnAr
 #pragma unroll
       for (int m = 0; m < TM; ++m)
         tok[m] = (m < mcount) ? (U.p0 >= 0 ? __ldg(a.plan.perm_tok + U.p0 + m0 + m) : m0 + m) : 0;
-      float acc[2 * kRowsPerItem][TM];
+      float acc[2 * RG][TM];
 #pragma unroll
-      for (int r = 0; r < 2 * kRowsPerItem; ++r)
+      for (int r = 0; r < 2 * RG; ++r)
 #pragma unroll
         for (int m = 0; m < TM; ++m) acc[r][m] = 0.f;
 #pragma unroll 2
       for (int c = lane; c < nch; c += 32) {
-        uint4 w[2 * kRowsPerItem];
-        uint32_t mb[2 * kRowsPerItem];
+        uint4 w[2 * RG];
+        uint32_t mb[2 * RG];
         if (U.miss) {
 #pragma unroll
-          for (int r = 0; r < 2 * kRowsPerItem; ++r) {
+          for (int r = 0; r < 2 * RG; ++r) {
             w[r] = ld_host(q[r] + c * 16);
             mb[r] = ld_meta_host<Q>(s[r], c);
           }
           if (m0 == 0) {
 #pragma unroll
-            for (int r = 0; r < 2 * kRowsPerItem; ++r) {
+            for (int r = 0; r < 2 * RG; ++r) {
               *reinterpret_cast<uint4*>(U.dst + (q[r] - U.base) + c * 16) = w[r];
               st_meta<Q>(U.dst + (s[r] - U.base), c, mb[r]);
             }
           }
         } else {
 #pragma unroll
-          for (int r = 0; r < 2 * kRowsPerItem; ++r) {
+          for (int r = 0; r < 2 * RG; ++r) {
             w[r] = ldg_stream(q[r] + c * 16);
             mb[r] = ld_meta<Q>(s[r], c);
           }
         }
-        float d[2 * kRowsPerItem];
+        float d[2 * RG];
 #pragma unroll
-        for (int r = 0; r < 2 * kRowsPerItem; ++r) d[r] = meta_scale<Q>(mb[r]);
+        for (int r = 0; r < 2 * RG; ++r) d[r] = meta_scale<Q>(mb[r]);
 #pragma unroll
         for (int m = 0; m < TM; ++m) {
           if (m < mcount) {
@@ -377,14 +389,14 @@ __global__ void __launch_bounds__(kThreads, TM == 4 ? 2 : 1) gateup_kernel(FfnAr
               float xv[16];
               load_chunk16(xr, c, xv);
 #pragma unroll
-              for (int r = 0; r < 2 * kRowsPerItem; ++r)
+              for (int r = 0; r < 2 * RG; ++r)
                 acc[r][m] = fmaf(d[r], dot_q8(w[r], xv), acc[r][m]);
             } else if (Q == MOE_Q4_0) {
               float xl[16], xh[16];
               load_chunk16(xr, 2 * c, xl);
               load_chunk16(xr, 2 * c + 1, xh);
 #pragma unroll
-              for (int r = 0; r < 2 * kRowsPerItem; ++r)
+              for (int r = 0; r < 2 * RG; ++r)
                 acc[r][m] = fmaf(d[r], dot_q4(w[r], xl, xh), acc[r][m]);
             } else {
               float xl[16], xh[16];
@@ -392,14 +404,14 @@ __global__ void __launch_bounds__(kThreads, TM == 4 ? 2 : 1) gateup_kernel(FfnAr
               load_chunk16(xr, 2 * c + 1, xh);
               const float xsum = sum32(xl, xh);
 #pragma unroll
-              for (int r = 0; r < 2 * kRowsPerItem; ++r)
+              for (int r = 0; r < 2 * RG; ++r)
                 acc[r][m] = fmaf(d[r], dot_u4(w[r], xl, xh), fmaf(meta_bias<Q>(mb[r]), xsum, acc[r][m]));
             }
           }
         }
       }
 #pragma unroll
-      for (int r = 0; r < 2 * kRowsPerItem; ++r)
+      for (int r = 0; r < 2 * RG; ++r)
 #pragma unroll
         for (int m = 0; m < TM; ++m)
 #pragma unroll
@@ -415,9 +427,9 @@ __global__ void __launch_bounds__(kThreads, TM == 4 ? 2 : 1) gateup_kernel(FfnAr
           if (m < mcount) {
             const int hrow = U.p0 >= 0 ? U.p0 + m0 + m : a.T * a.k + m0 + m;
 #pragma unroll
-            for (int r = 0; r < kRowsPerItem; ++r)
+            for (int r = 0; r < RG; ++r)
               a.h[static_cast<int64_t>(hrow) * a.ldh + r0 + r] =
-                  silu(acc[r][m]) * acc[kRowsPerItem + r][m];
+                  silu(acc[r][m]) * acc[RG + r][m];
           }
         }
       }
@@ -1457,8 +1469,8 @@ cudaError_t launch_tm(const FfnArgs& a, int num_sms, cudaStream_t st) {
   err = cudaFuncSetAttribute(down_kernel<Q, TM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem2));
   if (err != cudaSuccess) return err;
-  const int items1 = max_units * (std::max(a.I, a.Is) / kRowsPerItem);
-  const int grid1 = std::max(1, std::min((items1 + kWarps - 1) / kWarps, num_sms * 2));
+  const int items1 = max_units * (std::max(a.I, a.Is) / GateupRows<TM>::R);
+  const int grid1 = std::max(1, std::min((items1 + kWarps - 1) / kWarps, num_sms * 4));
   if (a.ev[0]) cudaEventRecord(a.ev[0], st);
   err = a.xt == MOE_BF16 ? pdl_launch(gateup_kernel<Q, TM, MOE_BF16>, dim3(grid1), dim3(kThreads), smem1, st, a)
                          : pdl_launch(gateup_kernel<Q, TM, MOE_F32>, dim3(grid1), dim3(kThreads), smem1, st, a);
