@@ -667,46 +667,54 @@ def run_int4_decode(args, dev, mode):
     routers = torch.stack([torch.from_numpy(W.router_weights(w, l)) for l in range(L)]).to(dev)
     x_dev = torch.from_numpy(np.stack([W.activations(w, l, n_steps * T) for l in range(L)]).view(np.int16)) \
         .view(torch.bfloat16).to(dev)
-    ctx = bec.Context(L, E, k, H, w.inter, w.shared_inter, w.quant, w.slots, w.policy, 3, 0, 262144, T,
-                      admit_on_device=mode)
-    ctx.bind_store(store)
-    for l in range(L):
-        ctx.bind_shared(l, shared[l])
     plan = bec.Plan(E, k, T, dev)
     idx = torch.empty((T, k), dtype=torch.int32, device=dev)
     wt = torch.empty((T, k), dtype=torch.float32, device=dev)
     y = torch.empty((L, T, H), dtype=torch.float32, device=dev)
     x_step = torch.empty((L, T, H), dtype=torch.bfloat16, device=dev)
-    for s in range(args.warmup - 1):
-        for l in range(L):
-            ctx.layer_forward(l, x_dev[l, s * T:(s + 1) * T], routers[l], None, idx, wt, plan, y[l])
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g):
-        for l in range(L):
-            ctx.layer_forward(l, x_step[l], routers[l], None, idx, wt, plan, y[l])
-    x_step.copy_(x_dev[:, (args.warmup - 1) * T:args.warmup * T])
-    g.replay()
-    torch.cuda.synchronize(dev)
-    st0 = ctx.stats()
     stream = torch.cuda.current_stream(dev)
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for s in range(args.warmup, n_steps):
-        x_step.copy_(x_dev[:, s * T:(s + 1) * T], non_blocking=True)
+
+    def graph_run():
+        ctx = bec.Context(L, E, k, H, w.inter, w.shared_inter, w.quant, w.slots, w.policy, 3, 0, 262144, T,
+                          admit_on_device=mode)
+        ctx.bind_store(store)
+        for l in range(L):
+            ctx.bind_shared(l, shared[l])
+        for s in range(args.warmup - 1):
+            for l in range(L):
+                ctx.layer_forward(l, x_dev[l, s * T:(s + 1) * T], routers[l], None, idx, wt, plan, y[l])
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for l in range(L):
+                ctx.layer_forward(l, x_step[l], routers[l], None, idx, wt, plan, y[l])
+        x_step.copy_(x_dev[:, (args.warmup - 1) * T:args.warmup * T])
         g.replay()
-    b.record(stream)
-    torch.cuda.synchronize(dev)
-    ctx.check_device_errors()
-    st1 = ctx.stats()
-    del g
-    ctx.close()
+        torch.cuda.synchronize(dev)
+        st0 = ctx.stats()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for s in range(args.warmup, n_steps):
+            x_step.copy_(x_dev[:, s * T:(s + 1) * T], non_blocking=True)
+            g.replay()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        ctx.check_device_errors()
+        st1 = ctx.stats()
+        del g
+        ctx.close()
+        return a.elapsed_time(b) / (n_steps - args.warmup), st1["misses"] - st0["misses"]
+
+    # the same timed steps from a fresh context, repeated: the first graph
+    # pass over a freshly pinned store can run far slower than later ones
+    reps = [graph_run() for _ in range(max(1, min(3, args.repeats)))]
     steps = n_steps - args.warmup
-    ms = a.elapsed_time(b) / steps
-    misses = (st1["misses"] - st0["misses"]) / steps
+    ms = statistics.median(r[0] for r in reps)
+    misses = reps[0][1] / steps
     return {"workload": f"decode shapes (hidden {H}, {E} experts top-{k} + 1 shared, inter {w.inter}), "
                         f"affine INT4 group-64 experts, bf16, 1 token/step x {L} layers, {w.slots} slots LRU",
             "admission": {2: "read-through", 1: "staging kernel"}[mode],
             "tokens_per_s": round(T / (ms / 1e3), 2), "ms_per_step": round(ms, 4), "steps": steps,
+            "repeats_tokens_per_s": sorted(round(T / (r[0] / 1e3), 2) for r in reps),
             "misses_per_step": round(misses, 2),
             "miss_mb_per_step": round(misses * w.payload_bytes / 1e6, 2)}
 
