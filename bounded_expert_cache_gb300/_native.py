@@ -52,7 +52,7 @@ class Stats(C.Structure):
                 ("uncertified_repairs", C.c_int64), ("prefetch_loads", C.c_int64),
                 ("prefetch_useful", C.c_int64), ("prefetch_wasted", C.c_int64),
                 ("prefetch_refreshes", C.c_int64), ("prefetch_probes", C.c_int64),
-                ("prefetch_bytes", C.c_int64)]
+                ("prefetch_bytes", C.c_int64), ("route_filter_fallbacks", C.c_int64)]
 
 
 class Budget(C.Structure):

@@ -157,6 +157,7 @@ extern "C" void moe_destroy(moe_ctx_t* ctx) {
   cudaFree(ctx->d_plan_local);
   cudaFree(ctx->d_norms);
   cudaFree(ctx->d_flags);
+  cudaFree(ctx->d_wsplit);
   cudaFree(ctx->d_lpart);
   cudaFreeHost(ctx->h_units);
   cudaFreeHost(ctx->h_pt);
@@ -236,8 +237,8 @@ extern "C" moe_status_t moe_create(const moe_config_t* cfg, moe_ctx_t** out) {
   CKC(cudaMalloc(&ctx->d_keys, sizeof(unsigned long long) * 3 * te));
   CKC(cudaMalloc(&ctx->d_ticket, sizeof(unsigned int)));
   CKC(cudaMemset(ctx->d_ticket, 0, sizeof(unsigned int)));
-  CKC(cudaMalloc(&ctx->d_repairs, sizeof(unsigned long long) * L));
-  CKC(cudaMemset(ctx->d_repairs, 0, sizeof(unsigned long long) * L));
+  CKC(cudaMalloc(&ctx->d_repairs, sizeof(unsigned long long) * 2 * L));
+  CKC(cudaMemset(ctx->d_repairs, 0, sizeof(unsigned long long) * 2 * L));
   ctx->ldh = static_cast<int32_t>(round_up(std::max(c.inter, c.shared_inter), 32));
   const int tdec = std::min(c.max_tokens, 8);
   CKC(cudaMalloc(&ctx->d_h, sizeof(float) * static_cast<size_t>(tdec * c.top_k + tdec) * ctx->ldh));
@@ -278,6 +279,7 @@ extern "C" moe_status_t moe_create(const moe_config_t* cfg, moe_ctx_t** out) {
     CKC(cudaMalloc(&ctx->d_norms, sizeof(float) * (c.max_tokens + E)));
     CKC(cudaMalloc(&ctx->d_flags, sizeof(int32_t) * c.max_tokens));
     CKC(cudaMalloc(&ctx->d_lpart, sizeof(float2) * 4 * static_cast<size_t>(c.max_tokens) * E));
+    if (c.hidden % 64 == 0) CKC(cudaMalloc(&ctx->d_wsplit, moe::router_split_bytes(E, c.hidden)));
   }
   ctx->dev_admit = c.admit_on_device >= 1;
   ctx->read_through = c.admit_on_device == 2;
@@ -439,7 +441,7 @@ static moe_status_t route_impl(moe_ctx_t* ctx, int32_t layer, const void* x, int
   a.topk_w = topk_w;
   a.keys = ctx->d_keys;
   a.ticket = ctx->d_ticket;
-  a.repairs = ctx->d_repairs + layer;
+  a.repairs = ctx->d_repairs + 2 * layer;
   a.err = ctx->d_err;
   if (plan) a.plan = *plan;
   if (admit) {
@@ -469,7 +471,7 @@ static moe_status_t route_impl(moe_ctx_t* ctx, int32_t layer, const void* x, int
     // and admission run as their own launches
     a.plan = moe_plan_t{};
     a.admit.enabled = 0;
-    CK(moe::launch_route_large(a, ctx->d_norms, ctx->d_flags, ctx->d_lpart, st));
+    CK(moe::launch_route_large(a, ctx->d_norms, ctx->d_flags, ctx->d_lpart, ctx->d_wsplit, st));
   } else {
     CK(moe::launch_route(a, ctx->num_sms, st));
   }
@@ -1224,9 +1226,9 @@ extern "C" moe_status_t moe_get_stats(const moe_ctx_t* cctx, int32_t layer, moe_
   if (!ctx || !out) return MOE_ERR_ARG;
   if (layer != -1 && !valid_layer(ctx, layer)) return fail(ctx, MOE_ERR_ARG, "stats: bad layer");
   const int L = ctx->cfg.n_layers;
-  std::vector<unsigned long long> rep(L);
+  std::vector<unsigned long long> rep(2 * static_cast<size_t>(L));
   CK(cudaDeviceSynchronize());
-  CK(cudaMemcpy(rep.data(), ctx->d_repairs, sizeof(unsigned long long) * L, cudaMemcpyDeviceToHost));
+  CK(cudaMemcpy(rep.data(), ctx->d_repairs, sizeof(unsigned long long) * 2 * L, cudaMemcpyDeviceToHost));
   std::vector<long long> ds;
   if (ctx->dev_admit) {
     ds.resize(static_cast<size_t>(L) * moe::kStatCount);
@@ -1253,7 +1255,8 @@ extern "C" moe_status_t moe_get_stats(const moe_ctx_t* cctx, int32_t layer, moe_
     t.materialized_bytes += s.materialized_bytes;
     t.tiles_staged += ctx->tiles_staged[l];
     t.bytes_staged += ctx->bytes_staged[l];
-    t.uncertified_repairs += static_cast<int64_t>(rep[l]);
+    t.uncertified_repairs += static_cast<int64_t>(rep[2 * l]);
+    t.route_filter_fallbacks += static_cast<int64_t>(rep[2 * l + 1]);
     t.prefetch_loads += s.prefetch_loads;
     t.prefetch_useful += s.prefetch_useful;
     t.prefetch_wasted += s.prefetch_wasted;

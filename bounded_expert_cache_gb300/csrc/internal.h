@@ -97,7 +97,7 @@ struct RouteArgs {
   float* topk_w;
   unsigned long long* keys;  // [3][T][E] scratch: logit, lower, upper keys
   unsigned int* ticket; // last-block counter, zero between launches
-  unsigned long long* repairs;  // repaired-token counter of the layer
+  unsigned long long* repairs;  // counters of the layer: [0] repaired tokens, [1] filter fallbacks
   uint32_t* err;
   // optional fused plan (plan.counts == nullptr: none)
   moe_plan_t plan;
@@ -114,10 +114,14 @@ struct PlanArgs {
   uint32_t* err;
 };
 cudaError_t launch_plan(const PlanArgs& a, cudaStream_t st);
-// Many-token routing (any T): norms [T + E] and flags [T] are scratch.
-// Many-token router; part holds up to 4 * T * E (hi, lo) pairs of split-K
-// partials.
-cudaError_t launch_route_large(const RouteArgs& a, float* norms, int* flags, float2* part, cudaStream_t st);
+// Many-token routing (any T): norms [T + E] and flags [T] are scratch; part
+// holds up to 4 * T * E (hi, lo) pairs of split-K partials (or T * E
+// approximate logits). wsplit (router_split_bytes(E, H), or nullptr): the
+// router weights' bf16 parts, which enable the tensor-core filter for bf16
+// activations with H % 64 == 0.
+size_t router_split_bytes(int E, int H);
+cudaError_t launch_route_large(const RouteArgs& a, float* norms, int* flags, float2* part, uint16_t* wsplit,
+                               cudaStream_t st);
 // Multi-block plan for any T*k: local is scratch [plan_blocks(T*k)][E].
 int plan_blocks(int A);
 cudaError_t launch_plan_large(const PlanArgs& a, int* local, cudaStream_t st);
@@ -219,7 +223,7 @@ struct moe_ctx {
   // scratch
   unsigned long long* d_keys = nullptr;
   unsigned int* d_ticket = nullptr;
-  unsigned long long* d_repairs = nullptr;  // [L]
+  unsigned long long* d_repairs = nullptr;  // [L][2]: repaired tokens, filter fallbacks
   float* d_h = nullptr;
   int32_t ldh = 0;
   uint32_t* d_err = nullptr;
@@ -255,6 +259,7 @@ struct moe_ctx {
   int max_items0 = 0, max_items1 = 0, ldh_p = 0;
   int32_t* d_plan_local = nullptr;         // multi-block plan scratch
   float* d_norms = nullptr;                // many-token router scratch
+  uint16_t* d_wsplit = nullptr;            // bf16 parts of the router weights (H % 64 == 0)
   int32_t* d_flags = nullptr;
   float2* d_lpart = nullptr;               // split-K logit partials [4][T][E]
   std::vector<cudaStream_t> streams;

@@ -128,7 +128,9 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* yp, const int
   }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+}  // namespace
+
+static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 cudaError_t encoder() {
   if (g_encode) return cudaSuccess;
@@ -151,6 +153,8 @@ cudaError_t map16(CUtensorMap* m, const void* base, CUtensorMapDataType t, int64
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
+
+namespace {
 
 // Q8_0 quant planes in every slot: bytes x rows x matrix x slot. The box is
 // 64 bytes x box_rows x n_mat: the gate/up GEMM reads the same rows of the

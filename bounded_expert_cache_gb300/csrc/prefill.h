@@ -76,6 +76,14 @@ struct PrefillArgs {
 };
 cudaError_t prefill_ffn(const PrefillArgs& p, cudaStream_t st);
 
+// The driver's tensor-map encoder, looked up once (cudaErrorNotSupported if
+// the driver has none).
+cudaError_t encoder();
+// Tensor map of a 16-bit [rows][cols] row-major matrix (cols a multiple of
+// 8): boxes of 64 columns x box_rows rows, 128-byte swizzle.
+cudaError_t map16(CUtensorMap* m, const void* base, CUtensorMapDataType t, int64_t rows, int64_t cols,
+                  int box_rows);
+
 int gemm_stages(int phase);
 size_t gemm_smem_bytes(int phase, int stages);
 cudaError_t launch_gemm(int phase, const GemmMaps& m, const GemmArgs& a, int grid, cudaStream_t st);

@@ -22,13 +22,18 @@
 // Expert-major plan ("Nanite for Experts" §5.3 union, §5.5 merge into the
 // original positions): counts, exclusive offsets, ascending union, and a
 // stable (token-ascending) scatter of the assignments.
+#include <algorithm>
 #include <cfloat>
 #include <climits>
 #include <mutex>
 #include <string>
 
+#include <cuda_bf16.h>
+
 #include "internal.h"
 #include "pdl.cuh"
+#include "prefill.h"
+#include "tc.cuh"
 
 namespace moe {
 namespace {
@@ -1958,11 +1963,32 @@ __global__ void __launch_bounds__(kLThreads, 4) logits_tiled_kernel(RouteArgs a,
   }
 }
 
+// Keys of a logit summed in chunks of at most 32 plain-FMA products whose
+// chunk sums were folded error-free into (hi, lo): the logit
+// l = hi + lo + b in fp64 and its outward-rounded bound interval. The bound
+// is formed in fp32 with every operation rounded up (an upper bound of the
+// fp64 expression gamma_32 * 1.01 * ||x|| ||w|| + |l| (2^-51 + 2^-50) +
+// (H+1) 2^-126; ||x|| ||w|| bounds sum |x w| by Cauchy-Schwarz), so only the
+// logit and the two interval ends use fp64. A non-finite logit or bound
+// gives the widest interval.
+__device__ __forceinline__ void chunked_keys(float hi, float lo, float bf, float xn, float wn, int H,
+                                             unsigned long long& kl, unsigned long long& klo,
+                                             unsigned long long& khi) {
+  const double l = (static_cast<double>(hi) + static_cast<double>(lo)) + static_cast<double>(bf);
+  // 1.01 * gamma_32 rounded up; gamma_32 = 32u / (1 - 32u), u = 2^-24
+  const float c1 = 1.9314e-6f;
+  const float A = __fmul_ru(xn, wn);
+  const float absl = __fadd_ru(__fadd_ru(fabsf(hi), fabsf(lo)), fabsf(bf));
+  const float wid =
+      __fadd_ru(__fadd_ru(__fmul_ru(c1, A), __fmul_ru(absl, 0x1.8p-50f)), static_cast<float>(H + 1) * 0x1p-126f);
+  const bool fin = isfinite(l) && isfinite(wid);
+  kl = okey(l);
+  klo = fin ? okey(__dsub_rd(l, static_cast<double>(wid))) : 0ull;
+  khi = fin ? okey(__dadd_ru(l, static_cast<double>(wid))) : ~0ull;
+}
+
 // Folds the slices' (hi, lo) pairs in slice order and writes the logit keys
-// and the outward-rounded bound keys (one thread per token and expert). The
-// bound is formed in fp32 with every operation rounded up (an upper bound
-// of the fp64 expression gamma_32 * 1.01 * |x||w| + |l| (2^-51 + 2^-50) +
-// (H+1) 2^-126), so only the logit and the two interval ends use fp64.
+// and the outward-rounded bound keys (one thread per token and expert).
 __global__ void __launch_bounds__(256) logits_keys_kernel(RouteArgs a, const float2* part, int slices,
                                                           const float* xn, const float* wn) {
   const size_t te = static_cast<size_t>(a.T) * a.E;
@@ -1979,22 +2005,19 @@ __global__ void __launch_bounds__(256) logits_keys_kernel(RouteArgs a, const flo
     lo = __fadd_rn(__fadd_rn(lo, v.y), es);
   }
   const float bf = a.bias ? a.bias[e] : 0.f;
-  const double l = (static_cast<double>(hi) + static_cast<double>(lo)) + static_cast<double>(bf);
-  // 1.01 * gamma_32 rounded up; gamma_32 = 32u / (1 - 32u), u = 2^-24
-  const float c1 = 1.9314e-6f;
-  const float A = __fmul_ru(__ldg(xn + t), __ldg(wn + e));
-  const float absl = __fadd_ru(__fadd_ru(fabsf(hi), fabsf(lo)), fabsf(bf));
-  const float wid =
-      __fadd_ru(__fadd_ru(__fmul_ru(c1, A), __fmul_ru(absl, 0x1.8p-50f)), static_cast<float>(a.H + 1) * 0x1p-126f);
-  const bool fin = isfinite(l) && isfinite(wid);
-  a.keys[o] = okey(l);
-  a.keys[te + o] = fin ? okey(__dsub_rd(l, static_cast<double>(wid))) : 0ull;
-  a.keys[2 * te + o] = fin ? okey(__dadd_ru(l, static_cast<double>(wid))) : ~0ull;
+  unsigned long long kl, klo, khi;
+  chunked_keys(hi, lo, bf, __ldg(xn + t), __ldg(wn + e), a.H, kl, klo, khi);
+  a.keys[o] = kl;
+  a.keys[te + o] = klo;
+  a.keys[2 * te + o] = khi;
 }
 
-__global__ void __launch_bounds__(256) select_kernel(RouteArgs a, int* flags) {
+// Per-token selection and certification from the keys (one warp per
+// token). gated: only the tokens the refining kernel left with flag 2.
+__global__ void __launch_bounds__(256) select_kernel(RouteArgs a, int* flags, int gated) {
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (t >= a.T) return;
+  if (gated && flags[t] != 2) return;
   const size_t te = static_cast<size_t>(a.T) * a.E, o = static_cast<size_t>(t) * a.E;
   const TokenKeys K{a.keys + o, a.keys + te + o, a.keys + 2 * te + o};
   int sel[16];
@@ -2013,60 +2036,698 @@ __global__ void __launch_bounds__(256) select_kernel(RouteArgs a, int* flags) {
 // recomputed exactly (its three keys collapse to the exact logit's). Every
 // other expert is either certainly outside the top k or certainly ordered
 // against each candidate, so selecting by the logit keys afterwards yields
-// the ranking of the exact logits, ties to the lower expert id.
+// the ranking of the exact logits, ties to the lower expert id. Each block
+// reads the flags of 32 tokens at once and repairs the flagged ones.
+constexpr int kRepairGrid = 512;  // blocks at most (32 tokens each per pass)
 template <int XT>
 __global__ void __launch_bounds__(kRouteThreads) repair_kernel(RouteArgs a, const int* flags) {
   __shared__ unsigned long long s_lo[1024], s_hi[1024];
   __shared__ unsigned char s_cand[1024];
   __shared__ int s_amb[1024];
   __shared__ int s_namb;
-  const int t = blockIdx.x;
-  if (t >= a.T || __ldg(flags + t) == 0) return;
+  __shared__ unsigned s_mask;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int E = a.E, H = a.H, k = a.k;
-  const size_t te = static_cast<size_t>(a.T) * E, o = static_cast<size_t>(t) * E;
-  for (int e = tid; e < E; e += kRouteThreads) {
-    s_lo[e] = __ldcg(a.keys + te + o + e);
-    s_hi[e] = __ldcg(a.keys + 2 * te + o + e);
-  }
-  if (tid == 0) s_namb = 0;
-  __syncthreads();
-  for (int e = tid; e < E; e += kRouteThreads) {
-    const unsigned long long h = s_hi[e];
-    int above = 0;
-    for (int j = 0; j < E; ++j) above += s_lo[j] > h ? 1 : 0;
-    s_cand[e] = above < k ? 1 : 0;
-  }
-  __syncthreads();
-  for (int e = tid; e < E; e += kRouteThreads) {
-    if (!s_cand[e]) continue;
-    const unsigned long long l = s_lo[e], h = s_hi[e];
-    bool meets = false;
-    for (int j = 0; j < E && !meets; ++j)
-      meets = j != e && s_cand[j] && !(l > s_hi[j] || s_lo[j] > h);
-    if (meets) s_amb[atomicAdd(&s_namb, 1)] = e;
-  }
-  __syncthreads();
-  const int namb = s_namb;
-  for (int i = warp; i < namb; i += kRouteWarps) {
-    const int ee = s_amb[i];
-    double v;
-    const bool fin = warp_exact_logit<XT>(a.x, static_cast<size_t>(t) * H, a.w + static_cast<size_t>(ee) * H,
-                                          H, a.bias, ee, v);
-    if (lane == 0) {
-      if (!fin) atomicOr(a.err, MOE_DEVERR_NONFINITE);
-      a.keys[o + ee] = a.keys[te + o + ee] = a.keys[2 * te + o + ee] = okey(v);
+  for (int base = blockIdx.x * 32; base < a.T; base += gridDim.x * 32) {
+    if (warp == 0) {
+      const unsigned m = __ballot_sync(0xffffffffu, base + lane < a.T && flags[base + lane] != 0);
+      if (lane == 0) s_mask = m;
+    }
+    __syncthreads();
+    unsigned mask = s_mask;
+    __syncthreads();
+    while (mask) {
+      const int t = base + __ffs(mask) - 1;
+      mask &= mask - 1;
+      const size_t te = static_cast<size_t>(a.T) * E, o = static_cast<size_t>(t) * E;
+      for (int e = tid; e < E; e += kRouteThreads) {
+        s_lo[e] = __ldcg(a.keys + te + o + e);
+        s_hi[e] = __ldcg(a.keys + 2 * te + o + e);
+      }
+      if (tid == 0) s_namb = 0;
+      __syncthreads();
+      for (int e = tid; e < E; e += kRouteThreads) {
+        const unsigned long long h = s_hi[e];
+        int above = 0;
+        for (int j = 0; j < E; ++j) above += s_lo[j] > h ? 1 : 0;
+        s_cand[e] = above < k ? 1 : 0;
+      }
+      __syncthreads();
+      for (int e = tid; e < E; e += kRouteThreads) {
+        if (!s_cand[e]) continue;
+        const unsigned long long l = s_lo[e], h = s_hi[e];
+        bool meets = false;
+        for (int j = 0; j < E && !meets; ++j)
+          meets = j != e && s_cand[j] && !(l > s_hi[j] || s_lo[j] > h);
+        if (meets) s_amb[atomicAdd(&s_namb, 1)] = e;
+      }
+      __syncthreads();
+      const int namb = s_namb;
+      for (int i = warp; i < namb; i += kRouteWarps) {
+        const int ee = s_amb[i];
+        double v;
+        const bool fin = warp_exact_logit<XT>(a.x, static_cast<size_t>(t) * H, a.w + static_cast<size_t>(ee) * H,
+                                              H, a.bias, ee, v);
+        if (lane == 0) {
+          if (!fin) atomicOr(a.err, MOE_DEVERR_NONFINITE);
+          a.keys[o + ee] = a.keys[te + o + ee] = a.keys[2 * te + o + ee] = okey(v);
+        }
+      }
+      __syncthreads();
+      if (warp == 0) {
+        const TokenKeys K{a.keys + o, a.keys + te + o, a.keys + 2 * te + o};
+        int sel[16];
+        unsigned long long selk[16];
+        warp_select(K, E, k, sel, selk, false);
+        warp_write_selection(sel, selk, k, a.topk_idx + static_cast<size_t>(t) * k,
+                             a.topk_w + static_cast<size_t>(t) * k);
+        if (lane == 0) atomicAdd(a.repairs, 1ull);
+      }
+      __syncthreads();
     }
   }
+}
+
+// ---- many-token logits on the tensor cores, as a filter
+// The router weights are split into two bf16 parts, w = hi + mid + r with
+// hi = bf16(w) and mid = bf16(w - hi), both rounded to nearest (w - hi is
+// exact in fp32, |r| <= 2^-16 |w|). One tcgen05 GEMM per 128-token x
+// 64-expert tile computes G = x hi^T and M = x mid^T (bf16 operands, so every
+// product is exact; fp32 accumulators in TMEM) and writes L = G + M. The
+// tensor cores' accumulation order and rounding are not specified, so L only
+// excludes experts, under a deliberately loose error model:
+//   |L - x.w| <= 2^-9 ||x|| ||w|| + 2^-22 |L| + 2^-124 sqrt(H) ||w|| + (2H+2) 2^-126,
+// i.e. an accumulation error of at most 2^-10 of the summed magnitudes (64
+// times the error of an fp32 accumulation that truncates after every
+// 16-product step at H = 2048), the split residual 2^-16, the fp32 sum
+// G + M, and flushed subnormal operands and products. An expert whose upper
+// bound lies below the k-th largest lower bound cannot be among the top k
+// (at least k experts are certainly above it, ties included). The others,
+// the candidates (about ten of 256 on the prefill workload), get certified
+// logits on the CUDA cores: first summed in chunks of 32 products (the same
+// keys as the CUDA-core path), and for a token they leave uncertified once
+// more as compensated dot products (error-free products and sums; Ogita,
+// Rump and Oishi 2005), whose bound is some five orders of magnitude
+// tighter. Each candidate's certified logit is also checked against its
+// filter interval; a token whose check fails, or whose filter is not
+// finite, takes every expert as a candidate. A token still uncertified gets
+// full keys (non-candidates a key below every logit) and goes through the
+// per-token selection and the exact repair.
+constexpr int kTcTok = 128;  // tokens per CTA (MMA M)
+constexpr int kTcExp = 64;   // experts per CTA; MMA N = 128: their hi rows, then their mid rows
+constexpr int kTcBK = 64;    // K per stage: 128 bytes of bf16 per row
+constexpr int kTcStages = 6;
+constexpr uint32_t kTcABytes = kTcTok * kTcBK * 2;      // 16 KiB of tokens
+constexpr uint32_t kTcBBytes = 2 * kTcExp * kTcBK * 2;  // 16 KiB of weight parts
+constexpr uint32_t kTcStage = kTcABytes + kTcBBytes;
+constexpr size_t kTcSmem = static_cast<size_t>(kTcStages) * kTcStage + 1024;
+constexpr long long kTcWaitCycles = 4000000000ll;  // about 2 s at the SM clock
+static_assert(kTcABytes % 1024 == 0 && kTcStage % 1024 == 0, "stage alignment");
+
+// ws: bf16 [ceil(E/64)][2][64][H]: block b holds the hi rows of experts
+// 64b .. 64b+63, then their mid rows; rows of experts >= E are zero.
+__global__ void __launch_bounds__(256) router_split_kernel(const float* w, int E, int H, uint16_t* ws) {
+  const int nb = (E + kTcExp - 1) / kTcExp;
+  const int64_t q = H / 4;
+  const int64_t total = static_cast<int64_t>(nb) * kTcExp * q;
+  for (int64_t i = blockIdx.x * 256ll + threadIdx.x; i < total; i += static_cast<int64_t>(gridDim.x) * 256) {
+    const int e = static_cast<int>(i / q);
+    const int c = static_cast<int>(i % q) * 4;
+    const float4 v = e < E ? __ldg(reinterpret_cast<const float4*>(w + static_cast<int64_t>(e) * H + c))
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float f[4] = {v.x, v.y, v.z, v.w};
+    uint32_t hb[2], mb[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const __nv_bfloat16 h0 = __float2bfloat16_rn(f[2 * j]), h1 = __float2bfloat16_rn(f[2 * j + 1]);
+      const __nv_bfloat16 m0 = __float2bfloat16_rn(f[2 * j] - __bfloat162float(h0));
+      const __nv_bfloat16 m1 = __float2bfloat16_rn(f[2 * j + 1] - __bfloat162float(h1));
+      hb[j] = static_cast<uint32_t>(__bfloat16_as_ushort(h0)) | (static_cast<uint32_t>(__bfloat16_as_ushort(h1)) << 16);
+      mb[j] = static_cast<uint32_t>(__bfloat16_as_ushort(m0)) | (static_cast<uint32_t>(__bfloat16_as_ushort(m1)) << 16);
+    }
+    const int b = e / kTcExp, r = e % kTcExp;
+    *reinterpret_cast<uint2*>(ws + (static_cast<int64_t>(2 * b) * kTcExp + r) * H + c) = make_uint2(hb[0], hb[1]);
+    *reinterpret_cast<uint2*>(ws + (static_cast<int64_t>(2 * b + 1) * kTcExp + r) * H + c) = make_uint2(mb[0], mb[1]);
+  }
+}
+
+struct TcArgs {
+  int T, E, H;
+  float* out;  // [T][E] approximate logits
+  uint32_t* err;
+  long long wait_cycles;
+};
+
+// D (TMEM) += A (shared-memory descriptor) * B (shared-memory descriptor)
+__device__ __forceinline__ void umma_ss(uint32_t dt, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{ .reg .pred p; setp.ne.b32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(dt),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+
+// One 128-token x 64-expert tile per CTA of 4 warps: lane 0 of warp 0 issues
+// the TMA copies (token rows and the hi + mid rows, 64 K per stage, 128-byte
+// swizzle), lane 0 of warp 1 the MMAs (M 128, N 128, K 16; A and B from
+// shared memory); then every warp reads its 32 TMEM lanes (tokens) and
+// writes G + M. Every wait is bounded: past the limit the CTA's abort flag
+// and the timeout bit are set, copies and MMAs in flight are drained, and no
+// logit is written.
+__global__ void __launch_bounds__(128, 1) logits_tc_kernel(const __grid_constant__ CUtensorMap map_x,
+                                                           const __grid_constant__ CUtensorMap map_w, TcArgs a) {
+  using namespace tc;
+  extern __shared__ unsigned char smraw[];
+  unsigned char* sm =
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
+  __shared__ uint64_t bar_full[kTcStages], bar_free[kTcStages], bar_acc, bar_drain;
+  __shared__ uint32_t tmem_holder;
+  __shared__ int s_abort;
+  volatile int* abort_flag = &s_abort;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t sbase = su32(sm);
+  const int t0 = blockIdx.x * kTcTok, eb = blockIdx.y;
+  const int nkb = a.H / kTcBK;
+  if (tid == 0) {
+    s_abort = 0;
+    for (int s = 0; s < kTcStages; ++s) {
+      mbar_init(su32(&bar_full[s]), 1);
+      mbar_init(su32(&bar_free[s]), 1);
+    }
+    mbar_init(su32(&bar_acc), 1);
+    mbar_init(su32(&bar_drain), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(&tmem_holder)),
+                 "r"(2 * kTcExp));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;");
   __syncthreads();
-  if (warp == 0) {
-    const TokenKeys K{a.keys + o, a.keys + te + o, a.keys + 2 * te + o};
-    int sel[16];
-    unsigned long long selk[16];
-    warp_select(K, E, k, sel, selk, false);
-    warp_write_selection(sel, selk, k, a.topk_idx + static_cast<size_t>(t) * k,
-                         a.topk_w + static_cast<size_t>(t) * k);
-    if (lane == 0) atomicAdd(a.repairs, 1ull);
+  asm volatile("tcgen05.fence::after_thread_sync;");
+  const uint32_t tmem = tmem_holder;
+
+  if (warp == 0 && lane == 0) {
+    uint32_t ring = 0;
+    RingPos rp;
+    for (int kb = 0; kb < nkb; ++kb, ++ring, rp.next(kTcStages)) {
+      if (ring >= static_cast<uint32_t>(kTcStages) &&
+          !mbar_wait(su32(&bar_free[rp.s]), rp.ph ^ 1u, abort_flag, a.err, a.wait_cycles))
+        break;
+      const uint32_t st = sbase + static_cast<uint32_t>(rp.s) * kTcStage, fb = su32(&bar_full[rp.s]);
+      mbar_expect_tx(fb, kTcStage);
+      tma2d(st, &map_x, fb, kb * kTcBK, t0);
+      tma2d(st + kTcABytes, &map_w, fb, kb * kTcBK, eb * 2 * kTcExp);
+    }
+    // drain: the last copies into each stage complete before exit
+    const uint32_t n = ring < static_cast<uint32_t>(kTcStages) ? ring : static_cast<uint32_t>(kTcStages);
+    for (uint32_t j = 0; j < n; ++j) {
+      const uint32_t r = ring - 1 - j;
+      mbar_drain(su32(&bar_full[r % kTcStages]), (r / kTcStages) & 1u, a.err, a.wait_cycles);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // kind::f16, bf16 A and B (K-major), fp32 D, N = 128, M = 128
+    const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((static_cast<uint32_t>(2 * kTcExp) >> 3) << 17) |
+                           ((static_cast<uint32_t>(kTcTok) >> 4) << 24);
+    RingPos rp;
+    bool ok = true;
+    for (int kb = 0; kb < nkb; ++kb, rp.next(kTcStages)) {
+      if (!(ok = mbar_wait(su32(&bar_full[rp.s]), rp.ph, abort_flag, a.err, a.wait_cycles))) break;
+      asm volatile("tcgen05.fence::after_thread_sync;");
+      const uint32_t st = sbase + static_cast<uint32_t>(rp.s) * kTcStage;
+      const uint64_t ad = sdesc(st), bd = sdesc(st + kTcABytes);
+#pragma unroll
+      for (int k = 0; k < kTcBK / 16; ++k)
+        umma_ss(tmem, ad + 2 * k, bd + 2 * k, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+      umma_commit(su32(&bar_free[rp.s]));
+    }
+    if (ok) umma_commit(su32(&bar_acc));
+    // drain: every MMA issued here has completed before TMEM is released
+    umma_commit(su32(&bar_drain));
+    mbar_drain(su32(&bar_drain), 0, a.err, a.wait_cycles);
+  }
+  __syncwarp();
+  // epilogue: warp w holds TMEM lanes 32w .. 32w+31, the tile's tokens
+  // t0 + 32w + lane; columns 0..63 G, 64..127 M
+  const bool ready = __all_sync(0xffffffffu, mbar_wait(su32(&bar_acc), 0, abort_flag, a.err, a.wait_cycles));
+  if (ready) {
+    asm volatile("tcgen05.fence::after_thread_sync;");
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const int t = t0 + warp * 32 + lane;
+#pragma unroll 1
+    for (int half = 0; half < 2; ++half) {
+      uint32_t g[32], m[32];
+      tmem_ld32(tmem + lane_base + half * 32, g);
+      tmem_ld32(tmem + lane_base + kTcExp + half * 32, m);
+      const int e0 = eb * kTcExp + half * 32;
+      if (t < a.T && e0 < a.E) {
+        float* dst = a.out + static_cast<int64_t>(t) * a.E + e0;
+        if (e0 + 32 <= a.E && (a.E & 3) == 0) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            reinterpret_cast<float4*>(dst)[j] = make_float4(
+                __uint_as_float(g[4 * j]) + __uint_as_float(m[4 * j]),
+                __uint_as_float(g[4 * j + 1]) + __uint_as_float(m[4 * j + 1]),
+                __uint_as_float(g[4 * j + 2]) + __uint_as_float(m[4 * j + 2]),
+                __uint_as_float(g[4 * j + 3]) + __uint_as_float(m[4 * j + 3]));
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (e0 + j < a.E) dst[j] = __uint_as_float(g[j]) + __uint_as_float(m[j]);
+        }
+      }
+    }
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;");
+  if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * kTcExp));
+}
+
+// Order-preserving key of a non-NaN float (-0 first made +0 by the caller).
+__device__ __forceinline__ uint32_t fkey(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Logit of token row xr (bf16) and weight row wr by the warp, summed in
+// chunks of at most 32 plain-FMA products per lane, each chunk sum folded
+// error-free into (hi, lo), the lanes combined by error-free sums (every
+// lane returns the same pair). The keys come from chunked_keys.
+__device__ void warp_dot_chunked(const uint16_t* xr, const float* wr, int H, float& hi, float& lo) {
+  const int lane = threadIdx.x & 31;
+  hi = 0.f;
+  lo = 0.f;
+  float p = 0.f;
+  int n = 0;
+  for (int g = lane; g < (H >> 2); g += 32) {
+    const float4 w4 = __ldg(reinterpret_cast<const float4*>(wr) + g);
+    const uint2 xb = __ldg(reinterpret_cast<const uint2*>(xr) + g);
+    p = fmaf(__uint_as_float(xb.x << 16), w4.x, p);
+    p = fmaf(__uint_as_float(xb.x & 0xFFFF0000u), w4.y, p);
+    p = fmaf(__uint_as_float(xb.y << 16), w4.z, p);
+    p = fmaf(__uint_as_float(xb.y & 0xFFFF0000u), w4.w, p);
+    if (++n == 8) {  // 32 products
+      float ns, es;
+      two_sum(hi, p, ns, es);
+      hi = ns;
+      lo = __fadd_rn(lo, es);
+      p = 0.f;
+      n = 0;
+    }
+  }
+  {
+    float ns, es;
+    two_sum(hi, p, ns, es);
+    hi = ns;
+    lo = __fadd_rn(lo, es);
+  }
+#pragma unroll
+  for (int off = 16; off; off >>= 1) {
+    const float h2 = __shfl_xor_sync(0xffffffffu, hi, off);
+    const float l2 = __shfl_xor_sync(0xffffffffu, lo, off);
+    float ns, es;
+    two_sum(hi, h2, ns, es);
+    hi = ns;
+    lo = __fadd_rn(__fadd_rn(lo, l2), es);
+  }
+}
+
+// Compensated logit (error-free products by FMA, error-free sums, an fp32
+// error accumulator) of token row xr (bf16) and weight row wr by the warp,
+// with the sum of |x w| for its bound; every lane returns the same values.
+// Keys as the few-token router's: |exact - (S + C)| <= (D u)^2 (1 + 2 D u)
+// sum |x w|, D = terms per lane + the lanes' reduction depth + 5.
+__device__ void warp_dot_compensated(const uint16_t* xr, const float* wr, int H, float bf,
+                                     unsigned long long& kl, unsigned long long& klo, unsigned long long& khi) {
+  const int lane = threadIdx.x & 31;
+  float s = 0.f, c = 0.f, ab = 0.f;
+  for (int g = lane; g < (H >> 2); g += 32) {
+    const float4 w4 = __ldg(reinterpret_cast<const float4*>(wr) + g);
+    const uint2 xb = __ldg(reinterpret_cast<const uint2*>(xr) + g);
+    const float xv[4] = {__uint_as_float(xb.x << 16), __uint_as_float(xb.x & 0xFFFF0000u),
+                         __uint_as_float(xb.y << 16), __uint_as_float(xb.y & 0xFFFF0000u)};
+    const float wv[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float pr = __fmul_rn(xv[j], wv[j]);
+      const float ep = fmaf(xv[j], wv[j], -pr);  // exact low part of the product
+      float ns, es;
+      two_sum(s, pr, ns, es);
+      s = ns;
+      c = __fadd_rn(c, __fadd_rn(ep, es));
+      ab = fmaf(fabsf(xv[j]), fabsf(wv[j]), ab);
+    }
+  }
+#pragma unroll
+  for (int off = 16; off; off >>= 1) {
+    const float s2 = __shfl_xor_sync(0xffffffffu, s, off);
+    const float c2 = __shfl_xor_sync(0xffffffffu, c, off);
+    const float a2 = __shfl_xor_sync(0xffffffffu, ab, off);
+    float ns, es;
+    two_sum(s, s2, ns, es);
+    s = ns;
+    c = __fadd_rn(__fadd_rn(c, c2), es);
+    ab = __fadd_rn(ab, a2);
+  }
+  const int nterm = 4 * (((H >> 2) + 31) / 32);
+  const double l = (static_cast<double>(s) + static_cast<double>(c)) + static_cast<double>(bf);
+  const double Du = static_cast<double>(nterm + 5 + 5) * 0x1p-24;
+  const double bnd = Du * Du * (1.0 + 2.0 * Du) * 1.01 * static_cast<double>(ab) + fabs(l) * 0x1p-51 +
+                     static_cast<double>(H + 1) * 0x1p-140;
+  const double wid = __dadd_ru(bnd, __dmul_ru(fabs(l), 0x1p-50));
+  const bool fin = isfinite(l) && isfinite(wid);
+  kl = okey(l);
+  klo = fin ? okey(__dsub_rd(l, wid)) : 0ull;
+  khi = fin ? okey(__dadd_ru(l, wid)) : ~0ull;
+}
+
+// Top-k of the candidates held one per lane (lane j < C: expert my_e, keys
+// my_l, my_lo, my_hi) by descending logit key, ties to the lower id. Lane
+// r < k ends with selection r (sel_e, sel_k). Returns whether the bound
+// intervals of consecutive selections, and of the k-th against every other
+// candidate, are disjoint (the other experts are excluded by the filter).
+__device__ bool cand_select(int C, int k, int my_e, unsigned long long my_l, unsigned long long my_lo,
+                            unsigned long long my_hi, int& sel_e, unsigned long long& sel_k) {
+  const int lane = threadIdx.x & 31;
+  const bool has = lane < C;
+  bool taken = false;
+  unsigned long long r_lo = 0ull, r_hi = 0ull;
+  for (int r = 0; r < k; ++r) {
+    unsigned long long key;
+    const int mi = warp_round(has && !taken, my_l, my_e, key);
+    const unsigned ow = __ballot_sync(0xffffffffu, has && !taken && my_e == mi);
+    const int owner = __ffs(ow) - 1;
+    const unsigned long long lo_o = __shfl_sync(0xffffffffu, my_lo, owner & 31);
+    const unsigned long long hi_o = __shfl_sync(0xffffffffu, my_hi, owner & 31);
+    if (lane == owner) taken = true;
+    if (lane == r) {
+      sel_e = mi;
+      sel_k = key;
+      r_lo = lo_o;
+      r_hi = hi_o;
+    }
+  }
+  const bool rest = has && !taken;
+  const uint32_t rh = __reduce_max_sync(0xffffffffu, rest ? static_cast<uint32_t>(my_hi >> 32) : 0u);
+  const uint32_t rl = __reduce_max_sync(
+      0xffffffffu, rest && static_cast<uint32_t>(my_hi >> 32) == rh ? static_cast<uint32_t>(my_hi) : 0u);
+  const bool any_rest = __any_sync(0xffffffffu, rest);
+  const unsigned long long restmax = (static_cast<unsigned long long>(rh) << 32) | rl;
+  const unsigned long long next_hi = __shfl_down_sync(0xffffffffu, r_hi, 1);
+  bool ok = true;
+  if (lane + 1 < k) ok = r_lo > next_hi;
+  if (lane == k - 1 && any_rest) ok = r_lo > restmax;
+  return __all_sync(0xffffffffu, ok);
+}
+
+constexpr int kRfWarps = 8;
+
+// Filter interval of expert e for token t: the approximate logit v plus the
+// bias, widened by the error model above, rounded outward (-0 made +0).
+__device__ __forceinline__ void filter_bounds(float v, float b, float xnt, float wne, float rs, float c0,
+                                              float& lv, float& uv) {
+  const float d = __fadd_ru(__fadd_ru(__fmul_ru(0x1p-9f, __fmul_ru(xnt, wne)), __fmul_ru(0x1p-22f, fabsf(v))),
+                            __fmaf_ru(rs, wne, c0));
+  lv = __fadd_rn(__fsub_rd(__fadd_rd(v, b), d), 0.f);
+  uv = __fadd_rn(__fadd_ru(__fadd_ru(v, b), d), 0.f);
+}
+
+// One chunk of a lane's share of a logit: groups g0 + 32 m (m < 8) of four
+// products each, 32 products; groups past the row are zero.
+struct RfChunk {
+  float4 w[8];
+  uint2 x[8];
+};
+__device__ __forceinline__ void rf_load(RfChunk& c, const uint16_t* xr, const float* wr, int g0, int ng) {
+#pragma unroll
+  for (int m = 0; m < 8; ++m) {
+    const int g = g0 + 32 * m;
+    if (g < ng) {
+      c.w[m] = __ldg(reinterpret_cast<const float4*>(wr) + g);
+      c.x[m] = __ldg(reinterpret_cast<const uint2*>(xr) + g);
+    } else {
+      c.w[m] = make_float4(0.f, 0.f, 0.f, 0.f);
+      c.x[m] = make_uint2(0u, 0u);
+    }
+  }
+}
+// The chunk's 32 products as four independent sums of eight (one per
+// component of the groups), combined error-free: chunk sum s plus the
+// error e of the combination.
+__device__ __forceinline__ void rf_dot(const RfChunk& c, float& s, float& e) {
+  float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
+#pragma unroll
+  for (int m = 0; m < 8; ++m) {
+    p0 = fmaf(__uint_as_float(c.x[m].x << 16), c.w[m].x, p0);
+    p1 = fmaf(__uint_as_float(c.x[m].x & 0xFFFF0000u), c.w[m].y, p1);
+    p2 = fmaf(__uint_as_float(c.x[m].y << 16), c.w[m].z, p2);
+    p3 = fmaf(__uint_as_float(c.x[m].y & 0xFFFF0000u), c.w[m].w, p3);
+  }
+  float s01, e01, s23, e23, e2;
+  two_sum(p0, p1, s01, e01);
+  two_sum(p2, p3, s23, e23);
+  two_sum(s01, s23, s, e2);
+  e = __fadd_rn(__fadd_rn(e01, e23), e2);
+}
+
+// Chunked logits of the warp's C <= 32 candidates cand[0..C) against token
+// row xr, as one stream of (candidate, chunk) steps with the loads of two
+// steps in flight. Each lane's chunk of 32 products is four plain-FMA sums
+// of eight; their combination and the fold of every chunk into (hi, lo) are
+// error-free, and the lanes are combined error-free, so the chunk error
+// stays within gamma_8 <= gamma_32 of its magnitudes and chunked_keys
+// applies. Lane j ends with candidate j's (hi, lo).
+__device__ void rf_candidate_logits(const RouteArgs& a, const uint16_t* xr, const int* cand, int C, float& my_hi,
+                                    float& my_lo) {
+  const int lane = threadIdx.x & 31;
+  const int H = a.H, ng = H >> 2;
+  const int nch = (((ng + 31) >> 5) + 7) >> 3;  // chunks per logit
+  const int S = C * nch;
+  RfChunk A, B;
+  auto load = [&](RfChunk& c, int s) {
+    const int j = s / nch, ch = s - j * nch;
+    rf_load(c, xr, a.w + static_cast<size_t>(cand[j]) * H, lane + 256 * ch, ng);
+  };
+  float hi = 0.f, lo = 0.f;
+  auto step = [&](const RfChunk& c, int s) {
+    float cs, ce, ns, es;
+    rf_dot(c, cs, ce);
+    two_sum(hi, cs, ns, es);
+    hi = ns;
+    lo = __fadd_rn(lo, __fadd_rn(ce, es));
+    const int j = s / nch;
+    if (s - j * nch == nch - 1) {  // the candidate's last chunk: combine the lanes
+#pragma unroll
+      for (int off = 16; off; off >>= 1) {
+        const float h2 = __shfl_xor_sync(0xffffffffu, hi, off);
+        const float l2 = __shfl_xor_sync(0xffffffffu, lo, off);
+        two_sum(hi, h2, ns, es);
+        hi = ns;
+        lo = __fadd_rn(__fadd_rn(lo, l2), es);
+      }
+      if (lane == j) {
+        my_hi = hi;
+        my_lo = lo;
+      }
+      hi = 0.f;
+      lo = 0.f;
+    }
+  };
+  if (S > 0) load(A, 0);
+  if (S > 1) load(B, 1);
+  for (int s = 0; s < S; s += 2) {
+    step(A, s);
+    if (s + 2 < S) load(A, s + 2);
+    if (s + 1 < S) {
+      step(B, s + 1);
+      if (s + 3 < S) load(B, s + 3);
+    }
+  }
+}
+
+// One warp per token: the filter over the approximate logits, certified
+// logits of the candidates, selection and combine weights; or, for a token
+// left uncertified, full keys and flag 2 for select_kernel and repair_kernel.
+template <int NPL>
+__global__ void __launch_bounds__(kRfWarps * 32, 2) refine_kernel(RouteArgs a, const float* approx, const float* xn,
+                                                                  const float* wn, int* flags) {
+  __shared__ float s_wn[1024], s_b[1024];
+  __shared__ int s_cand[kRfWarps][32];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int E = a.E, H = a.H, k = a.k;
+  for (int e = tid; e < E; e += kRfWarps * 32) {
+    s_wn[e] = __ldg(wn + e);
+    s_b[e] = a.bias ? __ldg(a.bias + e) : 0.f;
+  }
+  __syncthreads();
+  const int t = blockIdx.x * kRfWarps + warp;
+  if (t >= a.T) return;
+  const float xnt = __ldg(xn + t);
+  const float rs = __fmul_ru(0x1p-124f, __fsqrt_ru(static_cast<float>(H)));
+  const float c0 = static_cast<float>(2 * H + 2) * 0x1p-126f;
+  const float* ar = approx + static_cast<size_t>(t) * E;
+  const uint16_t* xr = static_cast<const uint16_t*>(a.x) + static_cast<size_t>(t) * H;
+  const size_t te = static_cast<size_t>(a.T) * E, o = static_cast<size_t>(t) * E;
+  const unsigned lt = (1u << lane) - 1u;
+  int* cand = s_cand[warp];
+  // the k-th largest lower bound (with multiplicity) and the candidates in
+  // expert order: upper bound >= it (every expert if a bound is not finite
+  // or, on the second pass, if the filter's model failed)
+  uint32_t thr = 0u;
+  uint32_t cmask = 0u;  // bit i: expert i * 32 + lane is a candidate
+  bool all;
+  {
+    uint32_t lk[NPL], uk[NPL];
+    bool bad = !isfinite(xnt);
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) {
+      const int e = i * 32 + lane;
+      lk[i] = uk[i] = 0u;  // below every finite bound
+      if (e < E) {
+        float lv, uv;
+        filter_bounds(__ldg(ar + e), s_b[e], xnt, s_wn[e], rs, c0, lv, uv);
+        bad |= !(isfinite(lv) && isfinite(uv));
+        lk[i] = fkey(lv);
+        uk[i] = fkey(uv);
+      }
+    }
+    all = __any_sync(0xffffffffu, bad);
+    if (!all) {
+      uint32_t taken = 0u;
+      for (int r = 0; r < k; ++r) {
+        uint32_t best = 0u;
+        int bi = -1;
+#pragma unroll
+        for (int i = 0; i < NPL; ++i)
+          if (i * 32 + lane < E && !((taken >> i) & 1u) && (bi < 0 || lk[i] > best)) {
+            best = lk[i];
+            bi = i;
+          }
+        const uint32_t m = __reduce_max_sync(0xffffffffu, bi >= 0 ? best : 0u);
+        const unsigned own = __ballot_sync(0xffffffffu, bi >= 0 && best == m);
+        if (lane == __ffs(own) - 1) taken |= 1u << bi;
+        thr = m;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < NPL; ++i)
+      if (i * 32 + lane < E && (all || uk[i] >= thr)) cmask |= 1u << i;
+  }
+  for (int pass = 0; pass < 2; ++pass) {
+    int C = 0;
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) {
+      const bool c = (cmask >> i) & 1u;
+      const unsigned bal = __ballot_sync(0xffffffffu, c);
+      if (c && C + __popc(bal & lt) < 32) cand[C + __popc(bal & lt)] = i * 32 + lane;
+      C += __popc(bal);
+    }
+    __syncwarp();
+    if (C <= 32) {
+      int my_e = lane < C ? cand[lane] : -1;
+      unsigned long long my_l = 0ull, my_lo = 0ull, my_hi = 0ull;
+      {
+        float ch = 0.f, cl = 0.f;
+        rf_candidate_logits(a, xr, cand, C, ch, cl);
+        if (lane < C) chunked_keys(ch, cl, s_b[my_e], xnt, s_wn[my_e], H, my_l, my_lo, my_hi);
+      }
+      // the certified interval must meet the filter interval (the model of
+      // the tensor cores' error, checked on every candidate)
+      bool consistent = true;
+      if (!all && lane < C) {
+        float lv, uv;
+        filter_bounds(__ldg(ar + my_e), s_b[my_e], xnt, s_wn[my_e], rs, c0, lv, uv);
+        consistent = !(okey_value(my_hi) < static_cast<double>(lv) || okey_value(my_lo) > static_cast<double>(uv));
+      }
+      if (__all_sync(0xffffffffu, consistent)) {
+        int sel_e = -1;
+        unsigned long long sel_k = 0ull;
+        bool ok = cand_select(C, k, my_e, my_l, my_lo, my_hi, sel_e, sel_k);
+        if (!ok) {
+          // the compensated logits, some five orders of magnitude tighter
+          for (int j = 0; j < C; ++j) {
+            const int e = cand[j];
+            unsigned long long kl, klo, khi;
+            warp_dot_compensated(xr, a.w + static_cast<size_t>(e) * H, H, s_b[e], kl, klo, khi);
+            if (lane == j) {
+              my_l = kl;
+              my_lo = klo;
+              my_hi = khi;
+            }
+          }
+          ok = cand_select(C, k, my_e, my_l, my_lo, my_hi, sel_e, sel_k);
+        }
+        if (ok) {
+          const unsigned long long k0 = __shfl_sync(0xffffffffu, sel_k, 0);
+          float z = 0.f;
+          if (lane < k) z = expf(static_cast<float>(okey_value(sel_k) - okey_value(k0)));
+          float sum = 0.f;
+          for (int j = 0; j < k; ++j) sum += __shfl_sync(0xffffffffu, z, j);  // fixed order
+          if (lane < k) {
+            a.topk_idx[static_cast<size_t>(t) * k + lane] = sel_e;
+            a.topk_w[static_cast<size_t>(t) * k + lane] = z / sum;
+          }
+          if (lane == 0) flags[t] = 0;
+          return;
+        }
+        // full keys: the candidates' (lane j holds the j-th), a key below
+        // every logit for the others
+        int base = 0;
+#pragma unroll
+        for (int i = 0; i < NPL; ++i) {
+          const int e = i * 32 + lane;
+          const bool c = (cmask >> i) & 1u;
+          const unsigned bal = __ballot_sync(0xffffffffu, c);
+          const int src = (base + __popc(bal & lt)) & 31;
+          const unsigned long long vl = __shfl_sync(0xffffffffu, my_l, src);
+          const unsigned long long vlo = __shfl_sync(0xffffffffu, my_lo, src);
+          const unsigned long long vhi = __shfl_sync(0xffffffffu, my_hi, src);
+          if (e < E) {
+            a.keys[o + e] = c ? vl : 1ull;
+            a.keys[te + o + e] = c ? vlo : 1ull;
+            a.keys[2 * te + o + e] = c ? vhi : 1ull;
+          }
+          base += __popc(bal);
+        }
+        if (lane == 0) flags[t] = 2;
+        return;
+      }
+      // the filter's model failed for this token: every expert
+      if (lane == 0) atomicAdd(a.repairs + 1, 1ull);
+      all = true;
+      cmask = 0u;
+#pragma unroll
+      for (int i = 0; i < NPL; ++i)
+        if (i * 32 + lane < E) cmask |= 1u << i;
+      __syncwarp();
+      continue;
+    }
+    // more than 32 candidates: every candidate's chunked keys, written by
+    // lane 0 in turn, the others a key below every logit
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) {
+      const int e = i * 32 + lane;
+      if (e < E && !((cmask >> i) & 1u)) a.keys[o + e] = a.keys[te + o + e] = a.keys[2 * te + o + e] = 1ull;
+    }
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) {
+      unsigned bal = __ballot_sync(0xffffffffu, (cmask >> i) & 1u);
+      while (bal) {
+        const int e = i * 32 + __ffs(bal) - 1;
+        bal &= bal - 1;
+        float hi, lo;
+        warp_dot_chunked(xr, a.w + static_cast<size_t>(e) * H, H, hi, lo);
+        if (lane == 0) {
+          unsigned long long kl, klo, khi;
+          chunked_keys(hi, lo, s_b[e], xnt, s_wn[e], H, kl, klo, khi);
+          a.keys[o + e] = kl;
+          a.keys[te + o + e] = klo;
+          a.keys[2 * te + o + e] = khi;
+        }
+      }
+    }
+    if (lane == 0) flags[t] = 2;
+    return;
   }
 }
 
@@ -2183,7 +2844,12 @@ __global__ void admit_kernel(AdmitArgs A, moe_plan_t P, uint32_t* err) {
 
 }  // namespace
 
-cudaError_t launch_route_large(const RouteArgs& a, float* norms, int* flags, float2* part, cudaStream_t st) {
+size_t router_split_bytes(int E, int H) {
+  return static_cast<size_t>((E + kTcExp - 1) / kTcExp) * 2 * kTcExp * static_cast<size_t>(H) * 2;
+}
+
+cudaError_t launch_route_large(const RouteArgs& a, float* norms, int* flags, float2* part, uint16_t* wsplit,
+                               cudaStream_t st) {
   if (a.T < 1 || a.k > 16 || a.E > 1024 || a.H % kLK) return cudaErrorInvalidValue;
   const int slices = a.H % (kLK * 4) == 0 ? 4 : (a.H % (kLK * 2) == 0 ? 2 : 1);
   float* xn = norms;
@@ -2193,17 +2859,51 @@ cudaError_t launch_route_large(const RouteArgs& a, float* norms, int* flags, flo
     row_norms_kernel<MOE_BF16><<<(nrows + 7) / 8, 256, 0, st>>>(a.x, a.T, a.w, a.E, a.H, xn, wn);
   else
     row_norms_kernel<MOE_F32><<<(nrows + 7) / 8, 256, 0, st>>>(a.x, a.T, a.w, a.E, a.H, xn, wn);
+  if (wsplit && a.xt == MOE_BF16 && a.H % kTcBK == 0 && encoder() == cudaSuccess) {
+    // tensor-core filter, certified logits of the candidates, then the
+    // per-token selection and exact repair of the tokens it left
+    const int nb = (a.E + kTcExp - 1) / kTcExp;
+    const int64_t n4 = static_cast<int64_t>(nb) * kTcExp * (a.H / 4);
+    const int gs = static_cast<int>(std::min<int64_t>((n4 + 255) / 256, 4096));
+    router_split_kernel<<<gs, 256, 0, st>>>(a.w, a.E, a.H, wsplit);
+    CUtensorMap mx, mw;
+    cudaError_t e = map16(&mx, a.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.T, a.H, kTcTok);
+    if (e != cudaSuccess) return e;
+    e = map16(&mw, wsplit, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<int64_t>(nb) * 2 * kTcExp, a.H, 2 * kTcExp);
+    if (e != cudaSuccess) return e;
+    float* approx = reinterpret_cast<float*>(part);
+    const TcArgs ta{a.T, a.E, a.H, approx, a.err, kTcWaitCycles};
+    e = cudaFuncSetAttribute(logits_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kTcSmem));
+    if (e != cudaSuccess) return e;
+    logits_tc_kernel<<<dim3((a.T + kTcTok - 1) / kTcTok, nb), 128, kTcSmem, st>>>(mx, mw, ta);
+    const int rg = (a.T + kRfWarps - 1) / kRfWarps;
+    if (a.E <= 32)
+      refine_kernel<1><<<rg, kRfWarps * 32, 0, st>>>(a, approx, xn, wn, flags);
+    else if (a.E <= 64)
+      refine_kernel<2><<<rg, kRfWarps * 32, 0, st>>>(a, approx, xn, wn, flags);
+    else if (a.E <= 128)
+      refine_kernel<4><<<rg, kRfWarps * 32, 0, st>>>(a, approx, xn, wn, flags);
+    else if (a.E <= 256)
+      refine_kernel<8><<<rg, kRfWarps * 32, 0, st>>>(a, approx, xn, wn, flags);
+    else if (a.E <= 512)
+      refine_kernel<16><<<rg, kRfWarps * 32, 0, st>>>(a, approx, xn, wn, flags);
+    else
+      refine_kernel<32><<<rg, kRfWarps * 32, 0, st>>>(a, approx, xn, wn, flags);
+    select_kernel<<<(a.T + 7) / 8, 256, 0, st>>>(a, flags, 1);
+    repair_kernel<MOE_BF16><<<std::min((a.T + 31) / 32, kRepairGrid), kRouteThreads, 0, st>>>(a, flags);
+    return cudaGetLastError();
+  }
   dim3 grid((a.E + kLE - 1) / kLE, (a.T + kLT - 1) / kLT, slices);
   if (a.xt == MOE_BF16)
     logits_tiled_kernel<MOE_BF16><<<grid, kLThreads, 0, st>>>(a, part);
   else
     logits_tiled_kernel<MOE_F32><<<grid, kLThreads, 0, st>>>(a, part);
   logits_keys_kernel<<<dim3((a.E + 255) / 256, a.T), 256, 0, st>>>(a, part, slices, xn, wn);
-  select_kernel<<<(a.T + 7) / 8, 256, 0, st>>>(a, flags);
+  select_kernel<<<(a.T + 7) / 8, 256, 0, st>>>(a, flags, 0);
   if (a.xt == MOE_BF16)
-    repair_kernel<MOE_BF16><<<a.T, kRouteThreads, 0, st>>>(a, flags);
+    repair_kernel<MOE_BF16><<<std::min((a.T + 31) / 32, kRepairGrid), kRouteThreads, 0, st>>>(a, flags);
   else
-    repair_kernel<MOE_F32><<<a.T, kRouteThreads, 0, st>>>(a, flags);
+    repair_kernel<MOE_F32><<<std::min((a.T + 31) / 32, kRepairGrid), kRouteThreads, 0, st>>>(a, flags);
   return cudaGetLastError();
 }
 

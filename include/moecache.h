@@ -150,6 +150,11 @@ typedef struct {
   int64_t prefetch_refreshes;  /* resident predictions touched like a hit */
   int64_t prefetch_probes;     /* resident predictions recorded, state unchanged */
   int64_t prefetch_bytes;      /* loads x payload */
+  /* Many-token routing with the tensor-core filter: tokens whose certified
+   * logit of a candidate fell outside the filter's interval, so that every
+   * expert was taken as a candidate (the filter's error model failed; 0 is
+   * expected, and the routing stays exact either way). */
+  int64_t route_filter_fallbacks;
 } moe_stats_t;
 
 /* Prefetch modes ([RT] §3.3): an absent predicted expert is loaded in both;

@@ -46,6 +46,42 @@ def test_route_many_tokens(bec, name, T):
     ridx, rw, _ = oracle.route(x_to_f64(w, x), Wr, bias, w.top_k)
     assert np.array_equal(idx.cpu().numpy(), ridx)
     assert np.allclose(wt.cpu().numpy(), rw, rtol=1e-5, atol=1e-7)
+    # the tensor-core filter's error model held for every candidate
+    assert ctx.stats()["route_filter_fallbacks"] == 0
+    ctx.close()
+
+
+@pytest.mark.parametrize("E,k", [(16, 2), (64, 4), (256, 8), (1024, 16)])
+def test_route_many_tokens_filter_ties_and_degenerate_tokens(bec, E, k):
+    # bf16 tokens with H % 64 == 0 take the tensor-core filter: exact ties
+    # (duplicated router rows and equal biases), an all-zero token (every
+    # logit equal: every expert a candidate), a token of one large value, and
+    # T = 150 (a ragged 128-token tile) must route as the oracle does, ties to
+    # the lower expert id
+    T = 150
+    w = W.with_changes(W.WORKLOADS["tiny"], x_dtype="bf16", hidden=256, n_experts=E, top_k=k,
+                       tokens_per_step=T, n_steps=1, slots=E)
+    ctx = make_context(bec, w, 1, max_tokens=T)
+    Wr = W.router_weights(w, 0)
+    for (a, b) in ((E - 1, 0), (E // 2, E // 2 + 1), (3, 1)):
+        Wr[a] = Wr[b]
+    x = W.activations(w, 0, T)
+    x[7] = 0                       # bf16 zero
+    x[9] = 0
+    x[9, 17] = 0x4480              # 1024.0
+    bias = (np.arange(E) % 4 == 0).astype(np.float32) * np.float32(0.5)
+    for b in (None, bias):
+        idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
+        wt = torch.empty((T, k), dtype=torch.float32, device="cuda")
+        ctx.route(0, x_to_torch(w, x), torch.from_numpy(Wr).cuda(),
+                  None if b is None else torch.from_numpy(b).cuda(), idx, wt)
+        ctx.check_device_errors()
+        ridx, rw, _ = oracle.route(x_to_f64(w, x), Wr, b, k)
+        assert np.array_equal(idx.cpu().numpy(), ridx)
+        assert np.allclose(wt.cpu().numpy(), rw, rtol=1e-5, atol=1e-7)
+        assert idx[7].tolist() == (list(range(k)) if b is None else [e for e in range(E) if e % 4 == 0][:k])
+    assert ctx.stats()["uncertified_repairs"] >= 2
+    assert ctx.stats()["route_filter_fallbacks"] == 0
     ctx.close()
 
 
@@ -147,6 +183,7 @@ def test_prefill_full_chunk_4096_every_expert(bec):
     ridx, rw = oracle_route_rows(x64, Wr, bias, k, range(T))
     assert np.array_equal(idx.cpu().numpy(), ridx)
     assert np.allclose(wt.cpu().numpy(), rw, rtol=1e-5, atol=1e-7)
+    assert ctx.stats()["route_filter_fallbacks"] == 0
     rplan = oracle.plan_union(ridx, rw, E)
     nu = int(plan.n_uniq.item())
     assert plan.uniq[:nu].cpu().numpy().tolist() == rplan["uniq"].tolist()
