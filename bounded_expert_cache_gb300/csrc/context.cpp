@@ -471,7 +471,7 @@ static moe_status_t route_impl(moe_ctx_t* ctx, int32_t layer, const void* x, int
     // and admission run as their own launches
     a.plan = moe_plan_t{};
     a.admit.enabled = 0;
-    CK(moe::launch_route_large(a, ctx->d_norms, ctx->d_flags, ctx->d_lpart, ctx->d_wsplit, st));
+    CK(moe::launch_route_large(a, ctx->d_norms, ctx->d_flags, ctx->d_lpart, ctx->d_wsplit, ctx->num_sms, st));
   } else {
     CK(moe::launch_route(a, ctx->num_sms, st));
   }

@@ -121,7 +121,7 @@ cudaError_t launch_plan(const PlanArgs& a, cudaStream_t st);
 // activations with H % 64 == 0.
 size_t router_split_bytes(int E, int H);
 cudaError_t launch_route_large(const RouteArgs& a, float* norms, int* flags, float2* part, uint16_t* wsplit,
-                               cudaStream_t st);
+                               int num_sms, cudaStream_t st);
 // Multi-block plan for any T*k: local is scratch [plan_blocks(T*k)][E].
 int plan_blocks(int A);
 cudaError_t launch_plan_large(const PlanArgs& a, int* local, cudaStream_t st);

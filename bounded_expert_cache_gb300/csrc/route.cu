@@ -2145,14 +2145,19 @@ constexpr long long kTcWaitCycles = 4000000000ll;  // about 2 s at the SM clock
 static_assert(kTcABytes % 1024 == 0 && kTcStage % 1024 == 0, "stage alignment");
 
 // ws: bf16 [ceil(E/64)][2][64][H]: block b holds the hi rows of experts
-// 64b .. 64b+63, then their mid rows; rows of experts >= E are zero.
-__global__ void __launch_bounds__(256) router_split_kernel(const float* w, int E, int H, uint16_t* ws) {
+// 64b .. 64b+63, then their mid rows; rows of experts >= E are zero. One
+// warp per row; it also writes the row's norm bound wn[e] = 1.001 *
+// sqrt(sum w^2) in fp32 (the fp32 sum of squares is within a relative
+// 1e-3 of the exact one), infinite if not finite.
+__global__ void __launch_bounds__(256) router_split_kernel(const float* w, int E, int H, uint16_t* ws, float* wn) {
+  const int e = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   const int nb = (E + kTcExp - 1) / kTcExp;
-  const int64_t q = H / 4;
-  const int64_t total = static_cast<int64_t>(nb) * kTcExp * q;
-  for (int64_t i = blockIdx.x * 256ll + threadIdx.x; i < total; i += static_cast<int64_t>(gridDim.x) * 256) {
-    const int e = static_cast<int>(i / q);
-    const int c = static_cast<int>(i % q) * 4;
+  if (e >= nb * kTcExp) return;
+  const int b = e / kTcExp, r = e % kTcExp;
+  uint16_t* hrow = ws + (static_cast<int64_t>(2 * b) * kTcExp + r) * H;
+  uint16_t* mrow = ws + (static_cast<int64_t>(2 * b + 1) * kTcExp + r) * H;
+  float s = 0.f;
+  for (int c = lane * 4; c < H; c += 128) {
     const float4 v = e < E ? __ldg(reinterpret_cast<const float4*>(w + static_cast<int64_t>(e) * H + c))
                            : make_float4(0.f, 0.f, 0.f, 0.f);
     const float f[4] = {v.x, v.y, v.z, v.w};
@@ -2165,10 +2170,14 @@ __global__ void __launch_bounds__(256) router_split_kernel(const float* w, int E
       hb[j] = static_cast<uint32_t>(__bfloat16_as_ushort(h0)) | (static_cast<uint32_t>(__bfloat16_as_ushort(h1)) << 16);
       mb[j] = static_cast<uint32_t>(__bfloat16_as_ushort(m0)) | (static_cast<uint32_t>(__bfloat16_as_ushort(m1)) << 16);
     }
-    const int b = e / kTcExp, r = e % kTcExp;
-    *reinterpret_cast<uint2*>(ws + (static_cast<int64_t>(2 * b) * kTcExp + r) * H + c) = make_uint2(hb[0], hb[1]);
-    *reinterpret_cast<uint2*>(ws + (static_cast<int64_t>(2 * b + 1) * kTcExp + r) * H + c) = make_uint2(mb[0], mb[1]);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) s = fmaf(f[j], f[j], s);
+    *reinterpret_cast<uint2*>(hrow + c) = make_uint2(hb[0], hb[1]);
+    *reinterpret_cast<uint2*>(mrow + c) = make_uint2(mb[0], mb[1]);
   }
+  for (int off = 16; off; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+  const float nrm = sqrtf(s) * 1.001f;
+  if (lane == 0 && e < E) wn[e] = isfinite(nrm) ? nrm : INFINITY;
 }
 
 struct TcArgs {
@@ -2352,55 +2361,6 @@ __device__ void warp_dot_chunked(const uint16_t* xr, const float* wr, int H, flo
   }
 }
 
-// Compensated logit (error-free products by FMA, error-free sums, an fp32
-// error accumulator) of token row xr (bf16) and weight row wr by the warp,
-// with the sum of |x w| for its bound; every lane returns the same values.
-// Keys as the few-token router's: |exact - (S + C)| <= (D u)^2 (1 + 2 D u)
-// sum |x w|, D = terms per lane + the lanes' reduction depth + 5.
-__device__ void warp_dot_compensated(const uint16_t* xr, const float* wr, int H, float bf,
-                                     unsigned long long& kl, unsigned long long& klo, unsigned long long& khi) {
-  const int lane = threadIdx.x & 31;
-  float s = 0.f, c = 0.f, ab = 0.f;
-  for (int g = lane; g < (H >> 2); g += 32) {
-    const float4 w4 = __ldg(reinterpret_cast<const float4*>(wr) + g);
-    const uint2 xb = __ldg(reinterpret_cast<const uint2*>(xr) + g);
-    const float xv[4] = {__uint_as_float(xb.x << 16), __uint_as_float(xb.x & 0xFFFF0000u),
-                         __uint_as_float(xb.y << 16), __uint_as_float(xb.y & 0xFFFF0000u)};
-    const float wv[4] = {w4.x, w4.y, w4.z, w4.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float pr = __fmul_rn(xv[j], wv[j]);
-      const float ep = fmaf(xv[j], wv[j], -pr);  // exact low part of the product
-      float ns, es;
-      two_sum(s, pr, ns, es);
-      s = ns;
-      c = __fadd_rn(c, __fadd_rn(ep, es));
-      ab = fmaf(fabsf(xv[j]), fabsf(wv[j]), ab);
-    }
-  }
-#pragma unroll
-  for (int off = 16; off; off >>= 1) {
-    const float s2 = __shfl_xor_sync(0xffffffffu, s, off);
-    const float c2 = __shfl_xor_sync(0xffffffffu, c, off);
-    const float a2 = __shfl_xor_sync(0xffffffffu, ab, off);
-    float ns, es;
-    two_sum(s, s2, ns, es);
-    s = ns;
-    c = __fadd_rn(__fadd_rn(c, c2), es);
-    ab = __fadd_rn(ab, a2);
-  }
-  const int nterm = 4 * (((H >> 2) + 31) / 32);
-  const double l = (static_cast<double>(s) + static_cast<double>(c)) + static_cast<double>(bf);
-  const double Du = static_cast<double>(nterm + 5 + 5) * 0x1p-24;
-  const double bnd = Du * Du * (1.0 + 2.0 * Du) * 1.01 * static_cast<double>(ab) + fabs(l) * 0x1p-51 +
-                     static_cast<double>(H + 1) * 0x1p-140;
-  const double wid = __dadd_ru(bnd, __dmul_ru(fabs(l), 0x1p-50));
-  const bool fin = isfinite(l) && isfinite(wid);
-  kl = okey(l);
-  klo = fin ? okey(__dsub_rd(l, wid)) : 0ull;
-  khi = fin ? okey(__dadd_ru(l, wid)) : ~0ull;
-}
-
 // Top-k of the candidates held one per lane (lane j < C: expert my_e, keys
 // my_l, my_lo, my_hi) by descending logit key, ties to the lower id. Lane
 // r < k ends with selection r (sel_e, sel_k). Returns whether the bound
@@ -2452,71 +2412,68 @@ __device__ __forceinline__ void filter_bounds(float v, float b, float xnt, float
   uv = __fadd_rn(__fadd_ru(__fadd_ru(v, b), d), 0.f);
 }
 
-// One chunk of a lane's share of a logit: groups g0 + 32 m (m < 8) of four
-// products each, 32 products; groups past the row are zero.
+// One chunk of a lane's share of a logit: the weights of groups g0 + 32 m
+// (m < 8) of four products each, 32 products; groups past the row are zero.
 struct RfChunk {
   float4 w[8];
-  uint2 x[8];
 };
-__device__ __forceinline__ void rf_load(RfChunk& c, const uint16_t* xr, const float* wr, int g0, int ng) {
+__device__ __forceinline__ void rf_load(RfChunk& c, const float* wr, int g0, int ng) {
 #pragma unroll
   for (int m = 0; m < 8; ++m) {
     const int g = g0 + 32 * m;
-    if (g < ng) {
-      c.w[m] = __ldg(reinterpret_cast<const float4*>(wr) + g);
-      c.x[m] = __ldg(reinterpret_cast<const uint2*>(xr) + g);
-    } else {
-      c.w[m] = make_float4(0.f, 0.f, 0.f, 0.f);
-      c.x[m] = make_uint2(0u, 0u);
-    }
+    c.w[m] = g < ng ? __ldg(reinterpret_cast<const float4*>(wr) + g) : make_float4(0.f, 0.f, 0.f, 0.f);
   }
 }
-// The chunk's 32 products as four independent sums of eight (one per
-// component of the groups), combined error-free: chunk sum s plus the
-// error e of the combination.
-__device__ __forceinline__ void rf_dot(const RfChunk& c, float& s, float& e) {
-  float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
+// The chunk's 32 products (activations xs: the token row in fp32, zero past
+// the row) as four independent sums of eight (one per component of the
+// groups), combined error-free: chunk sum s plus the error e of the
+// combination.
+__device__ __forceinline__ void rf_dot(const RfChunk& c, const float* xs, int g0, float& s, float& e) {
+  float2 p01 = make_float2(0.f, 0.f), p23 = make_float2(0.f, 0.f);  // paired FMAs, each lane of a pair rounded alone
 #pragma unroll
   for (int m = 0; m < 8; ++m) {
-    p0 = fmaf(__uint_as_float(c.x[m].x << 16), c.w[m].x, p0);
-    p1 = fmaf(__uint_as_float(c.x[m].x & 0xFFFF0000u), c.w[m].y, p1);
-    p2 = fmaf(__uint_as_float(c.x[m].y << 16), c.w[m].z, p2);
-    p3 = fmaf(__uint_as_float(c.x[m].y & 0xFFFF0000u), c.w[m].w, p3);
+    const float4 x4 = reinterpret_cast<const float4*>(xs)[g0 + 32 * m];
+    p01 = __ffma2_rn(make_float2(x4.x, x4.y), make_float2(c.w[m].x, c.w[m].y), p01);
+    p23 = __ffma2_rn(make_float2(x4.z, x4.w), make_float2(c.w[m].z, c.w[m].w), p23);
   }
   float s01, e01, s23, e23, e2;
-  two_sum(p0, p1, s01, e01);
-  two_sum(p2, p3, s23, e23);
+  two_sum(p01.x, p01.y, s01, e01);
+  two_sum(p23.x, p23.y, s23, e23);
   two_sum(s01, s23, s, e2);
   e = __fadd_rn(__fadd_rn(e01, e23), e2);
 }
 
-// Chunked logits of the warp's C <= 32 candidates cand[0..C) against token
-// row xr, as one stream of (candidate, chunk) steps with the loads of two
-// steps in flight. Each lane's chunk of 32 products is four plain-FMA sums
+// Chunked logits of the warp's C <= 32 candidates cand[0..C) against the
+// token row xs (fp32, shared memory), as one stream of (candidate, chunk)
+// steps with the weight loads of two steps in flight. Each lane's chunk of 32 products is four plain-FMA sums
 // of eight; their combination and the fold of every chunk into (hi, lo) are
 // error-free, and the lanes are combined error-free, so the chunk error
 // stays within gamma_8 <= gamma_32 of its magnitudes and chunked_keys
 // applies. Lane j ends with candidate j's (hi, lo).
-__device__ void rf_candidate_logits(const RouteArgs& a, const uint16_t* xr, const int* cand, int C, float& my_hi,
+__device__ void rf_candidate_logits(const RouteArgs& a, const float* xs, const int* cand, int C, float& my_hi,
                                     float& my_lo) {
   const int lane = threadIdx.x & 31;
   const int H = a.H, ng = H >> 2;
   const int nch = (((ng + 31) >> 5) + 7) >> 3;  // chunks per logit
   const int S = C * nch;
   RfChunk A, B;
-  auto load = [&](RfChunk& c, int s) {
-    const int j = s / nch, ch = s - j * nch;
-    rf_load(c, xr, a.w + static_cast<size_t>(cand[j]) * H, lane + 256 * ch, ng);
+  int lj = 0, lc = 0;  // (candidate, chunk) of the next load
+  auto load = [&](RfChunk& c) {
+    rf_load(c, a.w + static_cast<size_t>(cand[lj]) * H, lane + 256 * lc, ng);
+    if (++lc == nch) {
+      lc = 0;
+      ++lj;
+    }
   };
   float hi = 0.f, lo = 0.f;
-  auto step = [&](const RfChunk& c, int s) {
+  int sj = 0, sc = 0;  // (candidate, chunk) of the next step
+  auto step = [&](const RfChunk& c) {
     float cs, ce, ns, es;
-    rf_dot(c, cs, ce);
+    rf_dot(c, xs, lane + 256 * sc, cs, ce);
     two_sum(hi, cs, ns, es);
     hi = ns;
     lo = __fadd_rn(lo, __fadd_rn(ce, es));
-    const int j = s / nch;
-    if (s - j * nch == nch - 1) {  // the candidate's last chunk: combine the lanes
+    if (++sc == nch) {  // the candidate's last chunk: combine the lanes
 #pragma unroll
       for (int off = 16; off; off >>= 1) {
         const float h2 = __shfl_xor_sync(0xffffffffu, hi, off);
@@ -2525,23 +2482,123 @@ __device__ void rf_candidate_logits(const RouteArgs& a, const uint16_t* xr, cons
         hi = ns;
         lo = __fadd_rn(__fadd_rn(lo, l2), es);
       }
-      if (lane == j) {
+      if (lane == sj) {
         my_hi = hi;
         my_lo = lo;
       }
       hi = 0.f;
       lo = 0.f;
+      sc = 0;
+      ++sj;
     }
   };
-  if (S > 0) load(A, 0);
-  if (S > 1) load(B, 1);
+  if (S > 0) load(A);
+  if (S > 1) load(B);
   for (int s = 0; s < S; s += 2) {
-    step(A, s);
-    if (s + 2 < S) load(A, s + 2);
+    step(A);
+    if (s + 2 < S) load(A);
     if (s + 1 < S) {
-      step(B, s + 1);
-      if (s + 3 < S) load(B, s + 3);
+      step(B);
+      if (s + 3 < S) load(B);
     }
+  }
+}
+
+// Compensated logits (error-free products by FMA, error-free sums, fp32
+// error accumulators; Ogita, Rump and Oishi 2005) of the warp's C <= 32
+// candidates against the token row xs (fp32, shared memory), streamed as
+// rf_candidate_logits streams the chunked ones. Each lane keeps four such
+// sums (one per component of the groups), combined error-free per
+// candidate, then the lanes. Keys as the few-token router's:
+// |exact - (S + C)| <= (D u)^2 (1 + 2 D u) sum |x w| with D = terms per lane
+// + 10, above the summation depth. Lane j ends with candidate j's keys.
+__device__ void rf_candidate_compensated(const RouteArgs& a, const float* xs, const int* cand, int C,
+                                         const float* s_b, unsigned long long& my_l, unsigned long long& my_lo,
+                                         unsigned long long& my_hi) {
+  const int lane = threadIdx.x & 31;
+  const int H = a.H, ng = H >> 2;
+  const int nch = (((ng + 31) >> 5) + 7) >> 3;
+  const int S = C * nch;
+  RfChunk A, B;
+  int lj = 0, lc = 0;
+  auto load = [&](RfChunk& c) {
+    rf_load(c, a.w + static_cast<size_t>(cand[lj]) * H, lane + 256 * lc, ng);
+    if (++lc == nch) {
+      lc = 0;
+      ++lj;
+    }
+  };
+  float s[4] = {0.f, 0.f, 0.f, 0.f}, c[4] = {0.f, 0.f, 0.f, 0.f}, ab[4] = {0.f, 0.f, 0.f, 0.f};
+  float rs = 0.f, rc = 0.f, rab = 0.f;  // lane j: candidate j's sums
+  int sj = 0, sc = 0;
+  auto step = [&](const RfChunk& ch) {
+    const int g0 = lane + 256 * sc;
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      const float4 x4 = reinterpret_cast<const float4*>(xs)[g0 + 32 * m];
+      const float xv[4] = {x4.x, x4.y, x4.z, x4.w};
+      const float wv[4] = {ch.w[m].x, ch.w[m].y, ch.w[m].z, ch.w[m].w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float pr = __fmul_rn(xv[q], wv[q]);
+        const float ep = fmaf(xv[q], wv[q], -pr);  // exact low part of the product
+        float ns, es;
+        two_sum(s[q], pr, ns, es);
+        s[q] = ns;
+        c[q] = __fadd_rn(c[q], __fadd_rn(ep, es));
+        ab[q] = fmaf(fabsf(xv[q]), fabsf(wv[q]), ab[q]);
+      }
+    }
+    if (++sc == nch) {
+      float ss, es, s01, s23, e01, e23;
+      two_sum(s[0], s[1], s01, e01);
+      two_sum(s[2], s[3], s23, e23);
+      two_sum(s01, s23, ss, es);
+      float cc = __fadd_rn(__fadd_rn(__fadd_rn(c[0], c[1]), __fadd_rn(c[2], c[3])), __fadd_rn(__fadd_rn(e01, e23), es));
+      float aa = __fadd_rn(__fadd_rn(ab[0], ab[1]), __fadd_rn(ab[2], ab[3]));
+#pragma unroll
+      for (int off = 16; off; off >>= 1) {
+        const float s2 = __shfl_xor_sync(0xffffffffu, ss, off);
+        const float c2 = __shfl_xor_sync(0xffffffffu, cc, off);
+        const float a2 = __shfl_xor_sync(0xffffffffu, aa, off);
+        float ns, e2;
+        two_sum(ss, s2, ns, e2);
+        ss = ns;
+        cc = __fadd_rn(__fadd_rn(cc, c2), e2);
+        aa = __fadd_rn(aa, a2);
+      }
+      if (lane == sj) {
+        rs = ss;
+        rc = cc;
+        rab = aa;
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) s[q] = c[q] = ab[q] = 0.f;
+      sc = 0;
+      ++sj;
+    }
+  };
+  if (S > 0) load(A);
+  if (S > 1) load(B);
+  for (int st = 0; st < S; st += 2) {
+    step(A);
+    if (st + 2 < S) load(A);
+    if (st + 1 < S) {
+      step(B);
+      if (st + 3 < S) load(B);
+    }
+  }
+  if (lane < C) {
+    const int nterm = 4 * (((H >> 2) + 31) / 32);
+    const double l = (static_cast<double>(rs) + static_cast<double>(rc)) + static_cast<double>(s_b[cand[lane]]);
+    const double Du = static_cast<double>(nterm + 5 + 5) * 0x1p-24;
+    const double bnd = Du * Du * (1.0 + 2.0 * Du) * 1.01 * static_cast<double>(rab) + fabs(l) * 0x1p-51 +
+                       static_cast<double>(H + 1) * 0x1p-140;
+    const double wid = __dadd_ru(bnd, __dmul_ru(fabs(l), 0x1p-50));
+    const bool fin = isfinite(l) && isfinite(wid);
+    my_l = okey(l);
+    my_lo = fin ? okey(__dsub_rd(l, wid)) : 0ull;
+    my_hi = fin ? okey(__dadd_ru(l, wid)) : ~0ull;
   }
 }
 
@@ -2549,27 +2606,16 @@ __device__ void rf_candidate_logits(const RouteArgs& a, const uint16_t* xr, cons
 // logits of the candidates, selection and combine weights; or, for a token
 // left uncertified, full keys and flag 2 for select_kernel and repair_kernel.
 template <int NPL>
-__global__ void __launch_bounds__(kRfWarps * 32, 2) refine_kernel(RouteArgs a, const float* approx, const float* xn,
-                                                                  const float* wn, int* flags) {
-  __shared__ float s_wn[1024], s_b[1024];
-  __shared__ int s_cand[kRfWarps][32];
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+__device__ void refine_token(const RouteArgs& a, int t, const float* approx, float xnt, int* flags,
+                             const float* s_wn, const float* s_b, int* cand, float* xs) {
+  const int lane = threadIdx.x & 31;
   const int E = a.E, H = a.H, k = a.k;
-  for (int e = tid; e < E; e += kRfWarps * 32) {
-    s_wn[e] = __ldg(wn + e);
-    s_b[e] = a.bias ? __ldg(a.bias + e) : 0.f;
-  }
-  __syncthreads();
-  const int t = blockIdx.x * kRfWarps + warp;
-  if (t >= a.T) return;
-  const float xnt = __ldg(xn + t);
   const float rs = __fmul_ru(0x1p-124f, __fsqrt_ru(static_cast<float>(H)));
   const float c0 = static_cast<float>(2 * H + 2) * 0x1p-126f;
   const float* ar = approx + static_cast<size_t>(t) * E;
   const uint16_t* xr = static_cast<const uint16_t*>(a.x) + static_cast<size_t>(t) * H;
   const size_t te = static_cast<size_t>(a.T) * E, o = static_cast<size_t>(t) * E;
   const unsigned lt = (1u << lane) - 1u;
-  int* cand = s_cand[warp];
   // the k-th largest lower bound (with multiplicity) and the candidates in
   // expert order: upper bound >= it (every expert if a bound is not finite
   // or, on the second pass, if the filter's model failed)
@@ -2593,19 +2639,28 @@ __global__ void __launch_bounds__(kRfWarps * 32, 2) refine_kernel(RouteArgs a, c
     }
     all = __any_sync(0xffffffffu, bad);
     if (!all) {
-      uint32_t taken = 0u;
-      for (int r = 0; r < k; ++r) {
-        uint32_t best = 0u;
-        int bi = -1;
+      // each lane sorts its keys (descending; absent experts are 0, below
+      // every bound); each round the lowest lane holding the largest head
+      // pops it
+      uint32_t sk[NPL];
 #pragma unroll
-        for (int i = 0; i < NPL; ++i)
-          if (i * 32 + lane < E && !((taken >> i) & 1u) && (bi < 0 || lk[i] > best)) {
-            best = lk[i];
-            bi = i;
-          }
-        const uint32_t m = __reduce_max_sync(0xffffffffu, bi >= 0 ? best : 0u);
-        const unsigned own = __ballot_sync(0xffffffffu, bi >= 0 && best == m);
-        if (lane == __ffs(own) - 1) taken |= 1u << bi;
+      for (int i = 0; i < NPL; ++i) sk[i] = lk[i];
+#pragma unroll
+      for (int p = 0; p < NPL; ++p)
+#pragma unroll
+        for (int i = p & 1; i + 1 < NPL; i += 2) {
+          const uint32_t hi2 = max(sk[i], sk[i + 1]), lo2 = min(sk[i], sk[i + 1]);
+          sk[i] = hi2;
+          sk[i + 1] = lo2;
+        }
+      for (int r = 0; r < k; ++r) {
+        const uint32_t m = __reduce_max_sync(0xffffffffu, sk[0]);
+        const unsigned own = __ballot_sync(0xffffffffu, sk[0] == m);
+        if (lane == __ffs(own) - 1) {
+#pragma unroll
+          for (int i = 0; i + 1 < NPL; ++i) sk[i] = sk[i + 1];
+          sk[NPL - 1] = 0u;
+        }
         thr = m;
       }
     }
@@ -2628,7 +2683,7 @@ __global__ void __launch_bounds__(kRfWarps * 32, 2) refine_kernel(RouteArgs a, c
       unsigned long long my_l = 0ull, my_lo = 0ull, my_hi = 0ull;
       {
         float ch = 0.f, cl = 0.f;
-        rf_candidate_logits(a, xr, cand, C, ch, cl);
+        rf_candidate_logits(a, xs, cand, C, ch, cl);
         if (lane < C) chunked_keys(ch, cl, s_b[my_e], xnt, s_wn[my_e], H, my_l, my_lo, my_hi);
       }
       // the certified interval must meet the filter interval (the model of
@@ -2645,16 +2700,7 @@ __global__ void __launch_bounds__(kRfWarps * 32, 2) refine_kernel(RouteArgs a, c
         bool ok = cand_select(C, k, my_e, my_l, my_lo, my_hi, sel_e, sel_k);
         if (!ok) {
           // the compensated logits, some five orders of magnitude tighter
-          for (int j = 0; j < C; ++j) {
-            const int e = cand[j];
-            unsigned long long kl, klo, khi;
-            warp_dot_compensated(xr, a.w + static_cast<size_t>(e) * H, H, s_b[e], kl, klo, khi);
-            if (lane == j) {
-              my_l = kl;
-              my_lo = klo;
-              my_hi = khi;
-            }
-          }
+          rf_candidate_compensated(a, xs, cand, C, s_b, my_l, my_lo, my_hi);
           ok = cand_select(C, k, my_e, my_l, my_lo, my_hi, sel_e, sel_k);
         }
         if (ok) {
@@ -2729,6 +2775,61 @@ __global__ void __launch_bounds__(kRfWarps * 32, 2) refine_kernel(RouteArgs a, c
     if (lane == 0) flags[t] = 2;
     return;
   }
+}
+
+// Activations of one warp's token in shared memory: chunks of 256 groups of
+// four fp32 values (zero past the row).
+__device__ __forceinline__ int rf_chunks(int H) { return (((H >> 2) + 31) / 32 + 7) / 8; }
+size_t rf_smem_bytes(int H) { return static_cast<size_t>(kRfWarps) * ((((H >> 2) + 31) / 32 + 7) / 8) * 4096; }
+
+// One warp per token; the token's activations are staged once, in fp32, in
+// the warp's part of the shared memory.
+template <int NPL>
+__global__ void __launch_bounds__(kRfWarps * 32, 2) refine_kernel(RouteArgs a, const float* approx, const float* wn,
+                                                                  int* flags) {
+  extern __shared__ float4 rf_dyn[];
+  __shared__ float s_wn[1024], s_b[1024];
+  __shared__ int s_cand[kRfWarps][32];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  for (int e = tid; e < a.E; e += kRfWarps * 32) {
+    s_wn[e] = __ldg(wn + e);
+    s_b[e] = a.bias ? __ldg(a.bias + e) : 0.f;
+  }
+  __syncthreads();
+  const int t = blockIdx.x * kRfWarps + warp;
+  if (t >= a.T) return;
+  const int ngp = rf_chunks(a.H) * 256;  // groups of the padded row
+  float4* xs = rf_dyn + static_cast<size_t>(warp) * ngp;
+  const uint2* xr = reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(a.x) + static_cast<size_t>(t) * a.H);
+  float ss = 0.f;
+  for (int g = lane; g < ngp; g += 32) {
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (g < (a.H >> 2)) {
+      const uint2 b = __ldg(xr + g);
+      v = make_float4(__uint_as_float(b.x << 16), __uint_as_float(b.x & 0xFFFF0000u), __uint_as_float(b.y << 16),
+                      __uint_as_float(b.y & 0xFFFF0000u));
+    }
+    ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
+    xs[g] = v;
+  }
+  for (int off = 16; off; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+  // the token's norm bound, as row_norms_kernel's (within a relative 1e-3)
+  const float nrm = sqrtf(ss) * 1.001f;
+  __syncwarp();
+  refine_token<NPL>(a, t, approx, isfinite(nrm) ? nrm : INFINITY, flags, s_wn, s_b, s_cand[warp],
+                    reinterpret_cast<float*>(xs));
+}
+
+constexpr int kRfMaxH = 6144;  // the refining kernel's activations fit shared memory
+
+template <int NPL>
+cudaError_t launch_refine(int grid, size_t smem, const RouteArgs& a, const float* approx, const float* wn, int* flags,
+                          cudaStream_t st) {
+  cudaError_t e = cudaFuncSetAttribute(refine_kernel<NPL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  refine_kernel<NPL><<<grid, kRfWarps * 32, smem, st>>>(a, approx, wn, flags);
+  return cudaGetLastError();
 }
 
 // ---- multi-block plan: per-block counts, one scan, per-block stable scatter
@@ -2849,23 +2950,17 @@ size_t router_split_bytes(int E, int H) {
 }
 
 cudaError_t launch_route_large(const RouteArgs& a, float* norms, int* flags, float2* part, uint16_t* wsplit,
-                               cudaStream_t st) {
+                               int num_sms, cudaStream_t st) {
   if (a.T < 1 || a.k > 16 || a.E > 1024 || a.H % kLK) return cudaErrorInvalidValue;
   const int slices = a.H % (kLK * 4) == 0 ? 4 : (a.H % (kLK * 2) == 0 ? 2 : 1);
   float* xn = norms;
   float* wn = norms + a.T;
-  const int nrows = a.T + a.E;
-  if (a.xt == MOE_BF16)
-    row_norms_kernel<MOE_BF16><<<(nrows + 7) / 8, 256, 0, st>>>(a.x, a.T, a.w, a.E, a.H, xn, wn);
-  else
-    row_norms_kernel<MOE_F32><<<(nrows + 7) / 8, 256, 0, st>>>(a.x, a.T, a.w, a.E, a.H, xn, wn);
-  if (wsplit && a.xt == MOE_BF16 && a.H % kTcBK == 0 && encoder() == cudaSuccess) {
+  if (wsplit && a.xt == MOE_BF16 && a.H % kTcBK == 0 && a.H <= kRfMaxH && encoder() == cudaSuccess) {
     // tensor-core filter, certified logits of the candidates, then the
-    // per-token selection and exact repair of the tokens it left
+    // per-token selection and exact repair of the tokens it left (the norm
+    // bounds come from the split and the refining kernels)
     const int nb = (a.E + kTcExp - 1) / kTcExp;
-    const int64_t n4 = static_cast<int64_t>(nb) * kTcExp * (a.H / 4);
-    const int gs = static_cast<int>(std::min<int64_t>((n4 + 255) / 256, 4096));
-    router_split_kernel<<<gs, 256, 0, st>>>(a.w, a.E, a.H, wsplit);
+    router_split_kernel<<<nb * kTcExp / 8, 256, 0, st>>>(a.w, a.E, a.H, wsplit, wn);
     CUtensorMap mx, mw;
     cudaError_t e = map16(&mx, a.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.T, a.H, kTcTok);
     if (e != cudaSuccess) return e;
@@ -2877,22 +2972,30 @@ cudaError_t launch_route_large(const RouteArgs& a, float* norms, int* flags, flo
     if (e != cudaSuccess) return e;
     logits_tc_kernel<<<dim3((a.T + kTcTok - 1) / kTcTok, nb), 128, kTcSmem, st>>>(mx, mw, ta);
     const int rg = (a.T + kRfWarps - 1) / kRfWarps;
+    const size_t rsm = rf_smem_bytes(a.H);
+    (void)num_sms;
     if (a.E <= 32)
-      refine_kernel<1><<<rg, kRfWarps * 32, 0, st>>>(a, approx, xn, wn, flags);
+      e = launch_refine<1>(rg, rsm, a, approx, wn, flags, st);
     else if (a.E <= 64)
-      refine_kernel<2><<<rg, kRfWarps * 32, 0, st>>>(a, approx, xn, wn, flags);
+      e = launch_refine<2>(rg, rsm, a, approx, wn, flags, st);
     else if (a.E <= 128)
-      refine_kernel<4><<<rg, kRfWarps * 32, 0, st>>>(a, approx, xn, wn, flags);
+      e = launch_refine<4>(rg, rsm, a, approx, wn, flags, st);
     else if (a.E <= 256)
-      refine_kernel<8><<<rg, kRfWarps * 32, 0, st>>>(a, approx, xn, wn, flags);
+      e = launch_refine<8>(rg, rsm, a, approx, wn, flags, st);
     else if (a.E <= 512)
-      refine_kernel<16><<<rg, kRfWarps * 32, 0, st>>>(a, approx, xn, wn, flags);
+      e = launch_refine<16>(rg, rsm, a, approx, wn, flags, st);
     else
-      refine_kernel<32><<<rg, kRfWarps * 32, 0, st>>>(a, approx, xn, wn, flags);
+      e = launch_refine<32>(rg, rsm, a, approx, wn, flags, st);
+    if (e != cudaSuccess) return e;
     select_kernel<<<(a.T + 7) / 8, 256, 0, st>>>(a, flags, 1);
     repair_kernel<MOE_BF16><<<std::min((a.T + 31) / 32, kRepairGrid), kRouteThreads, 0, st>>>(a, flags);
     return cudaGetLastError();
   }
+  const int nrows = a.T + a.E;
+  if (a.xt == MOE_BF16)
+    row_norms_kernel<MOE_BF16><<<(nrows + 7) / 8, 256, 0, st>>>(a.x, a.T, a.w, a.E, a.H, xn, wn);
+  else
+    row_norms_kernel<MOE_F32><<<(nrows + 7) / 8, 256, 0, st>>>(a.x, a.T, a.w, a.E, a.H, xn, wn);
   dim3 grid((a.E + kLE - 1) / kLE, (a.T + kLT - 1) / kLT, slices);
   if (a.xt == MOE_BF16)
     logits_tiled_kernel<MOE_BF16><<<grid, kLThreads, 0, st>>>(a, part);
