@@ -53,47 +53,60 @@ __global__ void __launch_bounds__(256) gather_kernel(const void* x, int T, int k
 // Work items of both GEMMs from the unit table: per unit, 192-token tiles
 // times weight tiles (128 gate rows with the same 128 up rows, or 128 down
 // rows); the weight tile varies fastest so that consecutive CTAs share a
-// token tile.
+// token tile. Unit-major order; the items are written by the whole block
+// (each finds its unit by a binary search over the units' first items).
 __global__ void __launch_bounds__(1024) items_kernel(const int32_t* units, int I, int Is, int H,
                                                      int32_t* items0, int32_t* n0, int32_t* items1,
                                                      int32_t* n1) {
-  __shared__ int c0[1025], c1[1025];
-  const int nu = __ldg(units);
+  __shared__ int c0[1025], c1[1025], s_nt0[1024];
+  const int nu = min(__ldg(units), 1024);
   const int u = threadIdx.x;
-  int a = 0, b = 0, mt = 0, nt0 = 0, nt1 = 0;
+  const int nt1 = H / 128;
+  int a = 0, b = 0;
   if (u < nu) {
     const int4 U = __ldg(reinterpret_cast<const int4*>(units + kUnitHeader) + u);
-    mt = (U.z + kPrefillTok - 1) / kPrefillTok;
-    nt0 = ((U.x == -1 ? Is : I) + 127) / 128;
-    nt1 = H / 128;
+    const int mt = (U.z + kPrefillTok - 1) / kPrefillTok;
+    const int nt0 = ((U.x == -1 ? Is : I) + 127) / 128;
     a = mt * nt0;
     b = mt * nt1;
+    s_nt0[u] = nt0;
   }
   c0[u] = a;
   c1[u] = b;
   __syncthreads();
   if (u == 0) {
     int s0 = 0, s1 = 0;
-    for (int i = 0; i < min(nu, 1024); ++i) {
+    for (int i = 0; i < nu; ++i) {
       const int x0 = c0[i], x1 = c1[i];
       c0[i] = s0;
       c1[i] = s1;
       s0 += x0;
       s1 += x1;
     }
+    c0[nu] = s0;
+    c1[nu] = s1;
     *n0 = s0;
     *n1 = s1;
   }
   __syncthreads();
-  if (u < nu) {
-    int o = c0[u];
-    for (int m = 0; m < mt; ++m)
-      for (int n = 0; n < nt0; ++n, ++o)
-        reinterpret_cast<int4*>(items0)[o] = make_int4(u, m * kPrefillTok, n * 128, 0);
-    o = c1[u];
-    for (int m = 0; m < mt; ++m)
-      for (int n = 0; n < nt1; ++n, ++o)
-        reinterpret_cast<int4*>(items1)[o] = make_int4(u, m * kPrefillTok, n * 128, 0);
+  const int tot0 = c0[nu], tot1 = c1[nu];
+  for (int i = threadIdx.x; i < tot0; i += blockDim.x) {
+    int lo = 0, hi = nu - 1;  // the last unit whose first item is <= i
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (c0[mid] <= i) lo = mid; else hi = mid - 1;
+    }
+    const int j = i - c0[lo], nt = s_nt0[lo];
+    reinterpret_cast<int4*>(items0)[i] = make_int4(lo, (j / nt) * kPrefillTok, (j % nt) * 128, 0);
+  }
+  for (int i = threadIdx.x; i < tot1; i += blockDim.x) {
+    int lo = 0, hi = nu - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (c1[mid] <= i) lo = mid; else hi = mid - 1;
+    }
+    const int j = i - c1[lo];
+    reinterpret_cast<int4*>(items1)[i] = make_int4(lo, (j / nt1) * kPrefillTok, (j % nt1) * 128, 0);
   }
 }
 

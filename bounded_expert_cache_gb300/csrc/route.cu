@@ -2146,18 +2146,20 @@ static_assert(kTcABytes % 1024 == 0 && kTcStage % 1024 == 0, "stage alignment");
 
 // ws: bf16 [ceil(E/64)][2][64][H]: block b holds the hi rows of experts
 // 64b .. 64b+63, then their mid rows; rows of experts >= E are zero. One
-// warp per row; it also writes the row's norm bound wn[e] = 1.001 *
-// sqrt(sum w^2) in fp32 (the fp32 sum of squares is within a relative
-// 1e-3 of the exact one), infinite if not finite.
-__global__ void __launch_bounds__(256) router_split_kernel(const float* w, int E, int H, uint16_t* ws, float* wn) {
-  const int e = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-  const int nb = (E + kTcExp - 1) / kTcExp;
-  if (e >= nb * kTcExp) return;
+// 128-thread block per row (each warp a quarter of it); it also writes the
+// row's norm bound wn[e] = 1.001 * sqrt(sum w^2) in fp32 (the fp32 sum of
+// squares, its four quarters added in order, is within a relative 1e-3 of
+// the exact one), infinite if not finite.
+__global__ void __launch_bounds__(128) router_split_kernel(const float* w, int E, int H, uint16_t* ws, float* wn) {
+  __shared__ float s_part[4];
+  const int e = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = e / kTcExp, r = e % kTcExp;
   uint16_t* hrow = ws + (static_cast<int64_t>(2 * b) * kTcExp + r) * H;
   uint16_t* mrow = ws + (static_cast<int64_t>(2 * b + 1) * kTcExp + r) * H;
+  const int q = H / 4, c0 = warp * q;  // the warp's quarter (H % 64 == 0)
   float s = 0.f;
-  for (int c = lane * 4; c < H; c += 128) {
+#pragma unroll 4
+  for (int c = c0 + lane * 4; c < c0 + q; c += 128) {
     const float4 v = e < E ? __ldg(reinterpret_cast<const float4*>(w + static_cast<int64_t>(e) * H + c))
                            : make_float4(0.f, 0.f, 0.f, 0.f);
     const float f[4] = {v.x, v.y, v.z, v.w};
@@ -2176,8 +2178,12 @@ __global__ void __launch_bounds__(256) router_split_kernel(const float* w, int E
     *reinterpret_cast<uint2*>(mrow + c) = make_uint2(mb[0], mb[1]);
   }
   for (int off = 16; off; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-  const float nrm = sqrtf(s) * 1.001f;
-  if (lane == 0 && e < E) wn[e] = isfinite(nrm) ? nrm : INFINITY;
+  if (lane == 0) s_part[warp] = s;
+  __syncthreads();
+  if (threadIdx.x == 0 && e < E) {
+    const float nrm = sqrtf(((s_part[0] + s_part[1]) + s_part[2]) + s_part[3]) * 1.001f;
+    wn[e] = isfinite(nrm) ? nrm : INFINITY;
+  }
 }
 
 struct TcArgs {
@@ -2960,7 +2966,7 @@ cudaError_t launch_route_large(const RouteArgs& a, float* norms, int* flags, flo
     // per-token selection and exact repair of the tokens it left (the norm
     // bounds come from the split and the refining kernels)
     const int nb = (a.E + kTcExp - 1) / kTcExp;
-    router_split_kernel<<<nb * kTcExp / 8, 256, 0, st>>>(a.w, a.E, a.H, wsplit, wn);
+    router_split_kernel<<<nb * kTcExp, 128, 0, st>>>(a.w, a.E, a.H, wsplit, wn);
     CUtensorMap mx, mw;
     cudaError_t e = map16(&mx, a.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.T, a.H, kTcTok);
     if (e != cudaSuccess) return e;
