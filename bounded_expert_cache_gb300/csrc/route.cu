@@ -2512,7 +2512,7 @@ __device__ void rf_candidate_logits(const RouteArgs& a, const float* xs, const i
 
 // Compensated logits (error-free products by FMA, error-free sums, fp32
 // error accumulators; Ogita, Rump and Oishi 2005) of the warp's C <= 32
-// candidates against the token row xs (fp32, shared memory), streamed as
+// experts cand[0..C) against the token row xs (fp32, shared memory), streamed as
 // rf_candidate_logits streams the chunked ones. Each lane keeps four such
 // sums (one per component of the groups), combined error-free per
 // candidate, then the lanes. Keys as the few-token router's:
@@ -2613,7 +2613,7 @@ __device__ void rf_candidate_compensated(const RouteArgs& a, const float* xs, co
 // left uncertified, full keys and flag 2 for select_kernel and repair_kernel.
 template <int NPL>
 __device__ void refine_token(const RouteArgs& a, int t, const float* approx, float xnt, int* flags,
-                             const float* s_wn, const float* s_b, int* cand, float* xs) {
+                             const float* s_wn, const float* s_b, int* cand, int* amb_list, float* xs) {
   const int lane = threadIdx.x & 31;
   const int E = a.E, H = a.H, k = a.k;
   const float rs = __fmul_ru(0x1p-124f, __fsqrt_ru(static_cast<float>(H)));
@@ -2705,8 +2705,37 @@ __device__ void refine_token(const RouteArgs& a, int t, const float* approx, flo
         unsigned long long sel_k = 0ull;
         bool ok = cand_select(C, k, my_e, my_l, my_lo, my_hi, sel_e, sel_k);
         if (!ok) {
-          // the compensated logits, some five orders of magnitude tighter
-          rf_candidate_compensated(a, xs, cand, C, s_b, my_l, my_lo, my_hi);
+          // the candidates whose rank the intervals leave open (fewer than k
+          // others certainly above them) and whose interval meets another
+          // such candidate's get the compensated logits, some five orders of
+          // magnitude tighter
+          int above = 0;
+          for (int i = 0; i < C; ++i) {
+            const unsigned long long loi = __shfl_sync(0xffffffffu, my_lo, i);
+            above += (i != lane && loi > my_hi) ? 1 : 0;
+          }
+          const bool open = lane < C && above < k;
+          bool meets = false;
+          for (int i = 0; i < C; ++i) {
+            const unsigned long long loi = __shfl_sync(0xffffffffu, my_lo, i);
+            const unsigned long long hii = __shfl_sync(0xffffffffu, my_hi, i);
+            const bool oi = __shfl_sync(0xffffffffu, open, i);
+            meets |= open && oi && i != lane && !(my_lo > hii || loi > my_hi);
+          }
+          const unsigned amb = __ballot_sync(0xffffffffu, meets);
+          if (meets) amb_list[__popc(amb & lt)] = my_e;
+          __syncwarp();
+          unsigned long long kl = 0ull, klo = 0ull, khi = 0ull;
+          rf_candidate_compensated(a, xs, amb_list, __popc(amb), s_b, kl, klo, khi);
+          const int src = __popc(amb & lt) & 31;
+          const unsigned long long nl = __shfl_sync(0xffffffffu, kl, src);
+          const unsigned long long nlo = __shfl_sync(0xffffffffu, klo, src);
+          const unsigned long long nhi = __shfl_sync(0xffffffffu, khi, src);
+          if (meets) {
+            my_l = nl;
+            my_lo = nlo;
+            my_hi = nhi;
+          }
           ok = cand_select(C, k, my_e, my_l, my_lo, my_hi, sel_e, sel_k);
         }
         if (ok) {
@@ -2795,7 +2824,7 @@ __global__ void __launch_bounds__(kRfWarps * 32, 2) refine_kernel(RouteArgs a, c
                                                                   int* flags) {
   extern __shared__ float4 rf_dyn[];
   __shared__ float s_wn[1024], s_b[1024];
-  __shared__ int s_cand[kRfWarps][32];
+  __shared__ int s_cand[kRfWarps][32], s_amb[kRfWarps][32];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   for (int e = tid; e < a.E; e += kRfWarps * 32) {
     s_wn[e] = __ldg(wn + e);
@@ -2822,7 +2851,7 @@ __global__ void __launch_bounds__(kRfWarps * 32, 2) refine_kernel(RouteArgs a, c
   // the token's norm bound, as row_norms_kernel's (within a relative 1e-3)
   const float nrm = sqrtf(ss) * 1.001f;
   __syncwarp();
-  refine_token<NPL>(a, t, approx, isfinite(nrm) ? nrm : INFINITY, flags, s_wn, s_b, s_cand[warp],
+  refine_token<NPL>(a, t, approx, isfinite(nrm) ? nrm : INFINITY, flags, s_wn, s_b, s_cand[warp], s_amb[warp],
                     reinterpret_cast<float*>(xs));
 }
 
