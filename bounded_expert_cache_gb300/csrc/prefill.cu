@@ -19,34 +19,47 @@ namespace {
 
 // fp16 copy of the activations in expert-major order: row p < T*k is token
 // perm_tok[p]; rows T*k .. T*k+T-1 are tokens 0..T-1 (the shared expert's).
+// One warp per row; each lane keeps four 8-element loads in flight.
 template <int XT>
 __global__ void __launch_bounds__(256) gather_kernel(const void* x, int T, int k, int H,
-                                                     const int32_t* perm_tok, __half* out) {
-  const int p = blockIdx.x;
+                                                     const int32_t* perm_tok, __half* out, int rows) {
+  const int p = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (p >= rows) return;
   const int A = T * k;
   const int t = p < A ? __ldg(perm_tok + p) : p - A;
   __half* dst = out + static_cast<int64_t>(p) * H;
-  for (int i = threadIdx.x * 8; i < H; i += 256 * 8) {
-    float v[8];
-    if (XT == MOE_BF16) {
-      const uint4 b = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) +
-                                                          static_cast<int64_t>(t) * H + i));
-      const uint32_t w[4] = {b.x, b.y, b.z, b.w};
+  for (int i0 = lane * 8; i0 < H; i0 += 4 * 256) {
+    float v[4][8];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        v[2 * j] = __uint_as_float(w[j] << 16);
-        v[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+    for (int g = 0; g < 4; ++g) {
+      const int i = i0 + g * 256;
+      if (i >= H) continue;
+      if (XT == MOE_BF16) {
+        const uint4 b = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) +
+                                                            static_cast<int64_t>(t) * H + i));
+        const uint32_t w[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          v[g][2 * j] = __uint_as_float(w[j] << 16);
+          v[g][2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+        }
+      } else {
+        const float4* s = reinterpret_cast<const float4*>(static_cast<const float*>(x) +
+                                                          static_cast<int64_t>(t) * H + i);
+        const float4 c = __ldg(s), d = __ldg(s + 1);
+        v[g][0] = c.x, v[g][1] = c.y, v[g][2] = c.z, v[g][3] = c.w;
+        v[g][4] = d.x, v[g][5] = d.y, v[g][6] = d.z, v[g][7] = d.w;
       }
-    } else {
-      const float4* s = reinterpret_cast<const float4*>(static_cast<const float*>(x) +
-                                                        static_cast<int64_t>(t) * H + i);
-      const float4 a = __ldg(s), b = __ldg(s + 1);
-      v[0] = a.x, v[1] = a.y, v[2] = a.z, v[3] = a.w, v[4] = b.x, v[5] = b.y, v[6] = b.z, v[7] = b.w;
     }
-    __half2 h[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) h[j] = __floats2half2_rn(v[2 * j], v[2 * j + 1]);
-    *reinterpret_cast<uint4*>(dst + i) = *reinterpret_cast<uint4*>(h);
+    for (int g = 0; g < 4; ++g) {
+      const int i = i0 + g * 256;
+      if (i >= H) continue;
+      __half2 h[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) h[j] = __floats2half2_rn(v[g][2 * j], v[g][2 * j + 1]);
+      *reinterpret_cast<uint4*>(dst + i) = *reinterpret_cast<uint4*>(h);
+    }
   }
 }
 
@@ -269,9 +282,9 @@ cudaError_t prefill_ffn(const PrefillArgs& p, cudaStream_t st) {
   // 1. activations in expert-major order, fp16
   if (p.parts & kPartGather) {
     if (p.xt == MOE_BF16)
-      gather_kernel<MOE_BF16><<<rows, 256, 0, st>>>(p.x, p.T, p.k, p.H, p.plan.perm_tok, p.x16);
+      gather_kernel<MOE_BF16><<<(rows + 7) / 8, 256, 0, st>>>(p.x, p.T, p.k, p.H, p.plan.perm_tok, p.x16, rows);
     else
-      gather_kernel<MOE_F32><<<rows, 256, 0, st>>>(p.x, p.T, p.k, p.H, p.plan.perm_tok, p.x16);
+      gather_kernel<MOE_F32><<<(rows + 7) / 8, 256, 0, st>>>(p.x, p.T, p.k, p.H, p.plan.perm_tok, p.x16, rows);
   }
   if (p.parts & kPartGemm) {
     if ((e = prefill_gemms(p, st)) != cudaSuccess) return e;
