@@ -85,6 +85,31 @@ def test_route_many_tokens_filter_ties_and_degenerate_tokens(bec, E, k):
     ctx.close()
 
 
+@pytest.mark.parametrize("E,k,H", [(100, 6, 64), (48, 4, 6144), (40, 4, 6208)])
+def test_route_many_tokens_filter_shapes(bec, E, k, H):
+    # the tensor-core filter at one K stage (H 64), at the largest hidden size
+    # it takes (H 6,144: 96 stages, the refining kernel's activations at 192
+    # KiB of shared memory) with an expert count that fills no 64-expert
+    # tile, and just past it (H 6,208: the tiled CUDA-core router); routing
+    # bit-exact against the oracle, T = 200 (a ragged tile)
+    T = 200
+    w = W.with_changes(W.WORKLOADS["tiny"], x_dtype="bf16", hidden=H, n_experts=E, top_k=k,
+                       tokens_per_step=T, n_steps=1, slots=E)
+    ctx = make_context(bec, w, 1, max_tokens=T)
+    Wr = W.router_weights(w, 0)
+    x = W.activations(w, 0, T)
+    bias = (np.arange(E, dtype=np.float32) % 7) * np.float32(0.01)
+    idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    wt = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    ctx.route(0, x_to_torch(w, x), torch.from_numpy(Wr).cuda(), torch.from_numpy(bias).cuda(), idx, wt)
+    ctx.check_device_errors()
+    ridx, rw, _ = oracle.route(x_to_f64(w, x), Wr, bias, k)
+    assert np.array_equal(idx.cpu().numpy(), ridx)
+    assert np.allclose(wt.cpu().numpy(), rw, rtol=1e-5, atol=1e-7)
+    assert ctx.stats()["route_filter_fallbacks"] == 0
+    ctx.close()
+
+
 def test_plan_many_assignments(bec):
     rng = np.random.default_rng(11)
     for (T, E, k) in ((700, 256, 8), (333, 128, 8), (4096, 256, 8)):
