@@ -292,20 +292,22 @@ __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 // token: one gate and one up row per item, four blocks per SM (64
 // registers a thread, a few spilled): twice the warps of two-row items, 13.6
 // against 16.6 us a launch on the decode workload (16.0 at three blocks per
-// SM). Four-token groups: two rows, two blocks per SM (at most 128
-// registers, a few spilled): 29.5 against 32.4 us on the MTP-batched
-// workload. Eight-token groups: two rows, as many blocks as fit.
-template <int TM>
+// SM). Q4_0 groups of up to four tokens: one row pair, whose nibbles are
+// unpacked once per chunk for every token of the group; two blocks per SM.
+// Other groups: two rows, two blocks per SM for four tokens (at most 128
+// registers, a few spilled), as many blocks as fit for eight.
+template <int Q, int TM>
 struct GateupRows {
-  static constexpr int R = TM == 1 ? 1 : 2;
+  static constexpr bool kQ4Shared = Q == MOE_Q4_0 && TM > 1 && TM <= 4;
+  static constexpr int R = (TM == 1 || kQ4Shared) ? 1 : 2;
   static constexpr int kMinBlocks = TM == 1 ? 4 : (TM == 4 ? 2 : 1);
 };
 template <int Q, int TM, int XT>
-__global__ void __launch_bounds__(kThreads, GateupRows<TM>::kMinBlocks) gateup_kernel(FfnArgs a) {
+__global__ void __launch_bounds__(kThreads, GateupRows<Q, TM>::kMinBlocks) gateup_kernel(FfnArgs a) {
   extern __shared__ float xs[];  // [T][H] swizzled
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int H = a.H, T = a.T;
-  constexpr int RG = GateupRows<TM>::R;  // gate rows (and as many up rows) per warp item
+  constexpr int RG = GateupRows<Q, TM>::R;  // gate rows (and as many up rows) per warp item
   // x is the layer's input, complete once the router has passed its wait
   for (int i = tid; i < T * H; i += kThreads) {
     const int t = i / H, k = i - t * H;
@@ -354,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, GateupRows<TM>::kMinBlocks) gateup_k
       for (int r = 0; r < 2 * RG; ++r)
 #pragma unroll
         for (int m = 0; m < TM; ++m) acc[r][m] = 0.f;
-#pragma unroll 2
+#pragma unroll(GateupRows<Q, TM>::kQ4Shared ? 1 : 2)
       for (int c = lane; c < nch; c += 32) {
         uint4 w[2 * RG];
         uint32_t mb[2 * RG];
@@ -381,31 +383,77 @@ __global__ void __launch_bounds__(kThreads, GateupRows<TM>::kMinBlocks) gateup_k
         float d[2 * RG];
 #pragma unroll
         for (int r = 0; r < 2 * RG; ++r) d[r] = meta_scale<Q>(mb[r]);
+        if constexpr (GateupRows<Q, TM>::kQ4Shared) {
+          // the chunk's 32 nibbles of each row unpacked once (as dot_q4
+          // does) for every token of the group; each token's products are
+          // then summed in dot_q4's order, so the sums are bitwise dot_q4's
+          const unsigned long long bias = f2packf(8388616.0f, 8388616.0f);
+          unsigned long long qp[2 * RG][16];
 #pragma unroll
-        for (int m = 0; m < TM; ++m) {
-          if (m < mcount) {
-            const float* xr = xs + tok[m] * H;
-            if (Q == MOE_Q8_0) {
-              float xv[16];
-              load_chunk16(xr, c, xv);
+          for (int r = 0; r < 2 * RG; ++r) {
+            const uint32_t ws[4] = {w[r].x, w[r].y, w[r].z, w[r].w};
 #pragma unroll
-              for (int r = 0; r < 2 * RG; ++r)
-                acc[r][m] = fmaf(d[r], dot_q8(w[r], xv), acc[r][m]);
-            } else if (Q == MOE_Q4_0) {
+            for (int i = 0; i < 4; ++i) {
+              const uint32_t lo = ws[i] & 0x0F0F0F0Fu, hi = (ws[i] >> 4) & 0x0F0F0F0Fu;
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                qp[r][4 * i + 2 * h] = f2sub(f2pack(__byte_perm(lo, 0x4B000000u, 0x7540u | (2 * h)),
+                                                    __byte_perm(lo, 0x4B000000u, 0x7540u | (2 * h + 1))),
+                                             bias);
+                qp[r][4 * i + 2 * h + 1] = f2sub(f2pack(__byte_perm(hi, 0x4B000000u, 0x7540u | (2 * h)),
+                                                        __byte_perm(hi, 0x4B000000u, 0x7540u | (2 * h + 1))),
+                                                 bias);
+              }
+            }
+          }
+#pragma unroll
+          for (int m = 0; m < TM; ++m) {
+            if (m < mcount) {
+              const float* xr = xs + tok[m] * H;
               float xl[16], xh[16];
               load_chunk16(xr, 2 * c, xl);
               load_chunk16(xr, 2 * c + 1, xh);
 #pragma unroll
-              for (int r = 0; r < 2 * RG; ++r)
-                acc[r][m] = fmaf(d[r], dot_q4(w[r], xl, xh), acc[r][m]);
-            } else {
-              float xl[16], xh[16];
-              load_chunk16(xr, 2 * c, xl);
-              load_chunk16(xr, 2 * c + 1, xh);
-              const float xsum = sum32(xl, xh);
+              for (int r = 0; r < 2 * RG; ++r) {
+                unsigned long long sp = 0ull;
 #pragma unroll
-              for (int r = 0; r < 2 * RG; ++r)
-                acc[r][m] = fmaf(d[r], dot_u4(w[r], xl, xh), fmaf(meta_bias<Q>(mb[r]), xsum, acc[r][m]));
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                  for (int h = 0; h < 2; ++h) {
+                    sp = f2fma(qp[r][4 * i + 2 * h], f2packf(xl[4 * i + 2 * h], xl[4 * i + 2 * h + 1]), sp);
+                    sp = f2fma(qp[r][4 * i + 2 * h + 1], f2packf(xh[4 * i + 2 * h], xh[4 * i + 2 * h + 1]), sp);
+                  }
+                acc[r][m] = fmaf(d[r], f2sum(sp), acc[r][m]);
+              }
+            }
+          }
+        } else {
+#pragma unroll
+          for (int m = 0; m < TM; ++m) {
+            if (m < mcount) {
+              const float* xr = xs + tok[m] * H;
+              if (Q == MOE_Q8_0) {
+                float xv[16];
+                load_chunk16(xr, c, xv);
+#pragma unroll
+                for (int r = 0; r < 2 * RG; ++r)
+                  acc[r][m] = fmaf(d[r], dot_q8(w[r], xv), acc[r][m]);
+              } else if (Q == MOE_Q4_0) {
+                float xl[16], xh[16];
+                load_chunk16(xr, 2 * c, xl);
+                load_chunk16(xr, 2 * c + 1, xh);
+#pragma unroll
+                for (int r = 0; r < 2 * RG; ++r)
+                  acc[r][m] = fmaf(d[r], dot_q4(w[r], xl, xh), acc[r][m]);
+              } else {
+                float xl[16], xh[16];
+                load_chunk16(xr, 2 * c, xl);
+                load_chunk16(xr, 2 * c + 1, xh);
+                const float xsum = sum32(xl, xh);
+#pragma unroll
+                for (int r = 0; r < 2 * RG; ++r)
+                  acc[r][m] = fmaf(d[r], dot_u4(w[r], xl, xh), fmaf(meta_bias<Q>(mb[r]), xsum, acc[r][m]));
+              }
             }
           }
         }
@@ -1469,7 +1517,7 @@ cudaError_t launch_tm(const FfnArgs& a, int num_sms, cudaStream_t st) {
   err = cudaFuncSetAttribute(down_kernel<Q, TM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem2));
   if (err != cudaSuccess) return err;
-  const int items1 = max_units * (std::max(a.I, a.Is) / GateupRows<TM>::R);
+  const int items1 = max_units * (std::max(a.I, a.Is) / GateupRows<Q, TM>::R);
   const int grid1 = std::max(1, std::min((items1 + kWarps - 1) / kWarps, num_sms * 4));
   if (a.ev[0]) cudaEventRecord(a.ev[0], st);
   err = a.xt == MOE_BF16 ? pdl_launch(gateup_kernel<Q, TM, MOE_BF16>, dim3(grid1), dim3(kThreads), smem1, st, a)
