@@ -75,7 +75,7 @@ template <int PHASE> struct Shape {
   static constexpr int kAStages = PHASE == 0 ? 2 : 4;
   static constexpr uint32_t kAStride = 32u * kTiles;  // TMEM columns per A stage
   static constexpr int kAccBufs = PHASE == 0 ? 1 : 2;
-  static constexpr uint32_t kEpiBytes = PHASE == 0 ? 32u * kSP * 2 : 0u;
+  static constexpr uint32_t kEpiBytes = PHASE == 0 ? static_cast<uint32_t>(kTok) * kSP * 2 : 0u;
   static_assert(kAcc + kAStages * kAStride <= 512, "TMEM columns");
   static_assert(kStageBytes % 1024 == 0, "stage alignment");
 };
@@ -484,9 +484,10 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
       const uint32_t tb = tmem + lane_base + buf * static_cast<uint32_t>(kTok);
       const int64_t prow0 = static_cast<int64_t>(g.p0) + g.m0;
       if (PHASE == 0) {
-        // lane r holds G and U of weight row n0 + r: h column n0 + r; each
-        // chunk of 32 tokens goes through a transpose buffer so that rows of
-        // h are written 16 bytes at a time
+        // lane r holds G and U of weight row n0 + r: h column n0 + r. The
+        // whole tile's h goes to a transpose buffer first, so that the one
+        // accumulator pair is released to the next item's MMAs before the
+        // rows of h are written, 16 bytes at a time
         const int et = tid - kEpTid0;  // 0..127
         for (int ch = 0; ch < nch; ++ch) {
           uint32_t gv[32], uv[32];
@@ -495,23 +496,28 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const __nv_bfloat16 hb = __float2bfloat16_rn(silu_mul(__uint_as_float(gv[j]), __uint_as_float(uv[j])));
-            asm volatile("st.shared.u16 [%0], %1;" ::"r"(sepi + (j * kSP + r) * 2),
+            asm volatile("st.shared.u16 [%0], %1;" ::"r"(sepi + ((ch * 32 + j) * kSP + r) * 2),
                          "h"(*reinterpret_cast<const unsigned short*>(&hb))
                          : "memory");
           }
-          epi_sync();
-          // 32 tokens x 128 columns of bf16: 512 pieces of 16 bytes
+        }
+        asm volatile("tcgen05.fence::before_thread_sync;");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(su32(&bar_acce[buf]));  // the accumulators have been read
+        epi_sync();
+        // tokens x 128 columns of bf16, 16 bytes a piece
+        for (int ch = 0; ch < nch; ++ch) {
 #pragma unroll
           for (int rep = 0; rep < 4; ++rep) {
             const int piece = et + 128 * rep, j = piece >> 4, part = piece & 15;
             const int tok = ch * 32 + j;
             if (tok < g.ntok && part * 8 < g.nrows) {
-              const uint4 w = lds128(sepi + (j * kSP + part * 8) * 2);
+              const uint4 w = lds128(sepi + ((ch * 32 + j) * kSP + part * 8) * 2);
               *reinterpret_cast<uint4*>(a.h + (prow0 + tok) * a.ldh + g.n0 + part * 8) = w;
             }
           }
-          epi_sync();
         }
+        epi_sync();
       } else {
         for (int ch = 0; ch < nch; ++ch) {
           uint32_t v[32];
@@ -522,9 +528,11 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
             if (ch * 32 + j < g.ntok) dst[static_cast<int64_t>(j) * a.H] = __uint_as_float(v[j]);
         }
       }
-      asm volatile("tcgen05.fence::before_thread_sync;");
-      __syncwarp();
-      if (lane == 0) mbar_arrive(su32(&bar_acce[buf]));
+      if (PHASE != 0) {
+        asm volatile("tcgen05.fence::before_thread_sync;");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(su32(&bar_acce[buf]));
+      }
       ++acc_i;
     }
   }
