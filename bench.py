@@ -387,7 +387,8 @@ def run_ours(args, rank, world, dev):
              "graph": used_graph,
              "repeats": {"n": len(reps), "what": "the K timed steps from a fresh context, each repetition "
                                                  "timed on its own; value = the median",
-                         "tokens_per_s": rep_rates, "min": rep_rates[0], "max": rep_rates[-1]}}
+                         "tokens_per_s": rep_rates, "min": rep_rates[0], "max": rep_rates[-1],
+                         "in_run_order": [round(whole_job_rate(args.steps * T, world, r_ms), 2) for r_ms in reps]}}
     if not args.skip_e2e:
         # pass 3: the other miss paths: on-device admission with a separate
         # staging kernel (graph replay), and admission plus tile staging on
