@@ -2612,8 +2612,8 @@ __device__ void rf_candidate_compensated(const RouteArgs& a, const float* xs, co
 // logits of the candidates, selection and combine weights; or, for a token
 // left uncertified, full keys and flag 2 for select_kernel and repair_kernel.
 template <int NPL>
-__device__ void refine_token(const RouteArgs& a, int t, const float* approx, float xnt, int* flags,
-                             const float* s_wn, const float* s_b, int* cand, int* amb_list, float* xs) {
+__device__ void refine_token(const RouteArgs& a, int t, const float* approx, const float (&va)[NPL], float xnt,
+                             int* flags, const float* s_wn, const float* s_b, int* cand, int* amb_list, float* xs) {
   const int lane = threadIdx.x & 31;
   const int E = a.E, H = a.H, k = a.k;
   const float rs = __fmul_ru(0x1p-124f, __fsqrt_ru(static_cast<float>(H)));
@@ -2637,7 +2637,7 @@ __device__ void refine_token(const RouteArgs& a, int t, const float* approx, flo
       lk[i] = uk[i] = 0u;  // below every finite bound
       if (e < E) {
         float lv, uv;
-        filter_bounds(__ldg(ar + e), s_b[e], xnt, s_wn[e], rs, c0, lv, uv);
+        filter_bounds(va[i], s_b[e], xnt, s_wn[e], rs, c0, lv, uv);
         bad |= !(isfinite(lv) && isfinite(uv));
         lk[i] = fkey(lv);
         uk[i] = fkey(uv);
@@ -2835,6 +2835,14 @@ __global__ void __launch_bounds__(kRfWarps * 32, 2) refine_kernel(RouteArgs a, c
   if (t >= a.T) return;
   const int ngp = rf_chunks(a.H) * 256;  // groups of the padded row
   float4* xs = rf_dyn + static_cast<size_t>(warp) * ngp;
+  // the token's approximate logits are loaded first, so that their round
+  // trip overlaps the staging of the activations
+  float va[NPL];
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) {
+    const int e = i * 32 + lane;
+    va[i] = e < a.E ? __ldcs(approx + static_cast<size_t>(t) * a.E + e) : 0.f;
+  }
   const uint2* xr = reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(a.x) + static_cast<size_t>(t) * a.H);
   float ss = 0.f;
   for (int g = lane; g < ngp; g += 32) {
@@ -2851,7 +2859,7 @@ __global__ void __launch_bounds__(kRfWarps * 32, 2) refine_kernel(RouteArgs a, c
   // the token's norm bound, as row_norms_kernel's (within a relative 1e-3)
   const float nrm = sqrtf(ss) * 1.001f;
   __syncwarp();
-  refine_token<NPL>(a, t, approx, isfinite(nrm) ? nrm : INFINITY, flags, s_wn, s_b, s_cand[warp], s_amb[warp],
+  refine_token<NPL>(a, t, approx, va, isfinite(nrm) ? nrm : INFINITY, flags, s_wn, s_b, s_cand[warp], s_amb[warp],
                     reinterpret_cast<float*>(xs));
 }
 
