@@ -2125,10 +2125,10 @@ __global__ void __launch_bounds__(kRouteThreads) repair_kernel(RouteArgs a, cons
 // (at least k experts are certainly above it, ties included). The others,
 // the candidates (about ten of 256 on the prefill workload), get certified
 // logits on the CUDA cores: first summed in chunks of 32 products (the same
-// keys as the CUDA-core path), and for a token they leave uncertified once
-// more as compensated dot products (error-free products and sums; Ogita,
-// Rump and Oishi 2005), whose bound is some five orders of magnitude
-// tighter. Each candidate's certified logit is also checked against its
+// keys as the CUDA-core path); for a token they leave uncertified, the
+// candidates whose rank stays open are recomputed as compensated dot
+// products (error-free products and sums; Ogita, Rump and Oishi 2005),
+// whose bound is some five orders of magnitude tighter. Each candidate's certified logit is also checked against its
 // filter interval; a token whose check fails, or whose filter is not
 // finite, takes every expert as a candidate. A token still uncertified gets
 // full keys (non-candidates a key below every logit) and goes through the
