@@ -43,6 +43,35 @@ def test_library_exports_every_declared_symbol(bec):
     assert declared == bound, declared ^ bound
 
 
+def test_ctypes_structs_match_header(bec, tmp_path):
+    # the binding's structures have the header's size and field offsets, as a
+    # C compiler lays them out (the header needs no CUDA header of its own)
+    import ctypes
+
+    from bounded_expert_cache_gb300 import _native as N
+    pairs = {"moe_config_t": N.Config, "moe_plan_t": N.PlanT, "moe_miss_list_t": N.MissList,
+             "moe_stats_t": N.Stats, "moe_budget_t": N.Budget}
+    lines = ["#include <stdio.h>", "#include <stddef.h>", '#include "moecache.h"', "int main(void) {"]
+    for cname, cls in pairs.items():
+        lines.append('  printf("%s %%zu\\n", sizeof(%s));' % (cname, cname))
+        for fname, _ in cls._fields_:
+            lines.append('  printf("%s.%s %%zu\\n", offsetof(%s, %s));' % (cname, fname, cname, fname))
+    lines += ["  return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    r = subprocess.run(["gcc", "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)],
+                       capture_output=True, text=True)
+    if r.returncode != 0:
+        pytest.skip("no C compiler for the header: " + r.stderr[-200:])
+    got = dict(line.split() for line in subprocess.run([str(exe)], capture_output=True, text=True,
+                                                       check=True).stdout.splitlines())
+    for cname, cls in pairs.items():
+        assert int(got[cname]) == ctypes.sizeof(cls), cname
+        for fname, _ in cls._fields_:
+            assert int(got[cname + "." + fname]) == getattr(cls, fname).offset, (cname, fname)
+
+
 def test_splitmix64_published_vectors(bec, golden_dir):
     for line in open(os.path.join(golden_dir, "splitmix64.txt")):
         if line.startswith("#") or not line.strip():
