@@ -721,19 +721,64 @@ __device__ void admit_warp(const AdmitArgs& A, const moe_plan_t& P, unsigned cha
   int* upt = uq + nu;
   const int nwords = (E + 31) / 32;
   for (int w = lane; w < nwords; w += 32) bm[w] = 0u;
+  // global state is read in batches of kAdmB entries a lane, every load of a
+  // batch issued before the first is used
+  constexpr int kAdmB = 8;
   if (!st.slots) {
-    for (int s = lane; s < S; s += 32) {
-      s_last[s] = __ldcg(c.last + s);
-      s_owner[s] = __ldcg(c.owner + s);
-      s_sgen[s] = __ldcg(c.sgen + s);
+    for (int s0 = 0; s0 < S; s0 += 32 * kAdmB) {
+      unsigned long long vl[kAdmB];
+      int vo[kAdmB];
+      uint32_t vg[kAdmB];
+#pragma unroll
+      for (int j = 0; j < kAdmB; ++j) {
+        const int s = s0 + 32 * j + lane;
+        vl[j] = s < S ? __ldcg(c.last + s) : 0ull;
+        vo[j] = s < S ? __ldcg(c.owner + s) : 0;
+        vg[j] = s < S ? __ldcg(c.sgen + s) : 0u;
+      }
+#pragma unroll
+      for (int j = 0; j < kAdmB; ++j) {
+        const int s = s0 + 32 * j + lane;
+        if (s < S) {
+          s_last[s] = vl[j];
+          s_owner[s] = vo[j];
+          s_sgen[s] = vg[j];
+        }
+      }
     }
   }
   __syncwarp();
-  for (int u = lane; u < nu; u += 32) {
-    const int e = st.uniq ? st.uniq[u] : __ldcg(P.uniq + u);
-    uq[u] = e;
-    upt[u] = st.pt ? st.pt[e] : __ldcg(c.pt + e);
-    atomicOr(&bm[e >> 5], 1u << (e & 31));
+  if (st.uniq && st.pt) {
+    // staged in shared memory: nothing to overlap
+    for (int u = lane; u < nu; u += 32) {
+      const int e = st.uniq[u];
+      uq[u] = e;
+      upt[u] = st.pt[e];
+      atomicOr(&bm[e >> 5], 1u << (e & 31));
+    }
+  } else {
+    for (int u0 = 0; u0 < nu; u0 += 32 * kAdmB) {
+      int ve[kAdmB], vp[kAdmB];
+#pragma unroll
+      for (int j = 0; j < kAdmB; ++j) {
+        const int u = u0 + 32 * j + lane;
+        ve[j] = u < nu ? (st.uniq ? st.uniq[u] : __ldcg(P.uniq + u)) : 0;
+      }
+#pragma unroll
+      for (int j = 0; j < kAdmB; ++j) {
+        const int u = u0 + 32 * j + lane;
+        vp[j] = u < nu ? (st.pt ? st.pt[ve[j]] : __ldcg(c.pt + ve[j])) : 0;
+      }
+#pragma unroll
+      for (int j = 0; j < kAdmB; ++j) {
+        const int u = u0 + 32 * j + lane;
+        if (u < nu) {
+          uq[u] = ve[j];
+          upt[u] = vp[j];
+          atomicOr(&bm[ve[j] >> 5], 1u << (ve[j] & 31));
+        }
+      }
+    }
   }
   __syncwarp();
   auto in_u = [&](int o) { return o >= 0 && ((bm[o >> 5] >> (o & 31)) & 1u); };
@@ -771,72 +816,77 @@ __device__ void admit_warp(const AdmitArgs& A, const moe_plan_t& P, unsigned cha
   // misses in ascending id, one at a time
   unsigned long long rng = st.have_tick ? st.rng : __ldcg(c.rng);
   int nfill = 0, nevict = 0;
-  for (int u = 0; u < nu; ++u) {
-    if (upt[u] >= 0) continue;
-    const int e = uq[u];
-    ++tick;
-    int slot = -1;
-    for (int s0 = 0; s0 < S && slot < 0; s0 += 32) {
-      const int s = s0 + lane;
-      const unsigned fm = __ballot_sync(0xffffffffu, s < S && s_owner[s] < 0);
-      if (fm) slot = s0 + __ffs(fm) - 1;
-    }
-    if (slot < 0) {
-      if (A.policy == MOE_LRU) {
-        unsigned long long best = ~0ull;
-        int bs = INT_MAX;
-        for (int s = lane; s < S; s += 32) {
-          const unsigned long long v = s_last[s];
-          if (v < best || (v == best && s < bs)) {
-            best = v;
-            bs = s;
-          }
-        }
-        for (int off = 16; off; off >>= 1) {
-          const unsigned long long ov = __shfl_xor_sync(0xffffffffu, best, off);
-          const int os = __shfl_xor_sync(0xffffffffu, bs, off);
-          if (ov < best || (ov == best && os < bs)) {
-            best = ov;
-            bs = os;
-          }
-        }
-        slot = bs;
-      } else {
-        int n = 0;
-        for (int s0 = 0; s0 < S; s0 += 32) {
-          const int s = s0 + lane;
-          const int o = s < S ? s_owner[s] : -1;
-          n += __popc(__ballot_sync(0xffffffffu, o >= 0 && !in_u(o)));
-        }
-        const unsigned long long r = splitmix64_next(rng);
-        int target = static_cast<int>(r % static_cast<unsigned long long>(n));
-        for (int s0 = 0; s0 < S && slot < 0; s0 += 32) {
-          const int s = s0 + lane;
-          const int o = s < S ? s_owner[s] : -1;
-          unsigned cm = __ballot_sync(0xffffffffu, o >= 0 && !in_u(o));
-          const int pc = __popc(cm);
-          if (target < pc) {
-            for (int i = 0; i < target; ++i) cm &= cm - 1;
-            slot = s0 + __ffs(cm) - 1;
-          } else {
-            target -= pc;
-          }
-        }
+  for (int u0 = 0; u0 < nu; u0 += 32) {
+    // the chunk's misses, in ascending unit order (a miss changes only its own entry)
+    unsigned mm = __ballot_sync(0xffffffffu, u0 + lane < nu && upt[u0 + lane] < 0);
+    while (mm) {
+      const int u = u0 + __ffs(mm) - 1;
+      mm &= mm - 1;
+      const int e = uq[u];
+      ++tick;
+      int slot = -1;
+      for (int s0 = 0; s0 < S && slot < 0; s0 += 32) {
+        const int s = s0 + lane;
+        const unsigned fm = __ballot_sync(0xffffffffu, s < S && s_owner[s] < 0);
+        if (fm) slot = s0 + __ffs(fm) - 1;
       }
-      if (lane == 0) c.pt[s_owner[slot]] = -1;  // victims are never in the union
-      ++nevict;
+      if (slot < 0) {
+        if (A.policy == MOE_LRU) {
+          unsigned long long best = ~0ull;
+          int bs = INT_MAX;
+          for (int s = lane; s < S; s += 32) {
+            const unsigned long long v = s_last[s];
+            if (v < best || (v == best && s < bs)) {
+              best = v;
+              bs = s;
+            }
+          }
+          for (int off = 16; off; off >>= 1) {
+            const unsigned long long ov = __shfl_xor_sync(0xffffffffu, best, off);
+            const int os = __shfl_xor_sync(0xffffffffu, bs, off);
+            if (ov < best || (ov == best && os < bs)) {
+              best = ov;
+              bs = os;
+            }
+          }
+          slot = bs;
+        } else {
+          int n = 0;
+          for (int s0 = 0; s0 < S; s0 += 32) {
+            const int s = s0 + lane;
+            const int o = s < S ? s_owner[s] : -1;
+            n += __popc(__ballot_sync(0xffffffffu, o >= 0 && !in_u(o)));
+          }
+          const unsigned long long r = splitmix64_next(rng);
+          int target = static_cast<int>(r % static_cast<unsigned long long>(n));
+          for (int s0 = 0; s0 < S && slot < 0; s0 += 32) {
+            const int s = s0 + lane;
+            const int o = s < S ? s_owner[s] : -1;
+            unsigned cm = __ballot_sync(0xffffffffu, o >= 0 && !in_u(o));
+            const int pc = __popc(cm);
+            if (target < pc) {
+              for (int i = 0; i < target; ++i) cm &= cm - 1;
+              slot = s0 + __ffs(cm) - 1;
+            } else {
+              target -= pc;
+            }
+          }
+        }
+        if (lane == 0) c.pt[s_owner[slot]] = -1;  // victims are never in the union
+        ++nevict;
+      }
+      if (lane == 0) {
+        s_owner[slot] = e;
+        s_sgen[slot] += 1u;
+        s_last[slot] = tick;
+        upt[u] = -2 - slot;  // filled this step
+        A.fills[1 + 2 * nfill] = e;
+        A.fills[2 + 2 * nfill] = slot;
+        A.done[nfill] = 0u;
+      }
+      ++nfill;
+      __syncwarp();
     }
-    if (lane == 0) {
-      s_owner[slot] = e;
-      s_sgen[slot] += 1u;
-      s_last[slot] = tick;
-      upt[u] = -2 - slot;  // filled this step
-      A.fills[1 + 2 * nfill] = e;
-      A.fills[2 + 2 * nfill] = slot;
-      A.done[nfill] = 0u;
-    }
-    ++nfill;
-    __syncwarp();
   }
   // write back the slot state and the union's page-table entries
   for (int s = lane; s < S; s += 32) {
@@ -845,21 +895,39 @@ __device__ void admit_warp(const AdmitArgs& A, const moe_plan_t& P, unsigned cha
     c.sgen[s] = s_sgen[s];
   }
   long long assignments = 0;
-  for (int u = lane; u < nu; u += 32) {
+  // unit table: routed units in union order, then the shared expert
+  auto unit_entry = [&](int u, int cnt, int off) {
     const int e = uq[u];
     const bool was_miss = upt[u] <= -2;
     const int slot = was_miss ? -2 - upt[u] : upt[u];
-    const int cnt = st.cnt ? st.cnt[e] : __ldcg(P.counts + e);
     assignments += cnt;
     c.pt[e] = slot;
     c.ptgen[e] = s_sgen[slot];
-    // unit table: routed units in union order, then the shared expert
     int* U = A.units + kUnitHeader + kUnitInts * u;
     const bool filled = A.read_through && was_miss;
     U[0] = filled ? -2 - slot : slot;
-    U[1] = st.off ? st.off[e] : __ldcg(P.offsets + e);
+    U[1] = off;
     U[2] = cnt;
     U[3] = filled ? e : static_cast<int>(s_sgen[slot]);
+  };
+  if (st.cnt && st.off) {
+    for (int u = lane; u < nu; u += 32) unit_entry(u, st.cnt[uq[u]], st.off[uq[u]]);
+  } else {
+    for (int u0 = 0; u0 < nu; u0 += 32 * kAdmB) {
+      int vc[kAdmB], vo[kAdmB];
+#pragma unroll
+      for (int j = 0; j < kAdmB; ++j) {
+        const int u = u0 + 32 * j + lane;
+        const int e = u < nu ? uq[u] : 0;
+        vc[j] = u < nu ? (st.cnt ? st.cnt[e] : __ldcg(P.counts + e)) : 0;
+        vo[j] = u < nu ? (st.off ? st.off[e] : __ldcg(P.offsets + e)) : 0;
+      }
+#pragma unroll
+      for (int j = 0; j < kAdmB; ++j) {
+        const int u = u0 + 32 * j + lane;
+        if (u < nu) unit_entry(u, vc[j], vo[j]);
+      }
+    }
   }
   for (int off = 16; off; off >>= 1) assignments += __shfl_xor_sync(0xffffffffu, assignments, off);
   if (lane == 0) {
