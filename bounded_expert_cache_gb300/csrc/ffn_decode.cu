@@ -28,6 +28,8 @@
 // scheduling and is identical whatever the cache state.
 #include <cuda_fp16.h>
 
+#include <mutex>
+
 #include "internal.h"
 #include "pdl.cuh"
 
@@ -1493,6 +1495,25 @@ cudaError_t launch_fused_q(const FfnArgs& a, const FusedLaunch& fl, cudaStream_t
   return launch_fused_tm<Q, 8>(a, fl, st);
 }
 
+// Blocks of the gate/up kernel resident on one SM at a dynamic shared memory
+// size (the last size asked for is cached per instantiation).
+template <int Q, int TM, int XT>
+int gateup_blocks_per_sm(size_t smem) {
+  static std::mutex mu;
+  static size_t last_smem = 0;
+  static int last_n = 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (last_n == 0 || last_smem != smem) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gateup_kernel<Q, TM, XT>, kThreads, smem) != cudaSuccess ||
+        n < 1)
+      n = GateupRows<Q, TM>::kMinBlocks;
+    last_smem = smem;
+    last_n = n;
+  }
+  return last_n;
+}
+
 template <int Q, int TM>
 cudaError_t launch_tm(const FfnArgs& a, int num_sms, cudaStream_t st) {
   const size_t smem1 = sizeof(float) * static_cast<size_t>(a.T) * a.H;
@@ -1518,7 +1539,11 @@ cudaError_t launch_tm(const FfnArgs& a, int num_sms, cudaStream_t st) {
                              static_cast<int>(smem2));
   if (err != cudaSuccess) return err;
   const int items1 = max_units * (std::max(a.I, a.Is) / GateupRows<Q, TM>::R);
-  const int grid1 = std::max(1, std::min((items1 + kWarps - 1) / kWarps, num_sms * 4));
+  // one wave: the items are walked grid-stride by the blocks that fit at
+  // once (each block stages the step's activations once)
+  const int resident = a.xt == MOE_BF16 ? gateup_blocks_per_sm<Q, TM, MOE_BF16>(smem1)
+                                        : gateup_blocks_per_sm<Q, TM, MOE_F32>(smem1);
+  const int grid1 = std::max(1, std::min((items1 + kWarps - 1) / kWarps, num_sms * resident));
   if (a.ev[0]) cudaEventRecord(a.ev[0], st);
   err = a.xt == MOE_BF16 ? pdl_launch(gateup_kernel<Q, TM, MOE_BF16>, dim3(grid1), dim3(kThreads), smem1, st, a)
                          : pdl_launch(gateup_kernel<Q, TM, MOE_F32>, dim3(grid1), dim3(kThreads), smem1, st, a);
